@@ -1,0 +1,271 @@
+/*
+ * oracle.c -- plain CPU reference for the block-quantized projection GEMM
+ * and the fused gate/up SwiGLU projection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path
+ * (the CUDA library) shares no code with it and never calls it.
+ *
+ * Everything is computed in IEEE binary64.  No blocking, fusion or
+ * reordering beyond the definitions below: the weights are decoded block by
+ * block, every output is one dot product summed over k in increasing order,
+ * and SiLU(g)*u is applied to the two exact-as-fp64 dot products.
+ *
+ * Sources (m4-prefill-engine pages):
+ *  - "Releases", v0.3.0, PrismML Q2_0 ternary codec: a 128-weight block is
+ *    34 bytes, a 2-byte fp16 scale d plus 32 bytes of packed 2-bit codes
+ *    (2.125 bits per weight); a weight is (q - 1) * d and the reserved code
+ *    q = 3 decodes to +2 * d.
+ *  - "Releases", v0.3.0 / v0.2.3 and the project page's Table B: GGUF Q4_0
+ *    (block_q4_0) and Q8_0 are the other two codecs.  The pages name them
+ *    but do not print their formulas; the workload statement of this library
+ *    fixes them as 32-weight blocks with an fp16 scale d, Q4_0 w = (q - 8) * d
+ *    with a 4-bit q, Q8_0 w = q * d with a signed 8-bit q.
+ *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
+ *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
+ *    activation written out.
+ *
+ * Byte layouts (the reading this library takes; the pages print none):
+ *  - Q4_0 (18 B): d (fp16, little-endian) then 16 bytes; byte j holds weight
+ *    j in its low nibble and weight j + 16 in its high nibble.
+ *  - Q8_0 (34 B): d then 32 signed bytes, weight i in byte i.
+ *  - Q2_0 (34 B): d then 32 bytes; weight i is in byte i / 4 at bits
+ *    2 * (i % 4) .. 2 * (i % 4) + 1 (least significant pair first).
+ *
+ * Parity note: the Q2_0 code order and the Q4_0/Q8_0 byte layouts cannot be
+ * checked against real model files (none are available); they are pinned
+ * only by hand-decoded golden blocks written from the layouts above.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_Q4_0 = 0, ORACLE_Q8_0 = 1, ORACLE_Q2_0 = 2 };
+
+/* Weights per block, by codec. */
+long long oracle_block_size(int codec) {
+  switch (codec) {
+    case ORACLE_Q4_0: return 32;
+    case ORACLE_Q8_0: return 32;
+    case ORACLE_Q2_0: return 128;
+    default: return -1;
+  }
+}
+
+/* Bytes per block, by codec: a 2-byte scale plus the packed codes. */
+long long oracle_block_bytes(int codec) {
+  switch (codec) {
+    case ORACLE_Q4_0: return 2 + 32 / 2;   /* 16 bytes of nibbles */
+    case ORACLE_Q8_0: return 2 + 32;       /* 32 signed bytes */
+    case ORACLE_Q2_0: return 2 + 128 / 4;  /* 32 bytes of 2-bit codes */
+    default: return -1;
+  }
+}
+
+/* IEEE binary16 -> binary64, exact.  Written from the format definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_half_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -24);               /* subnormal: f * 2^-24 */
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(1024 + f), e - 25);   /* 1.f * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* binary64 -> binary16, round to nearest, ties to even (one rounding). */
+uint16_t oracle_double_to_half(double x) {
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return (uint16_t)(sign | 0x7e00);
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal range: the quantum is 2^-24 */
+    double r = nearbyint(a * 16777216.0);    /* exact scaling, then RNE */
+    return (uint16_t)(sign | (uint16_t)r);   /* r == 1024 is the smallest normal */
+  }
+  int e2;
+  (void)frexp(a, &e2);                       /* a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;                            /* unbiased half exponent */
+  if (E > 15) return (uint16_t)(sign | 0x7c00);
+  double r = nearbyint(ldexp(a, 10 - E));    /* significand in [1024, 2048] */
+  if (r == 2048.0) { r = 1024.0; E += 1; }
+  if (E > 15) return (uint16_t)(sign | 0x7c00);
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)r - 1024));
+}
+
+/* Decode the integer code of weight i of one block (the byte layouts above). */
+static int block_code(const uint8_t* blk, int codec, int i) {
+  const uint8_t* qs = blk + 2;
+  switch (codec) {
+    case ORACLE_Q4_0:
+      return (i < 16) ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);
+    case ORACLE_Q8_0:
+      return (int)(int8_t)qs[i];
+    case ORACLE_Q2_0:
+      return (qs[i / 4] >> (2 * (i % 4))) & 0x3;
+    default:
+      return 0;
+  }
+}
+
+/* The code value that decodes to zero: Q4_0 8, Q8_0 0, Q2_0 1. */
+static int code_zero(int codec) {
+  return codec == ORACLE_Q4_0 ? 8 : (codec == ORACLE_Q2_0 ? 1 : 0);
+}
+
+/* Dequantize one row of W (K weights) into binary64.  Each weight is
+ * (q - z) * d; the product of a <= 8-bit integer and an 11-bit significand
+ * is exact in binary64. */
+static void dequant_row(const uint8_t* row, int codec, long long K, double* out) {
+  long long B = oracle_block_size(codec), BB = oracle_block_bytes(codec);
+  int z = code_zero(codec);
+  for (long long b = 0; b < K / B; ++b) {
+    const uint8_t* blk = row + b * BB;
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    double d = oracle_half_to_double(dbits);
+    for (long long i = 0; i < B; ++i) {
+      int q = block_code(blk, codec, (int)i);
+      out[b * B + i] = (double)(q - z) * d;
+    }
+  }
+}
+
+static int check_shape(int codec, long long N, long long K) {
+  long long B = oracle_block_size(codec);
+  if (B <= 0) return -2;
+  if (N < 0 || K < 0 || K % B != 0) return -3;
+  return 0;
+}
+
+/* Wd[n*K + k] = exact value of weight (n, k).  Returns 0 or a negative code. */
+int oracle_dequant(const uint8_t* W, int codec, long long N, long long K, double* Wd) {
+  int rc = check_shape(codec, N, K);
+  if (rc) return rc;
+  long long row_bytes = (K / oracle_block_size(codec)) * oracle_block_bytes(codec);
+  for (long long n = 0; n < N; ++n) dequant_row(W + n * row_bytes, codec, K, Wd + n * K);
+  return 0;
+}
+
+/* Wh[n*K + k] = binary16 bits of the weight rounded once (RNE) to fp16. */
+int oracle_dequant_f16(const uint8_t* W, int codec, long long N, long long K, uint16_t* Wh) {
+  int rc = check_shape(codec, N, K);
+  if (rc) return rc;
+  long long row_bytes = (K / oracle_block_size(codec)) * oracle_block_bytes(codec);
+  double* tmp = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  if (!tmp) return -8;
+  for (long long n = 0; n < N; ++n) {
+    dequant_row(W + n * row_bytes, codec, K, tmp);
+    for (long long k = 0; k < K; ++k) Wh[n * K + k] = oracle_double_to_half(tmp[k]);
+  }
+  free(tmp);
+  return 0;
+}
+
+/* SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), in binary64. */
+double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ---- projections, split over output columns n across threads ---- */
+
+typedef struct {
+  const double* Xd;        /* [nrows, K] widened activations */
+  const uint8_t* W0;       /* gate (SwiGLU) or the only weight (GEMM) */
+  const uint8_t* W1;       /* up (SwiGLU) or NULL */
+  int codec;
+  long long nrows, N, K, row_bytes;
+  long long n_begin, n_end;
+  double* Y;               /* [nrows, N] */
+  int rc;
+} job_t;
+
+static double dot(const double* a, const double* b, long long K) {
+  double s = 0.0;
+  for (long long k = 0; k < K; ++k) s += a[k] * b[k];
+  return s;
+}
+
+static void* run_job(void* arg) {
+  job_t* j = (job_t*)arg;
+  double* w0 = (double*)malloc(sizeof(double) * (size_t)(j->K > 0 ? j->K : 1));
+  double* w1 = (double*)malloc(sizeof(double) * (size_t)(j->K > 0 ? j->K : 1));
+  if (!w0 || !w1) { free(w0); free(w1); j->rc = -8; return NULL; }
+  for (long long n = j->n_begin; n < j->n_end; ++n) {
+    dequant_row(j->W0 + n * j->row_bytes, j->codec, j->K, w0);
+    if (j->W1) dequant_row(j->W1 + n * j->row_bytes, j->codec, j->K, w1);
+    for (long long r = 0; r < j->nrows; ++r) {
+      const double* x = j->Xd + r * j->K;
+      double g = dot(x, w0, j->K);
+      if (j->W1) {
+        double u = dot(x, w1, j->K);
+        j->Y[r * j->N + n] = oracle_silu(g) * u;
+      } else {
+        j->Y[r * j->N + n] = g;
+      }
+    }
+  }
+  free(w0);
+  free(w1);
+  j->rc = 0;
+  return NULL;
+}
+
+static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int codec,
+                   long long M, long long N, long long K, const long long* rows,
+                   long long nrows, double* Y, int nthreads) {
+  int rc = check_shape(codec, N, K);
+  if (rc) return rc;
+  if (M < 0 || nrows < 0) return -3;
+  if (!rows) nrows = M;
+  double* Xd = (double*)malloc(sizeof(double) * (size_t)((nrows * K) > 0 ? nrows * K : 1));
+  if (!Xd) return -8;
+  for (long long r = 0; r < nrows; ++r) {
+    long long m = rows ? rows[r] : r;
+    if (m < 0 || m >= M) { free(Xd); return -1; }
+    for (long long k = 0; k < K; ++k) Xd[r * K + k] = oracle_half_to_double(X[m * K + k]);
+  }
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if (N < nthreads) nthreads = (int)(N > 0 ? N : 1);
+  job_t jobs[256];
+  pthread_t tids[256];
+  long long row_bytes = (K / oracle_block_size(codec)) * oracle_block_bytes(codec);
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (job_t){Xd, W0, W1, codec, nrows, N, K, row_bytes,
+                      N * t / nthreads, N * (t + 1) / nthreads, Y, 0};
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, run_job, &jobs[t]) != 0) break;
+    started = t;
+  }
+  run_job(&jobs[0]);
+  /* any job whose thread did not start runs here */
+  for (int t = started + 1; t < nthreads; ++t) run_job(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+  free(Xd);
+  for (int t = 0; t < nthreads; ++t)
+    if (jobs[t].rc) return jobs[t].rc;
+  return 0;
+}
+
+/* Y[r, n] = sum_k X[rows[r], k] * W[n, k]  (rows == NULL: every row of X).
+ * X is fp16 bits [M, K]; W is packed [N, K / block] blocks; Y is [nrows, N]. */
+int oracle_gemm(const uint16_t* X, const uint8_t* W, int codec, long long M, long long N,
+                long long K, const long long* rows, long long nrows, double* Y, int nthreads) {
+  return project(X, W, NULL, codec, M, N, K, rows, nrows, Y, nthreads);
+}
+
+/* Y[r, n] = SiLU(G) * U with G = X Wg^T, U = X Wu^T, both in binary64. */
+int oracle_swiglu(const uint16_t* X, const uint8_t* Wg, const uint8_t* Wu, int codec,
+                  long long M, long long N, long long K, const long long* rows,
+                  long long nrows, double* Y, int nthreads) {
+  if (!Wu) return -1;
+  return project(X, Wg, Wu, codec, M, N, K, rows, nrows, Y, nthreads);
+}

@@ -1,0 +1,280 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against something it cannot agree with by
+construction: hand-decoded golden blocks, numpy's IEEE conversions, exact
+rational arithmetic on tiny inputs, closed forms, the identity matrix, and
+invariants of SiLU.  A second group compiles copies of the oracle with a
+planted mistake and checks that at least one pin fails for each.
+"""
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+CODEC_BY_NAME = {"Q4_0": synth.Q4_0, "Q8_0": synth.Q8_0, "Q2_0": synth.Q2_0}
+ZERO_CODE = {synth.Q4_0: 8, synth.Q8_0: 0, synth.Q2_0: 1}
+
+
+def golden_packed(blk):
+    d = blk["d_bits"]
+    return np.array([d & 0xFF, d >> 8] + blk["code_bytes"], dtype=np.uint8)
+
+
+# ------------------------------------------------------------ block layout
+
+def test_block_sizes():
+    # "Releases" v0.3.0: Q2_0 is 128 weights in 34 bytes, 2.125 bits per weight.
+    assert oracle.block_size(synth.Q2_0) == 128
+    assert oracle.block_bytes(synth.Q2_0) == 34
+    assert oracle.block_bytes(synth.Q2_0) * 8 / oracle.block_size(synth.Q2_0) == 2.125
+    assert (oracle.block_size(synth.Q4_0), oracle.block_bytes(synth.Q4_0)) == (32, 18)
+    assert (oracle.block_size(synth.Q8_0), oracle.block_bytes(synth.Q8_0)) == (32, 34)
+    assert oracle.block_size(7) == -1
+
+
+def check_golden(blocks):
+    for blk in blocks:
+        codec = CODEC_BY_NAME[blk["codec"]]
+        B = oracle.block_size(codec)
+        w = oracle.dequant(golden_packed(blk), codec, 1, B)[0]
+        assert list(w) == blk["weights"], (blk["codec"], blk["name"])
+
+
+def test_golden_blocks(golden_blocks):
+    check_golden(golden_blocks)
+
+
+def test_q2_0_reserved_code_is_plus_two_d():
+    # "Releases" v0.3.0: q = 3 decodes to +2d (not clamped to +d).
+    for dbits, d in ((0x3C00, 1.0), (0x2E66, float(np.array([0x2E66], np.uint16).view(np.float16)[0]))):
+        W = synth.constant_weights(synth.Q2_0, 1, 128, 3, np.array([dbits], np.uint16).view(np.float16)[0])
+        assert np.all(oracle.dequant(W, synth.Q2_0, 1, 128) == 2 * d)
+
+
+def test_encoder_matches_golden(golden_blocks):
+    # The generator's encoder writes the same bytes as the hand-built blocks.
+    for blk in golden_blocks:
+        codec = CODEC_BY_NAME[blk["codec"]]
+        B = oracle.block_size(codec)
+        d = np.array([blk["d_bits"]], np.uint16).view(np.float16)
+        dval = float(d[0])
+        z = ZERO_CODE[codec]
+        q = np.array([[round(w / dval) + z for w in blk["weights"]]], dtype=np.int16)
+        assert np.array_equal(synth.pack(codec, q, d.reshape(1, 1)), golden_packed(blk).reshape(1, -1))
+
+
+# ------------------------------------------------------------ fp16 conversions
+
+def test_half_to_double_all_patterns():
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_double_to_half_matches_numpy():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000),
+        # exact ties between neighbouring fp16 values, normal and subnormal
+        (np.arange(1, 4000) + 0.5) * 2.0 ** -24,
+        (np.arange(1024, 2048) + 0.5) * 2.0 ** -10,
+        (np.arange(1024, 2048) + 0.5) * 2.0 ** 5,
+        np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -25,
+                  2.0 ** -25 * 1.0000001, 2.0 ** -14, 2.0 ** -14 * (1 - 2 ** -12)]),
+    ])
+    ours = oracle.double_to_half(vals)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------ projections
+
+def exact_gemm(q, d, codec, X16):
+    """Exact rational Y = X W^T from the generator's codes and scales."""
+    M, K = X16.shape
+    N = q.shape[0]
+    B = synth.BLOCK[codec]
+    z = ZERO_CODE[codec]
+    Xf = [[Fraction(float(v)) for v in row] for row in X16.astype(np.float64)]
+    Wf = [[(int(q[n, k]) - z) * Fraction(float(d[n, k // B])) for k in range(K)] for n in range(N)]
+    return [[sum(Xf[m][k] * Wf[n][k] for k in range(K)) for n in range(N)] for m in range(M)]
+
+
+@pytest.mark.parametrize("codec", synth.CODECS)
+def test_brute_force_exact(codec):
+    M, N = 4, 32
+    K = 32 if codec != synth.Q2_0 else 128
+    X = synth.activations(M, K, seed=11)
+    q = synth.codes(codec, N, K, seed=12, name="W")
+    d = synth.scales(codec, N, K, seed=12, name="W")
+    W = synth.pack(codec, q, d)
+    Y = oracle.gemm(X, W, codec, M, N, K)
+    E = exact_gemm(q, d, codec, X)
+    for m in range(M):
+        for n in range(N):
+            # recursive fp64 summation: |err| <= K * 2^-53 * sum |x w| (loose)
+            bound = K * 2.0 ** -52 * float(sum(abs(Fraction(float(X[m, k])) *
+                                                   (int(q[n, k]) - ZERO_CODE[codec]) *
+                                                   Fraction(float(d[n, k // synth.BLOCK[codec]])))
+                                               for k in range(K)))
+            assert abs(Fraction(Y[m, n]) - E[m][n]) <= Fraction(bound) + Fraction(1, 10 ** 30)
+
+
+@pytest.mark.parametrize("codec", synth.CODECS)
+def test_zero_code_gives_zero(codec):
+    # Q4_0 all q=8, Q8_0 all q=0, Q2_0 all q=1 decode to 0, so Y == 0 and SwiGLU == 0.
+    K = 256
+    X = synth.activations(8, K, seed=3)
+    W = synth.constant_weights(codec, 16, K, ZERO_CODE[codec], np.float16(0.37))
+    assert np.all(oracle.gemm(X, W, codec, 8, 16, K) == 0.0)
+    assert np.all(oracle.swiglu(X, W, W, codec, 8, 16, K) == 0.0)
+
+
+@pytest.mark.parametrize("codec,code", [(synth.Q4_0, 13), (synth.Q8_0, -57), (synth.Q2_0, 3), (synth.Q2_0, 0)])
+def test_constant_code_closed_form(codec, code):
+    # Constant code c and scale d: Y[m, n] = (c - z) * d * sum_k X[m, k].
+    M, N, K = 5, 8, 256
+    X = synth.activations(M, K, seed=4)
+    dv = np.float16(0.0173)
+    W = synth.constant_weights(codec, N, K, code, dv)
+    Y = oracle.gemm(X, W, codec, M, N, K)
+    for m in range(M):
+        exact = (code - ZERO_CODE[codec]) * float(dv) * math.fsum(X[m].astype(np.float64))
+        scale = abs(code - ZERO_CODE[codec]) * float(dv) * np.abs(X[m].astype(np.float64)).sum()
+        assert np.all(np.abs(Y[m] - exact) <= K * 2.0 ** -52 * scale + 1e-300)
+
+
+@pytest.mark.parametrize("codec", synth.CODECS)
+def test_identity_and_permutation_readout(codec):
+    # X = I (M = K): Y[k, n] = W[n, k] exactly -- one nonzero product per sum.
+    # X = a permutation P: Y[m, n] = W[n, p(m)], which a transposed operand breaks.
+    K = 128
+    N = 24
+    W = synth.weights(codec, N, K, seed=5)
+    Wd = oracle.dequant(W, codec, N, K)
+    I = np.eye(K, dtype=np.float16)
+    assert np.array_equal(oracle.gemm(I, W, codec, K, N, K), Wd.T)
+    perm = np.random.default_rng(2).permutation(K)
+    P = np.zeros((K, K), dtype=np.float16)
+    P[np.arange(K), perm] = 1
+    assert np.array_equal(oracle.gemm(P, W, codec, K, N, K), Wd[:, perm].T)
+
+
+def test_row_subset_matches_full():
+    M, N, K = 40, 16, 64
+    X = synth.activations(M, K, seed=6)
+    W = synth.weights(synth.Q4_0, N, K, seed=7)
+    full = oracle.gemm(X, W, synth.Q4_0, M, N, K)
+    rows = [39, 0, 17, 17, 5]
+    assert np.array_equal(oracle.gemm(X, W, synth.Q4_0, M, N, K, rows=rows), full[rows])
+
+
+def test_threads_do_not_change_results():
+    M, N, K = 9, 37, 96
+    X = synth.activations(M, K, seed=8)
+    W = synth.weights(synth.Q8_0, N, K, seed=9)
+    a = oracle.gemm(X, W, synth.Q8_0, M, N, K, nthreads=1)
+    b = oracle.gemm(X, W, synth.Q8_0, M, N, K, nthreads=7)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ SiLU and SwiGLU
+
+def sigmoid_decimal(x):
+    getcontext().prec = 50
+    return Decimal(1) / (Decimal(1) + (-Decimal(x)).exp())
+
+
+def test_silu_values_and_invariants():
+    assert oracle.silu(0.0) == 0.0
+    for x in (1.0, -1.0, 0.5, -3.25, 7.0, 20.0, -20.0):
+        ref = float(Decimal(x) * sigmoid_decimal(x))
+        assert abs(oracle.silu(x) - ref) <= 4e-16 * max(1.0, abs(ref))
+    # SiLU(x) - SiLU(-x) = x; SiLU(x) -> x for large x, -> 0 for very negative x
+    for x in np.linspace(-30, 30, 241):
+        assert abs(oracle.silu(x) - oracle.silu(-x) - x) <= 1e-14 * max(1.0, abs(x))
+    assert oracle.silu(60.0) == 60.0
+    assert abs(oracle.silu(-60.0)) < 1e-24
+
+
+@pytest.mark.parametrize("codec", synth.CODECS)
+def test_swiglu_fused_equals_unfused(codec):
+    # "v0.1 vs v0.2 comparison" section 2.2: fusion must not change the result.
+    M, N = 6, 20
+    K = 256
+    X = synth.activations(M, K, seed=10)
+    Wg = synth.weights(codec, N, K, seed=10, name="Wg")
+    Wu = synth.weights(codec, N, K, seed=10, name="Wu")
+    fused = oracle.swiglu(X, Wg, Wu, codec, M, N, K)
+    G = oracle.gemm(X, Wg, codec, M, N, K)
+    U = oracle.gemm(X, Wu, codec, M, N, K)
+    unfused = np.vectorize(oracle.silu)(G) * U
+    assert np.array_equal(fused, unfused)
+    # and against an independent SiLU (math.exp) within rounding
+    ind = G / (1.0 + np.exp(-G)) * U
+    assert np.allclose(fused, ind, rtol=1e-13, atol=1e-300)
+
+
+# ------------------------------------------------------------ planted mistakes
+
+MUTATIONS = {
+    # each: (text in oracle.c, replacement) -- plausible slips the pins must catch
+    "nibble_order": ("(i < 16) ? (qs[i] & 0x0f) : (qs[i - 16] >> 4)",
+                     "(i % 2 == 0) ? (qs[i / 2] & 0x0f) : (qs[i / 2] >> 4)"),
+    "q4_offset": ("return codec == ORACLE_Q4_0 ? 8 :", "return codec == ORACLE_Q4_0 ? 7 :"),
+    "q2_offset": ("(codec == ORACLE_Q2_0 ? 1 : 0)", "(codec == ORACLE_Q2_0 ? 0 : 0)"),
+    "q2_msb_first": ("(qs[i / 4] >> (2 * (i % 4))) & 0x3", "(qs[i / 4] >> (6 - 2 * (i % 4))) & 0x3"),
+    "q2_clamp_reserved": ("return (qs[i / 4] >> (2 * (i % 4))) & 0x3;",
+                          "{ int c = (qs[i / 4] >> (2 * (i % 4))) & 0x3; return c == 3 ? 2 : c; }"),
+    "q8_unsigned": ("return (int)(int8_t)qs[i];", "return (int)qs[i];"),
+    "scale_position": ("uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));",
+                       "uint16_t dbits = (uint16_t)(blk[1] | (blk[0] << 8));"),
+    "transposed_sum": ("const double* x = j->Xd + r * j->K;",
+                       "const double* x = j->Xd + ((r + 1) % (j->nrows ? j->nrows : 1)) * j->K;"),
+    "dropped_term": ("for (long long k = 0; k < K; ++k) s += a[k] * b[k];",
+                     "for (long long k = 1; k < K; ++k) s += a[k] * b[k];"),
+    "silu_sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    "silu_on_up": ("j->Y[r * j->N + n] = oracle_silu(g) * u;", "j->Y[r * j->N + n] = g * oracle_silu(u);"),
+    "half_rounding": ("double r = nearbyint(ldexp(a, 10 - E));", "double r = floor(ldexp(a, 10 - E));"),
+}
+
+
+def all_pins_pass(golden_blocks):
+    checks = [
+        lambda: check_golden(golden_blocks),
+        test_half_to_double_all_patterns,
+        test_double_to_half_matches_numpy,
+        lambda: [test_brute_force_exact(c) for c in synth.CODECS],
+        lambda: [test_zero_code_gives_zero(c) for c in synth.CODECS],
+        lambda: [test_identity_and_permutation_readout(c) for c in synth.CODECS],
+        test_silu_values_and_invariants,
+        lambda: [test_swiglu_fused_equals_unfused(c) for c in synth.CODECS],
+        lambda: test_q2_0_reserved_code_is_plus_two_d(),
+    ]
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path, golden_blocks):
+    old, new = MUTATIONS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, name
+    path = oracle.compile_variant(src.replace(old, new), str(tmp_path / ("mut_%s.so" % name)))
+    with oracle.use_library(path):
+        assert not all_pins_pass(golden_blocks), "mutation %s survived every pin" % name
