@@ -8,8 +8,10 @@
  *
  * Everything is computed in IEEE binary64.  No blocking, fusion or
  * reordering beyond the definitions below: the weights are decoded block by
- * block, every output is one dot product summed over k in increasing order,
- * and SiLU(g)*u is applied to the two exact-as-fp64 dot products.
+ * block, each decoded weight is rounded once to fp16 (the operand type the
+ * method multiplies, see below), every output is one dot product summed over
+ * k in increasing order, and SiLU(g)*u is applied to the two binary64 dot
+ * products.
  *
  * Sources (m4-prefill-engine pages):
  *  - "Releases", v0.3.0, PrismML Q2_0 ternary codec: a 128-weight block is
@@ -24,6 +26,12 @@
  *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
  *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
  *    activation written out.
+ *  - "v0.1 vs v0.2 comparison", section 2.1, and "Releases" v0.2.3: the
+ *    unpackers feed half-precision MMA fragments (simdgroup_matrix<half,8,8>),
+ *    so the weights the projection multiplies are fp16 values.  The oracle
+ *    therefore rounds each decoded weight (q - z) * d once to fp16 (nearest,
+ *    ties to even) before the binary64 dot product; oracle_dequant keeps the
+ *    exact values and oracle_dequant_f16 the rounded ones.
  *
  * Byte layouts (the reading this library takes; the pages print none):
  *  - Q4_0 (18 B): d (fp16, little-endian) then 16 bytes; byte j holds weight
@@ -191,6 +199,11 @@ static double dot(const double* a, const double* b, long long K) {
   return s;
 }
 
+/* The fp16 operand value of each decoded weight, widened back exactly. */
+static void round_row_to_f16(double* w, long long K) {
+  for (long long k = 0; k < K; ++k) w[k] = oracle_half_to_double(oracle_double_to_half(w[k]));
+}
+
 static void* run_job(void* arg) {
   job_t* j = (job_t*)arg;
   double* w0 = (double*)malloc(sizeof(double) * (size_t)(j->K > 0 ? j->K : 1));
@@ -198,7 +211,11 @@ static void* run_job(void* arg) {
   if (!w0 || !w1) { free(w0); free(w1); j->rc = -8; return NULL; }
   for (long long n = j->n_begin; n < j->n_end; ++n) {
     dequant_row(j->W0 + n * j->row_bytes, j->codec, j->K, w0);
-    if (j->W1) dequant_row(j->W1 + n * j->row_bytes, j->codec, j->K, w1);
+    round_row_to_f16(w0, j->K);
+    if (j->W1) {
+      dequant_row(j->W1 + n * j->row_bytes, j->codec, j->K, w1);
+      round_row_to_f16(w1, j->K);
+    }
     for (long long r = 0; r < j->nrows; ++r) {
       const double* x = j->Xd + r * j->K;
       double g = dot(x, w0, j->K);
@@ -255,7 +272,7 @@ static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int 
   return 0;
 }
 
-/* Y[r, n] = sum_k X[rows[r], k] * W[n, k]  (rows == NULL: every row of X).
+/* Y[r, n] = sum_k X[rows[r], k] * fp16(W[n, k])  (rows == NULL: every row of X).
  * X is fp16 bits [M, K]; W is packed [N, K / block] blocks; Y is [nrows, N]. */
 int oracle_gemm(const uint16_t* X, const uint8_t* W, int codec, long long M, long long N,
                 long long K, const long long* rows, long long nrows, double* Y, int nthreads) {

@@ -100,14 +100,21 @@ def test_double_to_half_matches_numpy():
 
 # ------------------------------------------------------------ projections
 
+def f16_weights(q, d, codec):
+    """Each weight (q - z) * d (exact in binary64) rounded once to fp16 by
+    numpy, as binary64 -- the operand values the method multiplies."""
+    B = synth.BLOCK[codec]
+    exact = (q.astype(np.float64) - ZERO_CODE[codec]) * np.repeat(d.astype(np.float64), B, axis=1)
+    return exact.astype(np.float16).astype(np.float64)
+
+
 def exact_gemm(q, d, codec, X16):
-    """Exact rational Y = X W^T from the generator's codes and scales."""
+    """Exact rational Y = X W16^T from the generator's codes and scales."""
     M, K = X16.shape
     N = q.shape[0]
-    B = synth.BLOCK[codec]
-    z = ZERO_CODE[codec]
+    W16 = f16_weights(q, d, codec)
     Xf = [[Fraction(float(v)) for v in row] for row in X16.astype(np.float64)]
-    Wf = [[(int(q[n, k]) - z) * Fraction(float(d[n, k // B])) for k in range(K)] for n in range(N)]
+    Wf = [[Fraction(float(W16[n, k])) for k in range(K)] for n in range(N)]
     return [[sum(Xf[m][k] * Wf[n][k] for k in range(K)) for n in range(N)] for m in range(M)]
 
 
@@ -121,13 +128,11 @@ def test_brute_force_exact(codec):
     W = synth.pack(codec, q, d)
     Y = oracle.gemm(X, W, codec, M, N, K)
     E = exact_gemm(q, d, codec, X)
+    W16 = f16_weights(q, d, codec)
     for m in range(M):
         for n in range(N):
-            # recursive fp64 summation: |err| <= K * 2^-53 * sum |x w| (loose)
-            bound = K * 2.0 ** -52 * float(sum(abs(Fraction(float(X[m, k])) *
-                                                   (int(q[n, k]) - ZERO_CODE[codec]) *
-                                                   Fraction(float(d[n, k // synth.BLOCK[codec]])))
-                                               for k in range(K)))
+            # recursive fp64 summation: |err| <= K * 2^-52 * sum |x w| (loose)
+            bound = K * 2.0 ** -52 * float(np.abs(X[m].astype(np.float64) * W16[n]).sum())
             assert abs(Fraction(Y[m, n]) - E[m][n]) <= Fraction(bound) + Fraction(1, 10 ** 30)
 
 
@@ -143,26 +148,27 @@ def test_zero_code_gives_zero(codec):
 
 @pytest.mark.parametrize("codec,code", [(synth.Q4_0, 13), (synth.Q8_0, -57), (synth.Q2_0, 3), (synth.Q2_0, 0)])
 def test_constant_code_closed_form(codec, code):
-    # Constant code c and scale d: Y[m, n] = (c - z) * d * sum_k X[m, k].
+    # Constant code c and scale d: Y[m, n] = fp16((c - z) * d) * sum_k X[m, k].
     M, N, K = 5, 8, 256
     X = synth.activations(M, K, seed=4)
     dv = np.float16(0.0173)
+    w16 = float(np.float16((code - ZERO_CODE[codec]) * float(dv)))
     W = synth.constant_weights(codec, N, K, code, dv)
     Y = oracle.gemm(X, W, codec, M, N, K)
     for m in range(M):
-        exact = (code - ZERO_CODE[codec]) * float(dv) * math.fsum(X[m].astype(np.float64))
-        scale = abs(code - ZERO_CODE[codec]) * float(dv) * np.abs(X[m].astype(np.float64)).sum()
+        exact = w16 * math.fsum(X[m].astype(np.float64))
+        scale = abs(w16) * np.abs(X[m].astype(np.float64)).sum()
         assert np.all(np.abs(Y[m] - exact) <= K * 2.0 ** -52 * scale + 1e-300)
 
 
 @pytest.mark.parametrize("codec", synth.CODECS)
 def test_identity_and_permutation_readout(codec):
-    # X = I (M = K): Y[k, n] = W[n, k] exactly -- one nonzero product per sum.
-    # X = a permutation P: Y[m, n] = W[n, p(m)], which a transposed operand breaks.
+    # X = I (M = K): Y[k, n] = W16[n, k] exactly -- one nonzero product per sum.
+    # X = a permutation P: Y[m, n] = W16[n, p(m)], which a transposed operand breaks.
     K = 128
     N = 24
     W = synth.weights(codec, N, K, seed=5)
-    Wd = oracle.dequant(W, codec, N, K)
+    Wd = oracle.dequant_f16(W, codec, N, K).view(np.float16).astype(np.float64)
     I = np.eye(K, dtype=np.float16)
     assert np.array_equal(oracle.gemm(I, W, codec, K, N, K), Wd.T)
     perm = np.random.default_rng(2).permutation(K)
@@ -247,6 +253,7 @@ MUTATIONS = {
     "silu_sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
     "silu_on_up": ("j->Y[r * j->N + n] = oracle_silu(g) * u;", "j->Y[r * j->N + n] = g * oracle_silu(u);"),
     "half_rounding": ("double r = nearbyint(ldexp(a, 10 - E));", "double r = floor(ldexp(a, 10 - E));"),
+    "unrounded_operands": ("    round_row_to_f16(w0, j->K);\n", "\n"),
 }
 
 
