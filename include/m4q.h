@@ -1,0 +1,128 @@
+/*
+ * m4q.h -- C ABI of the block-quantized projection library for one GB300
+ * (sm_103a).  Shared object: swiglu_block_quantized_gb300/_build/libm4q.so.
+ *
+ * The operation (m4-prefill-engine pages):
+ *  - "v0.1 vs v0.2 comparison", section 2.1, and the project page's Pillar 1
+ *    (Bricks 1 and 2): the prefill projection Y[M,N] = X[M,K] * W^T with fp16
+ *    activations and block-quantized weights unpacked inside the kernel.
+ *  - "Releases", v0.3.0 (M4QuantizedLinear): one linear layer dispatches to a
+ *    GEMV for decode-sized M and to a GEMM otherwise, across every codec.
+ *  - "v0.1 vs v0.2 comparison", section 2.2 (Brick 3): the fused gate/up
+ *    projection SiLU(X * Wg^T) x (X * Wu^T), computed on chip, writing only
+ *    the final activation.
+ *  - "Releases", v0.3.0, PrismML Q2_0 codec: 128 weights in 34 bytes,
+ *    w = (q - 1) * d with the reserved code 3 decoding to +2d.  Q4_0 and Q8_0
+ *    are GGUF's 32-weight blocks: w = (q - 8) * d and w = q * d.
+ *
+ * Conventions common to every call:
+ *  - Pointers X, W, Wg, Wu, Y, Wf16 are DEVICE pointers (cudaMalloc'd or from
+ *    PyTorch).  The caller owns every buffer; the library allocates nothing
+ *    during a call and keeps no pointer after it returns.
+ *  - Layouts are row-major and dense.  X is fp16 [M, K]; Y is fp16 [M, N].
+ *    W is [N rows][K / B blocks] of packed blocks (B = 32 for Q4_0 and Q8_0,
+ *    128 for Q2_0), block bytes 18 / 34 / 34, each block a little-endian fp16
+ *    scale d followed by its codes:
+ *      Q4_0: byte 2+j holds weight j in its low nibble, weight j+16 high;
+ *      Q8_0: byte 2+i holds weight i as a signed byte;
+ *      Q2_0: byte 2+i/4 holds weight i at bits 2*(i%4)..2*(i%4)+1.
+ *  - Shapes: M >= 1, N >= 8 with N % 8 == 0, K >= B with K % B == 0.
+ *    X, W, Wg, Wu, Y must be 16-byte aligned.
+ *  - Arithmetic: every weight is decoded to fp16 as (q - z) * d rounded once
+ *    to nearest even, products are accumulated in fp32, and each output is
+ *    rounded once to fp16 (SiLU(g) * u is formed in fp32 first).
+ *  - Asynchrony: calls enqueue work on `stream` and return; argument errors
+ *    are returned before anything is enqueued.  Launch failures return
+ *    M4Q_ERR_CUDA.  Device-side failures (a pipeline wait that gave up) are
+ *    recorded in a device status word that m4q_check_device_status() reads.
+ *  - Threading: calls may be made from several host threads.
+ */
+#ifndef M4Q_H_
+#define M4Q_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  NULL means the legacy default stream. */
+typedef struct CUstream_st* m4q_stream_t;
+
+/* Weight codecs. */
+enum m4q_codec { M4Q_Q4_0 = 0, M4Q_Q8_0 = 1, M4Q_Q2_0 = 2 };
+
+/* Execution paths for m4q_gemm_ex / m4q_swiglu_ex. */
+enum m4q_path {
+  M4Q_PATH_AUTO = 0, /* M <= 16: streaming GEMV; otherwise the tensor-core GEMM */
+  M4Q_PATH_GEMV = 1, /* weight-streaming GEMV (requires M <= 16) */
+  M4Q_PATH_TC = 2    /* tcgen05 tensor-core GEMM (any M) */
+};
+
+/* Status codes returned by every call. */
+enum m4q_status {
+  M4Q_OK = 0,
+  M4Q_ERR_INVALID_ARG = -1,        /* null pointer, M/N/K out of range, bad path */
+  M4Q_ERR_UNSUPPORTED_CODEC = -2,  /* codec not one of enum m4q_codec */
+  M4Q_ERR_BAD_SHAPE = -3,          /* K % B != 0 or N % 8 != 0 */
+  M4Q_ERR_MISALIGNED = -4,         /* a pointer is not 16-byte aligned */
+  M4Q_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
+  M4Q_ERR_NONFINITE = -6,          /* m4q_check_finite found NaN/Inf */
+  M4Q_ERR_TIMEOUT = -7,            /* a device pipeline wait gave up */
+  M4Q_ERR_UNSUPPORTED_DEVICE = -8  /* the current device is not sm_103 */
+};
+
+/* Y = X * W^T.  Dispatch: M <= 16 takes the GEMV path, else the tcgen05
+ * path.  Errors as listed in enum m4q_status. */
+int m4q_gemm(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K,
+             void* Y, m4q_stream_t stream);
+
+/* Y = SiLU(X * Wg^T) x (X * Wu^T); Wg and Wu share codec and shape [N, K].
+ * Neither intermediate product is written to memory. */
+int m4q_swiglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
+               int64_t N, int64_t K, void* Y, m4q_stream_t stream);
+
+/* As m4q_gemm / m4q_swiglu, with the path chosen by the caller (enum m4q_path). */
+int m4q_gemm_ex(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K,
+                void* Y, int path, m4q_stream_t stream);
+int m4q_swiglu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
+                  int64_t N, int64_t K, void* Y, int path, m4q_stream_t stream);
+
+/* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
+ * rounded once to nearest even.  The test hook for bit-exact decoding. */
+int m4q_dequant(const void* W, int codec, int64_t N, int64_t K, void* Wf16,
+                m4q_stream_t stream);
+
+/* Bytes of a packed [N, K] weight matrix: N * (K / B) * block_bytes, or 0 for
+ * an unknown codec or a K that is not a multiple of B. */
+size_t m4q_weight_bytes(int codec, int64_t N, int64_t K);
+
+/* NaN/Inf tripwire (the pages' "Releases" v0.3.0 bridge and the "v0.1 vs
+ * v0.2 comparison" metrology table: a non-finite output is a hard failure).
+ * Scans the device fp16 array x[n], synchronizes `stream` and returns
+ * M4Q_ERR_NONFINITE if any element is NaN or +-Inf, M4Q_OK otherwise. */
+int m4q_check_finite(const void* x, int64_t n, m4q_stream_t stream);
+
+/* Synchronize `stream`, read and clear the current device's status word.
+ * Returns M4Q_ERR_TIMEOUT if a kernel's bounded pipeline wait gave up since
+ * the last check, M4Q_OK otherwise. */
+int m4q_check_device_status(m4q_stream_t stream);
+
+/* Self-test of the bounded wait: launches one block that waits on a barrier
+ * nothing will complete, with a limit of `limit_ns` nanoseconds; the kernel
+ * records the timeout in the status word and returns.  The caller then sees
+ * M4Q_ERR_TIMEOUT from m4q_check_device_status().  Nothing faults or hangs. */
+int m4q_selftest_wait_timeout(int64_t limit_ns, m4q_stream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* m4q_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int m4q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M4Q_H_ */

@@ -1,0 +1,232 @@
+"""Python binding of libm4q.so: the block-quantized projection GEMM and the
+fused gate/up SwiGLU projection for one GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libm4q.so (see include/m4q.h).  PyTorch supplies device memory and
+streams.  There is no fallback: if the library is missing or the device is not
+sm_103, calls raise.
+
+Functions mirror the C ABI (same names without the ``m4q_`` prefix):
+    gemm(x, w, codec, n, k, out=None, path=PATH_AUTO)
+    swiglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
+    dequant(w, codec, n, k, out=None)
+    weight_bytes(codec, n, k), check_finite(t), check_device_status(),
+    selftest_wait_timeout(limit_ns), status_string(code), version()
+and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
+flattened into M; M <= 16 streams the weights, larger M uses tcgen05), the
+analogue of the pages' M4QuantizedLinear ("Releases" v0.3.0).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+Q4_0, Q8_0, Q2_0 = 0, 1, 2
+CODECS = (Q4_0, Q8_0, Q2_0)
+BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34}
+PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_CODEC = -2
+ERR_BAD_SHAPE = -3
+ERR_MISALIGNED = -4
+ERR_CUDA = -5
+ERR_NONFINITE = -6
+ERR_TIMEOUT = -7
+ERR_UNSUPPORTED_DEVICE = -8
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libm4q.so")
+
+# Every symbol declared in include/m4q.h, with its ctypes signature.
+_i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "m4q_gemm": (_i32, [_vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
+    "m4q_swiglu": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
+    "m4q_gemm_ex": (_i32, [_vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "m4q_swiglu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+    "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
+    "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
+    "m4q_check_device_status": (_i32, [_vp]),
+    "m4q_selftest_wait_timeout": (_i32, [_i64, _vp]),
+    "m4q_status_string": (ctypes.c_char_p, [_i32]),
+    "m4q_version": (_i32, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class M4QError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, status_string(code), code))
+
+
+def load(path: str | None = None):
+    """Load libm4q.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError("libm4q.so not built (run python -m swiglu_block_quantized_gb300.buildlib): %s" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().m4q_status_string(code).decode()
+    except ImportError:
+        return "status %d" % code
+
+
+def version() -> int:
+    return int(load().m4q_version())
+
+
+def weight_bytes(codec: int, n: int, k: int) -> int:
+    return int(load().m4q_weight_bytes(codec, n, k))
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise M4QError(rc, what)
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t, dtype, what):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % what)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+
+
+def _packed_check(w, codec, n, k, what):
+    import torch
+    _require(w, torch.uint8, what)
+    need = weight_bytes(codec, n, k)
+    if need == 0 or w.numel() != need:
+        raise ValueError("%s holds %d bytes, expected %d for %s [%d, %d]"
+                         % (what, w.numel(), need, codec, n, k))
+
+
+def gemm(x, w, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
+    """Y[M, n] = X[M, k] . W^T with W packed [n, k] (uint8 blocks)."""
+    import torch
+    _require(x, torch.float16, "x")
+    _packed_check(w, codec, n, k, "w")
+    m = x.numel() // k
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float16, device=x.device)
+    _require(out, torch.float16, "out")
+    _check(load().m4q_gemm_ex(x.data_ptr(), w.data_ptr(), codec, m, n, k, out.data_ptr(),
+                              path, _stream_ptr(stream)), "m4q_gemm")
+    return out
+
+
+def swiglu(x, wg, wu, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
+    """Y[M, n] = SiLU(X . Wg^T) * (X . Wu^T)."""
+    import torch
+    _require(x, torch.float16, "x")
+    _packed_check(wg, codec, n, k, "wg")
+    _packed_check(wu, codec, n, k, "wu")
+    m = x.numel() // k
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float16, device=x.device)
+    _require(out, torch.float16, "out")
+    _check(load().m4q_swiglu_ex(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), codec, m, n, k,
+                                out.data_ptr(), path, _stream_ptr(stream)), "m4q_swiglu")
+    return out
+
+
+def dequant(w, codec: int, n: int, k: int, out=None, stream=None):
+    """fp16 [n, k] decode of the packed weights (bit-exact test hook)."""
+    import torch
+    _packed_check(w, codec, n, k, "w")
+    if out is None:
+        out = torch.empty((n, k), dtype=torch.float16, device=w.device)
+    _require(out, torch.float16, "out")
+    _check(load().m4q_dequant(w.data_ptr(), codec, n, k, out.data_ptr(), _stream_ptr(stream)),
+           "m4q_dequant")
+    return out
+
+
+def check_finite(t, stream=None) -> bool:
+    """True if every element of the fp16 tensor is finite (synchronizes)."""
+    import torch
+    _require(t, torch.float16, "t")
+    rc = load().m4q_check_finite(t.data_ptr(), t.numel(), _stream_ptr(stream))
+    if rc == ERR_NONFINITE:
+        return False
+    _check(rc, "m4q_check_finite")
+    return True
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status: OK or ERR_TIMEOUT."""
+    return int(load().m4q_check_device_status(_stream_ptr(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(load().m4q_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)),
+           "m4q_selftest_wait_timeout")
+
+
+class QuantLinear:
+    """A linear layer over block-quantized weights [out_features, in_features]
+    (GEMV for M <= 16, tcgen05 otherwise); leading dims of x are flattened."""
+
+    def __init__(self, weight, codec: int, out_features: int, in_features: int):
+        _packed_check(weight, codec, out_features, in_features, "weight")
+        self.weight, self.codec = weight, codec
+        self.out_features, self.in_features = out_features, in_features
+
+    def __call__(self, x):
+        lead = x.shape[:-1]
+        if x.shape[-1] != self.in_features:
+            raise ValueError("last dim of x must be %d" % self.in_features)
+        x2 = x.reshape(-1, self.in_features)
+        y = gemm(x2, self.weight, self.codec, self.out_features, self.in_features)
+        return y.reshape(*lead, self.out_features)
+
+
+class QuantSwiGLU:
+    """The fused gate/up projection SiLU(x Wg^T) * (x Wu^T)."""
+
+    def __init__(self, wg, wu, codec: int, out_features: int, in_features: int):
+        _packed_check(wg, codec, out_features, in_features, "wg")
+        _packed_check(wu, codec, out_features, in_features, "wu")
+        self.wg, self.wu, self.codec = wg, wu, codec
+        self.out_features, self.in_features = out_features, in_features
+
+    def __call__(self, x):
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.in_features)
+        y = swiglu(x2, self.wg, self.wu, self.codec, self.out_features, self.in_features)
+        return y.reshape(*lead, self.out_features)

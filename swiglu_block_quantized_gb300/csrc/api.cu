@@ -1,0 +1,300 @@
+// api.cu -- the C ABI declared in include/m4q.h: argument checks, path
+// selection (GEMV for M <= 16, tcgen05 otherwise), TMA descriptor encoding
+// and kernel launch on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/m4q.h"
+#include "launch.h"
+
+namespace {
+
+using m4q::ProjLaunch;
+
+constexpr int kBlock[3] = {32, 32, 128};
+constexpr int kBlockBytes[3] = {18, 34, 34};
+constexpr int kStageK[3] = {256, 256, 1024};       // weights per packed stage (8 blocks)
+constexpr int kStageBytes[3] = {144, 272, 272};    // bytes per packed stage
+
+// Default limit of one device pipeline wait (ns); M4Q_WAIT_LIMIT_NS overrides.
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* s = getenv("M4Q_WAIT_LIMIT_NS");
+    unsigned long long x = s ? strtoull(s, nullptr, 10) : 0ull;
+    return x ? x : 2000000000ull;
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------ device facts
+
+struct DevInfo {
+  bool ok = false;
+  bool sm103 = false;
+  int sms = 0;
+};
+
+int current_device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[128];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return M4Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DevInfo& d = cache[dev];
+  if (!d.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return M4Q_ERR_CUDA;
+    d.sm103 = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.ok = true;
+  }
+  *out = d;
+  return M4Q_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D map: inner extent `inner` elements, `outer` rows, row pitch in bytes.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ validation
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int codec, int64_t M, int64_t N, int64_t K) {
+  if (codec < 0 || codec > 2) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (M < 1 || N < 1 || K < 1) return M4Q_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
+  if (K % kBlock[codec] != 0 || N % 8 != 0) return M4Q_ERR_BAD_SHAPE;
+  return M4Q_OK;
+}
+
+// ------------------------------------------------------------ dispatch
+
+int project(const void* X, const void* W0, const void* W1, int codec, int64_t M, int64_t N,
+            int64_t K, void* Y, int path, bool swiglu, m4q_stream_t stream) {
+  if (!X || !W0 || !Y || (swiglu && !W1)) return M4Q_ERR_INVALID_ARG;
+  int rc = check_shape(codec, M, N, K);
+  if (rc != M4Q_OK) return rc;
+  if (path < M4Q_PATH_AUTO || path > M4Q_PATH_TC) return M4Q_ERR_INVALID_ARG;
+  if (path == M4Q_PATH_GEMV && M > 16) return M4Q_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W0) || !aligned16(Y) || (swiglu && !aligned16(W1)))
+    return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+
+  ProjLaunch L{};
+  L.x = X;
+  L.w0 = W0;
+  L.w1 = swiglu ? W1 : nullptr;
+  L.y = Y;
+  L.M = (int)M;
+  L.N = (int)N;
+  L.K = (int)K;
+  L.row_bytes = (K / kBlock[codec]) * (long long)kBlockBytes[codec];
+  L.swiglu = swiglu;
+  L.wtma = (L.row_bytes % 16) == 0;  // then K is a multiple of the packed stage
+  L.status = m4q::status_words();
+  if (!L.status) return M4Q_ERR_CUDA;
+  L.limit_ns = wait_limit_ns();
+  L.stream = reinterpret_cast<cudaStream_t>(stream);
+
+  const bool gemv = (path == M4Q_PATH_GEMV) || (path == M4Q_PATH_AUTO && M <= 16);
+  cudaError_t e;
+  if (gemv) {
+    L.nstages = (int)((K + kStageK[codec] - 1) / kStageK[codec]);
+    int kw = 8;
+    while (kw > 1 && kw > L.nstages) kw >>= 1;
+    L.kw = kw;
+    L.mt = M <= 8 ? 1 : 2;
+    if (L.wtma) {
+      const uint32_t box_rows = 16;
+      if (!encode_2d(&L.tm_w0, CU_TENSOR_MAP_DATA_TYPE_UINT16, W0, L.row_bytes / 2, N,
+                     L.row_bytes, kStageBytes[codec] / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return M4Q_ERR_CUDA;
+      L.tm_w1 = L.tm_w0;
+      if (swiglu && !encode_2d(&L.tm_w1, CU_TENSOR_MAP_DATA_TYPE_UINT16, W1, L.row_bytes / 2, N,
+                               L.row_bytes, kStageBytes[codec] / 2, box_rows,
+                               CU_TENSOR_MAP_SWIZZLE_NONE))
+        return M4Q_ERR_CUDA;
+    }
+    e = m4q::launch_gemv(codec, L);
+  } else {
+    // Widest activation tile that still gives every SM a tile.
+    const int64_t out_rows = swiglu ? 64 : 128;
+    const int64_t ntiles = (N + out_rows - 1) / out_rows;
+    int nx = 64;
+    if (!L.wtma) {
+      nx = 128;
+    } else if (((M + 255) / 256) * ntiles >= dev.sms) {
+      nx = 256;
+    } else if (((M + 127) / 128) * ntiles >= dev.sms) {
+      nx = 128;
+    }
+    L.nx = nx;
+    if (!encode_2d(&L.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, K * 2, 64, nx,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return M4Q_ERR_CUDA;
+    L.tm_w0 = L.tm_x;
+    L.tm_w1 = L.tm_x;
+    if (L.wtma) {
+      const uint32_t box_rows = swiglu ? 64 : 128;
+      if (!encode_2d(&L.tm_w0, CU_TENSOR_MAP_DATA_TYPE_UINT16, W0, L.row_bytes / 2, N,
+                     L.row_bytes, kStageBytes[codec] / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return M4Q_ERR_CUDA;
+      if (swiglu && !encode_2d(&L.tm_w1, CU_TENSOR_MAP_DATA_TYPE_UINT16, W1, L.row_bytes / 2, N,
+                               L.row_bytes, kStageBytes[codec] / 2, box_rows,
+                               CU_TENSOR_MAP_SWIZZLE_NONE))
+        return M4Q_ERR_CUDA;
+    }
+    switch (codec) {
+      case M4Q_Q4_0: e = m4q::launch_tc_q4_0(L); break;
+      case M4Q_Q8_0: e = m4q::launch_tc_q8_0(L); break;
+      default: e = m4q::launch_tc_q2_0(L); break;
+    }
+  }
+  return e == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int m4q_gemm_ex(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K, void* Y,
+                int path, m4q_stream_t stream) {
+  return project(X, W, nullptr, codec, M, N, K, Y, path, false, stream);
+}
+
+int m4q_swiglu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
+                  int64_t K, void* Y, int path, m4q_stream_t stream) {
+  return project(X, Wg, Wu, codec, M, N, K, Y, path, true, stream);
+}
+
+int m4q_gemm(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K, void* Y,
+             m4q_stream_t stream) {
+  return project(X, W, nullptr, codec, M, N, K, Y, M4Q_PATH_AUTO, false, stream);
+}
+
+int m4q_swiglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
+               int64_t K, void* Y, m4q_stream_t stream) {
+  return project(X, Wg, Wu, codec, M, N, K, Y, M4Q_PATH_AUTO, true, stream);
+}
+
+size_t m4q_weight_bytes(int codec, int64_t N, int64_t K) {
+  if (codec < 0 || codec > 2 || N < 0 || K < 0 || K % kBlock[codec] != 0) return 0;
+  return (size_t)N * (size_t)(K / kBlock[codec]) * (size_t)kBlockBytes[codec];
+}
+
+int m4q_dequant(const void* W, int codec, int64_t N, int64_t K, void* Wf16, m4q_stream_t stream) {
+  if (!W || !Wf16) return M4Q_ERR_INVALID_ARG;
+  if (codec < 0 || codec > 2) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (N < 1 || K < 1 || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
+  if (K % kBlock[codec] != 0) return M4Q_ERR_BAD_SHAPE;
+  if (!aligned16(W) || !aligned16(Wf16)) return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+  const long long row_bytes = (K / kBlock[codec]) * (long long)kBlockBytes[codec];
+  return m4q::launch_dequant(codec, W, (int)N, (int)K, row_bytes, Wf16,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M4Q_OK
+             : M4Q_ERR_CUDA;
+}
+
+int m4q_check_finite(const void* x, int64_t n, m4q_stream_t stream) {
+  if (!x || n < 0) return M4Q_ERR_INVALID_ARG;
+  if (!aligned16(x)) return M4Q_ERR_MISALIGNED;
+  uint32_t* words = m4q::status_words();
+  if (!words) return M4Q_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m4q::launch_finite_check(x, n, words + 1, s) != cudaSuccess) return M4Q_ERR_CUDA;
+  uint32_t flag = 0;
+  if (cudaMemcpyAsync(&flag, words + 1, sizeof(flag), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return M4Q_ERR_CUDA;
+  return flag ? M4Q_ERR_NONFINITE : M4Q_OK;
+}
+
+int m4q_check_device_status(m4q_stream_t stream) {
+  uint32_t* words = m4q::status_words();
+  if (!words) return M4Q_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t st = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(&st, words, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return M4Q_ERR_CUDA;
+  if (st) {
+    if (cudaMemset(words, 0, sizeof(uint32_t)) != cudaSuccess) return M4Q_ERR_CUDA;
+    return M4Q_ERR_TIMEOUT;
+  }
+  return M4Q_OK;
+}
+
+int m4q_selftest_wait_timeout(int64_t limit_ns, m4q_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000) return M4Q_ERR_INVALID_ARG;
+  uint32_t* words = m4q::status_words();
+  if (!words) return M4Q_ERR_CUDA;
+  return m4q::launch_wait_selftest(words, (unsigned long long)limit_ns,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M4Q_OK
+             : M4Q_ERR_CUDA;
+}
+
+const char* m4q_status_string(int status) {
+  switch (status) {
+    case M4Q_OK: return "ok";
+    case M4Q_ERR_INVALID_ARG: return "invalid argument";
+    case M4Q_ERR_UNSUPPORTED_CODEC: return "unsupported codec";
+    case M4Q_ERR_BAD_SHAPE: return "bad shape (K must be a multiple of the block, N of 8)";
+    case M4Q_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case M4Q_ERR_CUDA: return "CUDA error";
+    case M4Q_ERR_NONFINITE: return "non-finite values found";
+    case M4Q_ERR_TIMEOUT: return "a device pipeline wait gave up";
+    case M4Q_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int m4q_version(void) { return 100; }
+
+}  // extern "C"

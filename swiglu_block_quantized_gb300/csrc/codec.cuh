@@ -1,0 +1,150 @@
+// codec.cuh -- device-side decoding of Q4_0, Q8_0 and PrismML Q2_0 blocks
+// into fp16 weights.
+//
+// Codecs (m4-prefill-engine "Releases" page, v0.3.0 and v0.2.3; GGUF for the
+// byte layout of Q4_0 / Q8_0):
+//   Q4_0  32 weights, 18 B: fp16 d, 16 B of nibbles  w = (q - 8) * d
+//   Q8_0  32 weights, 34 B: fp16 d, 32 signed bytes  w = q * d
+//   Q2_0 128 weights, 34 B: fp16 d, 32 B of 2-bit codes, w = (q - 1) * d,
+//         the reserved code 3 giving +2d.
+//
+// Every weight is produced with exactly one rounding: the code is placed in
+// the fraction field of an fp16 whose exponent makes one fraction step worth
+// 1 (so the fp16 holds bias + q exactly), the bias is subtracted exactly with
+// an fp16 subtract (the difference is a small integer), and the integer is
+// multiplied by d with one round-to-nearest-even fp16 multiply.  The result is
+// therefore RNE((q - z) * d), bit for bit, including subnormals and -0.
+//
+// A "packed stage" is 8 consecutive blocks of one weight row: 144 B (Q4_0),
+// 272 B (Q8_0, Q2_0), a multiple of 16 bytes so that TMA can move it.  It
+// covers KP = 256 (Q4_0, Q8_0) or 1024 (Q2_0) weights, split into SUB
+// sub-steps of 64 weights each.
+#pragma once
+
+#include "common.cuh"
+
+namespace m4q {
+
+template <int C>
+struct CodecTraits;
+
+template <>
+struct CodecTraits<kQ4_0> {
+  static constexpr int B = 32, BB = 18;
+};
+template <>
+struct CodecTraits<kQ8_0> {
+  static constexpr int B = 32, BB = 34;
+};
+template <>
+struct CodecTraits<kQ2_0> {
+  static constexpr int B = 128, BB = 34;
+};
+
+template <int C>
+struct Stage {
+  static constexpr int B = CodecTraits<C>::B;
+  static constexpr int BB = CodecTraits<C>::BB;
+  static constexpr int KP = 8 * B;          // weights per packed stage
+  static constexpr int KPB = 8 * BB;        // bytes per packed stage (row)
+  static constexpr int WORDS = KPB / 4;     // 32-bit words per packed stage
+  static constexpr int SUB = KP / 64;       // 64-weight sub-steps per stage
+  static_assert(KPB % 16 == 0, "packed stage must be a multiple of 16 bytes");
+};
+
+// fp16x2 arithmetic with explicit round-to-nearest-even (never contracted).
+__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 16-bit value at an even byte offset of a register-resident byte string.
+__device__ __forceinline__ uint32_t u16_at(const uint32_t* w, int off) {
+  return (off & 2) ? (w[off >> 2] >> 16) : (w[off >> 2] & 0xFFFFu);
+}
+
+// Bytes (off, off+1), off even, spread to [b0, 0, b1, 0].
+__device__ __forceinline__ uint32_t spread_pair(const uint32_t* w, int off) {
+  return __byte_perm(w[off >> 2], 0u, (off & 2) ? 0x4342u : 0x4140u);
+}
+
+// Byte off replicated to [b, 0, b, 0].
+__device__ __forceinline__ uint32_t spread_byte(const uint32_t* w, int off) {
+  const uint32_t b = (uint32_t)(off & 3);
+  return __byte_perm(w[off >> 2], 0u, 0x4040u | (b << 8) | b);
+}
+
+__device__ __forceinline__ uint32_t dup_scale(uint32_t dbits) { return dbits | (dbits << 16); }
+
+// Biased fp16x2 constants: 0x6400 = 1024 (step 1 at fraction bit 0),
+// 0x5C00 = 256 (step 1 at bit 2), 0x5400 = 64 (bit 4), 0x4C00 = 16 (bit 6).
+// Q4_0 low nibbles -> 1024 + q; high nibbles -> 64 + q.
+__device__ __forceinline__ void q4_pair(uint32_t t, uint32_t d2, uint32_t& lo, uint32_t& hi) {
+  lo = hmul2_rn(hsub2_rn((t & 0x000F000Fu) | 0x64006400u, 0x64086408u), d2);  // - 1032
+  hi = hmul2_rn(hsub2_rn((t & 0x00F000F0u) | 0x54005400u, 0x54805480u), d2);  // - 72
+}
+// Q8_0 signed byte: (q ^ 0x80) = q + 128 -> 1024 + 128 + q.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t t, uint32_t d2) {
+  return hmul2_rn(hsub2_rn((t ^ 0x00800080u) | 0x64006400u, 0x64806480u), d2);  // - 1152
+}
+// Q2_0 byte [v,0,v,0]: codes at bits 0-1, 2-3 -> (1024 + q0, 256 + q1);
+// bits 4-5, 6-7 -> (64 + q2, 16 + q3).
+__device__ __forceinline__ void q2_byte(uint32_t t, uint32_t d2, uint32_t& p01, uint32_t& p23) {
+  p01 = hmul2_rn(hsub2_rn((t & 0x000C0003u) | 0x5C006400u, 0x5C046401u), d2);  // -(257, 1025)
+  p23 = hmul2_rn(hsub2_rn((t & 0x00C00030u) | 0x4C005400u, 0x4C405410u), d2);  // -(17, 65)
+}
+
+// Decode sub-step j (weights 64j .. 64j+63 of a packed stage) of one row
+// into out[i] = fp16x2 (w[64j + 2i], w[64j + 2i + 1]).  `w` holds the row's
+// packed stage bytes; j must be a compile-time constant after unrolling.
+template <int C>
+__device__ __forceinline__ void decode_sub(const uint32_t* w, int j, uint32_t (&out)[32]);
+
+template <>
+__device__ __forceinline__ void decode_sub<kQ4_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int bo = (2 * j + h) * 18;
+    const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      uint32_t lo, hi;
+      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, lo, hi);
+      out[16 * h + p] = lo;      // weights 2p, 2p+1 of the block
+      out[16 * h + 8 + p] = hi;  // weights 16+2p, 17+2p
+    }
+  }
+}
+
+template <>
+__device__ __forceinline__ void decode_sub<kQ8_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int bo = (2 * j + h) * 34;
+    const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+    for (int p = 0; p < 16; ++p) out[16 * h + p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+  }
+}
+
+template <>
+__device__ __forceinline__ void decode_sub<kQ2_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+  const int bo = (j >> 1) * 34;
+  const int cb = bo + 2 + 16 * (j & 1);  // first code byte of this half block
+  const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    uint32_t p01, p23;
+    q2_byte(spread_byte(w, cb + c), d2, p01, p23);
+    out[2 * c] = p01;
+    out[2 * c + 1] = p23;
+  }
+}
+
+}  // namespace m4q

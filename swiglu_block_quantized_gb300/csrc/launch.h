@@ -1,0 +1,45 @@
+// launch.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  No kernel code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace m4q {
+
+// One projection launch, already validated by the ABI layer.
+struct ProjLaunch {
+  const void* x;          // fp16 [M, K]
+  const void* w0;         // packed weights (gate for SwiGLU)
+  const void* w1;         // up weights (SwiGLU) or null
+  void* y;                // fp16 [M, N]
+  int M, N, K;
+  long long row_bytes;
+  bool swiglu;
+  bool wtma;              // packed rows are 16-byte multiples: weights move by TMA
+  uint32_t* status;       // device status word
+  unsigned long long limit_ns;
+  cudaStream_t stream;
+  // tcgen05 path
+  int nx;                 // activation rows per tile: 64, 128 or 256
+  CUtensorMap tm_x, tm_w0, tm_w1;
+  // GEMV path
+  int kw;                 // warps per 16-row tile (split-K inside a CTA)
+  int nstages;            // packed stages per row
+  int mt;                 // 1 (M <= 8) or 2 (M <= 16)
+};
+
+cudaError_t launch_tc_q4_0(const ProjLaunch& L);
+cudaError_t launch_tc_q8_0(const ProjLaunch& L);
+cudaError_t launch_tc_q2_0(const ProjLaunch& L);
+cudaError_t launch_gemv(int codec, const ProjLaunch& L);
+
+// misc.cu
+uint32_t* status_words();  // [0] wait status, [1] non-finite flag; per current device
+cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row_bytes, void* out,
+                           cudaStream_t s);
+cudaError_t launch_finite_check(const void* x, long long n, uint32_t* flag, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace m4q

@@ -1,0 +1,126 @@
+// misc.cu -- device status word, the fp16 dequantization export, the
+// non-finite tripwire and the bounded-wait self-test.
+#include <mutex>
+
+#include "codec.cuh"
+#include "launch.h"
+
+namespace m4q {
+
+// [0]: bits set by kernels whose bounded waits gave up; [1]: non-finite flag.
+__device__ uint32_t g_status_words[2];
+
+uint32_t* status_words() {
+  static std::mutex mu;
+  static uint32_t* addr[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+// ---------------------------------------------------------------- dequant
+
+// One thread per (row n, 64-weight sub-step s): decode and write 64 (or, at
+// an odd block count, 32) fp16 values.
+template <int C>
+__global__ void __launch_bounds__(256)
+    dequant_kernel(const uint8_t* __restrict__ W, int N, int K, long long row_bytes,
+                   __half* __restrict__ out) {
+  using S = Stage<C>;
+  const int nsub = (K + 63) / 64;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)N * nsub) return;
+  const int n = (int)(idx / nsub), s = (int)(idx % nsub);
+  const uint8_t* row = W + (long long)n * row_bytes;
+
+  // Bytes of the blocks this sub-step needs, starting at word 0.
+  constexpr int kBytes = (C == kQ2_0) ? S::BB : 2 * S::BB;
+  const long long first = (C == kQ2_0) ? (long long)(s / 2) * S::BB : (long long)(2 * s) * S::BB;
+  uint32_t w[(kBytes + 3) / 4 + 1];
+#pragma unroll
+  for (int i = 0; i < (kBytes + 3) / 4 + 1; ++i) {
+    uint32_t lo = 0, hi = 0;
+    const long long o = first + 4 * i;
+    if (4 * i < kBytes && o < row_bytes) lo = __ldg(reinterpret_cast<const unsigned short*>(row + o));
+    if (4 * i + 2 < kBytes && o + 2 < row_bytes)
+      hi = __ldg(reinterpret_cast<const unsigned short*>(row + o + 2));
+    w[i] = lo | (hi << 16);
+  }
+  uint32_t v[32];
+  if (C == kQ2_0 && (s & 1)) decode_sub<C>(w, 1, v);
+  else decode_sub<C>(w, 0, v);
+
+  const int valid = (K - 64 * s) >= 64 ? 64 : (K - 64 * s);
+  uint4* dst = reinterpret_cast<uint4*>(out + (long long)n * K + 64 * s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (8 * i < valid) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row_bytes, void* out,
+                           cudaStream_t s) {
+  const long long threads = (long long)N * ((K + 63) / 64);
+  if (threads == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const auto* W = static_cast<const uint8_t*>(w);
+  auto* O = static_cast<__half*>(out);
+  switch (codec) {
+    case kQ4_0: dequant_kernel<kQ4_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
+    case kQ8_0: dequant_kernel<kQ8_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
+    default: dequant_kernel<kQ2_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- finite check
+
+__global__ void __launch_bounds__(256)
+    finite_kernel(const unsigned short* __restrict__ x, long long n, uint32_t* flag) {
+  bool bad = false;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    bad |= (x[i] & 0x7C00u) == 0x7C00u;  // exponent all ones: Inf or NaN
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(flag, 1u);
+}
+
+cudaError_t launch_finite_check(const void* x, long long n, uint32_t* flag, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  finite_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const unsigned short*>(x), n, flag);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- self-test
+
+// One thread waits on a barrier that nothing completes; the bounded wait
+// gives up after limit_ns, records the timeout and the kernel returns.
+__global__ void wait_selftest_kernel(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl ctl{&abort_flag, status, limit_ns};
+    (void)mbar_wait(&bar, 0, ctl);
+  }
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace m4q

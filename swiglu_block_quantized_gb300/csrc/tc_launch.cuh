@@ -1,0 +1,60 @@
+// tc_launch.cuh -- host launcher for the tcgen05 projection kernels of one
+// codec (instantiated once per codec in tc_q*.cu so they compile in parallel).
+#pragma once
+
+#include <atomic>
+
+#include "launch.h"
+#include "tc_proj.cuh"
+
+namespace m4q {
+
+template <int C, bool SWIGLU, int NX, bool WTMA>
+cudaError_t launch_tc_one(const ProjLaunch& L) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA>;
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  TcParams p;
+  p.w0 = static_cast<const uint8_t*>(L.w0);
+  p.w1 = static_cast<const uint8_t*>(L.w1);
+  p.y = static_cast<__half*>(L.y);
+  p.M = L.M;
+  p.N = L.N;
+  p.K = L.K;
+  p.row_bytes = L.row_bytes;
+  p.status = L.status;
+  p.limit_ns = L.limit_ns;
+  const dim3 grid((unsigned)((L.M + NX - 1) / NX), (unsigned)((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows));
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, p);
+  return cudaGetLastError();
+}
+
+template <int C, bool SWIGLU, bool WTMA>
+cudaError_t launch_tc_nx(const ProjLaunch& L) {
+  switch (L.nx) {
+    case 256: return launch_tc_one<C, SWIGLU, 256, WTMA>(L);
+    case 128: return launch_tc_one<C, SWIGLU, 128, WTMA>(L);
+    default: return launch_tc_one<C, SWIGLU, 64, WTMA>(L);
+  }
+}
+
+template <int C>
+cudaError_t launch_tc_impl(const ProjLaunch& L) {
+  if (L.wtma) {
+    return L.swiglu ? launch_tc_nx<C, true, true>(L) : launch_tc_nx<C, false, true>(L);
+  }
+  // Shapes whose packed rows are not 16-byte multiples: weights are read with
+  // plain loads; one tile width suffices for this path.
+  return L.swiglu ? launch_tc_one<C, true, 128, false>(L) : launch_tc_one<C, false, 128, false>(L);
+}
+
+}  // namespace m4q

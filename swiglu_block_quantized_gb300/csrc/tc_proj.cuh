@@ -1,0 +1,334 @@
+// tc_proj.cuh -- tcgen05 tensor-core kernel for the quantized projection
+// Y = X W^T and the fused gate/up projection Y = SiLU(X Wg^T) x (X Wu^T).
+//
+// Pages: "v0.1 vs v0.2 comparison" 2.1 (Bricks 1-2: a hardware-MMA GEMM core
+// fed by staged, unpacked weight tiles) and 2.2 (Brick 3: gate and up share
+// one staged X tile and the SiLU(G) x U epilogue stays on chip).
+//
+// Mapping onto sm_103a (one CTA per output tile, 8 warps):
+//   * The MMA computes D^T = W_tile * X_tile^T with M = 128 weight rows and
+//     N = NX activation rows: W is the A operand and lives in TMEM, X is the
+//     B operand and lives in shared memory (128-byte swizzled, K-major).
+//     D (fp32, 128 lanes x NX columns) accumulates in TMEM.
+//   * warp 0, one lane: TMA producer.  X sub-tiles [NX rows x 64 k] and packed
+//     weight stages [128 rows x 8 blocks] go into shared-memory rings.
+//   * warps 4..7 (128 threads, thread r owns weight row r = TMEM lane r):
+//     read the row's packed stage, decode 64 weights per sub-step to fp16
+//     (codec.cuh), and write them with tcgen05.st into a TMEM ring of A
+//     sub-tiles (32 columns each).  After the main loop they run the
+//     epilogue: tcgen05.ld of D, fp16 rounding (or SiLU(g)*u) and stores.
+//   * warp 1, one lane: issues tcgen05.mma (4 per 64-k sub-step) and commits
+//     stage releases to mbarriers.  Warp 1 also owns the TMEM allocation.
+//   * SwiGLU: A rows 0..63 are gate rows n0..n0+63 and rows 64..127 the up
+//     rows of the same outputs, so one MMA stream computes G and U for 64
+//     outputs; the epilogue pairs lane r with lane r + 64 through shared
+//     memory and writes only SiLU(G) x U.
+// Every mbarrier wait is bounded in time; on expiry the CTA records the
+// failure in the status word, drains what it has in flight, frees TMEM and
+// returns (results are then undefined and the host reports a timeout).
+#pragma once
+
+#include "codec.cuh"
+
+namespace m4q {
+
+struct TcParams {
+  const uint8_t* w0;   // weights (gate rows for SwiGLU); read directly when !WTMA
+  const uint8_t* w1;   // up weights for SwiGLU, else null
+  __half* y;           // [M, N]
+  int M, N, K;
+  long long row_bytes; // packed bytes per weight row
+  uint32_t* status;    // device status word
+  unsigned long long limit_ns;
+};
+
+template <int C, bool SWIGLU, int NX, bool WTMA>
+struct TcCfg {
+  using S = Stage<C>;
+  static constexpr int kThreads = 256;
+  static constexpr int kRows = 128;                               // MMA M
+  static constexpr int kOutRows = SWIGLU ? 64 : 128;              // outputs n per tile
+  static constexpr int kSX = NX == 256 ? 4 : (NX == 128 ? 6 : 8); // X ring depth
+  static constexpr int kSW = WTMA ? 2 : 0;                        // packed-W ring depth
+  static constexpr int kSA = 8;                                   // TMEM A ring depth
+  static constexpr int kXStage = NX * 128;                        // bytes
+  static constexpr int kWStage = kRows * S::KPB;                  // bytes
+  static constexpr int kTmemCols = 512;
+  static constexpr int kACol0 = 256;                              // A ring columns
+  static constexpr int kNumBars = 2 * kSX + 2 * kSW + 2 * kSA + 1;
+  static constexpr int kSmemUsed = kSX * kXStage + kSW * kWStage + kNumBars * 8 + 16;
+  // Request at least 116 KB so that two CTAs never share an SM (each takes
+  // all 512 TMEM columns).
+  static constexpr int kSmemBytes =
+      (kSmemUsed + 1024 > 116 * 1024) ? kSmemUsed + 1024 : 116 * 1024;
+  static_assert(NX % 16 == 0 && NX >= 32 && NX <= 256, "MMA N");
+  static_assert(kACol0 + 32 * kSA <= kTmemCols && NX <= kACol0, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0, "stage alignment");
+};
+
+// Pairwise fp16 stores of a 32-column chunk: this lane holds Y[m_base + j][n]
+// for j = 0..31; lanes 2i and 2i+1 hold n and n + 1.  Each even lane writes
+// (n, n+1) of row m_base + j, each odd lane (n-1, n) of row m_base + j + 1.
+__device__ __forceinline__ void store_pairs(__half* __restrict__ Y, int M, int N, int m_base,
+                                            int n, int lane, const float (&v)[32]) {
+  const int odd = lane & 1;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float send = odd ? v[j] : v[j + 1];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+    const int m = m_base + j + odd;
+    const int nn = n - odd;
+    const __half2 h = odd ? __floats2half2_rn(recv, v[j + 1]) : __floats2half2_rn(v[j], recv);
+    if (m < M && nn < N) *reinterpret_cast<__half2*>(Y + (size_t)m * N + nn) = h;
+  }
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+
+// Barrier-reduction OR over `count` threads of named barrier `id`.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// Read this row's packed stage `pk` straight from global memory (2-byte
+// loads; rows >= N and bytes past the row end read as zero, which decodes to
+// zero weights).
+template <int C>
+__device__ __forceinline__ void load_stage_global(const uint8_t* __restrict__ row, bool row_ok,
+                                                  long long row_bytes, int pk,
+                                                  uint32_t (&w)[Stage<C>::WORDS]) {
+  using S = Stage<C>;
+  const long long b0 = (long long)pk * S::KPB;
+#pragma unroll
+  for (int i = 0; i < S::WORDS; ++i) {
+    uint32_t lo = 0, hi = 0;
+    const long long o = b0 + 4 * i;
+    if (row_ok && o < row_bytes) lo = __ldg(reinterpret_cast<const unsigned short*>(row + o));
+    if (row_ok && o + 2 < row_bytes) hi = __ldg(reinterpret_cast<const unsigned short*>(row + o + 2));
+    w[i] = lo | (hi << 16);
+  }
+}
+
+template <int C, bool SWIGLU, int NX, bool WTMA>
+__global__ void __launch_bounds__(256, 1)
+    tc_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+                   const __grid_constant__ CUtensorMap tm_w1, const TcParams p) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  using S = Stage<C>;
+  constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SA = Cfg::kSA;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* xs = smem;
+  uint8_t* ws = xs + SX * Cfg::kXStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ws + SW * Cfg::kWStage);
+  uint64_t* x_full = bars;
+  uint64_t* x_empty = x_full + SX;
+  uint64_t* w_full = x_empty + SX;
+  uint64_t* w_empty = w_full + SW;
+  uint64_t* a_full = w_empty + SW;
+  uint64_t* a_empty = a_full + SA;
+  uint64_t* d_full = a_empty + SA;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(d_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * NX;
+  const int n0 = blockIdx.y * Cfg::kOutRows;
+  const int nks = (p.K + 63) / 64;                 // 64-weight sub-steps
+  const int npk = (p.K + S::KP - 1) / S::KP;       // packed stages
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
+    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 128); }
+    for (int i = 0; i < SA; ++i) { mbar_init(&a_full[i], 128); mbar_init(&a_empty[i], 1); }
+    mbar_init(d_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      if constexpr (WTMA) {
+        tma_prefetch_desc(&tm_w0);
+        if (SWIGLU) tma_prefetch_desc(&tm_w1);
+      }
+      int xi = 0, wi = 0;
+      bool ok = true;
+      for (int ks = 0; ks < nks; ++ks) {
+        if constexpr (WTMA) {
+          if ((ks % S::SUB) == 0) {
+          const int sp = wi % SW;
+          if (wi >= SW && !mbar_wait(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
+          uint8_t* dst = ws + sp * Cfg::kWStage;
+          const int xc = (ks / S::SUB) * (S::KPB / 2);  // uint16 elements
+          if (SWIGLU) {
+            tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
+            tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
+          } else {
+            tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
+          }
+          ++wi;
+          }
+        }
+        const int sx = xi % SX;
+        if (xi >= SX && !mbar_wait(&x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+        mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
+        tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx], ks * 64, m0);
+        ++xi;
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA exits.
+        for (int i = (xi > SX ? xi - SX : 0); i < xi; ++i)
+          mbar_wait_drain(&x_full[i % SX], (i / SX) & 1, 100000000ull);
+        if constexpr (WTMA) {
+          for (int i = (wi > SW ? wi - SW : 0); i < wi; ++i)
+            mbar_wait_drain(&w_full[i % SW], (i / SW) & 1, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, NX);
+      for (int ks = 0; ks < nks; ++ks) {
+        const int sx = ks % SX, sa = ks % SA;
+        if (!mbar_wait(&a_full[sa], (ks / SA) & 1, ctl)) break;
+        if (!mbar_wait(&x_full[sx], (ks / SX) & 1, ctl)) break;
+        tc_fence_after();
+        const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(xs + sx * Cfg::kXStage));
+        const uint32_t acol = tmem + Cfg::kACol0 + sa * 32;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+        tc_commit(&x_empty[sx]);
+        tc_commit(&a_empty[sa]);
+      }
+      tc_commit(d_full);  // always: fires once every MMA issued above is done
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ decode
+    const int r = threadIdx.x - 128;  // weight row of the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint8_t* grow = nullptr;
+    bool grow_ok = false;
+    if (!WTMA) {
+      const int n = SWIGLU ? n0 + (r & 63) : n0 + r;
+      grow_ok = n < p.N;
+      const uint8_t* base = (SWIGLU && r >= 64) ? p.w1 : p.w0;
+      grow = base + (grow_ok ? (long long)n * p.row_bytes : 0);
+    }
+    bool ok = true;
+    int ks = 0;
+    for (int pk = 0; pk < npk && ok; ++pk) {
+      uint32_t w[S::WORDS];
+      if constexpr (WTMA) {
+        const int sp = pk % SW;
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk / SW) & 1, ctl));
+        if (!ok) break;
+        const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + r * S::KPB);
+#pragma unroll
+        for (int i = 0; i < S::KPB / 16; ++i) {
+          const uint4 v = src[i];
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        mbar_arrive(&w_empty[sp]);
+      } else {
+        load_stage_global<C>(grow, grow_ok, p.row_bytes, pk, w);
+      }
+#pragma unroll
+      for (int j = 0; j < S::SUB; ++j) {
+        if (ks >= nks) break;
+        const int sa = ks % SA;
+        if (ks >= SA) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((ks / SA) - 1) & 1, ctl));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        uint32_t out[32];
+        decode_sub<C>(w, j, out);
+        tmem_st32_wait(tmem + lane_base + Cfg::kACol0 + sa * 32, out);
+        tc_fence_before();
+        mbar_arrive(&a_full[sa]);
+        ++ks;
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    bool dok = false;
+    if (!*abort_flag) dok = mbar_wait(d_full, 0, ctl);
+    // One decision for all four epilogue warps (they pair up below).
+    const bool bail = named_bar_any(3, 128, !dok || *abort_flag);
+    if (bail) {
+      mbar_wait_drain(d_full, 0, 200000000ull);  // let issued MMAs finish before TMEM is freed
+    } else {
+      tc_fence_after();
+      if (!SWIGLU) {
+        const int n = n0 + r;
+        for (int c0 = 0; c0 < NX && m0 + c0 < p.M; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32_wait(tmem + lane_base + c0, v);
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+          store_pairs(p.y, p.M, p.N, m0 + c0, n, lane, f);
+        }
+      } else {
+        const int q = warp & 3, pair = q & 1;
+        float* xch = reinterpret_cast<float*>(xs);  // the X ring is idle now
+        const int n = n0 + 32 * pair + lane;
+        int it = 0;
+        for (int c0 = 0; c0 < NX && m0 + c0 < p.M; c0 += 32, ++it) {
+          float* buf = xch + (pair * 2 + (it & 1)) * 1024;
+          uint32_t v[32];
+          tmem_ld32_wait(tmem + lane_base + c0, v);
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(v[j]);
+          }
+          named_bar_sync(1 + pair, 64);
+          if (q < 2) {
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] = silu_f32(__uint_as_float(v[j])) * buf[j * 32 + lane];
+            store_pairs(p.y, p.M, p.N, m0 + c0, n, lane, f);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace m4q

@@ -1,0 +1,6 @@
+// tc_q8_0.cu -- tcgen05 projection kernels for Q8_0 weights.
+#include "tc_launch.cuh"
+
+namespace m4q {
+cudaError_t launch_tc_q8_0(const ProjLaunch& L) { return launch_tc_impl<kQ8_0>(L); }
+}  // namespace m4q

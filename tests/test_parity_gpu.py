@@ -1,0 +1,205 @@
+"""GPU parity: every call of the C ABI against the CPU oracle on the same
+seeded inputs.
+
+Tolerance: per element |gpu - ref| <= 1e-2 * max(1, |ref|) with ref the
+binary64 oracle (fp32 accumulation, one fp16 rounding of the output).  The
+fp16 decode (m4q_dequant, and the tcgen05 path read out through X = I) must
+equal the oracle's once-rounded weights bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import swiglu_block_quantized_gb300 as m
+from _helpers import TOL, assert_close, dev, host, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+CODECS = [synth.Q4_0, synth.Q8_0, synth.Q2_0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    yield
+    assert m.check_device_status() == m.OK
+
+
+def kvals(codec, general):
+    """K values: multiples of the packed stage (TMA weights) or not (plain loads)."""
+    if codec == synth.Q2_0:
+        return [1024, 2048] if not general else [128, 384, 1152]
+    return [256, 512] if not general else [32, 96, 288]
+
+
+# ------------------------------------------------------------ dequant export
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("K", [128, 256, 1024, 1152])
+def test_dequant_bit_exact(codec, K):
+    N = 40
+    W = synth.weights(codec, N, K, seed=K)
+    got = host(m.dequant(dev(W), codec, N, K)).view(np.uint16)
+    assert np.array_equal(got, oracle.dequant_f16(W, codec, N, K))
+
+
+@pytest.mark.parametrize("codec", CODECS)
+def test_dequant_special_scales(codec):
+    # subnormal, zero, negative, large (overflow to inf) and NaN scales
+    B = synth.BLOCK[codec]
+    specials = np.array([0x0001, 0x03FF, 0x0000, 0x8000, 0xBC00, 0x7BFF, 0x7800, 0x7E00, 0x3C00],
+                        dtype=np.uint16).view(np.float16)
+    N, K = 8, B * len(specials)
+    q = synth.codes(codec, N, K, seed=1, name="W")
+    d = np.tile(specials, (N, 1))
+    W = synth.pack(codec, q, d)
+    got = host(m.dequant(dev(W), codec, N, K)).view(np.uint16)
+    ref = oracle.dequant_f16(W, codec, N, K)
+    nan = (ref & 0x7C00) == 0x7C00
+    nan &= (ref & 0x03FF) != 0
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(((got[nan] & 0x7C00) == 0x7C00) & ((got[nan] & 0x3FF) != 0))
+
+
+# ------------------------------------------------------------ tcgen05 path
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("general", [False, True])
+def test_tc_identity_readout_bit_exact(codec, general):
+    # X = I (M = K): every output is one exact product 1 * w, so Y^T must be
+    # the fp16 weights bit for bit -- checks decode, TMEM operand layout and
+    # the epilogue indexing of the tensor-core path at once.
+    K = kvals(codec, general)[0]
+    N = 136   # two weight tiles, the second ragged
+    W = synth.weights(codec, N, K, seed=3)
+    X = np.eye(K, dtype=np.float16)
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_TC)).view(np.uint16)
+    assert np.array_equal(Y.T, oracle.dequant_f16(W, codec, N, K))
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("general", [False, True])
+@pytest.mark.parametrize("M", [17, 64, 129, 300])
+def test_tc_gemm_parity(codec, general, M):
+    for K in kvals(codec, general):
+        N = 264
+        X = synth.activations(M, K, seed=M)
+        W = synth.weights(codec, N, K, seed=K)
+        Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_TC))
+        assert_close(Y, oracle.gemm(X, W, codec, M, N, K), "tc gemm %s M=%d K=%d" % (codec, M, K))
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("general", [False, True])
+@pytest.mark.parametrize("M", [20, 128, 257])
+def test_tc_swiglu_parity(codec, general, M):
+    for K in kvals(codec, general):
+        N = 200
+        X = synth.activations(M, K, seed=M + 1)
+        Wg = synth.weights(codec, N, K, seed=K, name="Wg")
+        Wu = synth.weights(codec, N, K, seed=K, name="Wu")
+        Y = host(m.swiglu(dev(X), dev(Wg), dev(Wu), codec, N, K, path=m.PATH_TC))
+        assert_close(Y, oracle.swiglu(X, Wg, Wu, codec, M, N, K), "tc swiglu %s M=%d K=%d" % (codec, M, K))
+
+
+def test_tc_tile_widths():
+    # M large enough for 256- and 128-wide activation tiles on a full GPU.
+    import torch
+    for M, N in ((2048, 8192), (512, 2048), (1000, 4096)):
+        K = 256
+        X = synth.activations(M, K, seed=5)
+        W = synth.weights(synth.Q4_0, N, K, seed=6)
+        Y = host(m.gemm(dev(X), dev(W), synth.Q4_0, N, K, path=m.PATH_TC))
+        rows = sample_rows(M)
+        assert_close(Y[rows], oracle.gemm(X, W, synth.Q4_0, M, N, K, rows=rows), "tile M=%d" % M)
+
+
+# ------------------------------------------------------------ GEMV path
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("general", [False, True])
+@pytest.mark.parametrize("M", [1, 2, 8, 9, 16])
+def test_gemv_parity(codec, general, M):
+    for K in kvals(codec, general):
+        N = 264
+        X = synth.activations(M, K, seed=M + 2)
+        W = synth.weights(codec, N, K, seed=K + 1)
+        Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_GEMV))
+        assert_close(Y, oracle.gemm(X, W, codec, M, N, K), "gemv %s M=%d K=%d" % (codec, M, K))
+        Wu = synth.weights(codec, N, K, seed=K + 2, name="Wu")
+        Ys = host(m.swiglu(dev(X), dev(W), dev(Wu), codec, N, K, path=m.PATH_GEMV))
+        assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "gemv swiglu %s M=%d" % (codec, M))
+
+
+def test_auto_dispatch_matches_explicit_paths():
+    K, N = 512, 256
+    W = synth.weights(synth.Q8_0, N, K, seed=9)
+    for M in (16, 17):
+        X = synth.activations(M, K, seed=10)
+        auto = host(m.gemm(dev(X), dev(W), synth.Q8_0, N, K))
+        path = m.PATH_GEMV if M <= 16 else m.PATH_TC
+        explicit = host(m.gemm(dev(X), dev(W), synth.Q8_0, N, K, path=path))
+        assert np.array_equal(auto.view(np.uint16), explicit.view(np.uint16))
+
+
+def test_results_are_repeatable():
+    M, N, K = 300, 512, 1024
+    X = synth.activations(M, K, seed=11)
+    Wg = synth.weights(synth.Q4_0, N, K, seed=12, name="Wg")
+    Wu = synth.weights(synth.Q4_0, N, K, seed=12, name="Wu")
+    a = host(m.swiglu(dev(X), dev(Wg), dev(Wu), synth.Q4_0, N, K)).view(np.uint16)
+    b = host(m.swiglu(dev(X), dev(Wg), dev(Wu), synth.Q4_0, N, K)).view(np.uint16)
+    assert np.array_equal(a, b)
+    x1 = dev(X[:4])
+    c = host(m.gemm(x1, dev(Wg), synth.Q4_0, N, K)).view(np.uint16)
+    d = host(m.gemm(x1, dev(Wg), synth.Q4_0, N, K)).view(np.uint16)
+    assert np.array_equal(c, d)
+
+
+def test_zero_code_weights_give_zero():
+    # Q4_0 all q=8 -> W = 0 -> Y = 0 and SwiGLU = 0 exactly, on both paths.
+    K, N = 256, 128
+    W = synth.constant_weights(synth.Q4_0, N, K, 8, np.float16(0.5))
+    for M in (3, 100):
+        X = synth.activations(M, K, seed=13)
+        Y = host(m.gemm(dev(X), dev(W), synth.Q4_0, N, K))
+        S = host(m.swiglu(dev(X), dev(W), dev(W), synth.Q4_0, N, K))
+        assert np.all(Y == 0) and np.all(S == 0)
+
+
+def test_quant_linear_flattens_leading_dims():
+    import torch
+    K, N = 256, 64
+    W = synth.weights(synth.Q4_0, N, K, seed=14)
+    X = synth.activations(2 * 3 * 5, K, seed=15)
+    layer = m.QuantLinear(dev(W), synth.Q4_0, N, K)
+    y = layer(dev(X).reshape(2, 3, 5, K))
+    assert tuple(y.shape) == (2, 3, 5, N)
+    assert_close(host(y).reshape(-1, N), oracle.gemm(X, W, synth.Q4_0, 30, N, K), "QuantLinear")
+
+
+# ------------------------------------------------------------ status words
+
+def test_wait_timeout_is_reported_and_context_survives():
+    m.selftest_wait_timeout(1_000_000)   # 1 ms limit on a barrier nothing completes
+    assert m.check_device_status() == m.ERR_TIMEOUT
+    assert m.check_device_status() == m.OK   # cleared
+    K, N, M = 256, 64, 4
+    X = synth.activations(M, K, seed=16)
+    W = synth.weights(synth.Q4_0, N, K, seed=17)
+    assert_close(host(m.gemm(dev(X), dev(W), synth.Q4_0, N, K)), oracle.gemm(X, W, synth.Q4_0, M, N, K))
+
+
+def test_finite_tripwire():
+    import torch
+    t = torch.zeros(1000, dtype=torch.float16, device="cuda")
+    assert m.check_finite(t)
+    t[777] = float("inf")
+    assert not m.check_finite(t)
+    t[777] = float("nan")
+    assert not m.check_finite(t)
