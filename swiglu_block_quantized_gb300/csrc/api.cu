@@ -174,6 +174,9 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     if (!encode_2d(&L.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, K * 2, 64, nx,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return M4Q_ERR_CUDA;
+    if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2, (uint32_t)out_rows, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return M4Q_ERR_CUDA;
     L.tm_w0 = L.tm_x;
     L.tm_w1 = L.tm_x;
     if (L.wtma) {

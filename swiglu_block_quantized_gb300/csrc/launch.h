@@ -23,7 +23,7 @@ struct ProjLaunch {
   cudaStream_t stream;
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
-  CUtensorMap tm_x, tm_w0, tm_w1;
+  CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path
   int kw;                 // warps per 16-row tile (split-K inside a CTA)
   int nstages;            // packed stages per row

@@ -34,7 +34,7 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   p.status = L.status;
   p.limit_ns = L.limit_ns;
   const dim3 grid((unsigned)((L.M + NX - 1) / NX), (unsigned)((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows));
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, p);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
   return cudaGetLastError();
 }
 

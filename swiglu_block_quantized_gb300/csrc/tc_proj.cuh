@@ -10,19 +10,24 @@
 //     N = NX activation rows: W is the A operand and lives in TMEM, X is the
 //     B operand and lives in shared memory (128-byte swizzled, K-major).
 //     D (fp32, 128 lanes x NX columns) accumulates in TMEM.
-//   * warp 0, one lane: TMA producer.  X sub-tiles [NX rows x 64 k] and packed
-//     weight stages [128 rows x 8 blocks] go into shared-memory rings.
-//   * warps 4..7 (128 threads, thread r owns weight row r = TMEM lane r):
-//     read the row's packed stage, decode 64 weights per sub-step to fp16
-//     (codec.cuh), and write them with tcgen05.st into a TMEM ring of A
-//     sub-tiles (32 columns each).  After the main loop they run the
-//     epilogue: tcgen05.ld of D, fp16 rounding (or SiLU(g)*u) and stores.
+//   * warp 0, one lane: TMA producer of X sub-tiles [NX rows x 64 k];
+//     warp 2, one lane: TMA producer of packed weight stages [128 rows x 8
+//     blocks].  Two independent shared-memory rings, so weight prefetch runs
+//     ahead of the X ring.
+//   * warps 4..11: two decode warpgroups (thread r of a group owns weight
+//     row r = TMEM lane r).  Group g decodes the sub-steps of parity g: it
+//     reads the row's packed stage, decodes 64 weights to fp16 (codec.cuh)
+//     and writes them with tcgen05.st into a TMEM ring of A sub-tiles (32
+//     columns each); each store completes while the group decodes its next
+//     sub-step.  After the main loop both groups run the epilogue, each on
+//     half of the activation columns: tcgen05.ld of D, fp16 rounding (or
+//     SiLU(g)*u), staging in shared memory and TMA bulk stores of Y.
 //   * warp 1, one lane: issues tcgen05.mma (4 per 64-k sub-step) and commits
 //     stage releases to mbarriers.  Warp 1 also owns the TMEM allocation.
-//   * SwiGLU: A rows 0..63 are gate rows n0..n0+63 and rows 64..127 the up
-//     rows of the same outputs, so one MMA stream computes G and U for 64
-//     outputs; the epilogue pairs lane r with lane r + 64 through shared
-//     memory and writes only SiLU(G) x U.
+//   * SwiGLU: A row 2i is gate row n0+i and row 2i+1 the up row of the same
+//     output, so one MMA stream computes G and U for 64 outputs and every
+//     (G, U) pair sits in adjacent TMEM lanes, i.e. adjacent threads of one
+//     warp: the epilogue pairs them with a shuffle and writes only SiLU(G) x U.
 // Every mbarrier wait is bounded in time; on expiry the CTA records the
 // failure in the status word, drains what it has in flight, frees TMEM and
 // returns (results are then undefined and the host reports a timeout).
@@ -45,17 +50,19 @@ struct TcParams {
 template <int C, bool SWIGLU, int NX, bool WTMA>
 struct TcCfg {
   using S = Stage<C>;
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 384;                            // 12 warps
+  static constexpr int kGroups = 2;                               // decode warpgroups
   static constexpr int kRows = 128;                               // MMA M
   static constexpr int kOutRows = SWIGLU ? 64 : 128;              // outputs n per tile
   static constexpr int kSX = NX == 256 ? 4 : (NX == 128 ? 6 : 8); // X ring depth
-  static constexpr int kSW = WTMA ? 2 : 0;                        // packed-W ring depth
+  static constexpr int kSW = WTMA ? (S::KPB <= 144 ? 4 : 2) : 0;   // packed-W ring depth
   static constexpr int kSA = 8;                                   // TMEM A ring depth
   static constexpr int kXStage = NX * 128;                        // bytes
   static constexpr int kWStage = kRows * S::KPB;                  // bytes
   static constexpr int kTmemCols = 512;
   static constexpr int kACol0 = 256;                              // A ring columns
   static constexpr int kNumBars = 2 * kSX + 2 * kSW + 2 * kSA + 1;
+  static constexpr int kYStage = 32 * kOutRows * 2;              // one staged Y chunk
   static constexpr int kSmemUsed = kSX * kXStage + kSW * kWStage + kNumBars * 8 + 16;
   // Request at least 116 KB so that two CTAs never share an SM (each takes
   // all 512 TMEM columns).
@@ -65,26 +72,8 @@ struct TcCfg {
   static_assert(kACol0 + 32 * kSA <= kTmemCols && NX <= kACol0, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0, "stage alignment");
+  static_assert(4 * kYStage <= kSX * kXStage, "Y staging reuses the X ring");
 };
-
-// Pairwise fp16 stores of a 32-column chunk: this lane holds Y[m_base + j][n]
-// for j = 0..31; lanes 2i and 2i+1 hold n and n + 1.  Each even lane writes
-// (n, n+1) of row m_base + j, each odd lane (n-1, n) of row m_base + j + 1.
-__device__ __forceinline__ void store_pairs(__half* __restrict__ Y, int M, int N, int m_base,
-                                            int n, int lane, const float (&v)[32]) {
-  const int odd = lane & 1;
-#pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    const float send = odd ? v[j] : v[j + 1];
-    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-    const int m = m_base + j + odd;
-    const int nn = n - odd;
-    const __half2 h = odd ? __floats2half2_rn(recv, v[j + 1]) : __floats2half2_rn(v[j], recv);
-    if (m < M && nn < N) *reinterpret_cast<__half2*>(Y + (size_t)m * N + nn) = h;
-  }
-}
-
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
 
 // Barrier-reduction OR over `count` threads of named barrier `id`.
 __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
@@ -120,9 +109,10 @@ __device__ __forceinline__ void load_stage_global(const uint8_t* __restrict__ ro
 }
 
 template <int C, bool SWIGLU, int NX, bool WTMA>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     tc_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
-                   const __grid_constant__ CUtensorMap tm_w1, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
+                   const TcParams p) {
   using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
   using S = Stage<C>;
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SA = Cfg::kSA;
@@ -151,7 +141,7 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
-    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 128); }
+    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 128 * Cfg::kGroups); }
     for (int i = 0; i < SA; ++i) { mbar_init(&a_full[i], 128); mbar_init(&a_empty[i], 1); }
     mbar_init(d_full, 1);
     *abort_flag = 0;
@@ -168,32 +158,13 @@ __global__ void __launch_bounds__(256, 1)
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ X producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
-      if constexpr (WTMA) {
-        tma_prefetch_desc(&tm_w0);
-        if (SWIGLU) tma_prefetch_desc(&tm_w1);
-      }
-      int xi = 0, wi = 0;
+      tma_prefetch_desc(&tm_y);
+      int xi = 0;
       bool ok = true;
       for (int ks = 0; ks < nks; ++ks) {
-        if constexpr (WTMA) {
-          if ((ks % S::SUB) == 0) {
-          const int sp = wi % SW;
-          if (wi >= SW && !mbar_wait(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
-          uint8_t* dst = ws + sp * Cfg::kWStage;
-          const int xc = (ks / S::SUB) * (S::KPB / 2);  // uint16 elements
-          if (SWIGLU) {
-            tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
-            tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
-          } else {
-            tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
-          }
-          ++wi;
-          }
-        }
         const int sx = xi % SX;
         if (xi >= SX && !mbar_wait(&x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
         mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
@@ -204,7 +175,27 @@ __global__ void __launch_bounds__(256, 1)
         // Let the copies already issued land before the CTA exits.
         for (int i = (xi > SX ? xi - SX : 0); i < xi; ++i)
           mbar_wait_drain(&x_full[i % SX], (i / SX) & 1, 100000000ull);
-        if constexpr (WTMA) {
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ W producer
+    if constexpr (WTMA) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_w0);
+        if (SWIGLU) tma_prefetch_desc(&tm_w1);
+        int wi = 0;
+        bool ok = true;
+        for (int pk = 0; pk < npk; ++pk) {
+          const int sp = wi % SW;
+          if (wi >= SW && !mbar_wait(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
+          uint8_t* dst = ws + sp * Cfg::kWStage;
+          const int xc = pk * (S::KPB / 2);  // uint16 elements
+          tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
+          if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
+          ++wi;
+        }
+        if (!ok) {
           for (int i = (wi > SW ? wi - SW : 0); i < wi; ++i)
             mbar_wait_drain(&w_full[i % SW], (i / SW) & 1, 100000000ull);
         }
@@ -232,25 +223,28 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ decode
-    const int r = threadIdx.x - 128;  // weight row of the tile == TMEM lane
+    const int group = (warp - 4) >> 2;          // sub-steps of parity `group`
+    const int r = (threadIdx.x - 128) & 127;    // weight row of the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint8_t* grow = nullptr;
     bool grow_ok = false;
+    // SwiGLU: lane 2i decodes gate row n0+i, lane 2i+1 the up row n0+i.
+    const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
     if (!WTMA) {
-      const int n = SWIGLU ? n0 + (r & 63) : n0 + r;
+      const int n = SWIGLU ? n0 + (r >> 1) : n0 + r;
       grow_ok = n < p.N;
-      const uint8_t* base = (SWIGLU && r >= 64) ? p.w1 : p.w0;
+      const uint8_t* base = (SWIGLU && (r & 1)) ? p.w1 : p.w0;
       grow = base + (grow_ok ? (long long)n * p.row_bytes : 0);
     }
     bool ok = true;
-    int ks = 0;
+    int pending = -1;  // A stage whose tcgen05.st is still in flight
     for (int pk = 0; pk < npk && ok; ++pk) {
       uint32_t w[S::WORDS];
       if constexpr (WTMA) {
         const int sp = pk % SW;
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk / SW) & 1, ctl));
         if (!ok) break;
-        const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + r * S::KPB);
+        const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + srow * S::KPB);
 #pragma unroll
         for (int i = 0; i < S::KPB / 16; ++i) {
           const uint4 v = src[i];
@@ -262,7 +256,9 @@ __global__ void __launch_bounds__(256, 1)
       }
 #pragma unroll
       for (int j = 0; j < S::SUB; ++j) {
+        const int ks = pk * S::SUB + j;   // S::SUB is even, so ks and j share parity
         if (ks >= nks) break;
+        if ((j & 1) != group) continue;
         const int sa = ks % SA;
         if (ks >= SA) {
           ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((ks / SA) - 1) & 1, ctl));
@@ -271,54 +267,73 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         uint32_t out[32];
         decode_sub<C>(w, j, out);
-        tmem_st32_wait(tmem + lane_base + Cfg::kACol0 + sa * 32, out);
-        tc_fence_before();
-        mbar_arrive(&a_full[sa]);
-        ++ks;
+        if (pending >= 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&a_full[pending]);
+        }
+        tmem_st32(tmem + lane_base + Cfg::kACol0 + sa * 32, out);
+        pending = sa;
       }
+    }
+    if (pending >= 0) {
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&a_full[pending]);
     }
 
     // ------------------------------------------------------------ epilogue
     bool dok = false;
     if (!*abort_flag) dok = mbar_wait(d_full, 0, ctl);
-    // One decision for all four epilogue warps (they pair up below).
-    const bool bail = named_bar_any(3, 128, !dok || *abort_flag);
+    // One decision for all eight epilogue warps (they pair up below).
+    const bool bail = named_bar_any(5, 256, !dok || *abort_flag);
     if (bail) {
       mbar_wait_drain(d_full, 0, 200000000ull);  // let issued MMAs finish before TMEM is freed
     } else {
       tc_fence_after();
-      if (!SWIGLU) {
-        const int n = n0 + r;
-        for (int c0 = 0; c0 < NX && m0 + c0 < p.M; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32_wait(tmem + lane_base + c0, v);
-          float f[32];
+      const int c_begin = group * (NX / 2), c_end = c_begin + NX / 2;  // this group's columns
+      uint8_t* ybuf = xs + group * 2 * Cfg::kYStage;  // the X ring is idle now
+      const bool leader = (threadIdx.x & 127) == 0;
+      const uint32_t bar_id = 1 + group;
+      const int odd = lane & 1;
+      int it = 0;
+      for (int c0 = c_begin; c0 < c_end && m0 + c0 < p.M; c0 += 32, ++it) {
+        uint8_t* stg = ybuf + (it & 1) * Cfg::kYStage;  // [32 m][kOutRows n] fp16
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_base + c0, v);
+        if (it >= 2 && leader) bulk_wait_read<1>();     // the store of chunk it-2 has read stg
+        named_bar_sync(bar_id, 128);
+        if (!SWIGLU) {
+          // lane r holds Y[m0+c0+j][n0+r]; lanes 2i, 2i+1 write (n, n+1) of rows j, j+1
 #pragma unroll
-          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-          store_pairs(p.y, p.M, p.N, m0 + c0, n, lane, f);
+          for (int j = 0; j < 32; j += 2) {
+            const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const __half2 h = odd ? __floats2half2_rn(recv, b) : __floats2half2_rn(a, recv);
+            *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
+          }
+        } else {
+          // lane 2i holds G, lane 2i+1 holds U of output n0 + r/2; the even lane
+          // forms the even columns, the odd lane the odd ones
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float a = __uint_as_float(v[2 * jj]), b = __uint_as_float(v[2 * jj + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const float g = odd ? recv : a;
+            const float u = odd ? b : recv;
+            const float y = __fdividef(g, 1.0f + __expf(-g)) * u;
+            *reinterpret_cast<__half*>(stg + (2 * jj + odd) * (Cfg::kOutRows * 2) + (r >> 1) * 2) =
+                __float2half_rn(y);
+          }
         }
-      } else {
-        const int q = warp & 3, pair = q & 1;
-        float* xch = reinterpret_cast<float*>(xs);  // the X ring is idle now
-        const int n = n0 + 32 * pair + lane;
-        int it = 0;
-        for (int c0 = 0; c0 < NX && m0 + c0 < p.M; c0 += 32, ++it) {
-          float* buf = xch + (pair * 2 + (it & 1)) * 1024;
-          uint32_t v[32];
-          tmem_ld32_wait(tmem + lane_base + c0, v);
-          if (q >= 2) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(v[j]);
-          }
-          named_bar_sync(1 + pair, 64);
-          if (q < 2) {
-            float f[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) f[j] = silu_f32(__uint_as_float(v[j])) * buf[j * 32 + lane];
-            store_pairs(p.y, p.M, p.N, m0 + c0, n, lane, f);
-          }
+        fence_proxy_async_smem();
+        named_bar_sync(bar_id, 128);
+        if (leader) {
+          tma_store_2d(&tm_y, stg, n0, m0 + c0);
+          bulk_commit();
         }
       }
+      if (leader) bulk_wait_all();
     }
   }
 
