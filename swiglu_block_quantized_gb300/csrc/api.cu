@@ -171,6 +171,7 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
       nx = 128;
     }
     L.nx = nx;
+    L.sms = dev.sms;
     if (!encode_2d(&L.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, K * 2, 64, nx,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return M4Q_ERR_CUDA;

@@ -147,4 +147,38 @@ __device__ __forceinline__ void decode_sub<kQ2_0>(const uint32_t* w, int j, uint
   }
 }
 
+// Half g (0 or 1) of sub-step j: out[i] = fp16x2 (w[64j + 32g + 2i],
+// w[64j + 32g + 2i + 1]), i < 16.  j and g must be compile-time constants
+// after unrolling.
+template <int C, int G>
+__device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (&out)[16]) {
+  if constexpr (C == kQ4_0) {
+    const int bo = (2 * j + G) * 18;  // block 2j + G
+    const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      uint32_t lo, hi;
+      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, lo, hi);
+      out[p] = lo;
+      out[8 + p] = hi;
+    }
+  } else if constexpr (C == kQ8_0) {
+    const int bo = (2 * j + G) * 34;
+    const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+    for (int p = 0; p < 16; ++p) out[p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+  } else {
+    const int bo = (j >> 1) * 34;
+    const int cb = bo + 2 + 16 * (j & 1) + 8 * G;  // 8 code bytes = 32 weights
+    const uint32_t d2 = dup_scale(u16_at(w, bo));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t p01, p23;
+      q2_byte(spread_byte(w, cb + c), d2, p01, p23);
+      out[2 * c] = p01;
+      out[2 * c + 1] = p23;
+    }
+  }
+}
+
 }  // namespace m4q

@@ -67,11 +67,9 @@ struct WaitCtl {
   uint64_t limit_ns;     // per-wait limit
 };
 
-// Wait for `bar` to complete the phase with the given parity.  Returns false
-// (after recording the failure) if the limit passes or another thread of the
-// CTA has already given up.  Never spins without bound.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: poll until the phase completes, the limit passes or
+// another thread of the CTA has given up.  Never spins without bound.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,6 +82,16 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
       }
     }
   }
+}
+
+// Wait for `bar` to complete the phase with the given parity.  Returns false
+// (after recording the failure) if the limit passes or another thread of the
+// CTA has already given up.  The first probe is inline: the MMA issuer must
+// not leave the tensor pipe idle while it checks a barrier that is already
+// complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctl);
 }
 
 // Wait used while tearing down after an abort: bounded, records nothing.
@@ -234,6 +242,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
       "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
       "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Store 16 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 

@@ -10,7 +10,7 @@ template <int C, bool SWIGLU, int MT, bool WTMA>
 cudaError_t launch_gemv_one(const ProjLaunch& L) {
   using Cfg = GemvCfg<C, SWIGLU>;
   auto kern = gemv_kernel<C, SWIGLU, MT, WTMA>;
-  static std::atomic<unsigned long long> configured{0};
+  std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 2, C, SWIGLU, MT, WTMA>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <utility>
+
 namespace m4q {
 
 // One projection launch, already validated by the ABI layer.
@@ -23,12 +26,24 @@ struct ProjLaunch {
   cudaStream_t stream;
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
+  int sms;                // multiprocessors (persistent grid size)
   CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path
   int kw;                 // warps per 16-row tile (split-K inside a CTA)
   int nstages;            // packed stages per row
   int mt;                 // 1 (M <= 8) or 2 (M <= 16)
 };
+
+// Per-kernel, per-device "dynamic shared memory attribute set" flags.  An
+// anonymous namespace gives them internal linkage, so two copies of the
+// library loaded into one process never share them.
+namespace {
+template <typename Tag>
+std::atomic<unsigned long long>& attr_flag() {
+  static std::atomic<unsigned long long> f{0};
+  return f;
+}
+}  // namespace
 
 cudaError_t launch_tc_q4_0(const ProjLaunch& L);
 cudaError_t launch_tc_q8_0(const ProjLaunch& L);

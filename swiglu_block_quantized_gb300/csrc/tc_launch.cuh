@@ -13,7 +13,7 @@ template <int C, bool SWIGLU, int NX, bool WTMA>
 cudaError_t launch_tc_one(const ProjLaunch& L) {
   using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
   auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA>;
-  static std::atomic<unsigned long long> configured{0};
+  std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 1, C, SWIGLU, NX, WTMA>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -26,14 +26,15 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   TcParams p;
   p.w0 = static_cast<const uint8_t*>(L.w0);
   p.w1 = static_cast<const uint8_t*>(L.w1);
-  p.y = static_cast<__half*>(L.y);
   p.M = L.M;
   p.N = L.N;
   p.K = L.K;
   p.row_bytes = L.row_bytes;
+  p.m_tiles = (L.M + NX - 1) / NX;
+  p.tiles = p.m_tiles * ((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows);
   p.status = L.status;
   p.limit_ns = L.limit_ns;
-  const dim3 grid((unsigned)((L.M + NX - 1) / NX), (unsigned)((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows));
+  const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
   return cudaGetLastError();
 }

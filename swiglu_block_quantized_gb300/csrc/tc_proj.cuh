@@ -5,25 +5,26 @@
 // fed by staged, unpacked weight tiles) and 2.2 (Brick 3: gate and up share
 // one staged X tile and the SiLU(G) x U epilogue stays on chip).
 //
-// Mapping onto sm_103a (one CTA per output tile, 8 warps):
+// Mapping onto sm_103a.  One persistent CTA per SM walks output tiles; a
+// tile is 128 weight rows (64 outputs for SwiGLU) x NX activation rows.
 //   * The MMA computes D^T = W_tile * X_tile^T with M = 128 weight rows and
 //     N = NX activation rows: W is the A operand and lives in TMEM, X is the
 //     B operand and lives in shared memory (128-byte swizzled, K-major).
 //     D (fp32, 128 lanes x NX columns) accumulates in TMEM.
-//   * warp 0, one lane: TMA producer of X sub-tiles [NX rows x 64 k];
+//   * warp 0, one lane: TMA producer of X sub-tiles [NX rows x 64 k].
 //     warp 2, one lane: TMA producer of packed weight stages [128 rows x 8
-//     blocks].  Two independent shared-memory rings, so weight prefetch runs
-//     ahead of the X ring.
-//   * warps 4..11: two decode warpgroups (thread r of a group owns weight
-//     row r = TMEM lane r).  Group g decodes the sub-steps of parity g: it
-//     reads the row's packed stage, decodes 64 weights to fp16 (codec.cuh)
-//     and writes them with tcgen05.st into a TMEM ring of A sub-tiles (32
-//     columns each); each store completes while the group decodes its next
-//     sub-step.  After the main loop both groups run the epilogue, each on
-//     half of the activation columns: tcgen05.ld of D, fp16 rounding (or
-//     SiLU(g)*u), staging in shared memory and TMA bulk stores of Y.
-//   * warp 1, one lane: issues tcgen05.mma (4 per 64-k sub-step) and commits
-//     stage releases to mbarriers.  Warp 1 also owns the TMEM allocation.
+//     blocks].  Independent rings; both run ahead across tile boundaries.
+//   * warp 1, one lane: issues tcgen05.mma (4 per 64-k sub-step), commits
+//     ring releases to mbarriers.  Warp 1 also owns the TMEM allocation.
+//   * warps 4..11, two decode warpgroups.  Thread r of a group owns weight
+//     row r = TMEM lane r; group g decodes weights [32g, 32g+32) of every
+//     64-k sub-step (codec.cuh) and writes them with tcgen05.st into a TMEM
+//     ring of A sub-tiles (32 columns each).  Each store completes while the
+//     thread decodes the next one.
+//   * warps 12..19, two epilogue warpgroups, each on half of the activation
+//     columns: tcgen05.ld of D (D is released to the next tile as soon as it
+//     is read), fp16 rounding or SiLU(g)*u, staging in shared memory and TMA
+//     bulk stores of Y.
 //   * SwiGLU: A row 2i is gate row n0+i and row 2i+1 the up row of the same
 //     output, so one MMA stream computes G and U for 64 outputs and every
 //     (G, U) pair sits in adjacent TMEM lanes, i.e. adjacent threads of one
@@ -40,9 +41,9 @@ namespace m4q {
 struct TcParams {
   const uint8_t* w0;   // weights (gate rows for SwiGLU); read directly when !WTMA
   const uint8_t* w1;   // up weights for SwiGLU, else null
-  __half* y;           // [M, N]
   int M, N, K;
   long long row_bytes; // packed bytes per weight row
+  int m_tiles, tiles;  // activation tiles, total output tiles
   uint32_t* status;    // device status word
   unsigned long long limit_ns;
 };
@@ -50,29 +51,30 @@ struct TcParams {
 template <int C, bool SWIGLU, int NX, bool WTMA>
 struct TcCfg {
   using S = Stage<C>;
-  static constexpr int kThreads = 384;                            // 12 warps
-  static constexpr int kGroups = 2;                               // decode warpgroups
+  static constexpr int kWarps = 20;
+  static constexpr int kThreads = 32 * kWarps;
   static constexpr int kRows = 128;                               // MMA M
   static constexpr int kOutRows = SWIGLU ? 64 : 128;              // outputs n per tile
-  static constexpr int kSX = NX == 256 ? 4 : (NX == 128 ? 6 : 8); // X ring depth
-  static constexpr int kSW = WTMA ? (S::KPB <= 144 ? 4 : 2) : 0;   // packed-W ring depth
+  static constexpr int kSW = WTMA ? (S::KPB <= 144 ? 3 : 2) : 0;  // packed-W ring depth
   static constexpr int kSA = 8;                                   // TMEM A ring depth
   static constexpr int kXStage = NX * 128;                        // bytes
   static constexpr int kWStage = kRows * S::KPB;                  // bytes
+  static constexpr int kYStage = 32 * kOutRows * 2;               // one staged Y chunk
+  static constexpr int kYBytes = 4 * kYStage;                     // 2 groups x 2 buffers
+  static constexpr int kFixed = kSW * kWStage + kYBytes + 1024 + 512;  // + align, barriers
+  static constexpr int kBudget = 227 * 1024;
+  static constexpr int kSX = (kFixed + 8 * kXStage <= kBudget) ? 8
+                             : (kFixed + 6 * kXStage <= kBudget) ? 6
+                             : (kFixed + 5 * kXStage <= kBudget) ? 5
+                             : (kFixed + 4 * kXStage <= kBudget) ? 4 : 3;
   static constexpr int kTmemCols = 512;
   static constexpr int kACol0 = 256;                              // A ring columns
-  static constexpr int kNumBars = 2 * kSX + 2 * kSW + 2 * kSA + 1;
-  static constexpr int kYStage = 32 * kOutRows * 2;              // one staged Y chunk
-  static constexpr int kSmemUsed = kSX * kXStage + kSW * kWStage + kNumBars * 8 + 16;
-  // Request at least 116 KB so that two CTAs never share an SM (each takes
-  // all 512 TMEM columns).
   static constexpr int kSmemBytes =
-      (kSmemUsed + 1024 > 116 * 1024) ? kSmemUsed + 1024 : 116 * 1024;
-  static_assert(NX % 16 == 0 && NX >= 32 && NX <= 256, "MMA N");
+      (kFixed + kSX * kXStage > 116 * 1024) ? kFixed + kSX * kXStage : 116 * 1024;
+  static_assert(NX % 16 == 0 && NX >= 64 && NX <= 256, "MMA N");
   static_assert(kACol0 + 32 * kSA <= kTmemCols && NX <= kACol0, "TMEM budget");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0, "stage alignment");
-  static_assert(4 * kYStage <= kSX * kXStage, "Y staging reuses the X ring");
+  static_assert(kSmemBytes <= kBudget, "shared memory budget");
+  static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0 && kYStage % 1024 == 0, "alignment");
 };
 
 // Barrier-reduction OR over `count` threads of named barrier `id`.
@@ -108,8 +110,163 @@ __device__ __forceinline__ void load_stage_global(const uint8_t* __restrict__ ro
   }
 }
 
+// Shared state of one CTA.
+struct TcSmem {
+  uint8_t* xs;  // X ring
+  uint8_t* ws;  // packed-W ring
+  uint8_t* ys;  // Y staging
+  uint64_t *x_full, *x_empty, *w_full, *w_empty, *a_full, *a_empty;
+  uint64_t *d_full, *d_empty, *drain;
+};
+
+// Decode role of group G (0 or 1): every tile, every sub-step, weights
+// [32G, 32G+32) of this thread's row.
+template <int C, bool SWIGLU, int NX, bool WTMA, int G>
+__device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                            const WaitCtl& ctl, int warp) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  using S = Stage<C>;
+  constexpr int SW = Cfg::kSW, SA = Cfg::kSA;
+  const int r = threadIdx.x & 127;  // weight row of the tile == TMEM lane
+  const uint32_t lane_addr =
+      tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + Cfg::kACol0 + 16 * G;
+  // SwiGLU: lane 2i decodes gate row n0+i, lane 2i+1 the up row n0+i.
+  const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
+  const int nks = (p.K + 63) / 64;
+  const int npk = (p.K + S::KP - 1) / S::KP;
+  bool ok = true;
+  int pending = -1;  // A stage whose tcgen05.st is still in flight
+  int ks_g = 0, pk_g = 0;
+  for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+    const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
+    const uint8_t* grow = nullptr;
+    bool grow_ok = false;
+    if (!WTMA) {
+      const int n = SWIGLU ? n0 + (r >> 1) : n0 + r;
+      grow_ok = n < p.N;
+      const uint8_t* base = (SWIGLU && (r & 1)) ? p.w1 : p.w0;
+      grow = base + (grow_ok ? (long long)n * p.row_bytes : 0);
+    }
+    int ks = 0;
+    for (int pk = 0; pk < npk && ok; ++pk, ++pk_g) {
+      uint32_t w[S::WORDS];
+      if constexpr (WTMA) {
+        const int sp = pk_g % SW;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.w_full[sp], (pk_g / SW) & 1, ctl));
+        if (!ok) break;
+        const uint4* src = reinterpret_cast<const uint4*>(sm.ws + sp * Cfg::kWStage + srow * S::KPB);
+#pragma unroll
+        for (int i = 0; i < S::KPB / 16; ++i) {
+          const uint4 v = src[i];
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        mbar_arrive(&sm.w_empty[sp]);
+      } else {
+        load_stage_global<C>(grow, grow_ok, p.row_bytes, pk, w);
+      }
+#pragma unroll
+      for (int j = 0; j < S::SUB; ++j) {
+        if (ks >= nks) break;
+        const int sa = ks_g % SA;
+        if (ks_g >= SA) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.a_empty[sa], ((ks_g / SA) - 1) & 1, ctl));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        uint32_t out[16];
+        decode_half<C, G>(w, j, out);
+        if (pending >= 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&sm.a_full[pending]);
+        }
+        tmem_st16(lane_addr + sa * 32, out);
+        pending = sa;
+        ++ks;
+        ++ks_g;
+      }
+    }
+  }
+  if (pending >= 0) {
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&sm.a_full[pending]);
+  }
+}
+
+// Epilogue role of group E (0 or 1): columns [E*NX/2, (E+1)*NX/2) of D.
 template <int C, bool SWIGLU, int NX, bool WTMA>
-__global__ void __launch_bounds__(384, 1)
+__device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                              const WaitCtl& ctl, const CUtensorMap* tm_y, int warp,
+                                              int E) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  const int lane = threadIdx.x & 31;
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const bool leader = r == 0;
+  const uint32_t bar_id = 1 + E;
+  const int odd = lane & 1;
+  uint8_t* ybuf = sm.ys + E * 2 * Cfg::kYStage;
+  int it = 0, lt = 0;
+  for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++lt) {
+    const int m0 = (tile % p.m_tiles) * NX;
+    const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
+    bool dok = false;
+    if (!*ctl.abort) dok = mbar_wait(sm.d_full, lt & 1, ctl);
+    // One decision for both epilogue groups (they synchronise below).
+    if (named_bar_any(5, 256, !dok || *ctl.abort)) break;
+    tc_fence_after();
+    const int c_begin = E * (NX / 2), c_end = c_begin + NX / 2;
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32_wait(tmem + lane_base + c0, v);
+      if (c0 + 32 == c_end) {
+        // This warp has read its last D columns of the tile: D may be reused.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.d_empty);
+      }
+      if (m0 + c0 >= p.M) continue;  // uniform: columns past M are padding
+      uint8_t* stg = ybuf + (it & 1) * Cfg::kYStage;  // [32 m][kOutRows n] fp16
+      if (it >= 2 && leader) bulk_wait_read<1>();     // the store of chunk it-2 has read stg
+      named_bar_sync(bar_id, 128);
+      if (!SWIGLU) {
+        // lane r holds Y[m0+c0+j][n0+r]; lanes 2i, 2i+1 write (n, n+1) of rows j, j+1
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+          const __half2 h = odd ? __floats2half2_rn(recv, b) : __floats2half2_rn(a, recv);
+          *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
+        }
+      } else {
+        // lane 2i holds G, lane 2i+1 holds U of output n0 + r/2; the even lane
+        // forms the even columns, the odd lane the odd ones
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float a = __uint_as_float(v[2 * jj]), b = __uint_as_float(v[2 * jj + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+          const float g = odd ? recv : a;
+          const float u = odd ? b : recv;
+          const float y = __fdividef(g, 1.0f + __expf(-g)) * u;
+          *reinterpret_cast<__half*>(stg + (2 * jj + odd) * (Cfg::kOutRows * 2) + (r >> 1) * 2) =
+              __float2half_rn(y);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, 128);
+      if (leader) {
+        tma_store_2d(tm_y, stg, n0, m0 + c0);
+        bulk_commit();
+      }
+      ++it;
+    }
+  }
+  if (leader) bulk_wait_all();
+}
+
+template <int C, bool SWIGLU, int NX, bool WTMA>
+__global__ void __launch_bounds__(640, 1)
     tc_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                    const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
                    const TcParams p) {
@@ -118,32 +275,36 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SA = Cfg::kSA;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* xs = smem;
-  uint8_t* ws = xs + SX * Cfg::kXStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ws + SW * Cfg::kWStage);
-  uint64_t* x_full = bars;
-  uint64_t* x_empty = x_full + SX;
-  uint64_t* w_full = x_empty + SX;
-  uint64_t* w_empty = w_full + SW;
-  uint64_t* a_full = w_empty + SW;
-  uint64_t* a_empty = a_full + SA;
-  uint64_t* d_full = a_empty + SA;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(d_full + 1);
+  TcSmem sm;
+  sm.xs = base;
+  sm.ys = sm.xs + SX * Cfg::kXStage;
+  sm.ws = sm.ys + Cfg::kYBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.ws + SW * Cfg::kWStage);
+  sm.x_full = bars;
+  sm.x_empty = sm.x_full + SX;
+  sm.w_full = sm.x_empty + SX;
+  sm.w_empty = sm.w_full + SW;
+  sm.a_full = sm.w_empty + SW;
+  sm.a_empty = sm.a_full + SA;
+  sm.d_full = sm.a_empty + SA;
+  sm.d_empty = sm.d_full + 1;
+  sm.drain = sm.d_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * NX;
-  const int n0 = blockIdx.y * Cfg::kOutRows;
-  const int nks = (p.K + 63) / 64;                 // 64-weight sub-steps
-  const int npk = (p.K + S::KP - 1) / S::KP;       // packed stages
+  const int nks = (p.K + 63) / 64;            // 64-weight sub-steps per tile
+  const int npk = (p.K + S::KP - 1) / S::KP;  // packed stages per tile
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
-    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 128 * Cfg::kGroups); }
-    for (int i = 0; i < SA; ++i) { mbar_init(&a_full[i], 128); mbar_init(&a_empty[i], 1); }
-    mbar_init(d_full, 1);
+    for (int i = 0; i < SX; ++i) { mbar_init(&sm.x_full[i], 1); mbar_init(&sm.x_empty[i], 1); }
+    for (int i = 0; i < SW; ++i) { mbar_init(&sm.w_full[i], 1); mbar_init(&sm.w_empty[i], 256); }
+    for (int i = 0; i < SA; ++i) { mbar_init(&sm.a_full[i], 256); mbar_init(&sm.a_empty[i], 1); }
+    mbar_init(sm.d_full, 1);
+    mbar_init(sm.d_empty, 8);  // one arrival per epilogue warp
+    mbar_init(sm.drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -161,20 +322,22 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ X producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_y);
       int xi = 0;
       bool ok = true;
-      for (int ks = 0; ks < nks; ++ks) {
-        const int sx = xi % SX;
-        if (xi >= SX && !mbar_wait(&x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
-        mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
-        tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx], ks * 64, m0);
-        ++xi;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % p.m_tiles) * NX;
+        for (int ks = 0; ks < nks; ++ks) {
+          const int sx = xi % SX;
+          if (xi >= SX && !mbar_wait(&sm.x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.x_full[sx], Cfg::kXStage);
+          tma_load_2d(sm.xs + sx * Cfg::kXStage, &tm_x, &sm.x_full[sx], ks * 64, m0);
+          ++xi;
+        }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
         for (int i = (xi > SX ? xi - SX : 0); i < xi; ++i)
-          mbar_wait_drain(&x_full[i % SX], (i / SX) & 1, 100000000ull);
+          mbar_wait_drain(&sm.x_full[i % SX], (i / SX) & 1, 100000000ull);
       }
     }
   } else if (warp == 2) {
@@ -185,19 +348,22 @@ __global__ void __launch_bounds__(384, 1)
         if (SWIGLU) tma_prefetch_desc(&tm_w1);
         int wi = 0;
         bool ok = true;
-        for (int pk = 0; pk < npk; ++pk) {
-          const int sp = wi % SW;
-          if (wi >= SW && !mbar_wait(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
-          uint8_t* dst = ws + sp * Cfg::kWStage;
-          const int xc = pk * (S::KPB / 2);  // uint16 elements
-          tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
-          if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
-          ++wi;
+        for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+          const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
+          for (int pk = 0; pk < npk; ++pk) {
+            const int sp = wi % SW;
+            if (wi >= SW && !mbar_wait(&sm.w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
+            mbar_arrive_expect_tx(&sm.w_full[sp], Cfg::kWStage);
+            uint8_t* dst = sm.ws + sp * Cfg::kWStage;
+            const int xc = pk * (S::KPB / 2);  // uint16 elements
+            tma_load_2d(dst, &tm_w0, &sm.w_full[sp], xc, n0);
+            if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &sm.w_full[sp], xc, n0);
+            ++wi;
+          }
         }
         if (!ok) {
           for (int i = (wi > SW ? wi - SW : 0); i < wi; ++i)
-            mbar_wait_drain(&w_full[i % SW], (i / SW) & 1, 100000000ull);
+            mbar_wait_drain(&sm.w_full[i % SW], (i / SW) & 1, 100000000ull);
         }
       }
     }
@@ -205,136 +371,38 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, NX);
-      for (int ks = 0; ks < nks; ++ks) {
-        const int sx = ks % SX, sa = ks % SA;
-        if (!mbar_wait(&a_full[sa], (ks / SA) & 1, ctl)) break;
-        if (!mbar_wait(&x_full[sx], (ks / SX) & 1, ctl)) break;
+      int ks_g = 0, lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++lt) {
+        // D must have been read out by the epilogue of the previous tile.
+        if (lt > 0 && !mbar_wait(sm.d_empty, (lt - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(xs + sx * Cfg::kXStage));
-        const uint32_t acol = tmem + Cfg::kACol0 + sa * 32;
+        for (int ks = 0; ks < nks; ++ks, ++ks_g) {
+          const int sx = ks_g % SX, sa = ks_g % SA;
+          if (!mbar_wait(&sm.a_full[sa], (ks_g / SA) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&sm.x_full[sx], (ks_g / SX) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(sm.xs + sx * Cfg::kXStage));
+          const uint32_t acol = tmem + Cfg::kACol0 + sa * 32;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks | kk) != 0);
-        tc_commit(&x_empty[sx]);
-        tc_commit(&a_empty[sa]);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+          tc_commit(&sm.x_empty[sx]);
+          tc_commit(&sm.a_empty[sa]);
+        }
+        if (ok) tc_commit(sm.d_full);
       }
-      tc_commit(d_full);  // always: fires once every MMA issued above is done
+      // Every MMA issued above completes before the CTA frees TMEM.
+      tc_commit(sm.drain);
+      mbar_wait_drain(sm.drain, 0, 200000000ull);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ decode
-    const int group = (warp - 4) >> 2;          // sub-steps of parity `group`
-    const int r = (threadIdx.x - 128) & 127;    // weight row of the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint8_t* grow = nullptr;
-    bool grow_ok = false;
-    // SwiGLU: lane 2i decodes gate row n0+i, lane 2i+1 the up row n0+i.
-    const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
-    if (!WTMA) {
-      const int n = SWIGLU ? n0 + (r >> 1) : n0 + r;
-      grow_ok = n < p.N;
-      const uint8_t* base = (SWIGLU && (r & 1)) ? p.w1 : p.w0;
-      grow = base + (grow_ok ? (long long)n * p.row_bytes : 0);
-    }
-    bool ok = true;
-    int pending = -1;  // A stage whose tcgen05.st is still in flight
-    for (int pk = 0; pk < npk && ok; ++pk) {
-      uint32_t w[S::WORDS];
-      if constexpr (WTMA) {
-        const int sp = pk % SW;
-        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk / SW) & 1, ctl));
-        if (!ok) break;
-        const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + srow * S::KPB);
-#pragma unroll
-        for (int i = 0; i < S::KPB / 16; ++i) {
-          const uint4 v = src[i];
-          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-        }
-        mbar_arrive(&w_empty[sp]);
-      } else {
-        load_stage_global<C>(grow, grow_ok, p.row_bytes, pk, w);
-      }
-#pragma unroll
-      for (int j = 0; j < S::SUB; ++j) {
-        const int ks = pk * S::SUB + j;   // S::SUB is even, so ks and j share parity
-        if (ks >= nks) break;
-        if ((j & 1) != group) continue;
-        const int sa = ks % SA;
-        if (ks >= SA) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((ks / SA) - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        tc_fence_after();
-        uint32_t out[32];
-        decode_sub<C>(w, j, out);
-        if (pending >= 0) {
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&a_full[pending]);
-        }
-        tmem_st32(tmem + lane_base + Cfg::kACol0 + sa * 32, out);
-        pending = sa;
-      }
-    }
-    if (pending >= 0) {
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&a_full[pending]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    bool dok = false;
-    if (!*abort_flag) dok = mbar_wait(d_full, 0, ctl);
-    // One decision for all eight epilogue warps (they pair up below).
-    const bool bail = named_bar_any(5, 256, !dok || *abort_flag);
-    if (bail) {
-      mbar_wait_drain(d_full, 0, 200000000ull);  // let issued MMAs finish before TMEM is freed
-    } else {
-      tc_fence_after();
-      const int c_begin = group * (NX / 2), c_end = c_begin + NX / 2;  // this group's columns
-      uint8_t* ybuf = xs + group * 2 * Cfg::kYStage;  // the X ring is idle now
-      const bool leader = (threadIdx.x & 127) == 0;
-      const uint32_t bar_id = 1 + group;
-      const int odd = lane & 1;
-      int it = 0;
-      for (int c0 = c_begin; c0 < c_end && m0 + c0 < p.M; c0 += 32, ++it) {
-        uint8_t* stg = ybuf + (it & 1) * Cfg::kYStage;  // [32 m][kOutRows n] fp16
-        uint32_t v[32];
-        tmem_ld32_wait(tmem + lane_base + c0, v);
-        if (it >= 2 && leader) bulk_wait_read<1>();     // the store of chunk it-2 has read stg
-        named_bar_sync(bar_id, 128);
-        if (!SWIGLU) {
-          // lane r holds Y[m0+c0+j][n0+r]; lanes 2i, 2i+1 write (n, n+1) of rows j, j+1
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
-            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-            const __half2 h = odd ? __floats2half2_rn(recv, b) : __floats2half2_rn(a, recv);
-            *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
-          }
-        } else {
-          // lane 2i holds G, lane 2i+1 holds U of output n0 + r/2; the even lane
-          // forms the even columns, the odd lane the odd ones
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float a = __uint_as_float(v[2 * jj]), b = __uint_as_float(v[2 * jj + 1]);
-            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-            const float g = odd ? recv : a;
-            const float u = odd ? b : recv;
-            const float y = __fdividef(g, 1.0f + __expf(-g)) * u;
-            *reinterpret_cast<__half*>(stg + (2 * jj + odd) * (Cfg::kOutRows * 2) + (r >> 1) * 2) =
-                __float2half_rn(y);
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(bar_id, 128);
-        if (leader) {
-          tma_store_2d(&tm_y, stg, n0, m0 + c0);
-          bulk_commit();
-        }
-      }
-      if (leader) bulk_wait_all();
-    }
+  } else if (warp >= 4 && warp < 8) {
+    decode_role<C, SWIGLU, NX, WTMA, 0>(sm, p, tmem, ctl, warp);
+  } else if (warp >= 8 && warp < 12) {
+    decode_role<C, SWIGLU, NX, WTMA, 1>(sm, p, tmem, ctl, warp);
+  } else if (warp >= 12) {
+    epilogue_role<C, SWIGLU, NX, WTMA>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
   }
 
   tc_fence_before();
