@@ -17,7 +17,6 @@ using m4q::ProjLaunch;
 
 constexpr int kBlock[3] = {32, 32, 128};
 constexpr int kBlockBytes[3] = {18, 34, 34};
-constexpr int kStageK[3] = {256, 256, 1024};       // weights per packed stage (8 blocks)
 constexpr int kStageBytes[3] = {144, 272, 272};    // bytes per packed stage
 
 // Default limit of one device pipeline wait (ns); M4Q_WAIT_LIMIT_NS overrides.
@@ -141,22 +140,8 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
   const bool gemv = (path == M4Q_PATH_GEMV) || (path == M4Q_PATH_AUTO && M <= 16);
   cudaError_t e;
   if (gemv) {
-    L.nstages = (int)((K + kStageK[codec] - 1) / kStageK[codec]);
-    int kw = 8;
-    while (kw > 1 && kw > L.nstages) kw >>= 1;
-    L.kw = kw;
     L.mt = M <= 8 ? 1 : 2;
-    if (L.wtma) {
-      const uint32_t box_rows = 16;
-      if (!encode_2d(&L.tm_w0, CU_TENSOR_MAP_DATA_TYPE_UINT16, W0, L.row_bytes / 2, N,
-                     L.row_bytes, kStageBytes[codec] / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return M4Q_ERR_CUDA;
-      L.tm_w1 = L.tm_w0;
-      if (swiglu && !encode_2d(&L.tm_w1, CU_TENSOR_MAP_DATA_TYPE_UINT16, W1, L.row_bytes / 2, N,
-                               L.row_bytes, kStageBytes[codec] / 2, box_rows,
-                               CU_TENSOR_MAP_SWIZZLE_NONE))
-        return M4Q_ERR_CUDA;
-    }
+    L.sms = dev.sms;
     e = m4q::launch_gemv(codec, L);
   } else {
     // Widest activation tile that still gives every SM a tile.

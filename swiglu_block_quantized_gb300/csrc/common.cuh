@@ -84,6 +84,26 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
 }
 
+// Slow path of mbar_wait_idle: like mbar_wait_slow, but the thread sleeps
+// between polls (32 ns doubling up to max_ns), so a warp that waits a long
+// time leaves the issue slots of its SM sub-partition to the working warps.
+static __device__ __noinline__ bool mbar_wait_idle_slow(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                                        uint32_t max_ns) {
+  const uint64_t t0 = global_timer_ns();
+  uint32_t ns = 32;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort) return false;
+    if (global_timer_ns() - t0 > ctl.limit_ns) {
+      *ctl.abort = 1;
+      atomicOr(ctl.status, kErrWaitTimeout);
+      return false;
+    }
+    __nanosleep(ns);
+    if (ns < max_ns) ns *= 2;
+  }
+}
+
 // Wait for `bar` to complete the phase with the given parity.  Returns false
 // (after recording the failure) if the limit passes or another thread of the
 // CTA has already given up.  The first probe is inline: the MMA issuer must
@@ -92,6 +112,15 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, ctl);
+}
+
+// Wait for a phase whose late detection costs little (a producer ahead of
+// its consumers by a deep ring, a warp that waits for a whole tile): same
+// contract as mbar_wait, with sleeps of at most max_ns between polls.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                               uint32_t max_ns = 256) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_idle_slow(bar, parity, ctl, max_ns);
 }
 
 // Wait used while tearing down after an abort: bounded, records nothing.

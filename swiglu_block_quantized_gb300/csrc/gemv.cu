@@ -1,4 +1,4 @@
-// gemv.cu -- host launcher for the decode-sized (M <= 16) streaming kernels.
+// gemv.cu -- host launcher for the decode-sized (M <= 16) streaming kernel.
 #include <atomic>
 
 #include "gemv.cuh"
@@ -6,11 +6,12 @@
 
 namespace m4q {
 
-template <int C, bool SWIGLU, int MT, bool WTMA>
-cudaError_t launch_gemv_one(const ProjLaunch& L) {
-  using Cfg = GemvCfg<C, SWIGLU>;
-  auto kern = gemv_kernel<C, SWIGLU, MT, WTMA>;
-  std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 2, C, SWIGLU, MT, WTMA>>();
+template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
+cudaError_t launch_gemv_one(const ProjLaunch& L, const GemvParams& p) {
+  using Cfg = GemvCfg<C>;
+  auto kern = gemv_kernel<C, SWIGLU, MT, WTMA, XH>;
+  std::atomic<unsigned long long>& configured =
+      attr_flag<std::integer_sequence<int, 2, C, SWIGLU, MT, WTMA, XH>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -20,6 +21,14 @@ cudaError_t launch_gemv_one(const ProjLaunch& L) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
+  const unsigned grid = (unsigned)(p.units < L.sms ? p.units : L.sms);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int C, bool SWIGLU, bool WTMA>
+cudaError_t launch_gemv_mt(const ProjLaunch& L) {
+  using Cfg = GemvCfg<C>;
   GemvParams p;
   p.x = static_cast<const __half*>(L.x);
   p.w0 = static_cast<const uint8_t*>(L.w0);
@@ -29,19 +38,23 @@ cudaError_t launch_gemv_one(const ProjLaunch& L) {
   p.N = L.N;
   p.K = L.K;
   p.row_bytes = L.row_bytes;
-  p.kw = L.kw;
-  p.nstages = L.nstages;
+  // Stage width: whole packed stages, at most kSBMax bytes per row.
+  const long long kpb = Stage<C>::KPB;
+  const long long padded = (L.row_bytes + kpb - 1) / kpb * kpb;
+  p.sb = (int)(padded < Cfg::kSBMax ? padded : Cfg::kSBMax);
+  p.nst = (int)((L.row_bytes + p.sb - 1) / p.sb);
+  const int per_unit = SWIGLU ? 8 : 16;
+  p.units = (L.N + per_unit - 1) / per_unit;
   p.status = L.status;
   p.limit_ns = L.limit_ns;
-  const int rows_per_cta = 16 * (8 / L.kw);
-  const unsigned grid = (unsigned)((L.N + rows_per_cta - 1) / rows_per_cta);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_w0, L.tm_w1, p);
-  return cudaGetLastError();
-}
-
-template <int C, bool SWIGLU, bool WTMA>
-cudaError_t launch_gemv_mt(const ProjLaunch& L) {
-  return L.mt == 1 ? launch_gemv_one<C, SWIGLU, 1, WTMA>(L) : launch_gemv_one<C, SWIGLU, 2, WTMA>(L);
+  // X fragments stay in registers when a full-width row is one stage and
+  // they fit (M <= 8, 4 registers per block; rows are whole stages under
+  // TMA-sized rows).
+  if (L.mt == 2) return launch_gemv_one<C, SWIGLU, 2, WTMA, false>(L, p);
+  if constexpr (C != kQ2_0 && WTMA) {
+    if (p.nst == 1 && p.sb == Cfg::kSBMax) return launch_gemv_one<C, SWIGLU, 1, WTMA, true>(L, p);
+  }
+  return launch_gemv_one<C, SWIGLU, 1, WTMA, false>(L, p);
 }
 
 template <int C>

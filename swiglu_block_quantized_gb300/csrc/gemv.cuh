@@ -1,25 +1,41 @@
 // gemv.cuh -- weight-streaming kernel for decode-sized M (1 <= M <= 16):
 // Y = X W^T and Y = SiLU(X Wg^T) x (X Wu^T).
 //
-// Pages: "Releases" v0.3.0 (M4QuantizedLinear dispatches M = 1 to a GEMV) and
+// Pages: "Releases" v0.3.0 (M4QuantizedLinear sends M = 1 to a GEMV) and
 // "v0.1 vs v0.2 comparison" 2.3 (register-level reductions).  At this M the
-// packed weights are the whole memory traffic, so the kernel streams every
-// weight byte exactly once with TMA and keeps all arithmetic in registers.
+// packed weights are the whole memory traffic, so the kernel reads every
+// weight byte once, in long contiguous row segments, and keeps all
+// arithmetic on chip.
 //
-// Layout of the work: a CTA has 8 warps; warp w handles a 16-row weight tile
-// (row tile w / KW of the CTA) over a contiguous range of packed stages
-// (part w % KW of K).  Each warp owns a 2-deep shared-memory ring filled by
-// TMA (one box = 16 rows x 8 blocks, per matrix).  The partial sums of the KW
-// warps of a row tile are added in a fixed order through shared memory.
+// Work unit: one 16-row weight tile over the whole of K -- 16 weight rows of
+// a GEMM (16 outputs), or 8 gate rows over 8 up rows of SwiGLU (8 outputs, so
+// that G and U of one output end up in the same thread).  Units are dealt
+// round robin to one persistent CTA per SM.
 //
-// Arithmetic: tensor-core mma.sync m16n8k16 with the weight tile as the A
-// operand (16 rows x 16 k) and X^T as B (16 k x 8 activation rows; two n8
-// tiles when M > 8), fp32 accumulation.  Weights are decoded exactly as on
-// the tcgen05 path (codec.cuh): each is RNE((q - z) * d) in fp16.
-//
-// Inside a block the assignment of k positions to MMA slots is permuted
-// (identically for W and X) so that every thread reads contiguous code
-// bytes and contiguous X values; the sum over a block is unchanged.
+// CTA roles (576 threads):
+//   warp 0      producer.  A unit arrives as stages of 16 rows x SB bytes
+//               (SB up to about 2.3 KB of whole blocks: one stage holds a
+//               whole row when K <= 4096), one bulk copy per row segment,
+//               issued by 16 lanes at once, into a ring of shared-memory
+//               stages.  Copies of 2 KB and more stream at close to the HBM
+//               rate; much shorter ones are limited by the copy issue rate.
+//               Rows sit at a pitch of SB + 16 bytes so the 16 rows of a stage
+//               fall into different shared-memory banks.
+//   warps 2..17 consumers.  Warp c takes blocks c, c + 16, ... of each stage
+//               (fully unrolled, alternating between two accumulator sets so
+//               that the MMA chains overlap; when a row fits in one stage
+//               each warp sees the same k range in every unit, so its X
+//               fragments are loaded once), decodes them exactly
+//               (codec.cuh) and multiplies them with
+//               mma.sync m16n8k16: the weight tile is A (16 rows x 16 k), X^T
+//               is B (16 k x 8 activation rows, two n8 tiles when M > 8),
+//               fp32 accumulation.  Inside a block the k order of the MMA
+//               slots is permuted identically for W and X so that each thread
+//               reads contiguous code bytes and contiguous X values.
+//   warp 1      reducer.  Adds the 16 consumers' partial tiles of a unit in a
+//               fixed order and writes Y (SwiGLU: SiLU(G) x U in registers).
+// Every wait is bounded in time; on expiry the CTA records the failure in the
+// status word, lets its copies in flight land and returns.
 #pragma once
 
 #include "codec.cuh"
@@ -33,22 +49,29 @@ struct GemvParams {
   __half* y;           // [M, N]
   int M, N, K;
   long long row_bytes;
-  int kw;              // warps per row tile: 1, 2, 4 or 8
-  int nstages;         // packed stages per row
+  int sb;              // stage bytes per row: whole packed stages, <= kSBMax
+  int nst;             // stages per unit (ceil(row_bytes / sb))
+  int units;           // 16-row weight tiles
   uint32_t* status;
   unsigned long long limit_ns;
 };
 
-template <int C, bool SWIGLU>
+template <int C>
 struct GemvCfg {
   using S = Stage<C>;
-  static constexpr int kThreads = 256;
-  static constexpr int kMats = SWIGLU ? 2 : 1;
-  static constexpr int kRing = 2;
-  static constexpr int kStageBytes = kMats * 16 * S::KPB;
-  static constexpr int kRedFloats = 8 * 32 * 2 * 2 * 4;   // warps x lanes x mats x MT x 4
-  static constexpr int kSmemBytes =
-      8 * kRing * kStageBytes + kRedFloats * 4 + 8 * kRing * 8 + 256;
+  static constexpr int kConsumers = 16;
+  static constexpr int kThreads = 32 * (kConsumers + 2);
+  static constexpr int kSBMax = (2400 / S::KPB) * S::KPB;   // 2304 (Q4_0) or 2176 B
+  static constexpr int kBlocks = kSBMax / S::BB;             // blocks per full stage
+  static constexpr int kBPW = kBlocks / kConsumers;          // blocks per consumer warp
+  static constexpr int kPitch = kSBMax + 16;                 // row pitch in a stage
+  static constexpr int kStage = 16 * kPitch;
+  static constexpr int kRing = 5;
+  static constexpr int kRedFloats = 2 * kConsumers * 32 * 8; // [buf][warp][lane][8]
+  static constexpr int kBars = 2 * kRing + 4;
+  static constexpr int kSmemBytes = kRing * kStage + kRedFloats * 4 + kBars * 8 + 16 + 128;
+  static_assert(kPitch % 16 == 0 && kStage % 128 == 0, "bulk-copy alignment");
+  static_assert(kBPW * kConsumers == kBlocks, "blocks split evenly over the consumers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -59,6 +82,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Contiguous global -> shared copy of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completing on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t lds_u16(const uint8_t* p) {
@@ -82,18 +115,15 @@ __device__ __forceinline__ void ldx(uint32_t* dst, const __half* xrow, bool ok) 
   }
 }
 
-// Accumulate block b of a stage.  `st` points at the stage in shared memory
-// ([mat][16 rows][KPB]); g = lane / 4, t = lane % 4; kb = k of the block's
-// first weight.
-template <int C, bool SWIGLU, int MT>
-__device__ __forceinline__ void gemv_block(const uint8_t* st, int b, int g, int t, int kb,
-                                           const GemvParams& p, float (&acc)[2][2][4]) {
-  using S = Stage<C>;
-  constexpr int NM = SWIGLU ? 2 : 1;
-  constexpr int BB = S::BB;
+// X fragments of one block for activation rows g and g + 8 (zero past M).
+template <int C>
+struct XFrag {
+  static constexpr int kRegs = C == kQ4_0 ? 4 : C == kQ8_0 ? 4 : 16;
+};
 
-  // X fragments (shared by both matrices).
-  uint32_t xf[MT][16];
+template <int C, int MT>
+__device__ __forceinline__ void load_xfrag(const GemvParams& p, int g, int t, int kb,
+                                           uint32_t (&xf)[MT][XFrag<C>::kRegs]) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const int m = g + 8 * mt;
@@ -108,210 +138,274 @@ __device__ __forceinline__ void gemv_block(const uint8_t* st, int b, int g, int 
       ldx<64>(&xf[mt][0], xr + 32 * t, ok);
     }
   }
+}
 
-#pragma unroll
-  for (int mat = 0; mat < NM; ++mat) {
-    const uint8_t* r0 = st + (mat * 16 + g) * S::KPB + b * BB;  // row g
-    const uint8_t* r1 = r0 + 8 * S::KPB;                       // row g + 8
-    const uint32_t d0 = dup_scale(lds_u16(r0)), d1 = dup_scale(lds_u16(r1));
-    float(&a)[2][4] = acc[mat];
+// Accumulate block b of a stage into the 16 x 8*MT tile.  `st` is the stage
+// ([16 rows][kPitch] bytes); g = lane / 4, t = lane % 4; xf holds the X
+// fragments of the block.
+template <int C, int MT>
+__device__ __forceinline__ void gemv_block(const uint8_t* st, int b, int g, int t,
+                                           const uint32_t (&xf)[MT][XFrag<C>::kRegs],
+                                           float (&acc)[MT][4]) {
+  using S = Stage<C>;
+  constexpr int BB = S::BB;
+  constexpr int PITCH = GemvCfg<C>::kPitch;
 
-    if constexpr (C == kQ4_0) {
-      const uint8_t* c0 = r0 + 2 + 4 * t;
-      const uint8_t* c1 = r1 + 2 + 4 * t;
-      uint32_t lo00, hi00, lo01, hi01, lo10, hi10, lo11, hi11;
-      q4_pair(spread16(lds_u16(c0)), d0, lo00, hi00);
-      q4_pair(spread16(lds_u16(c0 + 2)), d0, lo01, hi01);
-      q4_pair(spread16(lds_u16(c1)), d1, lo10, hi10);
-      q4_pair(spread16(lds_u16(c1 + 2)), d1, lo11, hi11);
+  const uint8_t* r0 = st + g * PITCH + b * BB;  // tile row g
+  const uint8_t* r1 = r0 + 8 * PITCH;           // tile row g + 8
+  const uint32_t d0 = dup_scale(lds_u16(r0)), d1 = dup_scale(lds_u16(r1));
+
+  if constexpr (C == kQ4_0) {
+    const uint8_t* c0 = r0 + 2 + 4 * t;
+    const uint8_t* c1 = r1 + 2 + 4 * t;
+    uint32_t lo00, hi00, lo01, hi01, lo10, hi10, lo11, hi11;
+    q4_pair(spread16(lds_u16(c0)), d0, lo00, hi00);
+    q4_pair(spread16(lds_u16(c0 + 2)), d0, lo01, hi01);
+    q4_pair(spread16(lds_u16(c1)), d1, lo10, hi10);
+    q4_pair(spread16(lds_u16(c1 + 2)), d1, lo11, hi11);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        mma_16816(a[mt], lo00, lo10, lo01, lo11, xf[mt][0], xf[mt][1]);
-        mma_16816(a[mt], hi00, hi10, hi01, hi11, xf[mt][2], xf[mt][3]);
-      }
-    } else if constexpr (C == kQ8_0) {
-      const uint8_t* c0 = r0 + 2 + 8 * t;
-      const uint8_t* c1 = r1 + 2 + 8 * t;
-      uint32_t w[2][4];
+    for (int mt = 0; mt < MT; ++mt) {
+      mma_16816(acc[mt], lo00, lo10, lo01, lo11, xf[mt][0], xf[mt][1]);
+      mma_16816(acc[mt], hi00, hi10, hi01, hi11, xf[mt][2], xf[mt][3]);
+    }
+  } else if constexpr (C == kQ8_0) {
+    const uint8_t* c0 = r0 + 2 + 8 * t;
+    const uint8_t* c1 = r1 + 2 + 8 * t;
+    uint32_t w[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[0][i] = q8_pair(spread16(lds_u16(c0 + 2 * i)), d0);
-        w[1][i] = q8_pair(spread16(lds_u16(c1 + 2 * i)), d1);
-      }
+    for (int i = 0; i < 4; ++i) {
+      w[0][i] = q8_pair(spread16(lds_u16(c0 + 2 * i)), d0);
+      w[1][i] = q8_pair(spread16(lds_u16(c1 + 2 * i)), d1);
+    }
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        mma_16816(a[mt], w[0][0], w[1][0], w[0][1], w[1][1], xf[mt][0], xf[mt][1]);
-        mma_16816(a[mt], w[0][2], w[1][2], w[0][3], w[1][3], xf[mt][2], xf[mt][3]);
-      }
-    } else {
-      const uint8_t* c0 = r0 + 2 + 8 * t;
-      const uint8_t* c1 = r1 + 2 + 8 * t;
-      uint32_t v0[4], v1[4];
+    for (int mt = 0; mt < MT; ++mt) {
+      mma_16816(acc[mt], w[0][0], w[1][0], w[0][1], w[1][1], xf[mt][0], xf[mt][1]);
+      mma_16816(acc[mt], w[0][2], w[1][2], w[0][3], w[1][3], xf[mt][2], xf[mt][3]);
+    }
+  } else {
+    const uint8_t* c0 = r0 + 2 + 8 * t;
+    const uint8_t* c1 = r1 + 2 + 8 * t;
+    uint32_t v0[4], v1[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { v0[i] = lds_u16(c0 + 2 * i); v1[i] = lds_u16(c1 + 2 * i); }
+    for (int i = 0; i < 4; ++i) { v0[i] = lds_u16(c0 + 2 * i); v1[i] = lds_u16(c1 + 2 * i); }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t sel = (c & 1) ? 0x4141u : 0x4040u;  // byte c of the pair, replicated
-        uint32_t a0, a1, a2, a3;
-        q2_byte(__byte_perm(v0[c >> 1], 0u, sel), d0, a0, a2);
-        q2_byte(__byte_perm(v1[c >> 1], 0u, sel), d1, a1, a3);
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t sel = (c & 1) ? 0x4141u : 0x4040u;  // byte c of the pair, replicated
+      uint32_t a0, a1, a2, a3;
+      q2_byte(__byte_perm(v0[c >> 1], 0u, sel), d0, a0, a2);
+      q2_byte(__byte_perm(v1[c >> 1], 0u, sel), d1, a1, a3);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          mma_16816(a[mt], a0, a1, a2, a3, xf[mt][2 * c], xf[mt][2 * c + 1]);
-      }
+      for (int mt = 0; mt < MT; ++mt) mma_16816(acc[mt], a0, a1, a2, a3, xf[mt][2 * c], xf[mt][2 * c + 1]);
     }
   }
 }
 
-template <int C, bool SWIGLU, int MT, bool WTMA>
-__global__ void __launch_bounds__(256)
-    gemv_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
-                const GemvParams p) {
-  using Cfg = GemvCfg<C, SWIGLU>;
+template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
+__global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_kernel(const GemvParams p) {
+  using Cfg = GemvCfg<C>;
   using S = Stage<C>;
   constexpr int R = Cfg::kRing;
-  constexpr int NM = Cfg::kMats;
+  constexpr int NC = Cfg::kConsumers;
+  constexpr int OU = SWIGLU ? 8 : 16;  // outputs per unit
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
+  float* red = reinterpret_cast<float*>(ring + R * Cfg::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
+  uint64_t* empty = full + R;
+  uint64_t* red_full = empty + R;
+  uint64_t* red_empty = red_full + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + 2);
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* ring = smem + warp * R * Cfg::kStageBytes;
-  float* red = reinterpret_cast<float*>(smem + 8 * R * Cfg::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats) + warp * R;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(
-      reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats) + 8 * R);
-
-  const int kw = p.kw;
-  const int rt = warp / kw, part = warp % kw;
-  const int n_base = (blockIdx.x * (8 / kw) + rt) * 16;
-  const int s_begin = (int)((long long)p.nstages * part / kw);
-  const int s_end = (int)((long long)p.nstages * (part + 1) / kw);
-  const int cnt = (n_base < p.N) ? s_end - s_begin : 0;  // tiles past N do nothing
-  const int g = lane >> 2, t = lane & 3;
-
-  if (threadIdx.x == 0) *abort_flag = 0;
-  if (WTMA && lane == 0) {
-    for (int i = 0; i < R; ++i) mbar_init(&full[i], 1);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&full[i], WTMA ? 1 : 32);
+      mbar_init(&empty[i], NC);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&red_full[i], NC);
+      mbar_init(&red_empty[i], 1);
+    }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
 
-  auto issue = [&](int i) {  // lane 0: load stage s_begin + i into slot i % R
-    uint8_t* dst = ring + (i % R) * Cfg::kStageBytes;
-    const int xc = (s_begin + i) * (S::KPB / 2);
-    mbar_arrive_expect_tx(&full[i % R], Cfg::kStageBytes);
-    tma_load_2d(dst, &tm_w0, &full[i % R], xc, n_base);
-    if (SWIGLU) tma_load_2d(dst + 16 * S::KPB, &tm_w1, &full[i % R], xc, n_base);
-  };
-
-  float acc[2][2][4];
-#pragma unroll
-  for (int a = 0; a < 2; ++a)
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
-
-  int issued = 0;
-  if constexpr (WTMA) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_w0);
-      for (; issued < R && issued < cnt; ++issued) issue(issued);
-    }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
-  }
-
-  bool ok = true;
-  int done = 0;  // stages consumed
-  for (int i = 0; i < cnt; ++i, done = i) {
-    uint8_t* st = ring + (i % R) * Cfg::kStageBytes;
-    const int s = s_begin + i;
-    int nb = 8;  // blocks of this stage inside K
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if constexpr (WTMA) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[i % R], (i / R) & 1, ctl));
-      if (!ok) break;
-    } else {
-      // General shapes: copy the stage with 2-byte loads, zero past the row
-      // end or past N.
-      for (int e = lane; e < Cfg::kStageBytes / 2; e += 32) {
-        const int mat = e / (16 * S::KPB / 2);
-        const int rem = e % (16 * S::KPB / 2);
-        const int row = rem / (S::KPB / 2);
-        const long long off = (long long)s * S::KPB + 2 * (rem % (S::KPB / 2));
-        const int n = n_base + row;
-        unsigned short v = 0;
-        if (n < p.N && off < p.row_bytes) {
-          const uint8_t* base = (SWIGLU && mat == 1) ? p.w1 : p.w0;
-          v = __ldg(reinterpret_cast<const unsigned short*>(base + (long long)n * p.row_bytes + off));
+      // Lane r < 16 copies tile row r (SwiGLU: rows 8..15 are the up rows).
+      int q = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const int n0 = u * OU;
+        const int rows = min(OU, p.N - n0);  // weight rows of each matrix inside N
+        const int r = lane & 7;
+        const bool mine = SWIGLU ? (lane < 16 && r < rows) : (lane < rows);
+        const uint8_t* src = (SWIGLU && lane >= 8) ? p.w1 : p.w0;
+        src += (long long)(n0 + (SWIGLU ? r : lane)) * p.row_bytes;
+        for (int s = 0; s < p.nst; ++s, ++q) {
+          const int slot = q % R;
+          if (q >= R) {
+            ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+            if (!ok) break;
+          }
+          const long long off = (long long)s * p.sb;
+          const long long left = p.row_bytes - off;
+          const uint32_t bytes = (uint32_t)(left < p.sb ? left : p.sb);
+          if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes * (SWIGLU ? 2 * rows : rows));
+          __syncwarp();
+          if (mine) bulk_load(ring + slot * Cfg::kStage + lane * Cfg::kPitch, src + off, bytes, &full[slot]);
         }
-        reinterpret_cast<unsigned short*>(st)[e] = v;
+      }
+      if (!ok && lane == 0) {
+        // Let the copies still in flight land before the CTA exits.
+        for (int i = (q > R ? q - R : 0); i < q; ++i)
+          mbar_wait_drain(&full[i % R], (i / R) & 1, 100000000ull);
+      }
+    } else {
+      // Rows that are not 16-byte multiples: the warp copies each stage with
+      // 2-byte loads (rows past N and bytes past the row end read as zero).
+      int q = 0;
+      bool ok = true;
+      const int half_sb = p.sb / 2;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        for (int s = 0; s < p.nst; ++s, ++q) {
+          const int slot = q % R;
+          if (q >= R) {
+            ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+            if (!ok) break;
+          }
+          uint8_t* dst = ring + slot * Cfg::kStage;
+          const long long off = (long long)s * p.sb;
+          for (int e = lane; e < 16 * half_sb; e += 32) {
+            const int r = e / half_sb;
+            const int c2 = e - r * half_sb;
+            const int n = SWIGLU ? u * OU + (r & 7) : u * OU + r;
+            const uint8_t* base = (SWIGLU && r >= 8) ? p.w1 : p.w0;
+            const long long o = off + 2 * c2;
+            unsigned short v = 0;
+            if (n < p.N && o < p.row_bytes)
+              v = __ldg(reinterpret_cast<const unsigned short*>(base + (long long)n * p.row_bytes + o));
+            *reinterpret_cast<unsigned short*>(dst + r * Cfg::kPitch + 2 * c2) = v;
+          }
+          mbar_arrive(&full[slot]);
+        }
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 2;
+    const int g = lane >> 2, t = lane & 3;
+    const int blocks_per_stage = p.sb / S::BB;
+    constexpr int XR = XFrag<C>::kRegs;
+    // XH: one stage per unit, so block b of every unit has the same k range.
+    uint32_t xh[XH ? Cfg::kBPW : 1][MT][XR];
+    if constexpr (XH) {
+#pragma unroll
+      for (int j = 0; j < Cfg::kBPW; ++j) load_xfrag<C, MT>(p, g, t, (cw + NC * j) * S::B, xh[j]);
+    }
+    int q = 0, i = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+      float acc[MT][4], acc1[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[mt][c] = acc1[mt][c] = 0.f;
+      bool ok = true;
+      for (int s = 0; s < p.nst; ++s, ++q) {
+        const int slot = q % R;
+        ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot], (q / R) & 1, ctl, 64));
+        if (!ok) break;
+        const uint8_t* st = ring + slot * Cfg::kStage;
+        const int kb0 = s * blocks_per_stage * S::B;
+        const int left = (p.K - kb0) / S::B;
+        const int nb = left < blocks_per_stage ? left : blocks_per_stage;
+        if (nb == Cfg::kBlocks) {
+          // Full stage: every block of this warp is inside K.
+#pragma unroll
+          for (int j = 0; j < Cfg::kBPW; ++j) {
+            const int b = cw + NC * j;
+            uint32_t xf[MT][XR];
+            if constexpr (XH) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int r = 0; r < XR; ++r) xf[mt][r] = xh[j][mt][r];
+            } else {
+              load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
+            }
+            if (j & 1) gemv_block<C, MT>(st, b, g, t, xf, acc1);
+            else gemv_block<C, MT>(st, b, g, t, xf, acc);
+          }
+        } else {
+          for (int b = cw; b < nb; b += NC) {
+            uint32_t xf[MT][XR];
+            load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
+            gemv_block<C, MT>(st, b, g, t, xf, acc);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[mt][c] += acc1[mt][c];
+      const int rb = i & 1;
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_idle(&red_empty[rb], ((i >> 1) - 1) & 1, ctl))) break;
+      float4* dst = reinterpret_cast<float4*>(red + ((rb * NC + cw) * 32 + lane) * 8);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) dst[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_full[rb]);
+    }
+  } else {
+    // ------------------------------------------------------------ reducer
+    const int g = lane >> 2, t = lane & 3;
+    int i = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+      const int rb = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_idle(&red_full[rb], (i >> 1) & 1, ctl))) break;
+      float v[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[mt][c] = 0.f;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) {
+        const float4* src = reinterpret_cast<const float4*>(red + ((rb * NC + w) * 32 + lane) * 8);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const float4 f = src[mt];
+          v[mt][0] += f.x; v[mt][1] += f.y; v[mt][2] += f.z; v[mt][3] += f.w;
+        }
       }
       __syncwarp();
-      const int left = (p.K - s * S::KP) / S::B;
-      nb = left < 8 ? left : 8;
-    }
+      if (lane == 0) mbar_arrive(&red_empty[rb]);
+      // v[mt][0..1]: tile row g, activation rows 8mt + 2t + {0,1}; v[mt][2..3]: row g + 8.
+      const int n0 = u * OU;
 #pragma unroll
-    for (int b = 0; b < 8; ++b)
-      if (b < nb) gemv_block<C, SWIGLU, MT>(st, b, g, t, s * S::KP + b * S::B, p, acc);
-    __syncwarp();
-    if constexpr (WTMA) {
-      if (lane == 0 && issued < cnt) {
-        fence_proxy_async_smem();
-        issue(issued);
-      }
-      ++issued;
-      if (issued > cnt) issued = cnt;
-      issued = __shfl_sync(0xffffffffu, issued, 0);
-    }
-  }
-  if constexpr (WTMA) {
-    if (!ok && lane == 0) {
-      // Let the copies still outstanding land before the CTA exits.
-      for (int i = done; i < issued; ++i) mbar_wait_drain(&full[i % R], (i / R) & 1, 100000000ull);
-    }
-  }
-
-  // Cross-warp reduction of the KW partial sums of each row tile.
-  float* mine = red + warp * (32 * 2 * 2 * 4) + lane * 16;
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) mine[a * 8 + b * 4 + c] = acc[a][b][c];
-  __syncthreads();
-  if (part == 0 && !*abort_flag) {
-    float sum[2][2][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) sum[a][b][c] = 0.f;
-    for (int wpart = 0; wpart < kw; ++wpart) {
-      const float* src = red + (rt * kw + wpart) * (32 * 2 * 2 * 4) + lane * 16;
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sum[a][b][c] += src[a * 8 + b * 4 + c];
-    }
-    // c0,c1: row g, columns 2t, 2t+1 of the n8 tile; c2,c3: row g + 8.
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int n = n_base + g + ((c & 2) ? 8 : 0);
-        const int m = 8 * mt + 2 * t + (c & 1);
-        if (m < p.M && n < p.N) {
-          float v = sum[0][mt][c];
-          if (SWIGLU) v = (v / (1.0f + __expf(-v))) * sum[1][mt][c];
-          p.y[(size_t)m * p.N + n] = __float2half_rn(v);
+        for (int c = 0; c < 2; ++c) {
+          const int m = 8 * mt + 2 * t + c;
+          if (m >= p.M) continue;
+          if (SWIGLU) {
+            const int n = n0 + g;
+            const float gv = v[mt][c], uv = v[mt][c + 2];
+            if (n < p.N) p.y[(size_t)m * p.N + n] = __float2half_rn((gv / (1.0f + __expf(-gv))) * uv);
+          } else {
+            const int n = n0 + g;
+            if (n < p.N) p.y[(size_t)m * p.N + n] = __float2half_rn(v[mt][c]);
+            if (n + 8 < p.N) p.y[(size_t)m * p.N + n + 8] = __float2half_rn(v[mt][c + 2]);
+          }
         }
-      }
+    }
   }
 }
 

@@ -26,11 +26,9 @@ struct ProjLaunch {
   cudaStream_t stream;
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
-  int sms;                // multiprocessors (persistent grid size)
+  int sms;                // multiprocessors (persistent grid size, both paths)
   CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path
-  int kw;                 // warps per 16-row tile (split-K inside a CTA)
-  int nstages;            // packed stages per row
   int mt;                 // 1 (M <= 8) or 2 (M <= 16)
 };
 

@@ -136,6 +136,22 @@ def test_gemv_parity(codec, general, M):
         assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "gemv swiglu %s M=%d" % (codec, M))
 
 
+@pytest.mark.parametrize("codec,K", [(synth.Q4_0, 4352), (synth.Q8_0, 2304), (synth.Q2_0, 5120),
+                                     (synth.Q4_0, 2400), (synth.Q8_0, 2080), (synth.Q2_0, 5248)])
+@pytest.mark.parametrize("M", [1, 11])
+def test_gemv_long_rows(codec, K, M):
+    # Rows longer than one streamed stage, with a ragged last stage; the
+    # second three K values give rows that are not 16-byte multiples.
+    N = 200
+    X = synth.activations(M, K, seed=M + 20)
+    W = synth.weights(codec, N, K, seed=K + 3)
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_GEMV))
+    assert_close(Y, oracle.gemm(X, W, codec, M, N, K), "gemv long %s M=%d K=%d" % (codec, M, K))
+    Wu = synth.weights(codec, N, K, seed=K + 4, name="Wu")
+    Ys = host(m.swiglu(dev(X), dev(W), dev(Wu), codec, N, K, path=m.PATH_GEMV))
+    assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "gemv long swiglu %s M=%d" % (codec, M))
+
+
 def test_auto_dispatch_matches_explicit_paths():
     K, N = 512, 256
     W = synth.weights(synth.Q8_0, N, K, seed=9)
