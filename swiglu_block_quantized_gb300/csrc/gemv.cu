@@ -38,21 +38,22 @@ cudaError_t launch_gemv_mt(const ProjLaunch& L) {
   p.N = L.N;
   p.K = L.K;
   p.row_bytes = L.row_bytes;
-  // Stage width: whole packed stages, at most kSBMax bytes per row.
-  const long long kpb = Stage<C>::KPB;
-  const long long padded = (L.row_bytes + kpb - 1) / kpb * kpb;
-  p.sb = (int)(padded < Cfg::kSBMax ? padded : Cfg::kSBMax);
+  // A row that fits one stage travels whole (row pairs are then contiguous);
+  // longer rows in segments of kSBMax bytes.
+  p.sb = (int)(L.row_bytes <= Cfg::kSBMax ? L.row_bytes : Cfg::kSBMax);
   p.nst = (int)((L.row_bytes + p.sb - 1) / p.sb);
-  const int per_unit = SWIGLU ? 8 : 16;
-  p.units = (L.N + per_unit - 1) / per_unit;
+  p.pp = 2 * p.sb + 16;
+  const int ring = Cfg::kRingBytes / (8 * p.pp);
+  p.ring = ring < Cfg::kRingMax ? ring : Cfg::kRingMax;
+  if (SWIGLU) p.ring &= ~1;  // gate and up tiles of a segment sit in adjacent slots
+  p.units = (L.N + 15) / 16;
   p.status = L.status;
   p.limit_ns = L.limit_ns;
-  // X fragments stay in registers when a full-width row is one stage and
-  // they fit (M <= 8, 4 registers per block; rows are whole stages under
-  // TMA-sized rows).
+  // X fragments stay in registers when the row is exactly one full stage
+  // (M <= 8; Q2_0 fragments are too large).
   if (L.mt == 2) return launch_gemv_one<C, SWIGLU, 2, WTMA, false>(L, p);
-  if constexpr (C != kQ2_0 && WTMA) {
-    if (p.nst == 1 && p.sb == Cfg::kSBMax) return launch_gemv_one<C, SWIGLU, 1, WTMA, true>(L, p);
+  if constexpr (C != kQ2_0) {
+    if (L.row_bytes == Cfg::kSBMax) return launch_gemv_one<C, SWIGLU, 1, WTMA, true>(L, p);
   }
   return launch_gemv_one<C, SWIGLU, 1, WTMA, false>(L, p);
 }

@@ -4,36 +4,36 @@
 // Pages: "Releases" v0.3.0 (M4QuantizedLinear sends M = 1 to a GEMV) and
 // "v0.1 vs v0.2 comparison" 2.3 (register-level reductions).  At this M the
 // packed weights are the whole memory traffic, so the kernel reads every
-// weight byte once, in long contiguous row segments, and keeps all
-// arithmetic on chip.
+// weight byte once, in long contiguous segments, and keeps all arithmetic on
+// chip.
 //
-// Work unit: one 16-row weight tile over the whole of K -- 16 weight rows of
-// a GEMM (16 outputs), or 8 gate rows over 8 up rows of SwiGLU (8 outputs, so
-// that G and U of one output end up in the same thread).  Units are dealt
-// round robin to one persistent CTA per SM.
+// Work unit: 16 outputs n0 .. n0+15 over the whole of K.  The MMA tile is 16
+// weight rows in which tile row g holds weight row n0 + 2g and tile row g + 8
+// holds row n0 + 2g + 1, so each pair of tile rows is one contiguous piece of
+// the packed matrix.  SwiGLU runs the gate tile and the up tile of the same
+// 16 outputs through the same thread fragments: G and U of an output land in
+// the same thread and SiLU(G) x U is formed in registers.
 //
-// CTA roles (576 threads):
-//   warp 0      producer.  A unit arrives as stages of 16 rows x SB bytes
-//               (SB up to about 2.3 KB of whole blocks: one stage holds a
-//               whole row when K <= 4096), one bulk copy per row segment,
-//               issued by 16 lanes at once, into a ring of shared-memory
-//               stages.  Copies of 2 KB and more stream at close to the HBM
-//               rate; much shorter ones are limited by the copy issue rate.
-//               Rows sit at a pitch of SB + 16 bytes so the 16 rows of a stage
-//               fall into different shared-memory banks.
-//   warps 2..17 consumers.  Warp c takes blocks c, c + 16, ... of each stage
-//               (fully unrolled, alternating between two accumulator sets so
-//               that the MMA chains overlap; when a row fits in one stage
-//               each warp sees the same k range in every unit, so its X
-//               fragments are loaded once), decodes them exactly
-//               (codec.cuh) and multiplies them with
-//               mma.sync m16n8k16: the weight tile is A (16 rows x 16 k), X^T
-//               is B (16 k x 8 activation rows, two n8 tiles when M > 8),
-//               fp32 accumulation.  Inside a block the k order of the MMA
-//               slots is permuted identically for W and X so that each thread
-//               reads contiguous code bytes and contiguous X values.
+// CTA roles (576 threads), one persistent CTA per SM, units dealt round robin:
+//   warp 0      producer.  A tile arrives as stages of 8 row pairs, one bulk
+//               copy per pair (both rows at once when a row fits one stage:
+//               4.6 KB at K = 4096 for Q4_0).  Few, long copies keep the
+//               stream at the HBM rate: a bulk copy has a fixed issue cost.
+//               Pairs sit 2 SB + 16 bytes apart in shared memory (SB = row
+//               bytes per stage), which puts tile rows 0..7 in distinct banks;
+//               rows g and g + 8 share banks but are read by different loads.
+//   warps 2..17 consumers.  Warp c takes blocks c, c + 16, ... of each stage,
+//               decodes them exactly (codec.cuh) and multiplies them with
+//               mma.sync m16n8k16 (weight tile = A, X^T = B, two n8 tiles when
+//               M > 8, fp32 accumulation, two accumulator sets so that the
+//               MMA chains overlap).  When a row is one stage of 16 kXH
+//               blocks, each warp keeps the X fragments of its blocks in
+//               registers for the whole launch.  Inside a block the k order
+//               of the MMA slots is permuted identically for W and X so that
+//               each thread reads contiguous code bytes and contiguous X
+//               values.
 //   warp 1      reducer.  Adds the 16 consumers' partial tiles of a unit in a
-//               fixed order and writes Y (SwiGLU: SiLU(G) x U in registers).
+//               fixed order and writes Y.
 // Every wait is bounded in time; on expiry the CTA records the failure in the
 // status word, lets its copies in flight land and returns.
 #pragma once
@@ -49,9 +49,11 @@ struct GemvParams {
   __half* y;           // [M, N]
   int M, N, K;
   long long row_bytes;
-  int sb;              // stage bytes per row: whole packed stages, <= kSBMax
-  int nst;             // stages per unit (ceil(row_bytes / sb))
-  int units;           // 16-row weight tiles
+  int sb;              // row bytes per stage: row_bytes if a row fits, else kSBMax
+  int nst;             // stages per row
+  int pp;              // shared-memory pitch of a row pair: 2 sb + 16
+  int ring;            // stages in the ring
+  int units;           // 16-output units
   uint32_t* status;
   unsigned long long limit_ns;
 };
@@ -62,16 +64,14 @@ struct GemvCfg {
   static constexpr int kConsumers = 16;
   static constexpr int kThreads = 32 * (kConsumers + 2);
   static constexpr int kSBMax = (2400 / S::KPB) * S::KPB;   // 2304 (Q4_0) or 2176 B
-  static constexpr int kBlocks = kSBMax / S::BB;             // blocks per full stage
-  static constexpr int kBPW = kBlocks / kConsumers;          // blocks per consumer warp
-  static constexpr int kPitch = kSBMax + 16;                 // row pitch in a stage
-  static constexpr int kStage = 16 * kPitch;
-  static constexpr int kRing = 5;
-  static constexpr int kRedFloats = 2 * kConsumers * 32 * 8; // [buf][warp][lane][8]
-  static constexpr int kBars = 2 * kRing + 4;
-  static constexpr int kSmemBytes = kRing * kStage + kRedFloats * 4 + kBars * 8 + 16 + 128;
-  static_assert(kPitch % 16 == 0 && kStage % 128 == 0, "bulk-copy alignment");
-  static_assert(kBPW * kConsumers == kBlocks, "blocks split evenly over the consumers");
+  static constexpr int kBlocks = kSBMax / S::BB;             // blocks of a full stage
+  static constexpr int kXH = kBlocks / kConsumers;           // blocks per warp of a full stage
+  static constexpr int kRingBytes = 160 * 1024;
+  static constexpr int kRingMax = 16;
+  static constexpr int kRedFloats = 2 * kConsumers * 32 * 16; // [buf][warp][lane][2 mats x MT x 4]
+  static constexpr int kBars = 2 * kRingMax + 4;
+  static constexpr int kSmemBytes = kRingBytes + kRedFloats * 4 + kBars * 8 + 16 + 128;
+  static_assert(kXH * kConsumers == kBlocks, "blocks split evenly over the consumers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -140,19 +140,13 @@ __device__ __forceinline__ void load_xfrag(const GemvParams& p, int g, int t, in
   }
 }
 
-// Accumulate block b of a stage into the 16 x 8*MT tile.  `st` is the stage
-// ([16 rows][kPitch] bytes); g = lane / 4, t = lane % 4; xf holds the X
-// fragments of the block.
+// Accumulate one block into the 16 x 8*MT tile.  r0 points at the block in
+// tile row g, r1 at the same block in tile row g + 8; t = lane % 4; xf holds
+// the X fragments of the block.
 template <int C, int MT>
-__device__ __forceinline__ void gemv_block(const uint8_t* st, int b, int g, int t,
+__device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1, int t,
                                            const uint32_t (&xf)[MT][XFrag<C>::kRegs],
                                            float (&acc)[MT][4]) {
-  using S = Stage<C>;
-  constexpr int BB = S::BB;
-  constexpr int PITCH = GemvCfg<C>::kPitch;
-
-  const uint8_t* r0 = st + g * PITCH + b * BB;  // tile row g
-  const uint8_t* r1 = r0 + 8 * PITCH;           // tile row g + 8
   const uint32_t d0 = dup_scale(lds_u16(r0)), d1 = dup_scale(lds_u16(r1));
 
   if constexpr (C == kQ4_0) {
@@ -201,20 +195,21 @@ __device__ __forceinline__ void gemv_block(const uint8_t* st, int b, int g, int 
 }
 
 template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
-__global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const GemvParams p) {
   using Cfg = GemvCfg<C>;
   using S = Stage<C>;
-  constexpr int R = Cfg::kRing;
   constexpr int NC = Cfg::kConsumers;
-  constexpr int OU = SWIGLU ? 8 : 16;  // outputs per unit
+  constexpr int NM = SWIGLU ? 2 : 1;  // tiles (matrices) per unit
+  const int R = p.ring;
+  const int stage_bytes = 8 * p.pp;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
-  float* red = reinterpret_cast<float*>(ring + R * Cfg::kStage);
+  float* red = reinterpret_cast<float*>(ring + Cfg::kRingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
-  uint64_t* empty = full + R;
-  uint64_t* red_full = empty + R;
+  uint64_t* empty = full + Cfg::kRingMax;
+  uint64_t* red_full = empty + Cfg::kRingMax;
   uint64_t* red_empty = red_full + 2;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + 2);
 
@@ -236,29 +231,39 @@ __global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_ker
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Stage order of a unit: for each row segment s, the gate tile then (for
+    // SwiGLU) the up tile.
+    int q = 0;
+    bool ok = true;
     if constexpr (WTMA) {
-      // Lane r < 16 copies tile row r (SwiGLU: rows 8..15 are the up rows).
-      int q = 0;
-      bool ok = true;
+      // Lane g < 8 copies row pair g (weight rows n0 + 2g, n0 + 2g + 1).
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const int n0 = u * OU;
-        const int rows = min(OU, p.N - n0);  // weight rows of each matrix inside N
-        const int r = lane & 7;
-        const bool mine = SWIGLU ? (lane < 16 && r < rows) : (lane < rows);
-        const uint8_t* src = (SWIGLU && lane >= 8) ? p.w1 : p.w0;
-        src += (long long)(n0 + (SWIGLU ? r : lane)) * p.row_bytes;
-        for (int s = 0; s < p.nst; ++s, ++q) {
-          const int slot = q % R;
-          if (q >= R) {
-            ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
-            if (!ok) break;
-          }
+        const int n = u * 16 + 2 * lane;
+        const bool mine = lane < 8 && n < p.N;  // N is even: the pair is whole
+        const int pairs = __popc(__ballot_sync(0xffffffffu, mine));
+        for (int s = 0; s < p.nst && ok; ++s) {
           const long long off = (long long)s * p.sb;
           const long long left = p.row_bytes - off;
           const uint32_t bytes = (uint32_t)(left < p.sb ? left : p.sb);
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes * (SWIGLU ? 2 * rows : rows));
-          __syncwarp();
-          if (mine) bulk_load(ring + slot * Cfg::kStage + lane * Cfg::kPitch, src + off, bytes, &full[slot]);
+          for (int mat = 0; mat < NM; ++mat, ++q) {
+            const int slot = q % R;
+            if (q >= R) {
+              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+              if (!ok) break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * bytes * pairs);
+            __syncwarp();
+            if (mine) {
+              const uint8_t* src = (mat ? p.w1 : p.w0) + (long long)n * p.row_bytes + off;
+              uint8_t* dst = ring + slot * stage_bytes + lane * p.pp;
+              if (p.nst == 1) {
+                bulk_load(dst, src, 2u * bytes, &full[slot]);   // both rows: contiguous
+              } else {
+                bulk_load(dst, src, bytes, &full[slot]);
+                bulk_load(dst + p.sb, src + p.row_bytes, bytes, &full[slot]);
+              }
+            }
+          }
         }
       }
       if (!ok && lane == 0) {
@@ -269,30 +274,31 @@ __global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_ker
     } else {
       // Rows that are not 16-byte multiples: the warp copies each stage with
       // 2-byte loads (rows past N and bytes past the row end read as zero).
-      int q = 0;
-      bool ok = true;
       const int half_sb = p.sb / 2;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        for (int s = 0; s < p.nst; ++s, ++q) {
-          const int slot = q % R;
-          if (q >= R) {
-            ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
-            if (!ok) break;
+        for (int s = 0; s < p.nst && ok; ++s) {
+          for (int mat = 0; mat < NM; ++mat, ++q) {
+            const int slot = q % R;
+            if (q >= R) {
+              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+              if (!ok) break;
+            }
+            uint8_t* dst = ring + slot * stage_bytes;
+            const uint8_t* base = mat ? p.w1 : p.w0;
+            const long long off = (long long)s * p.sb;
+            for (int e = lane; e < 16 * half_sb; e += 32) {
+              const int r = e / half_sb;          // tile row
+              const int c2 = e - r * half_sb;
+              const int gg = r & 7, hi = r >> 3;  // pair, row within the pair
+              const int n = u * 16 + 2 * gg + hi;
+              const long long o = off + 2 * c2;
+              unsigned short v = 0;
+              if (n < p.N && o < p.row_bytes)
+                v = __ldg(reinterpret_cast<const unsigned short*>(base + (long long)n * p.row_bytes + o));
+              *reinterpret_cast<unsigned short*>(dst + gg * p.pp + hi * p.sb + 2 * c2) = v;
+            }
+            mbar_arrive(&full[slot]);
           }
-          uint8_t* dst = ring + slot * Cfg::kStage;
-          const long long off = (long long)s * p.sb;
-          for (int e = lane; e < 16 * half_sb; e += 32) {
-            const int r = e / half_sb;
-            const int c2 = e - r * half_sb;
-            const int n = SWIGLU ? u * OU + (r & 7) : u * OU + r;
-            const uint8_t* base = (SWIGLU && r >= 8) ? p.w1 : p.w0;
-            const long long o = off + 2 * c2;
-            unsigned short v = 0;
-            if (n < p.N && o < p.row_bytes)
-              v = __ldg(reinterpret_cast<const unsigned short*>(base + (long long)n * p.row_bytes + o));
-            *reinterpret_cast<unsigned short*>(dst + r * Cfg::kPitch + 2 * c2) = v;
-          }
-          mbar_arrive(&full[slot]);
         }
       }
     }
@@ -300,35 +306,43 @@ __global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_ker
     // ------------------------------------------------------------ consumers
     const int cw = warp - 2;
     const int g = lane >> 2, t = lane & 3;
-    const int blocks_per_stage = p.sb / S::BB;
+    const int bps = p.sb / S::BB;  // blocks per full stage
     constexpr int XR = XFrag<C>::kRegs;
-    // XH: one stage per unit, so block b of every unit has the same k range.
-    uint32_t xh[XH ? Cfg::kBPW : 1][MT][XR];
+    // XH: one full stage per row; warp cw always handles blocks cw + 16 j.
+    uint32_t xh[XH ? Cfg::kXH : 1][MT][XR];
     if constexpr (XH) {
 #pragma unroll
-      for (int j = 0; j < Cfg::kBPW; ++j) load_xfrag<C, MT>(p, g, t, (cw + NC * j) * S::B, xh[j]);
+      for (int j = 0; j < Cfg::kXH; ++j) load_xfrag<C, MT>(p, g, t, (cw + NC * j) * S::B, xh[j]);
     }
+    const int row_off = g * p.pp + cw * S::BB;  // this thread's row g, this warp's first block
     int q = 0, i = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
-      float acc[MT][4], acc1[MT][4];
+      float acc[NM][MT][4], acc1[NM][MT][4];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int mat = 0; mat < NM; ++mat)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[mt][c] = acc1[mt][c] = 0.f;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[mat][mt][c] = acc1[mat][mt][c] = 0.f;
       bool ok = true;
-      for (int s = 0; s < p.nst; ++s, ++q) {
-        const int slot = q % R;
-        ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot], (q / R) & 1, ctl, 64));
-        if (!ok) break;
-        const uint8_t* st = ring + slot * Cfg::kStage;
-        const int kb0 = s * blocks_per_stage * S::B;
+      for (int s = 0; s < p.nst && ok; ++s) {
+        const int kb0 = s * bps * S::B;
         const int left = (p.K - kb0) / S::B;
-        const int nb = left < blocks_per_stage ? left : blocks_per_stage;
-        if (nb == Cfg::kBlocks) {
+        const int nb = left < bps ? left : bps;  // blocks of this segment
+        // The NM tiles (gate, up) of this segment are adjacent ring slots:
+        // wait for both, then run them block by block (independent MMA chains
+        // that share the X fragments).
+        const int slot = q % R;
+        for (int mat = 0; mat < NM && ok; ++mat)
+          ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot + mat], ((q + mat) / R) & 1, ctl, 64));
+        if (!ok) break;
+        const uint8_t* r0 = ring + slot * stage_bytes + row_off;  // block cw, row g, tile 0
+        const uint8_t* r1 = r0 + p.sb;                            // block cw, row g + 8
+        if (XH || nb == Cfg::kBlocks) {
           // Full stage: every block of this warp is inside K.
 #pragma unroll
-          for (int j = 0; j < Cfg::kBPW; ++j) {
-            const int b = cw + NC * j;
+          for (int j = 0; j < Cfg::kXH; ++j) {
+            const int bo = NC * j * S::BB;
             uint32_t xf[MT][XR];
             if constexpr (XH) {
 #pragma unroll
@@ -336,31 +350,43 @@ __global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_ker
 #pragma unroll
                 for (int r = 0; r < XR; ++r) xf[mt][r] = xh[j][mt][r];
             } else {
-              load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
+              load_xfrag<C, MT>(p, g, t, kb0 + (cw + NC * j) * S::B, xf);
             }
-            if (j & 1) gemv_block<C, MT>(st, b, g, t, xf, acc1);
-            else gemv_block<C, MT>(st, b, g, t, xf, acc);
+#pragma unroll
+            for (int mat = 0; mat < NM; ++mat) {
+              const int to = mat * stage_bytes + bo;
+              if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat]);
+              else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat]);
+            }
           }
         } else {
-          for (int b = cw; b < nb; b += NC) {
+          for (int b = cw, j = 0; b < nb; b += NC, ++j) {
+            const int bo = (b - cw) * S::BB;
             uint32_t xf[MT][XR];
             load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
-            gemv_block<C, MT>(st, b, g, t, xf, acc);
+#pragma unroll
+            for (int mat = 0; mat < NM; ++mat) {
+              const int to = mat * stage_bytes + bo;
+              if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat]);
+              else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat]);
+            }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0)
+          for (int mat = 0; mat < NM; ++mat) mbar_arrive(&empty[slot + mat]);
+        q += NM;
       }
       if (!ok) break;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[mt][c] += acc1[mt][c];
       const int rb = i & 1;
       if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_idle(&red_empty[rb], ((i >> 1) - 1) & 1, ctl))) break;
-      float4* dst = reinterpret_cast<float4*>(red + ((rb * NC + cw) * 32 + lane) * 8);
+      float4* dst = reinterpret_cast<float4*>(red + ((rb * NC + cw) * 32 + lane) * 16);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) dst[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+      for (int mat = 0; mat < NM; ++mat)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          dst[mat * MT + mt] = make_float4(acc[mat][mt][0] + acc1[mat][mt][0], acc[mat][mt][1] + acc1[mat][mt][1],
+                                           acc[mat][mt][2] + acc1[mat][mt][2], acc[mat][mt][3] + acc1[mat][mt][3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[rb]);
     }
@@ -371,40 +397,44 @@ __global__ void __launch_bounds__(32 * (GemvCfg<C>::kConsumers + 2), 1) gemv_ker
     for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
       const int rb = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_idle(&red_full[rb], (i >> 1) & 1, ctl))) break;
-      float v[MT][4];
+      float v[NM][MT][4];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int mat = 0; mat < NM; ++mat)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v[mt][c] = 0.f;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) v[mat][mt][c] = 0.f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float4* src = reinterpret_cast<const float4*>(red + ((rb * NC + w) * 32 + lane) * 8);
+        const float4* src = reinterpret_cast<const float4*>(red + ((rb * NC + w) * 32 + lane) * 16);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const float4 f = src[mt];
-          v[mt][0] += f.x; v[mt][1] += f.y; v[mt][2] += f.z; v[mt][3] += f.w;
-        }
+        for (int mat = 0; mat < NM; ++mat)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const float4 f = src[mat * MT + mt];
+            v[mat][mt][0] += f.x; v[mat][mt][1] += f.y; v[mat][mt][2] += f.z; v[mat][mt][3] += f.w;
+          }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rb]);
-      // v[mt][0..1]: tile row g, activation rows 8mt + 2t + {0,1}; v[mt][2..3]: row g + 8.
-      const int n0 = u * OU;
+      // v[.][mt][c], c < 2: tile row g = output n0 + 2g, activation row
+      // 8 mt + 2t + c; v[.][mt][c + 2]: tile row g + 8 = output n0 + 2g + 1.
+      const int n = u * 16 + 2 * g;
+      if (n < p.N) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int m = 8 * mt + 2 * t + c;
-          if (m >= p.M) continue;
-          if (SWIGLU) {
-            const int n = n0 + g;
-            const float gv = v[mt][c], uv = v[mt][c + 2];
-            if (n < p.N) p.y[(size_t)m * p.N + n] = __float2half_rn((gv / (1.0f + __expf(-gv))) * uv);
-          } else {
-            const int n = n0 + g;
-            if (n < p.N) p.y[(size_t)m * p.N + n] = __float2half_rn(v[mt][c]);
-            if (n + 8 < p.N) p.y[(size_t)m * p.N + n + 8] = __float2half_rn(v[mt][c + 2]);
+          for (int c = 0; c < 2; ++c) {
+            const int m = 8 * mt + 2 * t + c;
+            if (m >= p.M) continue;
+            float a = v[0][mt][c], b = v[0][mt][c + 2];
+            if constexpr (SWIGLU) {
+              a = (a / (1.0f + __expf(-a))) * v[NM - 1][mt][c];
+              b = (b / (1.0f + __expf(-b))) * v[NM - 1][mt][c + 2];
+            }
+            *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(a, b);
           }
-        }
+      }
     }
   }
 }
