@@ -160,8 +160,10 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     if (!encode_2d(&L.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, K * 2, 64, nx,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return M4Q_ERR_CUDA;
-    if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2, (uint32_t)out_rows, 32,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    // Y boxes: GEMM stages [32 m][128 n] chunks per warpgroup; SwiGLU stores
+    // one [nx/2 m][16 n] slab per epilogue warp.
+    if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2, swiglu ? 16u : (uint32_t)out_rows,
+                   swiglu ? (uint32_t)(nx / 2) : 32u, CU_TENSOR_MAP_SWIZZLE_NONE))
       return M4Q_ERR_CUDA;
     L.tm_w0 = L.tm_x;
     L.tm_w1 = L.tm_x;

@@ -59,8 +59,9 @@ struct TcCfg {
   static constexpr int kSA = 8;                                   // TMEM A ring depth
   static constexpr int kXStage = NX * 128;                        // bytes
   static constexpr int kWStage = kRows * S::KPB;                  // bytes
-  static constexpr int kYStage = 32 * kOutRows * 2;               // one staged Y chunk
-  static constexpr int kYBytes = 4 * kYStage;                     // 2 groups x 2 buffers
+  static constexpr int kYStage = 32 * kOutRows * 2;               // one staged Y chunk (GEMM)
+  static constexpr int kYSlab = (NX / 2) * 16 * 2;                // one warp's Y slab (SwiGLU)
+  static constexpr int kYBytes = SWIGLU ? 8 * kYSlab : 4 * kYStage;  // GEMM: 2 groups x 2 buffers
   static constexpr int kFixed = kSW * kWStage + kYBytes + 1024 + 512;  // + align, barriers
   static constexpr int kBudget = 227 * 1024;
   static constexpr int kSX = (kFixed + 8 * kXStage <= kBudget) ? 8
@@ -74,7 +75,8 @@ struct TcCfg {
   static_assert(NX % 16 == 0 && NX >= 64 && NX <= 256, "MMA N");
   static_assert(kACol0 + 32 * kSA <= kTmemCols && NX <= kACol0, "TMEM budget");
   static_assert(kSmemBytes <= kBudget, "shared memory budget");
-  static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0 && kYStage % 1024 == 0, "alignment");
+  static_assert(kXStage % 1024 == 0 && kWStage % 16 == 0 && kYStage % 1024 == 0 && kYSlab % 1024 == 0,
+                "alignment");
 };
 
 // Barrier-reduction OR over `count` threads of named barrier `id`.
@@ -195,6 +197,14 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
 }
 
 // Epilogue role of group E (0 or 1): columns [E*NX/2, (E+1)*NX/2) of D.
+//
+// SwiGLU: each warp reads all its columns of D first (SiLU(G) x U halves
+// them: every lane keeps 16 outputs per 32 columns as packed fp16), then
+// releases D to the next tile, and only then stages its [NX/2 m][16 n] slab
+// of Y and stores it with one TMA bulk store.  D is held only for the
+// tcgen05.ld round trips.
+// GEMM: per 32-column chunk, fp16 rounding, group-wide staging and store;
+// D is released after the last chunk load.
 template <int C, bool SWIGLU, int NX, bool WTMA>
 __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                               const WaitCtl& ctl, const CUtensorMap* tm_y, int warp,
@@ -207,12 +217,78 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
   const uint32_t bar_id = 1 + E;
   const int odd = lane & 1;
   uint8_t* ybuf = sm.ys + E * 2 * Cfg::kYStage;
+  if constexpr (SWIGLU) {
+    constexpr int NCH = (NX / 2) / 32;  // 32-column chunks of this group
+    const int q = warp & 3;             // TMEM lane quadrant = outputs n0 + 16q .. n0 + 16q + 15
+    uint8_t* slab = sm.ys + (warp - 12) * Cfg::kYSlab;  // [NX/2 m][16 n] fp16
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++lt) {
+      const int m0 = (tile % p.m_tiles) * NX;
+      const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
+      // The accumulator of a tile takes the whole MMA loop: sleep between
+      // polls so the decode warps keep the issue slots.
+      const bool dok = !*ctl.abort && mbar_wait_idle(sm.d_full, lt & 1, ctl, 128);
+      if (!__all_sync(0xffffffffu, dok)) break;
+      tc_fence_after();
+      const int c_begin = E * (NX / 2);
+      uint32_t y2[NCH][8];  // outputs of columns c_begin + 32 ch + 2 jj + odd, two per register
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_base + c_begin + 32 * ch, v);
+        // lane 2i holds G, lane 2i+1 holds U of output n0 + 16q + i; the even
+        // lane forms the even columns, the odd lane the odd ones
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 2) {
+          float y[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float a = __uint_as_float(v[2 * (jj + h)]), b = __uint_as_float(v[2 * (jj + h) + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const float g = odd ? recv : a;
+            const float u = odd ? b : recv;
+            y[h] = __fdividef(g, 1.0f + __expf(-g)) * u;
+          }
+          const __half2 hy = __floats2half2_rn(y[0], y[1]);
+          y2[ch][jj / 2] = *reinterpret_cast<const uint32_t*>(&hy);
+        }
+      }
+      // Every column of this warp is in registers: D may be reused.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.d_empty);
+      if (m0 + c_begin >= p.M || n0 + 16 * q >= p.N) continue;  // uniform: slab entirely padding
+      if (lane == 0) bulk_wait_read<0>();  // the previous store has read the slab
+      __syncwarp();
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t w = y2[ch][k];
+          const int m = 32 * ch + 4 * k + odd;  // columns 2jj + odd for jj = 2k, 2k + 1
+          __half* row0 = reinterpret_cast<__half*>(slab + m * 32);
+          __half* row1 = reinterpret_cast<__half*>(slab + (m + 2) * 32);
+          row0[lane >> 1] = __ushort_as_half((unsigned short)(w & 0xFFFFu));
+          row1[lane >> 1] = __ushort_as_half((unsigned short)(w >> 16));
+        }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_y, slab, n0 + 16 * q, m0 + c_begin);
+        bulk_commit();
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    return;
+  }
   int it = 0, lt = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++lt) {
     const int m0 = (tile % p.m_tiles) * NX;
     const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
     bool dok = false;
-    if (!*ctl.abort) dok = mbar_wait(sm.d_full, lt & 1, ctl);
+    // The accumulator of a tile takes the whole MMA loop: sleep between
+    // polls so the decode warps keep the issue slots.
+    if (!*ctl.abort) dok = mbar_wait_idle(sm.d_full, lt & 1, ctl, 128);
     // One decision for both epilogue groups (they synchronise below).
     if (named_bar_any(5, 256, !dok || *ctl.abort)) break;
     tc_fence_after();
@@ -328,7 +404,7 @@ __global__ void __launch_bounds__(640, 1)
         const int m0 = (tile % p.m_tiles) * NX;
         for (int ks = 0; ks < nks; ++ks) {
           const int sx = xi % SX;
-          if (xi >= SX && !mbar_wait(&sm.x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+          if (xi >= SX && !mbar_wait_idle(&sm.x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.x_full[sx], Cfg::kXStage);
           tma_load_2d(sm.xs + sx * Cfg::kXStage, &tm_x, &sm.x_full[sx], ks * 64, m0);
           ++xi;
@@ -352,7 +428,7 @@ __global__ void __launch_bounds__(640, 1)
           const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
           for (int pk = 0; pk < npk; ++pk) {
             const int sp = wi % SW;
-            if (wi >= SW && !mbar_wait(&sm.w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
+            if (wi >= SW && !mbar_wait_idle(&sm.w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
             mbar_arrive_expect_tx(&sm.w_full[sp], Cfg::kWStage);
             uint8_t* dst = sm.ws + sp * Cfg::kWStage;
             const int xc = pk * (S::KPB / 2);  // uint16 elements
