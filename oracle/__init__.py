@@ -65,6 +65,10 @@ def _bind(path: str):
     lib.oracle_gemm.restype = i32
     lib.oracle_swiglu.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, i64, vp, i32]
     lib.oracle_swiglu.restype = i32
+    lib.oracle_geglu.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, i64, vp, i32]
+    lib.oracle_geglu.restype = i32
+    lib.oracle_gelu.argtypes = [ctypes.c_double]
+    lib.oracle_gelu.restype = ctypes.c_double
     return lib
 
 
@@ -154,6 +158,10 @@ def silu(g: float) -> float:
     return float(_L().oracle_silu(float(g)))
 
 
+def gelu(g: float) -> float:
+    return float(_L().oracle_gelu(float(g)))
+
+
 def _as_packed(W: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(W, dtype=np.uint8))
 
@@ -210,4 +218,17 @@ def swiglu(X, Wg, Wu, codec: int, M: int, N: int, K: int, rows=None,
                                None if r is None else _ptr(r), nrows, _ptr(out),
                                nthreads or default_threads())
     _check(rc, "swiglu")
+    return out
+
+
+def geglu(X, Wg, Wu, codec: int, M: int, N: int, K: int, rows=None,
+          nthreads: int | None = None):
+    """binary64 Y = GELU(X Wg^T) * (X Wu^T) for the selected rows."""
+    Xb, Gp, Up = _as_xbits(X), _as_packed(Wg), _as_packed(Wu)
+    r, nrows = _rows_arg(rows, M)
+    out = np.empty((nrows, N), dtype=np.float64)
+    rc = _L().oracle_geglu(_ptr(Xb), _ptr(Gp), _ptr(Up), codec, M, N, K,
+                              None if r is None else _ptr(r), nrows, _ptr(out),
+                              nthreads or default_threads())
+    _check(rc, "geglu")
     return out

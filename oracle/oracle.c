@@ -26,6 +26,10 @@
  *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
  *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
  *    activation written out.
+ *  - "Releases", v0.3.0 (TransformerBlock: "SwiGLU / GeGLU activations",
+ *    Gemma 2 configurations): the same gated projection with GELU in place
+ *    of SiLU.  The pages do not define GELU; this oracle takes the textbook
+ *    definition GELU(g) = g * Phi(g) = g/2 * erfc(-g / sqrt 2).
  *  - "v0.1 vs v0.2 comparison", section 2.1, and "Releases" v0.2.3: the
  *    unpackers feed half-precision MMA fragments (simdgroup_matrix<half,8,8>),
  *    so the weights the projection multiplies are fp16 values.  The oracle
@@ -180,13 +184,20 @@ int oracle_dequant_f16(const uint8_t* W, int codec, long long N, long long K, ui
 /* SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), in binary64. */
 double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
 
+/* GELU(g) = g * Phi(g), Phi the standard normal CDF, in binary64.
+ * Phi(g) = erfc(-g / sqrt 2) / 2, which does not cancel for negative g. */
+double oracle_gelu(double g) { return 0.5 * g * erfc(-g / sqrt(2.0)); }
+
+enum { ORACLE_ACT_SILU = 0, ORACLE_ACT_GELU = 1 };
+
 /* ---- projections, split over output columns n across threads ---- */
 
 typedef struct {
   const double* Xd;        /* [nrows, K] widened activations */
   const uint8_t* W0;       /* gate (SwiGLU) or the only weight (GEMM) */
-  const uint8_t* W1;       /* up (SwiGLU) or NULL */
+  const uint8_t* W1;       /* up (gated projections) or NULL */
   int codec;
+  int act;                 /* ORACLE_ACT_*: activation of the gate */
   long long nrows, N, K, row_bytes;
   long long n_begin, n_end;
   double* Y;               /* [nrows, N] */
@@ -221,7 +232,7 @@ static void* run_job(void* arg) {
       double g = dot(x, w0, j->K);
       if (j->W1) {
         double u = dot(x, w1, j->K);
-        j->Y[r * j->N + n] = oracle_silu(g) * u;
+        j->Y[r * j->N + n] = (j->act == ORACLE_ACT_GELU ? oracle_gelu(g) : oracle_silu(g)) * u;
       } else {
         j->Y[r * j->N + n] = g;
       }
@@ -233,7 +244,7 @@ static void* run_job(void* arg) {
   return NULL;
 }
 
-static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int codec,
+static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int codec, int act,
                    long long M, long long N, long long K, const long long* rows,
                    long long nrows, double* Y, int nthreads) {
   int rc = check_shape(codec, N, K);
@@ -254,7 +265,7 @@ static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int 
   pthread_t tids[256];
   long long row_bytes = (K / oracle_block_size(codec)) * oracle_block_bytes(codec);
   for (int t = 0; t < nthreads; ++t) {
-    jobs[t] = (job_t){Xd, W0, W1, codec, nrows, N, K, row_bytes,
+    jobs[t] = (job_t){Xd, W0, W1, codec, act, nrows, N, K, row_bytes,
                       N * t / nthreads, N * (t + 1) / nthreads, Y, 0};
   }
   int started = 0;
@@ -276,7 +287,7 @@ static int project(const uint16_t* X, const uint8_t* W0, const uint8_t* W1, int 
  * X is fp16 bits [M, K]; W is packed [N, K / block] blocks; Y is [nrows, N]. */
 int oracle_gemm(const uint16_t* X, const uint8_t* W, int codec, long long M, long long N,
                 long long K, const long long* rows, long long nrows, double* Y, int nthreads) {
-  return project(X, W, NULL, codec, M, N, K, rows, nrows, Y, nthreads);
+  return project(X, W, NULL, codec, ORACLE_ACT_SILU, M, N, K, rows, nrows, Y, nthreads);
 }
 
 /* Y[r, n] = SiLU(G) * U with G = X Wg^T, U = X Wu^T, both in binary64. */
@@ -284,5 +295,13 @@ int oracle_swiglu(const uint16_t* X, const uint8_t* Wg, const uint8_t* Wu, int c
                   long long M, long long N, long long K, const long long* rows,
                   long long nrows, double* Y, int nthreads) {
   if (!Wu) return -1;
-  return project(X, Wg, Wu, codec, M, N, K, rows, nrows, Y, nthreads);
+  return project(X, Wg, Wu, codec, ORACLE_ACT_SILU, M, N, K, rows, nrows, Y, nthreads);
+}
+
+/* Y[r, n] = GELU(G) * U with G = X Wg^T, U = X Wu^T, both in binary64. */
+int oracle_geglu(const uint16_t* X, const uint8_t* Wg, const uint8_t* Wu, int codec,
+                 long long M, long long N, long long K, const long long* rows,
+                 long long nrows, double* Y, int nthreads) {
+  if (!Wu) return -1;
+  return project(X, Wg, Wu, codec, ORACLE_ACT_GELU, M, N, K, rows, nrows, Y, nthreads);
 }

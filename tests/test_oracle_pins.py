@@ -3,7 +3,7 @@
 Each test checks the oracle against something it cannot agree with by
 construction: hand-decoded golden blocks, numpy's IEEE conversions, exact
 rational arithmetic on tiny inputs, closed forms, the identity matrix, and
-invariants of SiLU.  A second group compiles copies of the oracle with a
+invariants of SiLU and GELU.  A second group compiles copies of the oracle with a
 planted mistake and checks that at least one pin fails for each.
 """
 import math
@@ -232,6 +232,83 @@ def test_swiglu_fused_equals_unfused(codec):
     assert np.allclose(fused, ind, rtol=1e-13, atol=1e-300)
 
 
+def phi_decimal(x, digits=40):
+    """Standard normal CDF in exact decimal arithmetic, independent of the C
+    library's erf: the Maclaurin series of erf for |x| <= 8, the asymptotic
+    tail series phi(x)/|x| * sum (-1)^n (2n-1)!! / x^(2n) beyond."""
+    getcontext().prec = digits + 10
+    xd = Decimal(x)
+    if abs(xd) > 8:
+        t = abs(xd)
+        dens = (-(t * t) / 2).exp() / (2 * _sqrt_pi() / Decimal(2).sqrt())  # phi(t) = e^(-t^2/2) / sqrt(2 pi)
+        term, total, n = Decimal(1), Decimal(1), 0
+        while n < 30:
+            n += 1
+            term = -term * (2 * n - 1) / (t * t)
+            total += term
+        tail = dens / t * total                          # Phi(-t)
+        return tail if xd < 0 else 1 - tail
+    z = xd / Decimal(2).sqrt()
+    term, total, n = z, z, 0
+    while True:
+        n += 1
+        term = -term * z * z / n                      # (-1)^n z^(2n+1) / n!
+        add = term / (2 * n + 1)
+        total += add
+        if abs(add) < Decimal(10) ** (-(digits + 5)):
+            break
+    erf = 2 * total / _sqrt_pi()
+    return (1 + erf) / 2
+
+
+def _sqrt_pi():
+    # pi from Machin's formula, exact to the working precision
+    def arctan_inv(k):
+        x = Decimal(1) / k
+        x2, term, total, n = x * x, x, x, 1
+        while True:
+            term = -term * x2
+            add = term / (2 * n + 1)
+            if abs(add) < Decimal(10) ** (-(getcontext().prec + 2)):
+                return total
+            total += add
+            n += 1
+    return (4 * (4 * arctan_inv(5) - arctan_inv(239))).sqrt()
+
+
+def test_gelu_values_and_invariants():
+    # "Releases" v0.3.0 names GeGLU; GELU(g) = g * Phi(g) (textbook reading).
+    assert oracle.gelu(0.0) == 0.0
+    for x in (1.0, -1.0, 0.5, -2.25, 3.0, 6.0, -6.0):
+        ref = float(Decimal(x) * phi_decimal(x))
+        assert abs(oracle.gelu(x) - ref) <= 4e-15 * max(1.0, abs(ref)), x
+    # tabulated value: Phi(1) = 0.8413447460685429...
+    assert abs(oracle.gelu(1.0) - 0.8413447460685429) <= 2e-16
+    # GELU(x) - GELU(-x) = x; GELU(x) -> x for large x, -> 0 for very negative x
+    for x in np.linspace(-12, 12, 97):
+        assert abs(oracle.gelu(x) - oracle.gelu(-x) - x) <= 1e-14 * max(1.0, abs(x))
+    assert oracle.gelu(40.0) == 40.0
+    assert abs(oracle.gelu(-40.0)) < 1e-300
+
+
+@pytest.mark.parametrize("codec", synth.CODECS)
+def test_geglu_fused_equals_unfused(codec):
+    M, N = 5, 24
+    K = 256
+    X = synth.activations(M, K, seed=11)
+    Wg = synth.weights(codec, N, K, seed=11, name="Wg")
+    Wu = synth.weights(codec, N, K, seed=11, name="Wu")
+    fused = oracle.geglu(X, Wg, Wu, codec, M, N, K)
+    G = oracle.gemm(X, Wg, codec, M, N, K)
+    U = oracle.gemm(X, Wu, codec, M, N, K)
+    assert np.array_equal(fused, np.vectorize(oracle.gelu)(G) * U)
+    # and against an independent GELU (the series above) within rounding
+    ind = np.array([[float(Decimal(g) * phi_decimal(g, 60)) for g in row] for row in G]) * U
+    assert np.allclose(fused, ind, rtol=1e-13, atol=1e-300)
+    # the activation is applied to the gate, not to the up projection
+    assert not np.allclose(fused, G * np.vectorize(oracle.gelu)(U))
+
+
 # ------------------------------------------------------------ planted mistakes
 
 MUTATIONS = {
@@ -251,9 +328,14 @@ MUTATIONS = {
     "dropped_term": ("for (long long k = 0; k < K; ++k) s += a[k] * b[k];",
                      "for (long long k = 1; k < K; ++k) s += a[k] * b[k];"),
     "silu_sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
-    "silu_on_up": ("j->Y[r * j->N + n] = oracle_silu(g) * u;", "j->Y[r * j->N + n] = g * oracle_silu(u);"),
+    "silu_on_up": ("(j->act == ORACLE_ACT_GELU ? oracle_gelu(g) : oracle_silu(g)) * u;",
+                   "(j->act == ORACLE_ACT_GELU ? oracle_gelu(g) : g * oracle_silu(u) / u) * u;"),
     "half_rounding": ("double r = nearbyint(ldexp(a, 10 - E));", "double r = floor(ldexp(a, 10 - E));"),
     "unrounded_operands": ("    round_row_to_f16(w0, j->K);\n", "\n"),
+    "gelu_scale": ("return 0.5 * g * erfc(-g / sqrt(2.0));", "return 0.5 * g * erfc(-g / 2.0);"),
+    "gelu_half_missing": ("return 0.5 * g * erfc(-g / sqrt(2.0));", "return g * erfc(-g / sqrt(2.0));"),
+    "gelu_sign": ("return 0.5 * g * erfc(-g / sqrt(2.0));", "return 0.5 * g * erfc(g / sqrt(2.0));"),
+    "geglu_uses_silu": ("(j->act == ORACLE_ACT_GELU ? oracle_gelu(g) : oracle_silu(g))", "oracle_silu(g)"),
 }
 
 
@@ -267,6 +349,8 @@ def all_pins_pass(golden_blocks):
         lambda: [test_identity_and_permutation_readout(c) for c in synth.CODECS],
         test_silu_values_and_invariants,
         lambda: [test_swiglu_fused_equals_unfused(c) for c in synth.CODECS],
+        test_gelu_values_and_invariants,
+        lambda: [test_geglu_fused_equals_unfused(c) for c in synth.CODECS],
         lambda: test_q2_0_reserved_code_is_plus_two_d(),
     ]
     for c in checks:
