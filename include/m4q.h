@@ -10,7 +10,8 @@
  *    GEMV for decode-sized M and to a GEMM otherwise, across every codec.
  *  - "v0.1 vs v0.2 comparison", section 2.2 (Brick 3): the fused gate/up
  *    projection SiLU(X * Wg^T) x (X * Wu^T), computed on chip, writing only
- *    the final activation.
+ *    the final activation.  "Releases" v0.3.0 (TransformerBlock: SwiGLU /
+ *    GeGLU activations) adds the GELU-gated form, GELU(g) = g * Phi(g).
  *  - "Releases", v0.3.0, PrismML Q2_0 codec: 128 weights in 34 bytes,
  *    w = (q - 1) * d with the reserved code 3 decoding to +2d.  Q4_0 and Q8_0
  *    are GGUF's 32-weight blocks: w = (q - 8) * d and w = q * d.
@@ -30,7 +31,8 @@
  *    X, W, Wg, Wu, Y must be 16-byte aligned.
  *  - Arithmetic: every weight is decoded to fp16 as (q - z) * d rounded once
  *    to nearest even, products are accumulated in fp32, and each output is
- *    rounded once to fp16 (SiLU(g) * u is formed in fp32 first).
+ *    rounded once to fp16 (SiLU(g) * u or GELU(g) * u is formed in fp32
+ *    first).
  *  - Asynchrony: calls enqueue work on `stream` and return; argument errors
  *    are returned before anything is enqueued.  Launch failures return
  *    M4Q_ERR_CUDA.  Device-side failures (a pipeline wait that gave up) are
@@ -60,6 +62,12 @@ enum m4q_path {
   M4Q_PATH_TC = 2    /* tcgen05 tensor-core GEMM (any M) */
 };
 
+/* Activations of the gated projection (m4q_glu_ex). */
+enum m4q_act {
+  M4Q_ACT_SILU = 0, /* SiLU(g) = g / (1 + e^-g): SwiGLU */
+  M4Q_ACT_GELU = 1  /* GELU(g) = g * Phi(g) = g/2 * erfc(-g / sqrt 2): GeGLU */
+};
+
 /* Status codes returned by every call. */
 enum m4q_status {
   M4Q_OK = 0,
@@ -83,11 +91,38 @@ int m4q_gemm(const void* X, const void* W, int codec, int64_t M, int64_t N, int6
 int m4q_swiglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
                int64_t N, int64_t K, void* Y, m4q_stream_t stream);
 
+/* Y = GELU(X * Wg^T) x (X * Wu^T) ("Releases" v0.3.0, GeGLU); otherwise as
+ * m4q_swiglu. */
+int m4q_geglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
+              int64_t N, int64_t K, void* Y, m4q_stream_t stream);
+
 /* As m4q_gemm / m4q_swiglu, with the path chosen by the caller (enum m4q_path). */
 int m4q_gemm_ex(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K,
                 void* Y, int path, m4q_stream_t stream);
 int m4q_swiglu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
                   int64_t N, int64_t K, void* Y, int path, m4q_stream_t stream);
+
+/* The gated projection Y = act(X * Wg^T) x (X * Wu^T) with the activation
+ * (enum m4q_act) and the path (enum m4q_path) chosen by the caller.  An
+ * unknown act returns M4Q_ERR_INVALID_ARG. */
+int m4q_glu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
+               int64_t K, void* Y, int act, int path, m4q_stream_t stream);
+
+/* The gated MLP block of a transformer layer ("Releases" v0.3.0:
+ * TransformerBlock with SwiGLU / GeGLU activations):
+ *     H = act(X * Wg^T) x (X * Wu^T)      fp16 [M, F]
+ *     Y = H * Wd^T                         fp16 [M, D]
+ * enqueued as two launches on `stream` (the gated projection, then the down
+ * projection), each with the M <= 16 / tcgen05 dispatch of m4q_gemm.
+ * X is fp16 [M, D]; Wg, Wu are packed [F, D] in codec_gu; Wd is packed
+ * [D, F] in codec_d.  H is caller-provided device scratch of M * F fp16
+ * (16-byte aligned) that receives the intermediate activation; it may be
+ * reused once the call's work on `stream` has completed.  Shape rules of
+ * m4q_gemm apply to both projections (D and F multiples of 8 and of the
+ * block sizes).  act: enum m4q_act. */
+int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int codec_gu,
+            int codec_d, int64_t M, int64_t D, int64_t F, void* H, void* Y, int act,
+            m4q_stream_t stream);
 
 /* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
  * rounded once to nearest even.  The test hook for bit-exact decoding. */

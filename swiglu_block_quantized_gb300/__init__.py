@@ -9,12 +9,17 @@ sm_103, calls raise.
 Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     gemm(x, w, codec, n, k, out=None, path=PATH_AUTO)
     swiglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
+    geglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
+    glu(x, wg, wu, codec, n, k, act, out=None, path=PATH_AUTO)
+    mlp(x, wg, wu, wd, codec_gu, codec_d, d, f, act=ACT_SILU, h=None, out=None)
     dequant(w, codec, n, k, out=None)
     weight_bytes(codec, n, k), check_finite(t), check_device_status(),
     selftest_wait_timeout(limit_ns), status_string(code), version()
 and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
 flattened into M; M <= 16 streams the weights, larger M uses tcgen05), the
-analogue of the pages' M4QuantizedLinear ("Releases" v0.3.0).
+analogue of the pages' M4QuantizedLinear ("Releases" v0.3.0); ``QuantGLU``
+wraps the gated gate/up projection (SwiGLU or GeGLU) and ``QuantMLP`` the
+whole gated MLP block (gate/up then down, one stream).
 """
 from __future__ import annotations
 
@@ -27,6 +32,7 @@ CODECS = (Q4_0, Q8_0, Q2_0)
 BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34}
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+ACT_SILU, ACT_GELU = 0, 1
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -48,6 +54,9 @@ SIGNATURES = {
     "m4q_swiglu": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
     "m4q_gemm_ex": (_i32, [_vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_swiglu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "m4q_geglu": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
+    "m4q_glu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _i32, _vp]),
+    "m4q_mlp": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
@@ -150,8 +159,8 @@ def gemm(x, w, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stre
     return out
 
 
-def swiglu(x, wg, wu, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
-    """Y[M, n] = SiLU(X . Wg^T) * (X . Wu^T)."""
+def glu(x, wg, wu, codec: int, n: int, k: int, act: int, out=None, path: int = PATH_AUTO, stream=None):
+    """Y[M, n] = act(X . Wg^T) * (X . Wu^T), act = ACT_SILU or ACT_GELU."""
     import torch
     _require(x, torch.float16, "x")
     _packed_check(wg, codec, n, k, "wg")
@@ -160,8 +169,41 @@ def swiglu(x, wg, wu, codec: int, n: int, k: int, out=None, path: int = PATH_AUT
     if out is None:
         out = torch.empty((m, n), dtype=torch.float16, device=x.device)
     _require(out, torch.float16, "out")
-    _check(load().m4q_swiglu_ex(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), codec, m, n, k,
-                                out.data_ptr(), path, _stream_ptr(stream)), "m4q_swiglu")
+    _check(load().m4q_glu_ex(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), codec, m, n, k,
+                             out.data_ptr(), act, path, _stream_ptr(stream)), "m4q_glu_ex")
+    return out
+
+
+def swiglu(x, wg, wu, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
+    """Y[M, n] = SiLU(X . Wg^T) * (X . Wu^T)."""
+    return glu(x, wg, wu, codec, n, k, ACT_SILU, out=out, path=path, stream=stream)
+
+
+def geglu(x, wg, wu, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
+    """Y[M, n] = GELU(X . Wg^T) * (X . Wu^T)."""
+    return glu(x, wg, wu, codec, n, k, ACT_GELU, out=out, path=path, stream=stream)
+
+
+def mlp(x, wg, wu, wd, codec_gu: int, codec_d: int, d: int, f: int, act: int = ACT_SILU,
+        h=None, out=None, stream=None):
+    """Y[M, d] = (act(X Wg^T) * (X Wu^T)) Wd^T; Wg, Wu packed [f, d], Wd packed
+    [d, f].  h (fp16 [M, f]) receives the intermediate; allocated if None."""
+    import torch
+    _require(x, torch.float16, "x")
+    _packed_check(wg, codec_gu, f, d, "wg")
+    _packed_check(wu, codec_gu, f, d, "wu")
+    _packed_check(wd, codec_d, d, f, "wd")
+    m = x.numel() // d
+    if h is None:
+        h = torch.empty((m, f), dtype=torch.float16, device=x.device)
+    if out is None:
+        out = torch.empty((m, d), dtype=torch.float16, device=x.device)
+    _require(h, torch.float16, "h")
+    _require(out, torch.float16, "out")
+    if h.numel() < m * f:
+        raise ValueError("h holds %d elements, needs %d" % (h.numel(), m * f))
+    _check(load().m4q_mlp(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), wd.data_ptr(), codec_gu, codec_d,
+                          m, d, f, h.data_ptr(), out.data_ptr(), act, _stream_ptr(stream)), "m4q_mlp")
     return out
 
 
@@ -216,17 +258,52 @@ class QuantLinear:
         return y.reshape(*lead, self.out_features)
 
 
-class QuantSwiGLU:
-    """The fused gate/up projection SiLU(x Wg^T) * (x Wu^T)."""
+class QuantGLU:
+    """The fused gate/up projection act(x Wg^T) * (x Wu^T) (SwiGLU or GeGLU);
+    leading dims of x are flattened."""
 
-    def __init__(self, wg, wu, codec: int, out_features: int, in_features: int):
+    def __init__(self, wg, wu, codec: int, out_features: int, in_features: int, act: int = ACT_SILU):
         _packed_check(wg, codec, out_features, in_features, "wg")
         _packed_check(wu, codec, out_features, in_features, "wu")
-        self.wg, self.wu, self.codec = wg, wu, codec
+        self.wg, self.wu, self.codec, self.act = wg, wu, codec, act
         self.out_features, self.in_features = out_features, in_features
 
     def __call__(self, x):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.in_features)
-        y = swiglu(x2, self.wg, self.wu, self.codec, self.out_features, self.in_features)
+        y = glu(x2, self.wg, self.wu, self.codec, self.out_features, self.in_features, self.act)
         return y.reshape(*lead, self.out_features)
+
+
+class QuantSwiGLU(QuantGLU):
+    """The fused gate/up projection SiLU(x Wg^T) * (x Wu^T)."""
+
+    def __init__(self, wg, wu, codec: int, out_features: int, in_features: int):
+        super().__init__(wg, wu, codec, out_features, in_features, ACT_SILU)
+
+
+class QuantMLP:
+    """The gated MLP block: down(act(x Wg^T) * (x Wu^T)).  Wg, Wu: packed
+    [hidden_ff, hidden]; Wd: packed [hidden, hidden_ff].  The fp16
+    intermediate buffer is kept and reused across calls of the same M."""
+
+    def __init__(self, wg, wu, wd, codec_gu: int, codec_d: int, hidden: int, hidden_ff: int,
+                 act: int = ACT_SILU):
+        _packed_check(wg, codec_gu, hidden_ff, hidden, "wg")
+        _packed_check(wu, codec_gu, hidden_ff, hidden, "wu")
+        _packed_check(wd, codec_d, hidden, hidden_ff, "wd")
+        self.wg, self.wu, self.wd = wg, wu, wd
+        self.codec_gu, self.codec_d, self.act = codec_gu, codec_d, act
+        self.hidden, self.hidden_ff = hidden, hidden_ff
+        self._h = None
+
+    def __call__(self, x):
+        import torch
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.hidden)
+        m = x2.shape[0]
+        if self._h is None or self._h.shape[0] != m or self._h.device != x2.device:
+            self._h = torch.empty((m, self.hidden_ff), dtype=torch.float16, device=x2.device)
+        y = mlp(x2, self.wg, self.wu, self.wd, self.codec_gu, self.codec_d, self.hidden, self.hidden_ff,
+                act=self.act, h=self._h)
+        return y.reshape(*lead, self.hidden)

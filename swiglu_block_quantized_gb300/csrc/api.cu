@@ -108,8 +108,9 @@ int check_shape(int codec, int64_t M, int64_t N, int64_t K) {
 // ------------------------------------------------------------ dispatch
 
 int project(const void* X, const void* W0, const void* W1, int codec, int64_t M, int64_t N,
-            int64_t K, void* Y, int path, bool swiglu, m4q_stream_t stream) {
+            int64_t K, void* Y, int path, bool swiglu, int act, m4q_stream_t stream) {
   if (!X || !W0 || !Y || (swiglu && !W1)) return M4Q_ERR_INVALID_ARG;
+  if (act != M4Q_ACT_SILU && act != M4Q_ACT_GELU) return M4Q_ERR_INVALID_ARG;
   int rc = check_shape(codec, M, N, K);
   if (rc != M4Q_OK) return rc;
   if (path < M4Q_PATH_AUTO || path > M4Q_PATH_TC) return M4Q_ERR_INVALID_ARG;
@@ -131,6 +132,7 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
   L.K = (int)K;
   L.row_bytes = (K / kBlock[codec]) * (long long)kBlockBytes[codec];
   L.swiglu = swiglu;
+  L.act = act;
   L.wtma = (L.row_bytes % 16) == 0;  // then K is a multiple of the packed stage
   L.status = m4q::status_words();
   if (!L.status) return M4Q_ERR_CUDA;
@@ -192,22 +194,47 @@ extern "C" {
 
 int m4q_gemm_ex(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K, void* Y,
                 int path, m4q_stream_t stream) {
-  return project(X, W, nullptr, codec, M, N, K, Y, path, false, stream);
+  return project(X, W, nullptr, codec, M, N, K, Y, path, false, M4Q_ACT_SILU, stream);
 }
 
 int m4q_swiglu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
                   int64_t K, void* Y, int path, m4q_stream_t stream) {
-  return project(X, Wg, Wu, codec, M, N, K, Y, path, true, stream);
+  return project(X, Wg, Wu, codec, M, N, K, Y, path, true, M4Q_ACT_SILU, stream);
+}
+
+int m4q_glu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
+               int64_t K, void* Y, int act, int path, m4q_stream_t stream) {
+  return project(X, Wg, Wu, codec, M, N, K, Y, path, true, act, stream);
+}
+
+int m4q_geglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
+              int64_t K, void* Y, m4q_stream_t stream) {
+  return project(X, Wg, Wu, codec, M, N, K, Y, M4Q_PATH_AUTO, true, M4Q_ACT_GELU, stream);
 }
 
 int m4q_gemm(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K, void* Y,
              m4q_stream_t stream) {
-  return project(X, W, nullptr, codec, M, N, K, Y, M4Q_PATH_AUTO, false, stream);
+  return project(X, W, nullptr, codec, M, N, K, Y, M4Q_PATH_AUTO, false, M4Q_ACT_SILU, stream);
 }
 
 int m4q_swiglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
                int64_t K, void* Y, m4q_stream_t stream) {
-  return project(X, Wg, Wu, codec, M, N, K, Y, M4Q_PATH_AUTO, true, stream);
+  return project(X, Wg, Wu, codec, M, N, K, Y, M4Q_PATH_AUTO, true, M4Q_ACT_SILU, stream);
+}
+
+int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int codec_gu,
+            int codec_d, int64_t M, int64_t D, int64_t F, void* H, void* Y, int act,
+            m4q_stream_t stream) {
+  if (!H || !Wd) return M4Q_ERR_INVALID_ARG;
+  // Validate both projections before enqueueing either.
+  int rc = check_shape(codec_gu, M, F, D);
+  if (rc != M4Q_OK) return rc;
+  rc = check_shape(codec_d, M, D, F);
+  if (rc != M4Q_OK) return rc;
+  if (!aligned16(H) || !aligned16(Wd)) return M4Q_ERR_MISALIGNED;
+  rc = project(X, Wg, Wu, codec_gu, M, F, D, H, M4Q_PATH_AUTO, true, act, stream);
+  if (rc != M4Q_OK) return rc;
+  return project(H, Wd, nullptr, codec_d, M, D, F, Y, M4Q_PATH_AUTO, false, M4Q_ACT_SILU, stream);
 }
 
 size_t m4q_weight_bytes(int codec, int64_t N, int64_t K) {

@@ -24,6 +24,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// GELU(g) = g * Phi(g) = g/2 * erfc(-g / sqrt 2), in fp32 (the GeGLU gate).
+__device__ __forceinline__ float gelu_f(float g) { return 0.5f * g * erfcf(-g * 0.70710678118654752f); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

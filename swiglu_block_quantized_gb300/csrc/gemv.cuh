@@ -54,6 +54,7 @@ struct GemvParams {
   int pp;              // shared-memory pitch of a row pair: 2 sb + 16
   int ring;            // stages in the ring
   int units;           // 16-output units
+  int act;             // SwiGLU units: gate activation, 0 SiLU, 1 GELU
   uint32_t* status;
   unsigned long long limit_ns;
 };
@@ -429,8 +430,8 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
             if (m >= p.M) continue;
             float a = v[0][mt][c], b = v[0][mt][c + 2];
             if constexpr (SWIGLU) {
-              a = (a / (1.0f + __expf(-a))) * v[NM - 1][mt][c];
-              b = (b / (1.0f + __expf(-b))) * v[NM - 1][mt][c + 2];
+              a = (p.act ? gelu_f(a) : a / (1.0f + __expf(-a))) * v[NM - 1][mt][c];
+              b = (p.act ? gelu_f(b) : b / (1.0f + __expf(-b))) * v[NM - 1][mt][c + 2];
             }
             *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(a, b);
           }

@@ -19,7 +19,8 @@ struct ProjLaunch {
   void* y;                // fp16 [M, N]
   int M, N, K;
   long long row_bytes;
-  bool swiglu;
+  bool swiglu;            // gated projection (gate and up weights)
+  int act;                // gate activation: 0 SiLU, 1 GELU
   bool wtma;              // packed rows are 16-byte multiples: weights move by TMA
   uint32_t* status;       // device status word
   unsigned long long limit_ns;

@@ -9,11 +9,12 @@
 
 namespace m4q {
 
-template <int C, bool SWIGLU, int NX, bool WTMA>
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
 cudaError_t launch_tc_one(const ProjLaunch& L) {
   using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
-  auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA>;
-  std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 1, C, SWIGLU, NX, WTMA>>();
+  auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA, ACT>;
+  std::atomic<unsigned long long>& configured =
+      attr_flag<std::integer_sequence<int, 1, C, SWIGLU, NX, WTMA, ACT>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -39,23 +40,32 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   return cudaGetLastError();
 }
 
-template <int C, bool SWIGLU, bool WTMA>
+template <int C, bool SWIGLU, bool WTMA, int ACT>
 cudaError_t launch_tc_nx(const ProjLaunch& L) {
   switch (L.nx) {
-    case 256: return launch_tc_one<C, SWIGLU, 256, WTMA>(L);
-    case 128: return launch_tc_one<C, SWIGLU, 128, WTMA>(L);
-    default: return launch_tc_one<C, SWIGLU, 64, WTMA>(L);
+    case 256: return launch_tc_one<C, SWIGLU, 256, WTMA, ACT>(L);
+    case 128: return launch_tc_one<C, SWIGLU, 128, WTMA, ACT>(L);
+    default: return launch_tc_one<C, SWIGLU, 64, WTMA, ACT>(L);
   }
+}
+
+// The gate activation is a template argument: the SiLU epilogue stays
+// exactly as it is without the GELU code beside it.
+template <int C, bool WTMA>
+cudaError_t launch_tc_glu(const ProjLaunch& L) {
+  return L.act ? launch_tc_nx<C, true, WTMA, 1>(L) : launch_tc_nx<C, true, WTMA, 0>(L);
 }
 
 template <int C>
 cudaError_t launch_tc_impl(const ProjLaunch& L) {
   if (L.wtma) {
-    return L.swiglu ? launch_tc_nx<C, true, true>(L) : launch_tc_nx<C, false, true>(L);
+    return L.swiglu ? launch_tc_glu<C, true>(L) : launch_tc_nx<C, false, true, 0>(L);
   }
   // Shapes whose packed rows are not 16-byte multiples: weights are read with
   // plain loads; one tile width suffices for this path.
-  return L.swiglu ? launch_tc_one<C, true, 128, false>(L) : launch_tc_one<C, false, 128, false>(L);
+  if (L.swiglu)
+    return L.act ? launch_tc_one<C, true, 128, false, 1>(L) : launch_tc_one<C, true, 128, false, 0>(L);
+  return launch_tc_one<C, false, 128, false, 0>(L);
 }
 
 }  // namespace m4q

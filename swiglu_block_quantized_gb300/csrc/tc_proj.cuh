@@ -205,7 +205,7 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
 // tcgen05.ld round trips.
 // GEMM: per 32-column chunk, fp16 rounding, group-wide staging and store;
 // D is released after the last chunk load.
-template <int C, bool SWIGLU, int NX, bool WTMA>
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
 __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                               const WaitCtl& ctl, const CUtensorMap* tm_y, int warp,
                                               int E) {
@@ -247,7 +247,7 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
             const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
             const float g = odd ? recv : a;
             const float u = odd ? b : recv;
-            y[h] = __fdividef(g, 1.0f + __expf(-g)) * u;
+            y[h] = (ACT ? gelu_f(g) : __fdividef(g, 1.0f + __expf(-g))) * u;
           }
           const __half2 hy = __floats2half2_rn(y[0], y[1]);
           y2[ch][jj / 2] = *reinterpret_cast<const uint32_t*>(&hy);
@@ -341,7 +341,8 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
   if (leader) bulk_wait_all();
 }
 
-template <int C, bool SWIGLU, int NX, bool WTMA>
+// ACT (gated projections): 0 SiLU, 1 GELU.
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
 __global__ void __launch_bounds__(640, 1)
     tc_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                    const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(640, 1)
   } else if (warp >= 8 && warp < 12) {
     decode_role<C, SWIGLU, NX, WTMA, 1>(sm, p, tmem, ctl, warp);
   } else if (warp >= 12) {
-    epilogue_role<C, SWIGLU, NX, WTMA>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
+    epilogue_role<C, SWIGLU, NX, WTMA, ACT>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
   }
 
   tc_fence_before();

@@ -71,6 +71,16 @@ def test_argument_errors_return_before_any_cuda_call(lib):
     assert lib.m4q_swiglu(P(good), P(good), P(good + 4), 0, 4, 8, 32, P(good), s) == m.ERR_MISALIGNED
     assert lib.m4q_gemm_ex(P(good), P(good), 0, 17, 8, 32, P(good), m.PATH_GEMV, s) == m.ERR_INVALID_ARG
     assert lib.m4q_gemm_ex(P(good), P(good), 0, 4, 8, 32, P(good), 7, s) == m.ERR_INVALID_ARG
+    assert lib.m4q_glu_ex(P(good), P(good), P(good), 0, 4, 8, 32, P(good), 2, 0, s) == m.ERR_INVALID_ARG  # act
+    assert lib.m4q_glu_ex(P(good), P(good), P(good), 0, 4, 8, 32, P(good), -1, 0, s) == m.ERR_INVALID_ARG
+    assert lib.m4q_geglu(P(good), P(good), None, 0, 4, 8, 32, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_geglu(P(good), P(good), P(good), 0, 4, 12, 32, P(good), s) == m.ERR_BAD_SHAPE
+    # m4q_mlp validates both projections before enqueueing anything
+    assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 128, None, P(good), 0, s) == m.ERR_INVALID_ARG
+    assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 132, P(good), P(good), 0, s) == m.ERR_BAD_SHAPE
+    assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 2, 4, 64, 192, P(good), P(good), 0, s) == m.ERR_BAD_SHAPE
+    assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 128, P(good + 8), P(good), 0, s) == m.ERR_MISALIGNED
+    assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 128, P(good), P(good), 5, s) == m.ERR_INVALID_ARG
     assert lib.m4q_dequant(None, 0, 8, 32, P(good), s) == m.ERR_INVALID_ARG
     assert lib.m4q_dequant(P(good), 0, 8, 40, P(good), s) == m.ERR_BAD_SHAPE
     assert lib.m4q_check_finite(None, 10, s) == m.ERR_INVALID_ARG

@@ -119,6 +119,59 @@ def test_tc_tile_widths():
         assert_close(Y[rows], oracle.gemm(X, W, synth.Q4_0, M, N, K, rows=rows), "tile M=%d" % M)
 
 
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("general", [False, True])
+@pytest.mark.parametrize("M", [1, 9, 20, 257])
+def test_geglu_parity(codec, general, M):
+    # GELU-gated projection on both paths (M <= 16: GEMV, else tcgen05).
+    for K in kvals(codec, general)[:1]:
+        N = 200
+        X = synth.activations(M, K, seed=M + 3)
+        Wg = synth.weights(codec, N, K, seed=K + 5, name="Wg")
+        Wu = synth.weights(codec, N, K, seed=K + 5, name="Wu")
+        Y = host(m.geglu(dev(X), dev(Wg), dev(Wu), codec, N, K))
+        assert_close(Y, oracle.geglu(X, Wg, Wu, codec, M, N, K), "geglu %s M=%d K=%d" % (codec, M, K))
+        # the same through the explicit-activation entry point on the other path
+        path = m.PATH_TC if M <= 16 else m.PATH_AUTO
+        Y2 = host(m.glu(dev(X), dev(Wg), dev(Wu), codec, N, K, m.ACT_GELU, path=path))
+        assert_close(Y2, oracle.geglu(X, Wg, Wu, codec, M, N, K), "glu gelu %s M=%d" % (codec, M))
+
+
+def test_quant_glu_layer():
+    K, N = 256, 64
+    Wg = synth.weights(synth.Q8_0, N, K, seed=18, name="Wg")
+    Wu = synth.weights(synth.Q8_0, N, K, seed=18, name="Wu")
+    X = synth.activations(2 * 7, K, seed=19)
+    for act, ref in ((m.ACT_SILU, oracle.swiglu), (m.ACT_GELU, oracle.geglu)):
+        layer = m.QuantGLU(dev(Wg), dev(Wu), synth.Q8_0, N, K, act=act)
+        y = layer(dev(X).reshape(2, 7, K))
+        assert tuple(y.shape) == (2, 7, N)
+        assert_close(host(y).reshape(-1, N), ref(X, Wg, Wu, synth.Q8_0, 14, N, K), "QuantGLU act=%d" % act)
+
+
+def mlp_reference(X, Wg, Wu, Wd, cgu, cd, M, D, F, act):
+    """Oracle composition of the MLP block: the gated projection, its output
+    rounded to fp16 (the intermediate the library materialises), then the
+    down projection."""
+    glu_ref = oracle.geglu if act == m.ACT_GELU else oracle.swiglu
+    H16 = glu_ref(X, Wg, Wu, cgu, M, F, D).astype(np.float16)
+    return oracle.gemm(H16, Wd, cd, M, D, F)
+
+
+@pytest.mark.parametrize("M", [1, 3, 40])
+@pytest.mark.parametrize("cgu,cd", [(synth.Q4_0, synth.Q4_0), (synth.Q4_0, synth.Q8_0), (synth.Q2_0, synth.Q8_0)])
+@pytest.mark.parametrize("act", [0, 1])
+def test_mlp_parity(M, cgu, cd, act):
+    D, F = 256, 1024
+    X = synth.activations(M, D, seed=M + 30)
+    Wg = synth.weights(cgu, F, D, seed=31, name="Wg")
+    Wu = synth.weights(cgu, F, D, seed=31, name="Wu")
+    Wd = synth.weights(cd, D, F, seed=32, name="Wd")
+    layer = m.QuantMLP(dev(Wg), dev(Wu), dev(Wd), cgu, cd, D, F, act=act)
+    Y = host(layer(dev(X)))
+    assert_close(Y, mlp_reference(X, Wg, Wu, Wd, cgu, cd, M, D, F, act), "mlp M=%d %s/%s act=%d" % (M, cgu, cd, act))
+
+
 # ------------------------------------------------------------ GEMV path
 
 @pytest.mark.parametrize("codec", CODECS)
