@@ -78,7 +78,8 @@ enum m4q_status {
   M4Q_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
   M4Q_ERR_NONFINITE = -6,          /* m4q_check_finite found NaN/Inf */
   M4Q_ERR_TIMEOUT = -7,            /* a device pipeline wait gave up */
-  M4Q_ERR_UNSUPPORTED_DEVICE = -8  /* the current device is not sm_103 */
+  M4Q_ERR_UNSUPPORTED_DEVICE = -8, /* the current device is not sm_103 */
+  M4Q_ERR_SCRATCH_LIMIT = -9       /* m4q_mlp_noalloc: M * F above its fixed scratch */
 };
 
 /* Y = X * W^T.  Dispatch: M <= 16 takes the GEMV path, else the tcgen05
@@ -123,6 +124,23 @@ int m4q_glu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t
 int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int codec_gu,
             int codec_d, int64_t M, int64_t D, int64_t F, void* H, void* Y, int act,
             m4q_stream_t stream);
+
+/* m4q_mlp for callers that cannot allocate device memory (a runtime that
+ * owns all device memory and gives plug-ins no allocator, or a loop that must
+ * not call cudaMalloc, which may synchronize the device).  The pages have no
+ * counterpart: this is a deployment variant of m4q_mlp.  Same arguments and
+ * result as m4q_mlp without H: the fp16 intermediate is kept in one fixed
+ * device array of the library, 1 << 20 elements (2 MiB, held on every GPU
+ * that loads the library until the process exits).  M * F above that returns
+ * M4Q_ERR_SCRATCH_LIMIT before anything is enqueued.  The call allocates
+ * nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and should come before any stream capture on that
+ * device.  All calls share the array: each one overwrites the part it uses
+ * before reading it, but calls whose work overlaps on the GPU (no stream
+ * order between them) race. */
+int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* Wd, int codec_gu,
+                    int codec_d, int64_t M, int64_t D, int64_t F, void* Y, int act,
+                    m4q_stream_t stream);
 
 /* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
  * rounded once to nearest even.  The test hook for bit-exact decoding. */

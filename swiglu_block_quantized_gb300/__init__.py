@@ -43,6 +43,7 @@ ERR_CUDA = -5
 ERR_NONFINITE = -6
 ERR_TIMEOUT = -7
 ERR_UNSUPPORTED_DEVICE = -8
+ERR_SCRATCH_LIMIT = -9
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libm4q.so")
@@ -57,6 +58,7 @@ SIGNATURES = {
     "m4q_geglu": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
     "m4q_glu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _i32, _vp]),
     "m4q_mlp": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp]),
+    "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),

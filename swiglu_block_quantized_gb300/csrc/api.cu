@@ -309,6 +309,7 @@ const char* m4q_status_string(int status) {
     case M4Q_ERR_NONFINITE: return "non-finite values found";
     case M4Q_ERR_TIMEOUT: return "a device pipeline wait gave up";
     case M4Q_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+    case M4Q_ERR_SCRATCH_LIMIT: return "M * F exceeds the fixed scratch of m4q_mlp_noalloc (1 << 20 fp16)";
     default: return "unknown status";
   }
 }
