@@ -92,6 +92,18 @@ int m4q_gemm(const void* X, const void* W, int codec, int64_t M, int64_t N, int6
 int m4q_swiglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,
                int64_t N, int64_t K, void* Y, m4q_stream_t stream);
 
+/* Y = X * W^T written head-major: Y[h][m][d] = (X * W^T)[m][h * head_dim + d],
+ * Y fp16 [N / head_dim][M][head_dim], so each head's [M, head_dim] block is
+ * contiguous and attention reads it without a transpose ("v0.1 vs v0.2
+ * comparison" section 4 and "Releases" v0.2.1: direct-head [H, M, D]
+ * projection).  head_dim is 64 or 128 (else M4Q_ERR_INVALID_ARG) and must
+ * divide N (else M4Q_ERR_BAD_SHAPE).  A fused Q/K/V projection is one call
+ * on the row concatenation of Wq, Wk and Wv (packed rows are independent, so
+ * concatenating the packed matrices concatenates the rows): the first
+ * N_q / head_dim heads of Y are Q, then K, then V.  Otherwise as m4q_gemm. */
+int m4q_gemm_heads(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K,
+                   int64_t head_dim, void* Y, m4q_stream_t stream);
+
 /* Y = GELU(X * Wg^T) x (X * Wu^T) ("Releases" v0.3.0, GeGLU); otherwise as
  * m4q_swiglu. */
 int m4q_geglu(const void* X, const void* Wg, const void* Wu, int codec, int64_t M,

@@ -8,6 +8,7 @@ sm_103, calls raise.
 
 Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     gemm(x, w, codec, n, k, out=None, path=PATH_AUTO)
+    gemm_heads(x, w, codec, n, k, head_dim, out=None)
     swiglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
     geglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
     glu(x, wg, wu, codec, n, k, act, out=None, path=PATH_AUTO)
@@ -18,8 +19,9 @@ Functions mirror the C ABI (same names without the ``m4q_`` prefix):
 and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
 flattened into M; M <= 16 streams the weights, larger M uses tcgen05), the
 analogue of the pages' M4QuantizedLinear ("Releases" v0.3.0); ``QuantGLU``
-wraps the gated gate/up projection (SwiGLU or GeGLU) and ``QuantMLP`` the
-whole gated MLP block (gate/up then down, one stream).
+wraps the gated gate/up projection (SwiGLU or GeGLU), ``QuantMLP`` the
+whole gated MLP block (gate/up then down, one stream) and ``QuantQKV`` the
+fused Q/K/V projection with head-major outputs.
 """
 from __future__ import annotations
 
@@ -56,6 +58,7 @@ SIGNATURES = {
     "m4q_gemm_ex": (_i32, [_vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_swiglu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_geglu": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp]),
+    "m4q_gemm_heads": (_i32, [_vp, _vp, _i32, _i64, _i64, _i64, _i64, _vp, _vp]),
     "m4q_glu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _i32, _vp]),
     "m4q_mlp": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp]),
     "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
@@ -158,6 +161,20 @@ def gemm(x, w, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stre
     _require(out, torch.float16, "out")
     _check(load().m4q_gemm_ex(x.data_ptr(), w.data_ptr(), codec, m, n, k, out.data_ptr(),
                               path, _stream_ptr(stream)), "m4q_gemm")
+    return out
+
+
+def gemm_heads(x, w, codec: int, n: int, k: int, head_dim: int, out=None, stream=None):
+    """Y[n / head_dim, M, head_dim] with Y[h, m, d] = (X . W^T)[m, h * head_dim + d]."""
+    import torch
+    _require(x, torch.float16, "x")
+    _packed_check(w, codec, n, k, "w")
+    m = x.numel() // k
+    if out is None:
+        out = torch.empty((n // head_dim, m, head_dim), dtype=torch.float16, device=x.device)
+    _require(out, torch.float16, "out")
+    _check(load().m4q_gemm_heads(x.data_ptr(), w.data_ptr(), codec, m, n, k, head_dim, out.data_ptr(),
+                                 _stream_ptr(stream)), "m4q_gemm_heads")
     return out
 
 
@@ -309,3 +326,25 @@ class QuantMLP:
         y = mlp(x2, self.wg, self.wu, self.wd, self.codec_gu, self.codec_d, self.hidden, self.hidden_ff,
                 act=self.act, h=self._h)
         return y.reshape(*lead, self.hidden)
+
+
+class QuantQKV:
+    """Fused Q/K/V projection: one GEMM on the row concatenation of Wq [hq * hd,
+    hidden], Wk and Wv [hkv * hd, hidden], written head-major, returning the
+    views q [hq, M, hd], k [hkv, M, hd], v [hkv, M, hd] (no transposes)."""
+
+    def __init__(self, wq, wk, wv, codec: int, hidden: int, head_dim: int, q_heads: int, kv_heads: int):
+        import torch
+        _packed_check(wq, codec, q_heads * head_dim, hidden, "wq")
+        _packed_check(wk, codec, kv_heads * head_dim, hidden, "wk")
+        _packed_check(wv, codec, kv_heads * head_dim, hidden, "wv")
+        self.w = torch.cat([wq, wk, wv]).contiguous()
+        self.codec, self.hidden, self.head_dim = codec, hidden, head_dim
+        self.q_heads, self.kv_heads = q_heads, kv_heads
+
+    def __call__(self, x):
+        x2 = x.reshape(-1, self.hidden)
+        n = (self.q_heads + 2 * self.kv_heads) * self.head_dim
+        y = gemm_heads(x2, self.w, self.codec, n, self.hidden, self.head_dim)
+        hq, hk = self.q_heads, self.kv_heads
+        return y[:hq], y[hq:hq + hk], y[hq + hk:]

@@ -93,6 +93,20 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Head-major Y [N / hd][M][hd] as a 3-D tensor (d, m, head), boxes of
+// [128 / hd heads][32 m][hd] (one staged GEMM chunk of 128 outputs).
+bool encode_heads(CUtensorMap* map, const void* base, uint64_t M, uint64_t N, uint32_t hd) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {hd, M, N / hd};
+  const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)M * hd * 2};
+  const cuuint32_t box[3] = {hd, 32, 128 / hd};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ validation
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -108,9 +122,12 @@ int check_shape(int codec, int64_t M, int64_t N, int64_t K) {
 // ------------------------------------------------------------ dispatch
 
 int project(const void* X, const void* W0, const void* W1, int codec, int64_t M, int64_t N,
-            int64_t K, void* Y, int path, bool swiglu, int act, m4q_stream_t stream) {
+            int64_t K, void* Y, int path, bool swiglu, int act, m4q_stream_t stream,
+            int64_t head_dim = 0) {
   if (!X || !W0 || !Y || (swiglu && !W1)) return M4Q_ERR_INVALID_ARG;
   if (act != M4Q_ACT_SILU && act != M4Q_ACT_GELU) return M4Q_ERR_INVALID_ARG;
+  if (head_dim != 0 && (swiglu || (head_dim != 64 && head_dim != 128))) return M4Q_ERR_INVALID_ARG;
+  if (head_dim != 0 && N % head_dim != 0) return M4Q_ERR_BAD_SHAPE;
   int rc = check_shape(codec, M, N, K);
   if (rc != M4Q_OK) return rc;
   if (path < M4Q_PATH_AUTO || path > M4Q_PATH_TC) return M4Q_ERR_INVALID_ARG;
@@ -133,6 +150,7 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
   L.row_bytes = (K / kBlock[codec]) * (long long)kBlockBytes[codec];
   L.swiglu = swiglu;
   L.act = act;
+  L.head_dim = (int)head_dim;
   L.wtma = (L.row_bytes % 16) == 0;  // then K is a multiple of the packed stage
   L.status = m4q::status_words();
   if (!L.status) return M4Q_ERR_CUDA;
@@ -164,9 +182,13 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
       return M4Q_ERR_CUDA;
     // Y boxes: GEMM stages [32 m][128 n] chunks per warpgroup; SwiGLU stores
     // one [nx/2 m][16 n] slab per epilogue warp.
-    if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2, swiglu ? 16u : (uint32_t)out_rows,
-                   swiglu ? (uint32_t)(nx / 2) : 32u, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (head_dim != 0) {
+      if (!encode_heads(&L.tm_y, Y, M, N, (uint32_t)head_dim)) return M4Q_ERR_CUDA;
+    } else if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2,
+                          swiglu ? 16u : (uint32_t)out_rows, swiglu ? (uint32_t)(nx / 2) : 32u,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) {
       return M4Q_ERR_CUDA;
+    }
     L.tm_w0 = L.tm_x;
     L.tm_w1 = L.tm_x;
     if (L.wtma) {
@@ -200,6 +222,12 @@ int m4q_gemm_ex(const void* X, const void* W, int codec, int64_t M, int64_t N, i
 int m4q_swiglu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,
                   int64_t K, void* Y, int path, m4q_stream_t stream) {
   return project(X, Wg, Wu, codec, M, N, K, Y, path, true, M4Q_ACT_SILU, stream);
+}
+
+int m4q_gemm_heads(const void* X, const void* W, int codec, int64_t M, int64_t N, int64_t K,
+                   int64_t head_dim, void* Y, m4q_stream_t stream) {
+  if (head_dim == 0) return M4Q_ERR_INVALID_ARG;
+  return project(X, W, nullptr, codec, M, N, K, Y, M4Q_PATH_AUTO, false, M4Q_ACT_SILU, stream, head_dim);
 }
 
 int m4q_glu_ex(const void* X, const void* Wg, const void* Wu, int codec, int64_t M, int64_t N,

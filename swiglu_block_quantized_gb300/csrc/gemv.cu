@@ -48,6 +48,7 @@ cudaError_t launch_gemv_mt(const ProjLaunch& L) {
   if (SWIGLU) p.ring &= ~1;  // gate and up tiles of a segment sit in adjacent slots
   p.units = (L.N + 15) / 16;
   p.act = L.act;
+  p.head_dim = L.head_dim;
   p.status = L.status;
   p.limit_ns = L.limit_ns;
   // X fragments stay in registers when the row is exactly one full stage

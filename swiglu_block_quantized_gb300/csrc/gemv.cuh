@@ -55,6 +55,7 @@ struct GemvParams {
   int ring;            // stages in the ring
   int units;           // 16-output units
   int act;             // SwiGLU units: gate activation, 0 SiLU, 1 GELU
+  int head_dim;        // GEMM: 0 row-major Y, else head-major Y[N / head_dim][M][head_dim]
   uint32_t* status;
   unsigned long long limit_ns;
 };
@@ -433,7 +434,10 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
               a = (p.act ? gelu_f(a) : a / (1.0f + __expf(-a))) * v[NM - 1][mt][c];
               b = (p.act ? gelu_f(b) : b / (1.0f + __expf(-b))) * v[NM - 1][mt][c + 2];
             }
-            *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(a, b);
+            // outputs n, n + 1 (same head: n is even and head_dim is too)
+            const size_t off = p.head_dim == 0 ? (size_t)m * p.N + n
+                                               : ((size_t)(n / p.head_dim) * p.M + m) * p.head_dim + n % p.head_dim;
+            *reinterpret_cast<__half2*>(p.y + off) = __floats2half2_rn(a, b);
           }
       }
     }

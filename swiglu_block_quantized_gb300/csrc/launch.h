@@ -21,6 +21,7 @@ struct ProjLaunch {
   long long row_bytes;
   bool swiglu;            // gated projection (gate and up weights)
   int act;                // gate activation: 0 SiLU, 1 GELU
+  int head_dim;           // GEMM output: 0 row-major [M, N], else head-major [N / head_dim][M][head_dim]
   bool wtma;              // packed rows are 16-byte multiples: weights move by TMA
   uint32_t* status;       // device status word
   unsigned long long limit_ns;

@@ -9,12 +9,12 @@
 
 namespace m4q {
 
-template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT, int HD>
 cudaError_t launch_tc_one(const ProjLaunch& L) {
   using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
-  auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA, ACT>;
+  auto kern = tc_proj_kernel<C, SWIGLU, NX, WTMA, ACT, HD>;
   std::atomic<unsigned long long>& configured =
-      attr_flag<std::integer_sequence<int, 1, C, SWIGLU, NX, WTMA, ACT>>();
+      attr_flag<std::integer_sequence<int, 1, C, SWIGLU, NX, WTMA, ACT, HD>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -40,12 +40,22 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   return cudaGetLastError();
 }
 
-template <int C, bool SWIGLU, bool WTMA, int ACT>
+template <int C, bool SWIGLU, bool WTMA, int ACT, int HD>
 cudaError_t launch_tc_nx(const ProjLaunch& L) {
   switch (L.nx) {
-    case 256: return launch_tc_one<C, SWIGLU, 256, WTMA, ACT>(L);
-    case 128: return launch_tc_one<C, SWIGLU, 128, WTMA, ACT>(L);
-    default: return launch_tc_one<C, SWIGLU, 64, WTMA, ACT>(L);
+    case 256: return launch_tc_one<C, SWIGLU, 256, WTMA, ACT, HD>(L);
+    case 128: return launch_tc_one<C, SWIGLU, 128, WTMA, ACT, HD>(L);
+    default: return launch_tc_one<C, SWIGLU, 64, WTMA, ACT, HD>(L);
+  }
+}
+
+// GEMM: row-major Y or the direct-head layout for head dim 64 or 128.
+template <int C, bool WTMA>
+cudaError_t launch_tc_gemm(const ProjLaunch& L) {
+  switch (L.head_dim) {
+    case 64: return launch_tc_nx<C, false, WTMA, 0, 64>(L);
+    case 128: return launch_tc_nx<C, false, WTMA, 0, 128>(L);
+    default: return launch_tc_nx<C, false, WTMA, 0, 0>(L);
   }
 }
 
@@ -53,19 +63,23 @@ cudaError_t launch_tc_nx(const ProjLaunch& L) {
 // exactly as it is without the GELU code beside it.
 template <int C, bool WTMA>
 cudaError_t launch_tc_glu(const ProjLaunch& L) {
-  return L.act ? launch_tc_nx<C, true, WTMA, 1>(L) : launch_tc_nx<C, true, WTMA, 0>(L);
+  return L.act ? launch_tc_nx<C, true, WTMA, 1, 0>(L) : launch_tc_nx<C, true, WTMA, 0, 0>(L);
 }
 
 template <int C>
 cudaError_t launch_tc_impl(const ProjLaunch& L) {
   if (L.wtma) {
-    return L.swiglu ? launch_tc_glu<C, true>(L) : launch_tc_nx<C, false, true, 0>(L);
+    return L.swiglu ? launch_tc_glu<C, true>(L) : launch_tc_gemm<C, true>(L);
   }
   // Shapes whose packed rows are not 16-byte multiples: weights are read with
   // plain loads; one tile width suffices for this path.
   if (L.swiglu)
-    return L.act ? launch_tc_one<C, true, 128, false, 1>(L) : launch_tc_one<C, true, 128, false, 0>(L);
-  return launch_tc_one<C, false, 128, false, 0>(L);
+    return L.act ? launch_tc_one<C, true, 128, false, 1, 0>(L) : launch_tc_one<C, true, 128, false, 0, 0>(L);
+  switch (L.head_dim) {
+    case 64: return launch_tc_one<C, false, 128, false, 0, 64>(L);
+    case 128: return launch_tc_one<C, false, 128, false, 0, 128>(L);
+    default: return launch_tc_one<C, false, 128, false, 0, 0>(L);
+  }
 }
 
 }  // namespace m4q

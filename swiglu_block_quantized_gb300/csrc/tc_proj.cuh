@@ -25,6 +25,10 @@
 //     columns: tcgen05.ld of D (D is released to the next tile as soon as it
 //     is read), fp16 rounding or SiLU(g)*u, staging in shared memory and TMA
 //     bulk stores of Y.
+//   * Direct-head output (GEMM, HD = head dim 64 or 128): each staged chunk
+//     is laid out [heads][32 m][HD] and stored with a 3-D TMA box into
+//     Y[N / HD][M][HD], so a Q/K/V projection needs no transpose afterwards
+//     ("v0.1 vs v0.2 comparison" section 4, v0.2.1 direct-head layout).
 //   * SwiGLU: A row 2i is gate row n0+i and row 2i+1 the up row of the same
 //     output, so one MMA stream computes G and U for 64 outputs and every
 //     (G, U) pair sits in adjacent TMEM lanes, i.e. adjacent threads of one
@@ -205,7 +209,7 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
 // tcgen05.ld round trips.
 // GEMM: per 32-column chunk, fp16 rounding, group-wide staging and store;
 // D is released after the last chunk load.
-template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT, int HD>
 __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                               const WaitCtl& ctl, const CUtensorMap* tm_y, int warp,
                                               int E) {
@@ -313,7 +317,12 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
           const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
           const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
           const __half2 h = odd ? __floats2half2_rn(recv, b) : __floats2half2_rn(a, recv);
-          *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
+          if constexpr (HD == 0) {
+            *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
+          } else {  // [head][32 m][HD]: n and n+1 are in the same head
+            const int nl = r - odd;
+            *reinterpret_cast<__half2*>(stg + ((nl / HD) * 32 + j + odd) * (HD * 2) + (nl % HD) * 2) = h;
+          }
         }
       } else {
         // lane 2i holds G, lane 2i+1 holds U of output n0 + r/2; the even lane
@@ -332,7 +341,8 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       if (leader) {
-        tma_store_2d(tm_y, stg, n0, m0 + c0);
+        if constexpr (HD == 0) tma_store_2d(tm_y, stg, n0, m0 + c0);
+        else tma_store_3d(tm_y, stg, 0, m0 + c0, n0 / HD);
         bulk_commit();
       }
       ++it;
@@ -341,8 +351,9 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
   if (leader) bulk_wait_all();
 }
 
-// ACT (gated projections): 0 SiLU, 1 GELU.
-template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
+// ACT (gated projections): 0 SiLU, 1 GELU.  HD (GEMM): 0 row-major Y, else
+// the head dim of the direct-head output.
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT, int HD>
 __global__ void __launch_bounds__(640, 1)
     tc_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                    const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(640, 1)
   } else if (warp >= 8 && warp < 12) {
     decode_role<C, SWIGLU, NX, WTMA, 1>(sm, p, tmem, ctl, warp);
   } else if (warp >= 12) {
-    epilogue_role<C, SWIGLU, NX, WTMA, ACT>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
+    epilogue_role<C, SWIGLU, NX, WTMA, ACT, HD>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
   }
 
   tc_fence_before();

@@ -75,6 +75,9 @@ def test_argument_errors_return_before_any_cuda_call(lib):
     assert lib.m4q_glu_ex(P(good), P(good), P(good), 0, 4, 8, 32, P(good), -1, 0, s) == m.ERR_INVALID_ARG
     assert lib.m4q_geglu(P(good), P(good), None, 0, 4, 8, 32, P(good), s) == m.ERR_INVALID_ARG
     assert lib.m4q_geglu(P(good), P(good), P(good), 0, 4, 12, 32, P(good), s) == m.ERR_BAD_SHAPE
+    assert lib.m4q_gemm_heads(P(good), P(good), 0, 4, 128, 32, 96, P(good), s) == m.ERR_INVALID_ARG   # head dim
+    assert lib.m4q_gemm_heads(P(good), P(good), 0, 4, 128, 32, 0, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_gemm_heads(P(good), P(good), 0, 4, 192, 32, 128, P(good), s) == m.ERR_BAD_SHAPE  # N % hd
     # m4q_mlp validates both projections before enqueueing anything
     assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 128, None, P(good), 0, s) == m.ERR_INVALID_ARG
     assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 132, P(good), P(good), 0, s) == m.ERR_BAD_SHAPE

@@ -172,6 +172,38 @@ def test_mlp_parity(M, cgu, cd, act):
     assert_close(Y, mlp_reference(X, Wg, Wu, Wd, cgu, cd, M, D, F, act), "mlp M=%d %s/%s act=%d" % (M, cgu, cd, act))
 
 
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("M", [1, 9, 70, 300])
+@pytest.mark.parametrize("hd", [64, 128])
+def test_direct_head_output(codec, M, hd):
+    # "v0.1 vs v0.2 comparison" section 4 (v0.2.1): Q/K/V projected straight
+    # into [H, M, D].  The head-major output is the row-major GEMM output
+    # permuted, bit for bit, and matches the oracle.
+    K = kvals(codec, False)[0]
+    N = 5 * hd   # e.g. 3 query heads + 1 key head + 1 value head
+    X = synth.activations(M, K, seed=M + 40)
+    W = synth.weights(codec, N, K, seed=41)
+    Yh = host(m.gemm_heads(dev(X), dev(W), codec, N, K, hd))
+    assert Yh.shape == (N // hd, M, hd)
+    Yr = host(m.gemm(dev(X), dev(W), codec, N, K))
+    assert np.array_equal(Yh.view(np.uint16), Yr.reshape(M, N // hd, hd).transpose(1, 0, 2).view(np.uint16))
+    ref = oracle.gemm(X, W, codec, M, N, K).reshape(M, N // hd, hd).transpose(1, 0, 2)
+    assert_close(Yh, ref, "heads %s M=%d hd=%d" % (codec, M, hd))
+
+
+def test_fused_qkv_views():
+    K, hd, hq, hkv = 256, 64, 4, 2
+    Wq = synth.weights(synth.Q8_0, hq * hd, K, seed=42, name="Wq")
+    Wk = synth.weights(synth.Q8_0, hkv * hd, K, seed=42, name="Wk")
+    Wv = synth.weights(synth.Q8_0, hkv * hd, K, seed=42, name="Wv")
+    X = synth.activations(37, K, seed=43)
+    q, k, v = m.QuantQKV(dev(Wq), dev(Wk), dev(Wv), synth.Q8_0, K, hd, hq, hkv)(dev(X))
+    for got, W, h in ((q, Wq, hq), (k, Wk, hkv), (v, Wv, hkv)):
+        assert tuple(got.shape) == (h, 37, hd)
+        ref = oracle.gemm(X, W, synth.Q8_0, 37, h * hd, K).reshape(37, h, hd).transpose(1, 0, 2)
+        assert_close(host(got), ref, "qkv")
+
+
 # ------------------------------------------------------------ GEMV path
 
 @pytest.mark.parametrize("codec", CODECS)
