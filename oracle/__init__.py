@@ -24,8 +24,8 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-Q4_0, Q8_0, Q2_0 = 0, 1, 2
-CODEC_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q2_0: "Q2_0"}
+Q4_0, Q8_0, Q2_0, MLX4 = 0, 1, 2, 3
+CODEC_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q2_0: "Q2_0", MLX4: "MLX4"}
 
 
 def build(force: bool = False) -> str:
@@ -69,6 +69,8 @@ def _bind(path: str):
     lib.oracle_geglu.restype = i32
     lib.oracle_gelu.argtypes = [ctypes.c_double]
     lib.oracle_gelu.restype = ctypes.c_double
+    lib.oracle_mlx4_pack.argtypes = [vp, vp, vp, i64, i64, vp]
+    lib.oracle_mlx4_pack.restype = i32
     return lib
 
 
@@ -186,6 +188,17 @@ def dequant_f16(W: np.ndarray, codec: int, N: int, K: int) -> np.ndarray:
     Wp = _as_packed(W)
     out = np.empty((N, K), dtype=np.uint16)
     _check(_L().oracle_dequant_f16(_ptr(Wp), codec, N, K, _ptr(out)), "dequant_f16")
+    return out
+
+
+def mlx4_pack(words, scales, biases, N: int, K: int) -> np.ndarray:
+    """MLX planar arrays (uint32 words [N, K/8], fp16 scales and biases
+    [N, K/32]) -> MLX4 blocks uint8 [N, (K/32) * 20]."""
+    w = np.ascontiguousarray(np.asarray(words, dtype=np.uint32))
+    s = np.ascontiguousarray(np.asarray(scales, dtype=np.float16)).view(np.uint16)
+    b = np.ascontiguousarray(np.asarray(biases, dtype=np.float16)).view(np.uint16)
+    out = np.zeros((N, (K // 32) * 20), dtype=np.uint8)
+    _check(_L().oracle_mlx4_pack(_ptr(w), _ptr(s), _ptr(b), N, K, _ptr(out)), "mlx4_pack")
     return out
 
 

@@ -23,6 +23,15 @@
  *    but do not print their formulas; the workload statement of this library
  *    fixes them as 32-weight blocks with an fp16 scale d, Q4_0 w = (q - 8) * d
  *    with a 4-bit q, Q8_0 w = q * d with a signed 8-bit q.
+ *  - Project page, section 4 (v0.2.1, "mlx_4bit_planar") and Table B
+ *    ("identical MLX 4-bit weights (block_mlx_4bit)"), and "Releases" v0.2.1
+ *    and v0.3.0 (MLX 4-bit among the affine formats of the codec registry):
+ *    the MLX 4-bit block is a 20-byte struct.  The pages give its size but
+ *    not its fields; this oracle reads it as MLX's affine group quantization
+ *    at group size 32: an fp16 scale s, an fp16 bias b and 16 bytes of 4-bit
+ *    codes, w = q * s + b.  The planar form of the same weights (section 4:
+ *    codes, scales and biases in separate 16-byte aligned arrays) is MLX's
+ *    own storage, 32-bit words of eight codes each.
  *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
  *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
  *    activation written out.
@@ -33,9 +42,10 @@
  *  - "v0.1 vs v0.2 comparison", section 2.1, and "Releases" v0.2.3: the
  *    unpackers feed half-precision MMA fragments (simdgroup_matrix<half,8,8>),
  *    so the weights the projection multiplies are fp16 values.  The oracle
- *    therefore rounds each decoded weight (q - z) * d once to fp16 (nearest,
- *    ties to even) before the binary64 dot product; oracle_dequant keeps the
- *    exact values and oracle_dequant_f16 the rounded ones.
+ *    therefore rounds each decoded weight ((q - z) * d, or q * s + b) once to
+ *    fp16 (nearest, ties to even) before the binary64 dot product;
+ *    oracle_dequant keeps the exact values and oracle_dequant_f16 the rounded
+ *    ones.
  *
  * Byte layouts (the reading this library takes; the pages print none):
  *  - Q4_0 (18 B): d (fp16, little-endian) then 16 bytes; byte j holds weight
@@ -43,6 +53,9 @@
  *  - Q8_0 (34 B): d then 32 signed bytes, weight i in byte i.
  *  - Q2_0 (34 B): d then 32 bytes; weight i is in byte i / 4 at bits
  *    2 * (i % 4) .. 2 * (i % 4) + 1 (least significant pair first).
+ *  - MLX4 (20 B): s, then b (both fp16, little-endian), then 16 bytes; weight
+ *    i is in byte i / 2, even i in the low nibble.  That is MLX's order: code
+ *    k of a row sits at bits 4 * (k % 8) of little-endian 32-bit word k / 8.
  *
  * Parity note: the Q2_0 code order and the Q4_0/Q8_0 byte layouts cannot be
  * checked against real model files (none are available); they are pinned
@@ -54,7 +67,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_Q4_0 = 0, ORACLE_Q8_0 = 1, ORACLE_Q2_0 = 2 };
+enum { ORACLE_Q4_0 = 0, ORACLE_Q8_0 = 1, ORACLE_Q2_0 = 2, ORACLE_MLX4 = 3 };
 
 /* Weights per block, by codec. */
 long long oracle_block_size(int codec) {
@@ -62,16 +75,19 @@ long long oracle_block_size(int codec) {
     case ORACLE_Q4_0: return 32;
     case ORACLE_Q8_0: return 32;
     case ORACLE_Q2_0: return 128;
+    case ORACLE_MLX4: return 32;
     default: return -1;
   }
 }
 
-/* Bytes per block, by codec: a 2-byte scale plus the packed codes. */
+/* Bytes per block, by codec: a 2-byte scale (and, for MLX4, a 2-byte bias)
+ * plus the packed codes. */
 long long oracle_block_bytes(int codec) {
   switch (codec) {
     case ORACLE_Q4_0: return 2 + 32 / 2;   /* 16 bytes of nibbles */
     case ORACLE_Q8_0: return 2 + 32;       /* 32 signed bytes */
     case ORACLE_Q2_0: return 2 + 128 / 4;  /* 32 bytes of 2-bit codes */
+    case ORACLE_MLX4: return 4 + 32 / 2;   /* 16 bytes of nibbles */
     default: return -1;
   }
 }
@@ -115,7 +131,7 @@ uint16_t oracle_double_to_half(double x) {
 
 /* Decode the integer code of weight i of one block (the byte layouts above). */
 static int block_code(const uint8_t* blk, int codec, int i) {
-  const uint8_t* qs = blk + 2;
+  const uint8_t* qs = blk + (codec == ORACLE_MLX4 ? 4 : 2);
   switch (codec) {
     case ORACLE_Q4_0:
       return (i < 16) ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);
@@ -123,19 +139,24 @@ static int block_code(const uint8_t* blk, int codec, int i) {
       return (int)(int8_t)qs[i];
     case ORACLE_Q2_0:
       return (qs[i / 4] >> (2 * (i % 4))) & 0x3;
+    case ORACLE_MLX4:
+      return (qs[i / 2] >> (4 * (i % 2))) & 0x0f;
     default:
       return 0;
   }
 }
 
-/* The code value that decodes to zero: Q4_0 8, Q8_0 0, Q2_0 1. */
+/* The code value that decodes to zero in the scale-only codecs: Q4_0 8,
+ * Q8_0 0, Q2_0 1 (MLX4 has none: its zero point is the bias). */
 static int code_zero(int codec) {
   return codec == ORACLE_Q4_0 ? 8 : (codec == ORACLE_Q2_0 ? 1 : 0);
 }
 
 /* Dequantize one row of W (K weights) into binary64.  Each weight is
- * (q - z) * d; the product of a <= 8-bit integer and an 11-bit significand
- * is exact in binary64. */
+ * (q - z) * d, or q * s + b for MLX4.  Both are exact in binary64: the
+ * product of a <= 8-bit integer and an 11-bit significand has at most 19
+ * significant bits, and q * s and b are integer multiples of 2^-24 below
+ * 2^20 in magnitude, so their sum needs fewer than 53 bits. */
 static void dequant_row(const uint8_t* row, int codec, long long K, double* out) {
   long long B = oracle_block_size(codec), BB = oracle_block_bytes(codec);
   int z = code_zero(codec);
@@ -143,6 +164,11 @@ static void dequant_row(const uint8_t* row, int codec, long long K, double* out)
     const uint8_t* blk = row + b * BB;
     uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
     double d = oracle_half_to_double(dbits);
+    if (codec == ORACLE_MLX4) {
+      double bias = oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+      for (long long i = 0; i < B; ++i) out[b * B + i] = (double)block_code(blk, codec, (int)i) * d + bias;
+      continue;
+    }
     for (long long i = 0; i < B; ++i) {
       int q = block_code(blk, codec, (int)i);
       out[b * B + i] = (double)(q - z) * d;
@@ -178,6 +204,33 @@ int oracle_dequant_f16(const uint8_t* W, int codec, long long N, long long K, ui
     for (long long k = 0; k < K; ++k) Wh[n * K + k] = oracle_double_to_half(tmp[k]);
   }
   free(tmp);
+  return 0;
+}
+
+/* MLX planar arrays -> MLX4 blocks.  words [N, K/8]: code k of row n at bits
+ * 4 * (k % 8) of words[n * K/8 + k / 8]; scales, biases [N, K/32] fp16 bits.
+ * W receives N rows of K/32 blocks laid out as above.  Returns 0, or -3 when
+ * K is not a multiple of 32. */
+int oracle_mlx4_pack(const uint32_t* words, const uint16_t* scales, const uint16_t* biases,
+                     long long N, long long K, uint8_t* W) {
+  if (N < 0 || K < 0 || K % 32 != 0) return -3;
+  long long nb = K / 32;
+  for (long long n = 0; n < N; ++n) {
+    for (long long b = 0; b < nb; ++b) {
+      uint8_t* blk = W + (n * nb + b) * 20;
+      uint16_t s = scales[n * nb + b], t = biases[n * nb + b];
+      blk[0] = (uint8_t)(s & 0xff);
+      blk[1] = (uint8_t)(s >> 8);
+      blk[2] = (uint8_t)(t & 0xff);
+      blk[3] = (uint8_t)(t >> 8);
+      memset(blk + 4, 0, 16);
+      for (int i = 0; i < 32; ++i) {
+        long long k = 32 * b + i;
+        int q = (int)((words[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xf);
+        blk[4 + i / 2] |= (uint8_t)(q << (4 * (i % 2)));
+      }
+    }
+  }
   return 0;
 }
 

@@ -16,14 +16,22 @@ Block layouts written here (little-endian fp16 scale d first):
   Q4_0  18 B: byte 2+j holds code j (low nibble) and code j+16 (high nibble)
   Q8_0  34 B: byte 2+i holds code i as a signed byte
   Q2_0  34 B: byte 2+i//4 holds code i at bits 2*(i%4)..2*(i%4)+1
+  MLX4  20 B: scale s, then bias b (fp16), then byte 4+i//2 holds code i,
+        even i in the low nibble (MLX's packing order: code k of a row sits
+        at bits 4*(k%8) of little-endian 32-bit word k//8)
+MLX's own planar arrays (``planar``): codes as uint32 words [N, K/8] with
+code k at bits 4*(k%8) of word k//8, scales and biases fp16 [N, K/32].
 
 Value recipes of the pages' LLaMA-shaped workloads (synthetic weights, as the
 m4-prefill-engine v0.2 notes describe): X ~ N(0,1) rounded to fp16;
 Q4_0 d = |N(0,1)|*0.02, q uniform on 0..15; Q8_0 d = |N(0,1)|*0.01,
 q = clip(round(40*N(0,1)), -127, 127) with halves rounded away from zero;
 Q2_0 d = |N(0,1)|*0.02, q in {0,1,2} with probabilities 0.3/0.4/0.3, then each
-code independently replaced by the reserved code 3 with probability 0.01.
-Scales are drawn in binary64 and rounded to fp16 (round to nearest even).
+code independently replaced by the reserved code 3 with probability 0.01;
+MLX4 s = |N(0,1)|*0.02, q uniform on 0..15, b = -s*(7.5 + 0.5*N(0,1)) (the
+shape of an affine min/max fit of a zero-mean group: b near the group minimum
+-7.5 s).  Scales and biases are drawn in binary64 and rounded to fp16 (round to
+nearest even).
 """
 from __future__ import annotations
 
@@ -31,11 +39,11 @@ import zlib
 
 import numpy as np
 
-Q4_0, Q8_0, Q2_0 = 0, 1, 2
-CODECS = (Q4_0, Q8_0, Q2_0)
-CODEC_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q2_0: "Q2_0"}
-BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34}
+Q4_0, Q8_0, Q2_0, MLX4 = 0, 1, 2, 3
+CODECS = (Q4_0, Q8_0, Q2_0, MLX4)
+CODEC_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q2_0: "Q2_0", MLX4: "MLX4"}
+BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128, MLX4: 32}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34, MLX4: 20}
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -91,7 +99,7 @@ def activations(M: int, K: int, seed: int, name: str = "X") -> np.ndarray:
 def codes(codec: int, N: int, K: int, seed: int, name: str) -> np.ndarray:
     """Integer codes [N, K] drawn by the codec's recipe (int16)."""
     n = N * K
-    if codec == Q4_0:
+    if codec in (Q4_0, MLX4):
         words = u64(seed, name + ".q", (n + 15) // 16)
         nib = np.empty((words.size, 16), dtype=np.uint8)
         for j in range(16):
@@ -110,7 +118,7 @@ def codes(codec: int, N: int, K: int, seed: int, name: str) -> np.ndarray:
     raise ValueError("unknown codec %r" % codec)
 
 
-_SCALE = {Q4_0: 0.02, Q8_0: 0.01, Q2_0: 0.02}
+_SCALE = {Q4_0: 0.02, Q8_0: 0.01, Q2_0: 0.02, MLX4: 0.02}
 
 
 def scales(codec: int, N: int, K: int, seed: int, name: str, scale: float | None = None):
@@ -120,8 +128,27 @@ def scales(codec: int, N: int, K: int, seed: int, name: str, scale: float | None
     return to_f16(np.abs(normal(seed, name + ".d", N * nb)) * c).reshape(N, nb)
 
 
-def pack(codec: int, q: np.ndarray, d: np.ndarray) -> np.ndarray:
-    """Write codes q [N, K] and fp16 scales d [N, K/block] into packed blocks,
+def biases(codec: int, N: int, K: int, seed: int, name: str, d) -> np.ndarray | None:
+    """Block biases fp16 [N, K / block] for the affine codec (MLX4):
+    b = -s * (7.5 + 0.5 * N(0,1)) with s the block's scale.  None for the
+    scale-only codecs."""
+    if codec != MLX4:
+        return None
+    nb = K // BLOCK[codec]
+    s = np.asarray(d, dtype=np.float16).astype(np.float64).reshape(N, nb)
+    z = normal(seed, name + ".b", N * nb).reshape(N, nb)
+    return to_f16(-s * (7.5 + 0.5 * z))
+
+
+def _f16_bytes(v, N: int, nb: int) -> np.ndarray:
+    """fp16 values [N, nb] as their little-endian bytes [N, nb, 2]."""
+    b = np.ascontiguousarray(np.asarray(v, dtype=np.float16).reshape(N, nb)).view("<u2")
+    return b.view(np.uint8).reshape(N, nb, 2)
+
+
+def pack(codec: int, q: np.ndarray, d: np.ndarray, b=None) -> np.ndarray:
+    """Write codes q [N, K] and fp16 scales d [N, K/block] (and, for MLX4,
+    fp16 biases b [N, K/block], zero when omitted) into packed blocks,
     returned as uint8 [N, (K/block) * block_bytes]."""
     q = np.asarray(q)
     N, K = q.shape
@@ -129,8 +156,7 @@ def pack(codec: int, q: np.ndarray, d: np.ndarray) -> np.ndarray:
     if K % B:
         raise ValueError("K must be a multiple of the block size")
     nb = K // B
-    dbytes = np.ascontiguousarray(np.asarray(d, dtype=np.float16).reshape(N, nb)).view("<u2")
-    dbytes = dbytes.view(np.uint8).reshape(N, nb, 2)
+    head = [_f16_bytes(d, N, nb)]
     qb = q.reshape(N, nb, B)
     if codec == Q4_0:
         if qb.min(initial=0) < 0 or qb.max(initial=0) > 15:
@@ -146,26 +172,54 @@ def pack(codec: int, q: np.ndarray, d: np.ndarray) -> np.ndarray:
             raise ValueError("Q2_0 codes are 0..3")
         u = qb.astype(np.uint8).reshape(N, nb, 32, 4)
         body = (u[..., 0] | (u[..., 1] << 2) | (u[..., 2] << 4) | (u[..., 3] << 6)).astype(np.uint8)
+    elif codec == MLX4:
+        if qb.min(initial=0) < 0 or qb.max(initial=0) > 15:
+            raise ValueError("MLX4 codes are 0..15")
+        u = qb.astype(np.uint8)
+        body = (u[:, :, 0::2] | (u[:, :, 1::2] << 4)).astype(np.uint8)
+        head.append(_f16_bytes(np.zeros((N, nb)) if b is None else b, N, nb))
     else:
         raise ValueError("unknown codec %r" % codec)
-    out = np.concatenate([dbytes, body], axis=2)
+    out = np.concatenate(head + [body], axis=2)
     return np.ascontiguousarray(out.reshape(N, nb * BLOCK_BYTES[codec]))
+
+
+def planar(q: np.ndarray, d: np.ndarray, b: np.ndarray):
+    """MLX's own planar arrays for 4-bit codes q [N, K] (K % 32 == 0) with
+    group scales d and biases b [N, K/32]: (words uint32 [N, K/8] with code k
+    at bits 4*(k%8) of word k//8, scales fp16, biases fp16)."""
+    q = np.asarray(q)
+    N, K = q.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    if q.min(initial=0) < 0 or q.max(initial=0) > 15:
+        raise ValueError("codes are 0..15")
+    u = q.astype(np.uint32).reshape(N, K // 8, 8)
+    words = np.zeros((N, K // 8), dtype=np.uint32)
+    for e in range(8):
+        words |= u[:, :, e] << np.uint32(4 * e)
+    nb = K // 32
+    return (words, np.ascontiguousarray(np.asarray(d, np.float16).reshape(N, nb)),
+            np.ascontiguousarray(np.asarray(b, np.float16).reshape(N, nb)))
 
 
 def weights(codec: int, N: int, K: int, seed: int, name: str = "W", scale: float | None = None):
     """Packed weights uint8 [N, row_bytes] by the codec's recipe."""
-    return pack(codec, codes(codec, N, K, seed, name), scales(codec, N, K, seed, name, scale))
+    d = scales(codec, N, K, seed, name, scale)
+    return pack(codec, codes(codec, N, K, seed, name), d, biases(codec, N, K, seed, name, d))
 
 
 def row_bytes(codec: int, K: int) -> int:
     return (K // BLOCK[codec]) * BLOCK_BYTES[codec]
 
 
-def constant_weights(codec: int, N: int, K: int, code: int, d_f16) -> np.ndarray:
-    """Every code equal to ``code`` and every scale equal to ``d_f16``."""
+def constant_weights(codec: int, N: int, K: int, code: int, d_f16, b_f16=0.0) -> np.ndarray:
+    """Every code equal to ``code``, every scale equal to ``d_f16`` (and,
+    for MLX4, every bias equal to ``b_f16``)."""
     q = np.full((N, K), code, dtype=np.int16)
     d = np.full((N, K // BLOCK[codec]), d_f16, dtype=np.float16)
-    return pack(codec, q, d)
+    b = np.full((N, K // BLOCK[codec]), b_f16, dtype=np.float16)
+    return pack(codec, q, d, b if codec == MLX4 else None)
 
 
 # ---------------------------------------------------------------- workloads

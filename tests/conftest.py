@@ -33,6 +33,8 @@ def read_golden_blocks(fname):
                 cur["codec"] = vals[0]
             elif key == "d_bits":
                 cur["d_bits"] = int(vals[0], 16)
+            elif key == "b_bits":
+                cur["b_bits"] = int(vals[0], 16)
             elif key == "code_bytes":
                 cur["code_bytes"] = [int(v, 16) for v in vals]
             elif key == "weights":
@@ -43,6 +45,6 @@ def read_golden_blocks(fname):
 @pytest.fixture(scope="session")
 def golden_blocks():
     out = []
-    for f in ("q4_0_blocks.txt", "q8_0_blocks.txt", "q2_0_blocks.txt"):
+    for f in ("q4_0_blocks.txt", "q8_0_blocks.txt", "q2_0_blocks.txt", "mlx4_blocks.txt"):
         out.extend(read_golden_blocks(f))
     return out

@@ -17,13 +17,17 @@ import pytest
 import oracle
 import synth
 
-CODEC_BY_NAME = {"Q4_0": synth.Q4_0, "Q8_0": synth.Q8_0, "Q2_0": synth.Q2_0}
-ZERO_CODE = {synth.Q4_0: 8, synth.Q8_0: 0, synth.Q2_0: 1}
+CODEC_BY_NAME = {"Q4_0": synth.Q4_0, "Q8_0": synth.Q8_0, "Q2_0": synth.Q2_0, "MLX4": synth.MLX4}
+# The code that decodes to zero (MLX4: with a zero bias).
+ZERO_CODE = {synth.Q4_0: 8, synth.Q8_0: 0, synth.Q2_0: 1, synth.MLX4: 0}
 
 
 def golden_packed(blk):
     d = blk["d_bits"]
-    return np.array([d & 0xFF, d >> 8] + blk["code_bytes"], dtype=np.uint8)
+    head = [d & 0xFF, d >> 8]
+    if "b_bits" in blk:
+        head += [blk["b_bits"] & 0xFF, blk["b_bits"] >> 8]
+    return np.array(head + blk["code_bytes"], dtype=np.uint8)
 
 
 # ------------------------------------------------------------ block layout
@@ -35,6 +39,8 @@ def test_block_sizes():
     assert oracle.block_bytes(synth.Q2_0) * 8 / oracle.block_size(synth.Q2_0) == 2.125
     assert (oracle.block_size(synth.Q4_0), oracle.block_bytes(synth.Q4_0)) == (32, 18)
     assert (oracle.block_size(synth.Q8_0), oracle.block_bytes(synth.Q8_0)) == (32, 34)
+    # Project page section 4 (v0.2.1): the MLX 4-bit block is a 20-byte struct.
+    assert (oracle.block_size(synth.MLX4), oracle.block_bytes(synth.MLX4)) == (32, 20)
     assert oracle.block_size(7) == -1
 
 
@@ -64,9 +70,15 @@ def test_encoder_matches_golden(golden_blocks):
         B = oracle.block_size(codec)
         d = np.array([blk["d_bits"]], np.uint16).view(np.float16)
         dval = float(d[0])
-        z = ZERO_CODE[codec]
-        q = np.array([[round(w / dval) + z for w in blk["weights"]]], dtype=np.int16)
-        assert np.array_equal(synth.pack(codec, q, d.reshape(1, 1)), golden_packed(blk).reshape(1, -1))
+        if codec == synth.MLX4:
+            b = np.array([blk["b_bits"]], np.uint16).view(np.float16)
+            q = np.array([[round((w - float(b[0])) / dval) for w in blk["weights"]]], dtype=np.int16)
+            packed = synth.pack(codec, q, d.reshape(1, 1), b.reshape(1, 1))
+        else:
+            z = ZERO_CODE[codec]
+            q = np.array([[round(w / dval) + z for w in blk["weights"]]], dtype=np.int16)
+            packed = synth.pack(codec, q, d.reshape(1, 1))
+        assert np.array_equal(packed, golden_packed(blk).reshape(1, -1))
 
 
 # ------------------------------------------------------------ fp16 conversions
@@ -100,19 +112,24 @@ def test_double_to_half_matches_numpy():
 
 # ------------------------------------------------------------ projections
 
-def f16_weights(q, d, codec):
-    """Each weight (q - z) * d (exact in binary64) rounded once to fp16 by
-    numpy, as binary64 -- the operand values the method multiplies."""
+def f16_weights(q, d, codec, b=None):
+    """Each weight (q - z) * d, or q * s + b for MLX4 (exact in binary64),
+    rounded once to fp16 by numpy, as binary64 -- the operand values the
+    method multiplies."""
     B = synth.BLOCK[codec]
-    exact = (q.astype(np.float64) - ZERO_CODE[codec]) * np.repeat(d.astype(np.float64), B, axis=1)
+    scale = np.repeat(d.astype(np.float64), B, axis=1)
+    if codec == synth.MLX4:
+        exact = q.astype(np.float64) * scale + np.repeat(b.astype(np.float64), B, axis=1)
+    else:
+        exact = (q.astype(np.float64) - ZERO_CODE[codec]) * scale
     return exact.astype(np.float16).astype(np.float64)
 
 
-def exact_gemm(q, d, codec, X16):
+def exact_gemm(q, d, codec, X16, b=None):
     """Exact rational Y = X W16^T from the generator's codes and scales."""
     M, K = X16.shape
     N = q.shape[0]
-    W16 = f16_weights(q, d, codec)
+    W16 = f16_weights(q, d, codec, b)
     Xf = [[Fraction(float(v)) for v in row] for row in X16.astype(np.float64)]
     Wf = [[Fraction(float(W16[n, k])) for k in range(K)] for n in range(N)]
     return [[sum(Xf[m][k] * Wf[n][k] for k in range(K)) for n in range(N)] for m in range(M)]
@@ -125,10 +142,11 @@ def test_brute_force_exact(codec):
     X = synth.activations(M, K, seed=11)
     q = synth.codes(codec, N, K, seed=12, name="W")
     d = synth.scales(codec, N, K, seed=12, name="W")
-    W = synth.pack(codec, q, d)
+    b = synth.biases(codec, N, K, seed=12, name="W", d=d)
+    W = synth.pack(codec, q, d, b)
     Y = oracle.gemm(X, W, codec, M, N, K)
-    E = exact_gemm(q, d, codec, X)
-    W16 = f16_weights(q, d, codec)
+    E = exact_gemm(q, d, codec, X, b)
+    W16 = f16_weights(q, d, codec, b)
     for m in range(M):
         for n in range(N):
             # recursive fp64 summation: |err| <= K * 2^-52 * sum |x w| (loose)
@@ -146,7 +164,8 @@ def test_zero_code_gives_zero(codec):
     assert np.all(oracle.swiglu(X, W, W, codec, 8, 16, K) == 0.0)
 
 
-@pytest.mark.parametrize("codec,code", [(synth.Q4_0, 13), (synth.Q8_0, -57), (synth.Q2_0, 3), (synth.Q2_0, 0)])
+@pytest.mark.parametrize("codec,code", [(synth.Q4_0, 13), (synth.Q8_0, -57), (synth.Q2_0, 3), (synth.Q2_0, 0),
+                                        (synth.MLX4, 13)])
 def test_constant_code_closed_form(codec, code):
     # Constant code c and scale d: Y[m, n] = fp16((c - z) * d) * sum_k X[m, k].
     M, N, K = 5, 8, 256
@@ -193,6 +212,74 @@ def test_threads_do_not_change_results():
     a = oracle.gemm(X, W, synth.Q8_0, M, N, K, nthreads=1)
     b = oracle.gemm(X, W, synth.Q8_0, M, N, K, nthreads=7)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ MLX 4-bit affine
+
+def check_mlx4_affine_closed_form():
+    # Constant code c, scale s, bias b: every weight is fp16(c * s + b), so
+    # Y[m, n] = fp16(c s + b) * sum_k X[m, k].
+    M, N, K = 4, 8, 256
+    X = synth.activations(M, K, seed=21)
+    for c, s, b in ((13, 0.0173, -0.1), (0, 0.5, 0.3125), (15, -0.02, 0.15), (7, 0.0, -0.25)):
+        sv, bv = np.float16(s), np.float16(b)
+        w16 = float(np.float16(c * float(sv) + float(bv)))
+        W = synth.constant_weights(synth.MLX4, N, K, c, sv, bv)
+        Y = oracle.gemm(X, W, synth.MLX4, M, N, K)
+        for m in range(M):
+            exact = w16 * math.fsum(X[m].astype(np.float64))
+            scale = abs(w16) * np.abs(X[m].astype(np.float64)).sum()
+            assert np.all(np.abs(Y[m] - exact) <= K * 2.0 ** -52 * scale + 1e-300), (c, s, b)
+
+
+def test_mlx4_affine_closed_form():
+    check_mlx4_affine_closed_form()
+
+
+def check_mlx4_one_rounding():
+    # Block C of the golden file at the projection level: with s = 1 + 2^-10,
+    # b = -3 and code 3, each fp16 operand is 3 * 2^-10, so X = all ones gives
+    # Y = K * 3 * 2^-10 exactly (a product rounded to fp16 before the bias is
+    # added would give K * 2^-8).
+    K = 64
+    s = np.array([0x3C01], np.uint16).view(np.float16)[0]
+    b = np.array([0xC200], np.uint16).view(np.float16)[0]
+    W = synth.constant_weights(synth.MLX4, 2, K, 3, s, b)
+    assert np.all(oracle.dequant_f16(W, synth.MLX4, 2, K) == np.float16(3 * 2.0 ** -10).view(np.uint16))
+    X = np.ones((1, K), dtype=np.float16)
+    assert np.all(oracle.gemm(X, W, synth.MLX4, 1, 2, K) == K * 3 * 2.0 ** -10)
+
+
+def test_mlx4_one_rounding():
+    check_mlx4_one_rounding()
+
+
+def check_mlx4_pack():
+    # MLX's planar arrays (codes in uint32 words, code k at bits 4 (k % 8) of
+    # word k // 8; scales and biases in their own arrays) repack into exactly
+    # the blocks the layout writer produces from the same codes.
+    for N, K in ((3, 32), (5, 256), (2, 1024)):
+        q = synth.codes(synth.MLX4, N, K, seed=N, name="W")
+        d = synth.scales(synth.MLX4, N, K, seed=N, name="W")
+        b = synth.biases(synth.MLX4, N, K, seed=N, name="W", d=d)
+        words, s, bb = synth.planar(q, d, b)
+        assert np.array_equal(oracle.mlx4_pack(words, s, bb, N, K), synth.pack(synth.MLX4, q, d, b))
+
+
+def test_mlx4_pack():
+    check_mlx4_pack()
+    with pytest.raises(ValueError):
+        oracle.mlx4_pack(np.zeros((1, 2), np.uint32), np.zeros(1, np.float16), np.zeros(1, np.float16), 1, 16)
+
+
+def test_mlx4_scale_zero_gives_bias():
+    # s = 0: every weight equals the block's bias whatever its code.
+    K = 64
+    q = synth.codes(synth.MLX4, 4, K, seed=3, name="W")
+    d = np.zeros((4, 2), np.float16)
+    b = np.array([[0.125, -2.5], [3.0, 0.0], [-0.0078125, 1.5], [7.0, -7.0]], np.float16)
+    W = synth.pack(synth.MLX4, q, d, b)
+    assert np.array_equal(oracle.dequant(W, synth.MLX4, 4, K), np.repeat(b.astype(np.float64), 32, axis=1))
 
 
 # ------------------------------------------------------------ SiLU and SwiGLU
@@ -336,6 +423,27 @@ MUTATIONS = {
     "gelu_half_missing": ("return 0.5 * g * erfc(-g / sqrt(2.0));", "return g * erfc(-g / sqrt(2.0));"),
     "gelu_sign": ("return 0.5 * g * erfc(-g / sqrt(2.0));", "return 0.5 * g * erfc(g / sqrt(2.0));"),
     "geglu_uses_silu": ("(j->act == ORACLE_ACT_GELU ? oracle_gelu(g) : oracle_silu(g))", "oracle_silu(g)"),
+    "mlx4_q4_0_nibble_order": ("return (qs[i / 2] >> (4 * (i % 2))) & 0x0f;",
+                               "return (i < 16) ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);"),
+    "mlx4_high_nibble_first": ("return (qs[i / 2] >> (4 * (i % 2))) & 0x0f;",
+                               "return (qs[i / 2] >> (4 - 4 * (i % 2))) & 0x0f;"),
+    "mlx4_bias_dropped": ("(double)block_code(blk, codec, (int)i) * d + bias;",
+                          "(double)block_code(blk, codec, (int)i) * d;"),
+    "mlx4_bias_subtracted": ("(double)block_code(blk, codec, (int)i) * d + bias;",
+                             "(double)block_code(blk, codec, (int)i) * d - bias;"),
+    "mlx4_centred_codes": ("(double)block_code(blk, codec, (int)i) * d + bias;",
+                           "(double)(block_code(blk, codec, (int)i) - 8) * d + bias;"),
+    "mlx4_product_rounded_first": (
+        "(double)block_code(blk, codec, (int)i) * d + bias;",
+        "oracle_half_to_double(oracle_double_to_half((double)block_code(blk, codec, (int)i) * d)) + bias;"),
+    "mlx4_scale_bias_swapped": ("double bias = oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));",
+                                "double bias = d; d = oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));"),
+    "mlx4_codes_after_scale_only": ("const uint8_t* qs = blk + (codec == ORACLE_MLX4 ? 4 : 2);",
+                                    "const uint8_t* qs = blk + 2;"),
+    "mlx4_pack_word_order": ("int q = (int)((words[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xf);",
+                             "int q = (int)((words[n * (K / 8) + k / 8] >> (28 - 4 * (k % 8))) & 0xf);"),
+    "mlx4_pack_bias_scale_swapped": ("uint16_t s = scales[n * nb + b], t = biases[n * nb + b];",
+                                     "uint16_t t = scales[n * nb + b], s = biases[n * nb + b];"),
 }
 
 
@@ -352,6 +460,9 @@ def all_pins_pass(golden_blocks):
         test_gelu_values_and_invariants,
         lambda: [test_geglu_fused_equals_unfused(c) for c in synth.CODECS],
         lambda: test_q2_0_reserved_code_is_plus_two_d(),
+        check_mlx4_affine_closed_form,
+        check_mlx4_one_rounding,
+        check_mlx4_pack,
     ]
     for c in checks:
         try:

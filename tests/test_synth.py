@@ -50,3 +50,30 @@ def test_pack_shapes():
         K = 1024
         W = synth.weights(c, 8, K, 0)
         assert W.shape == (8, synth.row_bytes(c, K)) and W.dtype == np.uint8
+
+
+def test_mlx4_biases_follow_recipe():
+    d = synth.scales(synth.MLX4, 64, 1024, 0, "W")
+    b = synth.biases(synth.MLX4, 64, 1024, 0, "W", d)
+    assert b.dtype == np.float16 and b.shape == (64, 32)
+    big = d.astype(np.float64) > 1e-3
+    ratio = -(b.astype(np.float64) / d.astype(np.float64))[big]
+    assert abs(ratio.mean() - 7.5) < 0.05 and abs(ratio.std() - 0.5) < 0.05
+    assert synth.biases(synth.Q4_0, 64, 1024, 0, "W", d) is None
+
+
+def test_mlx4_planar_and_block_layouts():
+    N, K = 4, 64
+    q = synth.codes(synth.MLX4, N, K, 0, "W")
+    d = synth.scales(synth.MLX4, N, K, 0, "W")
+    b = synth.biases(synth.MLX4, N, K, 0, "W", d)
+    words, s, bb = synth.planar(q, d, b)
+    assert words.dtype == np.uint32 and words.shape == (N, K // 8)
+    # code k sits at bits 4 (k % 8) of word k // 8
+    for k in (0, 1, 7, 8, 37, 63):
+        assert np.array_equal((words[:, k // 8] >> np.uint32(4 * (k % 8))) & np.uint32(15), q[:, k])
+    W = synth.pack(synth.MLX4, q, d, b).reshape(N, K // 32, 20)
+    assert np.array_equal(W[:, :, 0:2].copy().view("<u2")[..., 0], d.view("<u2"))
+    assert np.array_equal(W[:, :, 2:4].copy().view("<u2")[..., 0], b.view("<u2"))
+    # the 16 code bytes of a block are the planar words' bytes of that group
+    assert np.array_equal(W[:, :, 4:].reshape(N, -1), words.view(np.uint8).reshape(N, -1))
