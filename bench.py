@@ -347,6 +347,8 @@ def run_ours(args, ws, rank, local):
            "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": M_ * N_ * 2,
            "weights": "resident in HBM (model parameters)"}
 
+    mlx4 = measure_mlx4(m, X, dev, steps=max(20, min(args.steps, 200)))
+
     if rank != 0:
         return
     line = {
@@ -359,10 +361,62 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs rotate through %d distinct copies (%.0f MB > L2)"
                          % (ROTATE, ROTATE * (X.nbytes + Wg.nbytes + Wu.nbytes + M_ * N_ * 2) / 1e6),
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "roofline": roofline, "m1": m1, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+        "roofline": roofline, "m1": m1, "e2e": e2e, "mlx4": mlx4, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_mlx4(m, X, dev, steps):
+    """The same layer on MLX 4-bit affine weights (the format of the pages'
+    MLX comparison): M = 2048 TFLOP/s and M = 1 GB/s, timed like the
+    headline (cold weights rotating through copies; CUDA events)."""
+    import torch
+
+    import synth
+    # ROTATE distinct weight sets (4 x 73 MB > L2), so each launch reads cold weights
+    wg = [torch.from_numpy(synth.weights(synth.MLX4, N_, K_, seed=2 + r, name="Wg")).to(dev) for r in range(ROTATE)]
+    wu = [torch.from_numpy(synth.weights(synth.MLX4, N_, K_, seed=2 + r, name="Wu")).to(dev) for r in range(ROTATE)]
+    x = torch.from_numpy(X).to(dev)
+    y = torch.empty((M_, N_), dtype=torch.float16, device=dev)
+    x1 = torch.from_numpy(X[:1].copy()).to(dev)
+    y1 = torch.empty((1, N_), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(4):
+        m.swiglu(x, wg[i % ROTATE], wu[i % ROTATE], m.MLX4, N_, K_, out=y)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        m.swiglu(x, wg[i % ROTATE], wu[i % ROTATE], m.MLX4, N_, K_, out=y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    reps = 64
+    graph = torch.cuda.CUDAGraph()
+    for i in range(4):
+        m.swiglu(x1, wg[i % ROTATE], wu[i % ROTATE], m.MLX4, N_, K_, out=y1)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        for i in range(reps):
+            m.swiglu(x1, wg[i % ROTATE], wu[i % ROTATE], m.MLX4, N_, K_, out=y1)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    m1_ms = e0.elapsed_time(e1) / reps
+    assert m.check_device_status() == m.OK
+    m1_bytes = 2 * m.weight_bytes(m.MLX4, N_, K_) + K_ * 2 + N_ * 2
+    pk, _ = peaks()
+    tflops = 4.0 * M_ * N_ * K_ / (ms * 1e-3) / 1e12
+    gbs = m1_bytes / (m1_ms * 1e-3) / 1e9
+    return {"workload": "8b_swiglu_mlx4_m2048", "codec": "MLX4 (w = q*s + b, 32-weight groups, 20-byte blocks)",
+            "value": tflops, "unit": "TFLOP/s", "ms_per_launch": ms, "steps": steps,
+            "frac": tflops / pk["bf16_tflops"],
+            "m1": {"workload": "8b_swiglu_mlx4_m1", "value": gbs, "unit": "GB/s", "us_per_launch": 1e3 * m1_ms,
+                   "bytes_per_launch": m1_bytes, "frac": gbs / pk["hbm_gbs"]}}
 
 
 def run_profile_case(case, local):
@@ -373,13 +427,19 @@ def run_profile_case(case, local):
     torch.cuda.set_device(local)
     m.build()
     X, Wg, Wu = make_inputs()
-    if case == "swiglu_m1":
+    codec = m.Q4_0
+    if "mlx4" in case:
+        import synth
+        codec = m.MLX4
+        Wg = synth.weights(synth.MLX4, N_, K_, seed=2, name="Wg")
+        Wu = synth.weights(synth.MLX4, N_, K_, seed=2, name="Wu")
+    if case.endswith("_m1"):
         X = X[:1].copy()
     x = torch.from_numpy(X).cuda()
     wg, wu = torch.from_numpy(Wg).cuda(), torch.from_numpy(Wu).cuda()
     y = torch.empty((X.shape[0], N_), dtype=torch.float16, device="cuda")
     for _ in range(3):
-        m.swiglu(x, wg, wu, m.Q4_0, N_, K_, out=y)
+        m.swiglu(x, wg, wu, codec, N_, K_, out=y)
     torch.cuda.synchronize()
     assert m.check_device_status() == m.OK
     print("profile case %s: 3 launches done" % case)
@@ -393,7 +453,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile-case", choices=["swiglu_m2048", "swiglu_m1"], default=None,
+    ap.add_argument("--profile-case", default=None,
+                    choices=["swiglu_m2048", "swiglu_m1", "swiglu_mlx4_m2048", "swiglu_mlx4_m1"],
                     help="only run 3 launches of one case (for ncu)")
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -15,22 +15,30 @@
  *  - "Releases", v0.3.0, PrismML Q2_0 codec: 128 weights in 34 bytes,
  *    w = (q - 1) * d with the reserved code 3 decoding to +2d.  Q4_0 and Q8_0
  *    are GGUF's 32-weight blocks: w = (q - 8) * d and w = q * d.
+ *  - Project page, section 4 (v0.2.1) and Table B: MLX 4-bit weights, a
+ *    20-byte block_mlx_4bit and its planar form.  Read as MLX's affine group
+ *    quantization at group size 32: w = q * s + b with an fp16 scale s and
+ *    bias b per group of 32 weights.
  *
  * Conventions common to every call:
  *  - Pointers X, W, Wg, Wu, Y, Wf16 are DEVICE pointers (cudaMalloc'd or from
  *    PyTorch).  The caller owns every buffer; the library allocates nothing
  *    during a call and keeps no pointer after it returns.
  *  - Layouts are row-major and dense.  X is fp16 [M, K]; Y is fp16 [M, N].
- *    W is [N rows][K / B blocks] of packed blocks (B = 32 for Q4_0 and Q8_0,
- *    128 for Q2_0), block bytes 18 / 34 / 34, each block a little-endian fp16
- *    scale d followed by its codes:
+ *    W is [N rows][K / B blocks] of packed blocks (B = 32 for Q4_0, Q8_0 and
+ *    MLX4, 128 for Q2_0), block bytes 18 / 34 / 34 / 20, each block a
+ *    little-endian fp16 scale d followed by its codes:
  *      Q4_0: byte 2+j holds weight j in its low nibble, weight j+16 high;
  *      Q8_0: byte 2+i holds weight i as a signed byte;
- *      Q2_0: byte 2+i/4 holds weight i at bits 2*(i%4)..2*(i%4)+1.
+ *      Q2_0: byte 2+i/4 holds weight i at bits 2*(i%4)..2*(i%4)+1;
+ *      MLX4: bytes 2-3 hold the fp16 bias b, byte 4+i/2 holds weight i,
+ *            even i in the low nibble (MLX's order; m4q_mlx4_pack builds
+ *            these blocks from MLX's planar arrays).
  *  - Shapes: M >= 1, N >= 8 with N % 8 == 0, K >= B with K % B == 0.
  *    X, W, Wg, Wu, Y must be 16-byte aligned.
- *  - Arithmetic: every weight is decoded to fp16 as (q - z) * d rounded once
- *    to nearest even, products are accumulated in fp32, and each output is
+ *  - Arithmetic: every weight is decoded to fp16 as (q - z) * d (MLX4:
+ *    q * s + b) rounded once to nearest even, products are accumulated in
+ *    fp32, and each output is
  *    rounded once to fp16 (SiLU(g) * u or GELU(g) * u is formed in fp32
  *    first).
  *  - Asynchrony: calls enqueue work on `stream` and return; argument errors
@@ -53,7 +61,7 @@ extern "C" {
 typedef struct CUstream_st* m4q_stream_t;
 
 /* Weight codecs. */
-enum m4q_codec { M4Q_Q4_0 = 0, M4Q_Q8_0 = 1, M4Q_Q2_0 = 2 };
+enum m4q_codec { M4Q_Q4_0 = 0, M4Q_Q8_0 = 1, M4Q_Q2_0 = 2, M4Q_MLX4 = 3 };
 
 /* Execution paths for m4q_gemm_ex / m4q_swiglu_ex. */
 enum m4q_path {
@@ -154,8 +162,23 @@ int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* W
                     int codec_d, int64_t M, int64_t D, int64_t F, void* Y, int act,
                     m4q_stream_t stream);
 
+/* Repack MLX 4-bit weights from MLX's planar arrays into MLX4 blocks
+ * (project page, section 4: the deinterleaved "mlx_4bit_planar" layout of
+ * the 20-byte block_mlx_4bit).  words: uint32 [N, K/8], code k of row n at
+ * bits 4*(k%8) of word k/8 (little-endian); scales, biases: fp16 [N, K/32],
+ * one per group of 32 weights.  W receives [N, K/32] 20-byte blocks
+ * (m4q_weight_bytes(M4Q_MLX4, N, K) bytes) for any call above.  A one-time
+ * layout step, not part of a projection: the tensor-core path moves whole
+ * 160-byte stages of 8 blocks by TMA, so the 20-byte block stride never
+ * splits a copy.  Requires N >= 1, K >= 32 with K % 32 == 0 (else
+ * M4Q_ERR_BAD_SHAPE); words and W 16-byte aligned, scales and biases 2-byte
+ * aligned (else M4Q_ERR_MISALIGNED).  Device pointers; enqueued on stream. */
+int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int64_t N, int64_t K,
+                  void* W, m4q_stream_t stream);
+
 /* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
- * rounded once to nearest even.  The test hook for bit-exact decoding. */
+ * (MLX4: q * s + b) rounded once to nearest even.  The test hook for
+ * bit-exact decoding. */
 int m4q_dequant(const void* W, int codec, int64_t N, int64_t K, void* Wf16,
                 m4q_stream_t stream);
 

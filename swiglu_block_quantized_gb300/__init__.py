@@ -14,6 +14,7 @@ Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     glu(x, wg, wu, codec, n, k, act, out=None, path=PATH_AUTO)
     mlp(x, wg, wu, wd, codec_gu, codec_d, d, f, act=ACT_SILU, h=None, out=None)
     dequant(w, codec, n, k, out=None)
+    mlx4_pack(words, scales, biases, n, k, out=None)
     weight_bytes(codec, n, k), check_finite(t), check_device_status(),
     selftest_wait_timeout(limit_ns), status_string(code), version()
 and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
@@ -29,10 +30,10 @@ import ctypes
 import os
 import threading
 
-Q4_0, Q8_0, Q2_0 = 0, 1, 2
-CODECS = (Q4_0, Q8_0, Q2_0)
-BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34}
+Q4_0, Q8_0, Q2_0, MLX4 = 0, 1, 2, 3
+CODECS = (Q4_0, Q8_0, Q2_0, MLX4)
+BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128, MLX4: 32}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34, MLX4: 20}
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 ACT_SILU, ACT_GELU = 0, 1
 
@@ -63,6 +64,7 @@ SIGNATURES = {
     "m4q_mlp": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp]),
     "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+    "m4q_mlx4_pack": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
     "m4q_check_device_status": (_i32, [_vp]),
@@ -235,6 +237,28 @@ def dequant(w, codec: int, n: int, k: int, out=None, stream=None):
     _require(out, torch.float16, "out")
     _check(load().m4q_dequant(w.data_ptr(), codec, n, k, out.data_ptr(), _stream_ptr(stream)),
            "m4q_dequant")
+    return out
+
+
+def mlx4_pack(words, scales, biases, n: int, k: int, out=None, stream=None):
+    """MLX planar arrays -> MLX4 blocks uint8 [n, (k/32) * 20].  words holds
+    the [n, k/8] little-endian uint32 code words (any contiguous CUDA tensor
+    of n * k / 2 bytes, e.g. int32 [n, k/8]); scales and biases are fp16
+    [n, k/32]."""
+    import torch
+    if not isinstance(words, torch.Tensor) or not words.is_cuda or not words.is_contiguous():
+        raise TypeError("words must be a contiguous CUDA tensor")
+    if k % 32 or words.numel() * words.element_size() != n * k // 2:
+        raise ValueError("words must hold n * k / 2 bytes with k % 32 == 0")
+    for t, what in ((scales, "scales"), (biases, "biases")):
+        _require(t, torch.float16, what)
+        if t.numel() != n * (k // 32):
+            raise ValueError("%s must hold n * k / 32 values" % what)
+    if out is None:
+        out = torch.empty((n, (k // 32) * 20), dtype=torch.uint8, device=words.device)
+    _packed_check(out, MLX4, n, k, "out")
+    _check(load().m4q_mlx4_pack(words.data_ptr(), scales.data_ptr(), biases.data_ptr(), n, k,
+                                out.data_ptr(), _stream_ptr(stream)), "m4q_mlx4_pack")
     return out
 
 

@@ -15,9 +15,10 @@ namespace {
 
 using m4q::ProjLaunch;
 
-constexpr int kBlock[3] = {32, 32, 128};
-constexpr int kBlockBytes[3] = {18, 34, 34};
-constexpr int kStageBytes[3] = {144, 272, 272};    // bytes per packed stage
+constexpr int kCodecs = 4;
+constexpr int kBlock[kCodecs] = {32, 32, 128, 32};
+constexpr int kBlockBytes[kCodecs] = {18, 34, 34, 20};
+constexpr int kStageBytes[kCodecs] = {144, 272, 272, 160};    // bytes per packed stage
 
 // Default limit of one device pipeline wait (ns); M4Q_WAIT_LIMIT_NS overrides.
 unsigned long long wait_limit_ns() {
@@ -111,8 +112,10 @@ bool encode_heads(CUtensorMap* map, const void* base, uint64_t M, uint64_t N, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool known_codec(int codec) { return codec >= 0 && codec < kCodecs; }
+
 int check_shape(int codec, int64_t M, int64_t N, int64_t K) {
-  if (codec < 0 || codec > 2) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (!known_codec(codec)) return M4Q_ERR_UNSUPPORTED_CODEC;
   if (M < 1 || N < 1 || K < 1) return M4Q_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
   if (K % kBlock[codec] != 0 || N % 8 != 0) return M4Q_ERR_BAD_SHAPE;
@@ -151,7 +154,12 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
   L.swiglu = swiglu;
   L.act = act;
   L.head_dim = (int)head_dim;
-  L.wtma = (L.row_bytes % 16) == 0;  // then K is a multiple of the packed stage
+  // Rows that are 16-byte multiples move by TMA.  For the 18- and 34-byte
+  // blocks that makes K a multiple of the packed stage; for MLX4 (20-byte
+  // blocks) a multiple of 128, and the TMA box of the last stage of a row
+  // then reads past the row end, which it fills with zeros (zero scale and
+  // bias: zero weights, multiplied by zero-filled X columns).
+  L.wtma = (L.row_bytes % 16) == 0;
   L.status = m4q::status_words();
   if (!L.status) return M4Q_ERR_CUDA;
   L.limit_ns = wait_limit_ns();
@@ -204,6 +212,7 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     switch (codec) {
       case M4Q_Q4_0: e = m4q::launch_tc_q4_0(L); break;
       case M4Q_Q8_0: e = m4q::launch_tc_q8_0(L); break;
+      case M4Q_MLX4: e = m4q::launch_tc_mlx4(L); break;
       default: e = m4q::launch_tc_q2_0(L); break;
     }
   }
@@ -266,13 +275,13 @@ int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int c
 }
 
 size_t m4q_weight_bytes(int codec, int64_t N, int64_t K) {
-  if (codec < 0 || codec > 2 || N < 0 || K < 0 || K % kBlock[codec] != 0) return 0;
+  if (!known_codec(codec) || N < 0 || K < 0 || K % kBlock[codec] != 0) return 0;
   return (size_t)N * (size_t)(K / kBlock[codec]) * (size_t)kBlockBytes[codec];
 }
 
 int m4q_dequant(const void* W, int codec, int64_t N, int64_t K, void* Wf16, m4q_stream_t stream) {
   if (!W || !Wf16) return M4Q_ERR_INVALID_ARG;
-  if (codec < 0 || codec > 2) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (!known_codec(codec)) return M4Q_ERR_UNSUPPORTED_CODEC;
   if (N < 1 || K < 1 || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
   if (K % kBlock[codec] != 0) return M4Q_ERR_BAD_SHAPE;
   if (!aligned16(W) || !aligned16(Wf16)) return M4Q_ERR_MISALIGNED;
@@ -283,6 +292,24 @@ int m4q_dequant(const void* W, int codec, int64_t N, int64_t K, void* Wf16, m4q_
   const long long row_bytes = (K / kBlock[codec]) * (long long)kBlockBytes[codec];
   return m4q::launch_dequant(codec, W, (int)N, (int)K, row_bytes, Wf16,
                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M4Q_OK
+             : M4Q_ERR_CUDA;
+}
+
+int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int64_t N, int64_t K,
+                  void* W, m4q_stream_t stream) {
+  if (!words || !scales || !biases || !W) return M4Q_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
+  if (K % 32 != 0) return M4Q_ERR_BAD_SHAPE;
+  if (!aligned16(words) || !aligned16(W) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(biases) & 1u))
+    return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+  return m4q::launch_mlx4_pack(words, scales, biases, (int)N, (int)K, W,
+                               reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? M4Q_OK
              : M4Q_ERR_CUDA;
 }
@@ -332,7 +359,7 @@ const char* m4q_status_string(int status) {
     case M4Q_ERR_INVALID_ARG: return "invalid argument";
     case M4Q_ERR_UNSUPPORTED_CODEC: return "unsupported codec";
     case M4Q_ERR_BAD_SHAPE: return "bad shape (K must be a multiple of the block, N of 8)";
-    case M4Q_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case M4Q_ERR_MISALIGNED: return "pointer not aligned (16 bytes; fp16 scale and bias arrays 2 bytes)";
     case M4Q_ERR_CUDA: return "CUDA error";
     case M4Q_ERR_NONFINITE: return "non-finite values found";
     case M4Q_ERR_TIMEOUT: return "a device pipeline wait gave up";

@@ -1,5 +1,5 @@
-// codec.cuh -- device-side decoding of Q4_0, Q8_0 and PrismML Q2_0 blocks
-// into fp16 weights.
+// codec.cuh -- device-side decoding of Q4_0, Q8_0, PrismML Q2_0 and MLX
+// 4-bit affine blocks into fp16 weights.
 //
 // Codecs (m4-prefill-engine "Releases" page, v0.3.0 and v0.2.3; GGUF for the
 // byte layout of Q4_0 / Q8_0):
@@ -7,6 +7,9 @@
 //   Q8_0  32 weights, 34 B: fp16 d, 32 signed bytes  w = q * d
 //   Q2_0 128 weights, 34 B: fp16 d, 32 B of 2-bit codes, w = (q - 1) * d,
 //         the reserved code 3 giving +2d.
+//   MLX4  32 weights, 20 B: fp16 scale s, fp16 bias b, 16 B of nibbles
+//         (code 2i in the low nibble of byte i), w = q * s + b (project page
+//         section 4 and Table B: the 20-byte block_mlx_4bit; group size 32).
 //
 // Every weight is produced with exactly one rounding: the code is placed in
 // the fraction field of an fp16 whose exponent makes one fraction step worth
@@ -14,11 +17,13 @@
 // an fp16 subtract (the difference is a small integer), and the integer is
 // multiplied by d with one round-to-nearest-even fp16 multiply.  The result is
 // therefore RNE((q - z) * d), bit for bit, including subnormals and -0.
+// MLX4 recovers q the same way and finishes with one fused multiply-add,
+// RNE(q * s + b).
 //
 // A "packed stage" is 8 consecutive blocks of one weight row: 144 B (Q4_0),
-// 272 B (Q8_0, Q2_0), a multiple of 16 bytes so that TMA can move it.  It
-// covers KP = 256 (Q4_0, Q8_0) or 1024 (Q2_0) weights, split into SUB
-// sub-steps of 64 weights each.
+// 272 B (Q8_0, Q2_0), 160 B (MLX4), a multiple of 16 bytes so that TMA can
+// move it.  It covers KP = 256 (Q4_0, Q8_0, MLX4) or 1024 (Q2_0) weights,
+// split into SUB sub-steps of 64 weights each.
 #pragma once
 
 #include "common.cuh"
@@ -39,6 +44,10 @@ struct CodecTraits<kQ8_0> {
 template <>
 struct CodecTraits<kQ2_0> {
   static constexpr int B = 128, BB = 34;
+};
+template <>
+struct CodecTraits<kMLX4> {
+  static constexpr int B = 32, BB = 20;
 };
 
 template <int C>
@@ -61,6 +70,13 @@ __device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// a * b + c with one round-to-nearest-even (fused).
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
 
@@ -100,6 +116,19 @@ __device__ __forceinline__ void q2_byte(uint32_t t, uint32_t d2, uint32_t& p01, 
   p23 = hmul2_rn(hsub2_rn((t & 0x00C00030u) | 0x4C005400u, 0x4C405410u), d2);  // -(17, 65)
 }
 
+// MLX4 byte [v,0,v,0]: low nibble -> 1024 + q0, high nibble -> 64 + q1;
+// subtract the biases exactly, then one fused q * s + b per half.
+__device__ __forceinline__ uint32_t mlx_pair(uint32_t t, uint32_t s2, uint32_t b2) {
+  return hfma2_rn(hsub2_rn((t & 0x00F0000Fu) | 0x54006400u, 0x54006400u), s2, b2);
+}
+
+// MLX4 scale and bias of the block at even byte offset bo, each duplicated
+// into both halves.
+__device__ __forceinline__ void mlx_scale_bias(const uint32_t* w, int bo, uint32_t& s2, uint32_t& b2) {
+  s2 = dup_scale(u16_at(w, bo));
+  b2 = dup_scale(u16_at(w, bo + 2));
+}
+
 // Decode sub-step j (weights 64j .. 64j+63 of a packed stage) of one row
 // into out[i] = fp16x2 (w[64j + 2i], w[64j + 2i + 1]).  `w` holds the row's
 // packed stage bytes; j must be a compile-time constant after unrolling.
@@ -130,6 +159,18 @@ __device__ __forceinline__ void decode_sub<kQ8_0>(const uint32_t* w, int j, uint
     const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
     for (int p = 0; p < 16; ++p) out[16 * h + p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+  }
+}
+
+template <>
+__device__ __forceinline__ void decode_sub<kMLX4>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int bo = (2 * j + h) * 20;
+    uint32_t s2, b2;
+    mlx_scale_bias(w, bo, s2, b2);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) out[16 * h + p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2);
   }
 }
 
@@ -167,6 +208,12 @@ __device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (
     const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
     for (int p = 0; p < 16; ++p) out[p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+  } else if constexpr (C == kMLX4) {
+    const int bo = (2 * j + G) * 20;
+    uint32_t s2, b2;
+    mlx_scale_bias(w, bo, s2, b2);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) out[p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2);
   } else {
     const int bo = (j >> 1) * 34;
     const int cb = bo + 2 + 16 * (j & 1) + 8 * G;  // 8 code bytes = 32 weights

@@ -9,7 +9,7 @@
 namespace m4q {
 
 // Codec ids (same values as enum m4q_codec in include/m4q.h).
-enum : int { kQ4_0 = 0, kQ8_0 = 1, kQ2_0 = 2 };
+enum : int { kQ4_0 = 0, kQ8_0 = 1, kQ2_0 = 2, kMLX4 = 3 };
 
 // Status-word bits written by kernels whose bounded waits gave up.
 enum : uint32_t { kErrWaitTimeout = 1u, kErrAborted = 2u };

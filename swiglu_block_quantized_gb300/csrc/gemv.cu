@@ -70,6 +70,7 @@ cudaError_t launch_gemv(int codec, const ProjLaunch& L) {
   switch (codec) {
     case kQ4_0: return launch_gemv_codec<kQ4_0>(L);
     case kQ8_0: return launch_gemv_codec<kQ8_0>(L);
+    case kMLX4: return launch_gemv_codec<kMLX4>(L);
     default: return launch_gemv_codec<kQ2_0>(L);
   }
 }

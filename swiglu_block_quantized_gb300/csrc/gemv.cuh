@@ -65,7 +65,12 @@ struct GemvCfg {
   using S = Stage<C>;
   static constexpr int kConsumers = 16;
   static constexpr int kThreads = 32 * (kConsumers + 2);
-  static constexpr int kSBMax = (2400 / S::KPB) * S::KPB;   // 2304 (Q4_0) or 2176 B
+  // Largest stage <= 2400 B that splits into 16 equal runs of whole blocks:
+  // 2304 (Q4_0), 2176 (Q8_0, Q2_0).  MLX4 takes 2560 B, a whole K = 4096 row,
+  // so that rows of that length stay one stage with the X fragments held in
+  // registers (11% faster at M = 1 than 2240 + 320 B stages, although the
+  // ring then holds only two stages).
+  static constexpr int kSBMax = C == kMLX4 ? 2560 : (2400 / (16 * S::BB)) * 16 * S::BB;
   static constexpr int kBlocks = kSBMax / S::BB;             // blocks of a full stage
   static constexpr int kXH = kBlocks / kConsumers;           // blocks per warp of a full stage
   static constexpr int kRingBytes = 160 * 1024;
@@ -120,7 +125,7 @@ __device__ __forceinline__ void ldx(uint32_t* dst, const __half* xrow, bool ok) 
 // X fragments of one block for activation rows g and g + 8 (zero past M).
 template <int C>
 struct XFrag {
-  static constexpr int kRegs = C == kQ4_0 ? 4 : C == kQ8_0 ? 4 : 16;
+  static constexpr int kRegs = C == kQ2_0 ? 16 : 4;
 };
 
 template <int C, int MT>
@@ -134,7 +139,7 @@ __device__ __forceinline__ void load_xfrag(const GemvParams& p, int g, int t, in
     if constexpr (C == kQ4_0) {
       ldx<8>(&xf[mt][0], xr + 4 * t, ok);
       ldx<8>(&xf[mt][2], xr + 16 + 4 * t, ok);
-    } else if constexpr (C == kQ8_0) {
+    } else if constexpr (C == kQ8_0 || C == kMLX4) {
       ldx<16>(&xf[mt][0], xr + 8 * t, ok);
     } else {
       ldx<64>(&xf[mt][0], xr + 32 * t, ok);
@@ -172,6 +177,24 @@ __device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1,
     for (int i = 0; i < 4; ++i) {
       w[0][i] = q8_pair(spread16(lds_u16(c0 + 2 * i)), d0);
       w[1][i] = q8_pair(spread16(lds_u16(c1 + 2 * i)), d1);
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      mma_16816(acc[mt], w[0][0], w[1][0], w[0][1], w[1][1], xf[mt][0], xf[mt][1]);
+      mma_16816(acc[mt], w[0][2], w[1][2], w[0][3], w[1][3], xf[mt][2], xf[mt][3]);
+    }
+  } else if constexpr (C == kMLX4) {
+    // Thread t: code bytes 4t .. 4t+3 = weights 8t .. 8t+7 in natural order,
+    // the same k slots as Q8_0 (and the same X fragments).
+    const uint32_t b0 = dup_scale(lds_u16(r0 + 2)), b1 = dup_scale(lds_u16(r1 + 2));
+    const uint32_t v0 = *reinterpret_cast<const uint32_t*>(r0 + 4 + 4 * t);
+    const uint32_t v1 = *reinterpret_cast<const uint32_t*>(r1 + 4 + 4 * t);
+    uint32_t w[2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t sel = 0x4040u | (uint32_t)(i << 8) | (uint32_t)i;  // byte i, replicated
+      w[0][i] = mlx_pair(__byte_perm(v0, 0u, sel), d0, b0);
+      w[1][i] = mlx_pair(__byte_perm(v1, 0u, sel), d1, b1);
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {

@@ -22,7 +22,8 @@ struct ProjLaunch {
   bool swiglu;            // gated projection (gate and up weights)
   int act;                // gate activation: 0 SiLU, 1 GELU
   int head_dim;           // GEMM output: 0 row-major [M, N], else head-major [N / head_dim][M][head_dim]
-  bool wtma;              // packed rows are 16-byte multiples: weights move by TMA
+  bool wtma;              // packed rows are 16-byte multiples: weights move by TMA (a
+                          // last stage past the row end is zero-filled)
   uint32_t* status;       // device status word
   unsigned long long limit_ns;
   cudaStream_t stream;
@@ -48,6 +49,7 @@ std::atomic<unsigned long long>& attr_flag() {
 cudaError_t launch_tc_q4_0(const ProjLaunch& L);
 cudaError_t launch_tc_q8_0(const ProjLaunch& L);
 cudaError_t launch_tc_q2_0(const ProjLaunch& L);
+cudaError_t launch_tc_mlx4(const ProjLaunch& L);
 cudaError_t launch_gemv(int codec, const ProjLaunch& L);
 
 // misc.cu
@@ -56,5 +58,7 @@ cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row
                            cudaStream_t s);
 cudaError_t launch_finite_check(const void* x, long long n, uint32_t* flag, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
+cudaError_t launch_mlx4_pack(const void* words, const void* scales, const void* biases, int N, int K,
+                             void* w, cudaStream_t s);
 
 }  // namespace m4q

@@ -73,8 +73,43 @@ cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row
   switch (codec) {
     case kQ4_0: dequant_kernel<kQ4_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
     case kQ8_0: dequant_kernel<kQ8_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
+    case kMLX4: dequant_kernel<kMLX4><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
     default: dequant_kernel<kQ2_0><<<blocks, 256, 0, s>>>(W, N, K, row_bytes, O); break;
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- MLX4 pack
+
+// MLX's planar arrays -> 20-byte MLX4 blocks.  In MLX's word order (code k of
+// a row at bits 4 (k % 8) of word k / 8, little-endian) the 16 code bytes of a
+// 32-weight group are exactly the 4 words of that group, so a block is the
+// group's scale and bias followed by those words, copied unchanged.  One
+// thread per block, grid-stride.
+__global__ void __launch_bounds__(256)
+    mlx4_pack_kernel(const uint4* __restrict__ words, const unsigned short* __restrict__ scales,
+                     const unsigned short* __restrict__ biases, long long blocks,
+                     uint32_t* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < blocks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 q = __ldg(words + i);  // a row of K/8 words is K/32 groups of 4
+    uint32_t* dst = out + 5 * i;       // 20-byte blocks, rows back to back
+    dst[0] = (uint32_t)__ldg(scales + i) | ((uint32_t)__ldg(biases + i) << 16);
+    dst[1] = q.x;
+    dst[2] = q.y;
+    dst[3] = q.z;
+    dst[4] = q.w;
+  }
+}
+
+cudaError_t launch_mlx4_pack(const void* words, const void* scales, const void* biases, int N, int K,
+                             void* w, cudaStream_t s) {
+  const long long blocks = (long long)N * (K / 32);
+  long long grid = (blocks + 255) / 256;
+  if (grid > 152 * 16) grid = 152 * 16;
+  mlx4_pack_kernel<<<(unsigned)grid, 256, 0, s>>>(
+      static_cast<const uint4*>(words), static_cast<const unsigned short*>(scales),
+      static_cast<const unsigned short*>(biases), blocks, static_cast<uint32_t*>(w));
   return cudaGetLastError();
 }
 

@@ -59,7 +59,7 @@ struct TcCfg {
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kRows = 128;                               // MMA M
   static constexpr int kOutRows = SWIGLU ? 64 : 128;              // outputs n per tile
-  static constexpr int kSW = WTMA ? (S::KPB <= 144 ? 3 : 2) : 0;  // packed-W ring depth
+  static constexpr int kSW = WTMA ? (S::KPB <= 160 ? 3 : 2) : 0;  // packed-W ring depth
   static constexpr int kSA = 8;                                   // TMEM A ring depth
   static constexpr int kXStage = NX * 128;                        // bytes
   static constexpr int kWStage = kRows * S::KPB;                  // bytes

@@ -42,6 +42,7 @@ def test_weight_bytes(lib):
     assert m.weight_bytes(m.Q8_0, 8192, 2048) == 8192 * 64 * 34
     assert m.weight_bytes(m.Q2_0, 4096, 4096) == 4096 * 32 * 34
     assert m.weight_bytes(m.Q2_0, 4096, 4000) == 0      # K not a multiple of 128
+    assert m.weight_bytes(m.MLX4, 8192, 2048) == 8192 * 64 * 20
     assert m.weight_bytes(7, 16, 32) == 0
 
 
@@ -86,6 +87,15 @@ def test_argument_errors_return_before_any_cuda_call(lib):
     assert lib.m4q_mlp(P(good), P(good), P(good), P(good), 0, 1, 4, 64, 128, P(good), P(good), 5, s) == m.ERR_INVALID_ARG
     assert lib.m4q_dequant(None, 0, 8, 32, P(good), s) == m.ERR_INVALID_ARG
     assert lib.m4q_dequant(P(good), 0, 8, 40, P(good), s) == m.ERR_BAD_SHAPE
+    assert lib.m4q_dequant(P(good), 4, 8, 32, P(good), s) == m.ERR_UNSUPPORTED_CODEC
+    assert lib.m4q_gemm(P(good), P(good), 3, 4, 8, 48, P(good), s) == m.ERR_BAD_SHAPE   # MLX4 K % 32
+    assert lib.m4q_mlx4_pack(None, P(good), P(good), 8, 32, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_mlx4_pack(P(good), P(good), P(good), 0, 32, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_mlx4_pack(P(good), P(good), P(good), 8, 48, P(good), s) == m.ERR_BAD_SHAPE
+    assert lib.m4q_mlx4_pack(P(good + 4), P(good), P(good), 8, 32, P(good), s) == m.ERR_MISALIGNED
+    assert lib.m4q_mlx4_pack(P(good), P(good + 1), P(good), 8, 32, P(good), s) == m.ERR_MISALIGNED
+    assert lib.m4q_mlx4_pack(P(good), P(good), P(good + 3), 8, 32, P(good), s) == m.ERR_MISALIGNED
+    assert lib.m4q_mlx4_pack(P(good), P(good), P(good), 8, 32, P(good + 4), s) == m.ERR_MISALIGNED
     assert lib.m4q_check_finite(None, 10, s) == m.ERR_INVALID_ARG
     assert lib.m4q_selftest_wait_timeout(10, s) == m.ERR_INVALID_ARG
 

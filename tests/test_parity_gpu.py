@@ -16,7 +16,7 @@ from _helpers import TOL, assert_close, dev, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-CODECS = [synth.Q4_0, synth.Q8_0, synth.Q2_0]
+CODECS = [synth.Q4_0, synth.Q8_0, synth.Q2_0, synth.MLX4]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -34,6 +34,9 @@ def kvals(codec, general):
     """K values: multiples of the packed stage (TMA weights) or not (plain loads)."""
     if codec == synth.Q2_0:
         return [1024, 2048] if not general else [128, 384, 1152]
+    if codec == synth.MLX4:
+        # 384: 240-byte rows, TMA-able, the last 160-byte stage half past the row end
+        return [256, 384] if not general else [32, 96, 288]
     return [256, 512] if not general else [32, 96, 288]
 
 
@@ -64,6 +67,43 @@ def test_dequant_special_scales(codec):
     nan &= (ref & 0x03FF) != 0
     assert np.array_equal(got[~nan], ref[~nan])
     assert np.all(((got[nan] & 0x7C00) == 0x7C00) & ((got[nan] & 0x3FF) != 0))
+
+
+@pytest.mark.parametrize("K", [32, 256, 384])
+def test_mlx4_dequant_special_biases(K):
+    # Biases that are subnormal, signed zeros, large (q * s + b overflows to
+    # inf for the larger codes) or NaN, with ordinary and zero scales.
+    N = 16
+    specials = np.array([0x0001, 0x8000, 0x0000, 0x7BFF, 0xFBFF, 0x7E00, 0x3555, 0xB001],
+                        dtype=np.uint16).view(np.float16)
+    nb = K // 32
+    q = synth.codes(synth.MLX4, N, K, seed=K, name="W")
+    d = np.where(np.arange(N * nb).reshape(N, nb) % 3 == 0, np.float16(0), np.float16(2.0)).astype(np.float16)
+    b = specials[np.arange(N * nb).reshape(N, nb) % len(specials)]
+    W = synth.pack(synth.MLX4, q, d, b)
+    got = host(m.dequant(dev(W), synth.MLX4, N, K)).view(np.uint16)
+    ref = oracle.dequant_f16(W, synth.MLX4, N, K)
+    nan = ((ref & 0x7C00) == 0x7C00) & ((ref & 0x03FF) != 0)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(((got[nan] & 0x7C00) == 0x7C00) & ((got[nan] & 0x3FF) != 0))
+
+
+@pytest.mark.parametrize("N,K", [(8, 32), (40, 256), (264, 4096), (3000, 2048)])
+def test_mlx4_pack_bit_exact(N, K):
+    # MLX planar arrays -> blocks on the GPU equals the oracle's repack byte
+    # for byte, and the repacked weights project like the generator's blocks.
+    import torch
+    q = synth.codes(synth.MLX4, N, K, seed=N, name="W")
+    d = synth.scales(synth.MLX4, N, K, seed=N, name="W")
+    b = synth.biases(synth.MLX4, N, K, seed=N, name="W", d=d)
+    words, s, bb = synth.planar(q, d, b)
+    wt = torch.from_numpy(words.view(np.int32)).cuda()
+    got = host(m.mlx4_pack(wt, dev(s), dev(bb), N, K))
+    assert np.array_equal(got, oracle.mlx4_pack(words, s, bb, N, K))
+    if N <= 264:
+        X = synth.activations(20, K, seed=5)
+        Y = host(m.gemm(dev(X), dev(got), synth.MLX4, N, K))
+        assert_close(Y, oracle.gemm(X, synth.pack(synth.MLX4, q, d, b), synth.MLX4, 20, N, K), "packed mlx4")
 
 
 # ------------------------------------------------------------ tcgen05 path
@@ -159,7 +199,8 @@ def mlp_reference(X, Wg, Wu, Wd, cgu, cd, M, D, F, act):
 
 
 @pytest.mark.parametrize("M", [1, 3, 40])
-@pytest.mark.parametrize("cgu,cd", [(synth.Q4_0, synth.Q4_0), (synth.Q4_0, synth.Q8_0), (synth.Q2_0, synth.Q8_0)])
+@pytest.mark.parametrize("cgu,cd", [(synth.Q4_0, synth.Q4_0), (synth.Q4_0, synth.Q8_0), (synth.Q2_0, synth.Q8_0),
+                                    (synth.MLX4, synth.MLX4)])
 @pytest.mark.parametrize("act", [0, 1])
 def test_mlp_parity(M, cgu, cd, act):
     D, F = 256, 1024
@@ -222,7 +263,9 @@ def test_gemv_parity(codec, general, M):
 
 
 @pytest.mark.parametrize("codec,K", [(synth.Q4_0, 4352), (synth.Q8_0, 2304), (synth.Q2_0, 5120),
-                                     (synth.Q4_0, 2400), (synth.Q8_0, 2080), (synth.Q2_0, 5248)])
+                                     (synth.MLX4, 4096),
+                                     (synth.Q4_0, 2400), (synth.Q8_0, 2080), (synth.Q2_0, 5248),
+                                     (synth.MLX4, 4000)])
 @pytest.mark.parametrize("M", [1, 11])
 def test_gemv_long_rows(codec, K, M):
     # Rows longer than one streamed stage, with a ragged last stage; the
