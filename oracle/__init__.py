@@ -25,6 +25,7 @@ _lock = threading.Lock()
 _lib = None
 
 Q4_0, Q8_0, Q2_0, MLX4 = 0, 1, 2, 3
+KV_F16 = 16   # fp16 KV cache values (the other KV cache codec is Q8_0)
 CODEC_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q2_0: "Q2_0", MLX4: "MLX4"}
 
 
@@ -71,6 +72,9 @@ def _bind(path: str):
     lib.oracle_gelu.restype = ctypes.c_double
     lib.oracle_mlx4_pack.argtypes = [vp, vp, vp, i64, i64, vp]
     lib.oracle_mlx4_pack.restype = i32
+    lib.oracle_attention.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32,
+                                     ctypes.c_double, vp, i64, vp, i32]
+    lib.oracle_attention.restype = i32
     return lib
 
 
@@ -244,4 +248,26 @@ def geglu(X, Wg, Wu, codec: int, M: int, N: int, K: int, rows=None,
                               None if r is None else _ptr(r), nrows, _ptr(out),
                               nthreads or default_threads())
     _check(rc, "geglu")
+    return out
+
+
+def attention(Q, K, V, kv_codec: int, H: int, Hkv: int, M: int, T: int, D: int,
+              q_offset: int = 0, causal: bool = True, scale: float | None = None, rows=None,
+              nthreads: int | None = None):
+    """binary64 O [len(rows) or M, H * D]: softmax attention of fp16 Q
+    [H, M, D] over the KV cache K, V [Hkv, T, D] (fp16 values for KV_F16, or
+    Q8_0 blocks along D as uint8 [Hkv, T, D / 32 * 34])."""
+    Qb = _as_xbits(Q)
+    if kv_codec == KV_F16:
+        Kb = np.ascontiguousarray(np.asarray(K, dtype=np.float16)).view(np.uint8)
+        Vb = np.ascontiguousarray(np.asarray(V, dtype=np.float16)).view(np.uint8)
+    else:
+        Kb, Vb = _as_packed(K), _as_packed(V)
+    r, nrows = _rows_arg(rows, M)
+    out = np.empty((nrows, H * D), dtype=np.float64)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    rc = _L().oracle_attention(_ptr(Qb), _ptr(Kb), _ptr(Vb), kv_codec, H, Hkv, M, T, D, q_offset,
+                               int(bool(causal)), sc, None if r is None else _ptr(r), nrows, _ptr(out),
+                               nthreads or default_threads())
+    _check(rc, "attention")
     return out

@@ -32,6 +32,18 @@
  *    codes, w = q * s + b.  The planar form of the same weights (section 4:
  *    codes, scales and biases in separate 16-byte aligned arrays) is MLX's
  *    own storage, 32-bit words of eight codes each.
+ *  - "v0.1 vs v0.2 comparison", section 2.3 (Brick 4: FlashAttention with a
+ *    Q8_0 KV cache, dequantized on the fly), "Releases" v0.3.0
+ *    (TransformerBlock: grouped-query attention, causal masking, RoPE
+ *    sequence offsets; flash_attn core for head dims 64 and 128) and the
+ *    project page, section 4 (Q, K, V projected straight into [H, M, D]):
+ *    softmax attention O = softmax(scale * Q K^T) V per head, query head h
+ *    reading KV head h / (H / Hkv), query i seeing keys j <= q_offset + i
+ *    when causal.  FlashAttention computes exactly this (its online softmax
+ *    is a reordering), so the oracle is the definition: scores, one max,
+ *    exponentials, one sum, the weighted sum of V.  K and V cache values
+ *    are the fp16 operands the attention multiplies: fp16 as stored, or a
+ *    Q8_0 block along the head dimension decoded and rounded once to fp16.
  *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
  *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
  *    activation written out.
@@ -357,4 +369,122 @@ int oracle_geglu(const uint16_t* X, const uint8_t* Wg, const uint8_t* Wu, int co
                  long long nrows, double* Y, int nthreads) {
   if (!Wu) return -1;
   return project(X, Wg, Wu, codec, ORACLE_ACT_GELU, M, N, K, rows, nrows, Y, nthreads);
+}
+
+/* ---- attention over a KV cache ---- */
+
+enum { ORACLE_KV_F16 = 16 };
+
+typedef struct {
+  const uint16_t* Q;    /* fp16 bits [H, M, D] */
+  const uint8_t* K;     /* [Hkv, T] rows of D values: fp16 or Q8_0 blocks */
+  const uint8_t* V;
+  int kv_codec;
+  long long H, Hkv, M, T, D, q_offset;
+  int causal;
+  double scale;
+  const long long* qrows; /* query indices to compute (NULL: all M) */
+  long long nq;
+  long long h_begin, h_end;
+  double* O;            /* [nq, H * D] */
+  int rc;
+} attn_job_t;
+
+/* Row j of one KV head as binary64 values of the fp16 operands. */
+static void kv_row(const uint8_t* base, int kv_codec, long long D, double* out) {
+  if (kv_codec == ORACLE_KV_F16) {
+    const uint16_t* h = (const uint16_t*)base;
+    for (long long d = 0; d < D; ++d) out[d] = oracle_half_to_double(h[d]);
+    return;
+  }
+  dequant_row(base, ORACLE_Q8_0, D, out);
+  round_row_to_f16(out, D);
+}
+
+static void* run_attn(void* arg) {
+  attn_job_t* j = (attn_job_t*)arg;
+  const long long D = j->D, T = j->T, G = j->H / j->Hkv;
+  const long long kv_bytes = j->kv_codec == ORACLE_KV_F16 ? 2 * D : (D / 32) * 34;
+  double* Kd = (double*)malloc(sizeof(double) * (size_t)(T * D > 0 ? T * D : 1));
+  double* Vd = (double*)malloc(sizeof(double) * (size_t)(T * D > 0 ? T * D : 1));
+  double* s = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+  double* q = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!Kd || !Vd || !s || !q) { free(Kd); free(Vd); free(s); free(q); j->rc = -8; return NULL; }
+  long long cached = -1;
+  for (long long h = j->h_begin; h < j->h_end; ++h) {
+    const long long hk = h / G;
+    if (hk != cached) {
+      for (long long t = 0; t < T; ++t) {
+        kv_row(j->K + (hk * T + t) * kv_bytes, j->kv_codec, D, Kd + t * D);
+        kv_row(j->V + (hk * T + t) * kv_bytes, j->kv_codec, D, Vd + t * D);
+      }
+      cached = hk;
+    }
+    for (long long r = 0; r < j->nq; ++r) {
+      const long long i = j->qrows ? j->qrows[r] : r;
+      for (long long d = 0; d < D; ++d) q[d] = oracle_half_to_double(j->Q[(h * j->M + i) * D + d]);
+      long long nvis = T;
+      if (j->causal && j->q_offset + i + 1 < nvis) nvis = j->q_offset + i + 1;
+      double* o = j->O + r * j->H * D + h * D;
+      if (nvis <= 0) {
+        for (long long d = 0; d < D; ++d) o[d] = 0.0;
+        continue;
+      }
+      double mx = -INFINITY;
+      for (long long t = 0; t < nvis; ++t) {
+        s[t] = j->scale * dot(q, Kd + t * D, D);
+        if (s[t] > mx) mx = s[t];
+      }
+      double l = 0.0;
+      for (long long t = 0; t < nvis; ++t) {
+        s[t] = exp(s[t] - mx);
+        l += s[t];
+      }
+      for (long long d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (long long t = 0; t < nvis; ++t) acc += s[t] * Vd[t * D + d];
+        o[d] = acc / l;
+      }
+    }
+  }
+  free(Kd); free(Vd); free(s); free(q);
+  j->rc = 0;
+  return NULL;
+}
+
+/* O[r, h*D + d] = sum_j softmax_j(scale * Q[h, i] . K[hk, j]) V[hk, j, d] for
+ * query i = qrows[r] (all M when qrows is NULL), over the keys the query
+ * sees.  kv_codec: ORACLE_KV_F16 (fp16 bits) or ORACLE_Q8_0 (D % 32 == 0).
+ * A query that sees no key (causal with q_offset + i < 0) gets O = 0.
+ * Returns 0 or a negative code. */
+int oracle_attention(const uint16_t* Q, const uint8_t* K, const uint8_t* V, int kv_codec,
+                     long long H, long long Hkv, long long M, long long T, long long D,
+                     long long q_offset, int causal, double scale, const long long* qrows,
+                     long long nq, double* O, int nthreads) {
+  if (kv_codec != ORACLE_KV_F16 && kv_codec != ORACLE_Q8_0) return -2;
+  if (H < 1 || Hkv < 1 || H % Hkv != 0 || M < 0 || T < 0 || D < 1) return -3;
+  if (kv_codec == ORACLE_Q8_0 && D % 32 != 0) return -3;
+  if (!qrows) nq = M;
+  for (long long r = 0; qrows && r < nq; ++r)
+    if (qrows[r] < 0 || qrows[r] >= M) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if (H < nthreads) nthreads = (int)H;
+  attn_job_t jobs[256];
+  pthread_t tids[256];
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (attn_job_t){Q, K, V, kv_codec, H, Hkv, M, T, D, q_offset, causal, scale, qrows, nq,
+                           H * t / nthreads, H * (t + 1) / nthreads, O, 0};
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, run_attn, &jobs[t]) != 0) break;
+    started = t;
+  }
+  run_attn(&jobs[0]);
+  for (int t = started + 1; t < nthreads; ++t) run_attn(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+  for (int t = 0; t < nthreads; ++t)
+    if (jobs[t].rc) return jobs[t].rc;
+  return 0;
 }

@@ -222,6 +222,28 @@ def constant_weights(codec: int, N: int, K: int, code: int, d_f16, b_f16=0.0) ->
     return pack(codec, q, d, b if codec == MLX4 else None)
 
 
+# ---------------------------------------------------------------- KV cache
+
+KV_F16 = 16   # fp16 KV cache values; the quantized KV cache uses Q8_0
+
+
+def kv_cache(codec: int, Hkv: int, T: int, D: int, seed: int, name: str) -> np.ndarray:
+    """One KV cache tensor [Hkv, T, D] by token rows: fp16 values ~ N(0,1)
+    (KV_F16), or Q8_0 blocks along D by the Q8_0 recipe, uint8 [Hkv, T,
+    D / 32 * 34]."""
+    if codec == KV_F16:
+        return activations(Hkv * T, D, seed, name).reshape(Hkv, T, D)
+    if codec == Q8_0:
+        return weights(Q8_0, Hkv * T, D, seed, name).reshape(Hkv, T, row_bytes(Q8_0, D))
+    raise ValueError("KV cache codec must be KV_F16 or Q8_0")
+
+
+def queries(H: int, M: int, D: int, seed: int, name: str = "Q") -> np.ndarray:
+    """Q fp16 [H, M, D] ~ N(0,1) (head-major, as the direct-head projection
+    writes it)."""
+    return activations(H * M, D, seed, name).reshape(H, M, D)
+
+
 # ---------------------------------------------------------------- workloads
 # Shapes of the pages' LLaMA-shaped layers (1B tier: hidden 2048, MLP 8192;
 # 8B tier: hidden 4096, MLP 14336).  Each entry: (kind, codec, M, N, K).

@@ -77,3 +77,11 @@ def test_mlx4_planar_and_block_layouts():
     assert np.array_equal(W[:, :, 2:4].copy().view("<u2")[..., 0], b.view("<u2"))
     # the 16 code bytes of a block are the planar words' bytes of that group
     assert np.array_equal(W[:, :, 4:].reshape(N, -1), words.view(np.uint8).reshape(N, -1))
+
+
+def test_kv_cache_layouts():
+    K = synth.kv_cache(synth.KV_F16, 2, 10, 64, 0, "K")
+    assert K.dtype == np.float16 and K.shape == (2, 10, 64)
+    Kq = synth.kv_cache(synth.Q8_0, 2, 10, 128, 0, "K")
+    assert Kq.dtype == np.uint8 and Kq.shape == (2, 10, 4 * 34)
+    assert synth.queries(4, 3, 64, 0).shape == (4, 3, 64)
