@@ -348,6 +348,7 @@ def run_ours(args, ws, rank, local):
            "weights": "resident in HBM (model parameters)"}
 
     mlx4 = measure_mlx4(m, X, dev, steps=max(20, min(args.steps, 200)))
+    attention = measure_attention(m, dev)
 
     if rank != 0:
         return
@@ -361,7 +362,8 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs rotate through %d distinct copies (%.0f MB > L2)"
                          % (ROTATE, ROTATE * (X.nbytes + Wg.nbytes + Wu.nbytes + M_ * N_ * 2) / 1e6),
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "roofline": roofline, "m1": m1, "e2e": e2e, "mlx4": mlx4, "cpu_baseline": cpu, "clocks": clocks,
+        "roofline": roofline, "m1": m1, "e2e": e2e, "mlx4": mlx4, "attention": attention,
+        "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
@@ -417,6 +419,64 @@ def measure_mlx4(m, X, dev, steps):
             "frac": tflops / pk["bf16_tflops"],
             "m1": {"workload": "8b_swiglu_mlx4_m1", "value": gbs, "unit": "GB/s", "us_per_launch": 1e3 * m1_ms,
                    "bytes_per_launch": m1_bytes, "frac": gbs / pk["hbm_gbs"]}}
+
+
+def measure_attention(m, dev, reps=20):
+    """Attention of the 8B layer (H = 32, 8 KV heads, D = 128) over an fp16
+    and a Q8_0 KV cache: causal prefill M = T = 2048 (TFLOP/s, causal FLOPs
+    4 H D sum_i (i + 1)) and one decode token over T = 32768 (GB/s of KV
+    cache read).  CUDA events around `reps` launches."""
+    import torch
+
+    import synth
+    H, Hkv, D = 32, 8, 128
+    out = {}
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pk, _ = peaks()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for name, codec in (("q8_0", synth.Q8_0), ("f16", synth.KV_F16)):
+        M = T = 2048
+        q = torch.from_numpy(synth.queries(H, M, D, seed=1)).to(dev)
+        k = torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=2, name="K")).to(dev)
+        v = torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=2, name="V")).to(dev)
+        o = torch.empty((M, H * D), dtype=torch.float16, device=dev)
+        ms = timed(lambda: m.attention(q, k, v, codec, Hkv, T, q_offset=0, out=o))
+        flops = 4.0 * H * D * (M * (M + 1) / 2)
+        out["prefill_" + name] = {"workload": "8b_attention_causal_m2048_t2048_%s" % name,
+                                  "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_launch": ms}
+        T = 32768
+        q1 = torch.from_numpy(synth.queries(H, 1, D, seed=3)).to(dev)
+        kc = [torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=4 + r, name="K")).to(dev) for r in range(2)]
+        vc = [torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=4 + r, name="V")).to(dev) for r in range(2)]
+        o1 = torch.empty((1, H * D), dtype=torch.float16, device=dev)
+        ws = torch.empty(max(1, m.load().m4q_attention_workspace_bytes(H, Hkv, 1, T, D)), dtype=torch.uint8,
+                         device=dev)
+        it = [0]
+
+        def dec():
+            j = it[0] % 2
+            it[0] += 1
+            m.attention(q1, kc[j], vc[j], codec, Hkv, T, out=o1, workspace=ws)
+        ms = timed(dec)
+        kv_bytes = 2 * kc[0].numel() * kc[0].element_size()
+        out["decode_" + name] = {"workload": "8b_attention_decode_t32768_%s" % name,
+                                 "value": kv_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "us_per_launch": 1e3 * ms,
+                                 "kv_bytes": kv_bytes, "frac": kv_bytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                 "l2": "two cache copies alternate (%.0f MB each)" % (kv_bytes / 1e6)}
+    assert m.check_device_status() == m.OK
+    return out
 
 
 def run_profile_case(case, local):

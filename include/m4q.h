@@ -176,6 +176,41 @@ int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* W
 int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int64_t N, int64_t K,
                   void* W, m4q_stream_t stream);
 
+/* KV cache value formats for m4q_attention: fp16 values, or M4Q_Q8_0 blocks
+ * along the head dimension. */
+enum m4q_kv_codec { M4Q_KV_F16 = 16 };
+
+/* Attention of fp16 queries over a KV cache ("v0.1 vs v0.2 comparison" 2.3:
+ * FlashAttention with the Q8_0 KV cache dequantized on the fly; "Releases"
+ * v0.3.0: grouped-query attention, causal masking with a sequence offset,
+ * head dims 64 and 128; v0.2: chunked attention, running max and sum merged
+ * exactly across key chunks):
+ *   O[i, h*D + d] = sum_j softmax_j(scale * Q[h, i, :] . K[h / G, j, :]) V[h / G, j, d]
+ * with G = H / Hkv, over keys j < T, and, when causal != 0, j <= q_offset + i.
+ *  - Q: fp16 [H, M, D] (head-major, as m4q_gemm_heads writes it).
+ *  - K, V: [Hkv, T] rows of D values: fp16 (kv_codec M4Q_KV_F16, 2 D bytes a
+ *    row) or Q8_0 (kv_codec M4Q_Q8_0: D / 32 blocks of 34 bytes a row, the
+ *    same block as the Q8_0 weights).  Each value enters the products as
+ *    fp16 (Q8_0: RNE(q * d)).
+ *  - O: fp16 [M, H * D] (token-major: the o-projection's input).
+ *  - D is 64 or 128, H % Hkv == 0 (else M4Q_ERR_BAD_SHAPE); M, T >= 1,
+ *    q_offset >= 0, scale finite (else M4Q_ERR_INVALID_ARG; the usual scale
+ *    is 1 / sqrt(D)); Q, K, V, O and workspace 16-byte aligned.
+ *  - Scores and the softmax are fp32; the probabilities are rounded to fp16
+ *    for the P V product, which accumulates in fp32; O is rounded once.
+ *  - workspace: when the query rows alone would leave SMs idle (decode), the
+ *    keys are split across CTAs and merged by a second kernel, which needs
+ *    m4q_attention_workspace_bytes() bytes of device memory.  NULL (or a
+ *    smaller size) runs without the split: same result up to fp32 rounding,
+ *    slower at small M.  The library allocates nothing. */
+int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
+                  int64_t M, int64_t T, int64_t D, int64_t q_offset, int causal, float scale, void* O,
+                  void* workspace, size_t workspace_bytes, m4q_stream_t stream);
+
+/* Workspace bytes m4q_attention uses for this shape on the current device
+ * (0: no key split; also 0 for an invalid shape). */
+size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D);
+
 /* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
  * (MLX4: q * s + b) rounded once to nearest even.  The test hook for
  * bit-exact decoding. */

@@ -15,6 +15,7 @@ Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     mlp(x, wg, wu, wd, codec_gu, codec_d, d, f, act=ACT_SILU, h=None, out=None)
     dequant(w, codec, n, k, out=None)
     mlx4_pack(words, scales, biases, n, k, out=None)
+    attention(q, k, v, kv_codec, hkv, t, q_offset=None, causal=True, scale=None, out=None)
     weight_bytes(codec, n, k), check_finite(t), check_device_status(),
     selftest_wait_timeout(limit_ns), status_string(code), version()
 and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
@@ -34,6 +35,7 @@ Q4_0, Q8_0, Q2_0, MLX4 = 0, 1, 2, 3
 CODECS = (Q4_0, Q8_0, Q2_0, MLX4)
 BLOCK = {Q4_0: 32, Q8_0: 32, Q2_0: 128, MLX4: 32}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q2_0: 34, MLX4: 20}
+KV_F16 = 16   # fp16 KV cache values (the quantized KV cache uses Q8_0)
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 ACT_SILU, ACT_GELU = 0, 1
 
@@ -65,6 +67,9 @@ SIGNATURES = {
     "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_mlx4_pack": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp]),
+    "m4q_attention": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
+                             ctypes.c_float, _vp, _vp, _sz, _vp]),
+    "m4q_attention_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
     "m4q_check_device_status": (_i32, [_vp]),
@@ -259,6 +264,44 @@ def mlx4_pack(words, scales, biases, n: int, k: int, out=None, stream=None):
     _packed_check(out, MLX4, n, k, "out")
     _check(load().m4q_mlx4_pack(words.data_ptr(), scales.data_ptr(), biases.data_ptr(), n, k,
                                 out.data_ptr(), _stream_ptr(stream)), "m4q_mlx4_pack")
+    return out
+
+
+def attention(q, k, v, kv_codec: int, hkv: int, t: int, q_offset: int | None = None,
+              causal: bool = True, scale: float | None = None, out=None, workspace=None, stream=None):
+    """O fp16 [M, H * D] = attention of q fp16 [H, M, D] over the KV cache k,
+    v [hkv, t, D] (fp16 for KV_F16; uint8 Q8_0 blocks [hkv, t, D / 32 * 34]
+    for Q8_0).  q_offset defaults to t - M (the queries are the last M
+    positions); scale to 1 / sqrt(D).  The key-split workspace is allocated
+    here when not given."""
+    import torch
+    _require(q, torch.float16, "q")
+    if q.dim() != 3:
+        raise ValueError("q must be [H, M, D]")
+    h, m_, d = q.shape
+    row = 2 * d if kv_codec == KV_F16 else (d // 32) * 34
+    for x, what in ((k, "k"), (v, "v")):
+        _require(x, torch.float16 if kv_codec == KV_F16 else torch.uint8, what)
+        if x.numel() * x.element_size() != hkv * t * row:
+            raise ValueError("%s must hold [%d, %d] rows of %d bytes" % (what, hkv, t, row))
+    if q_offset is None:
+        q_offset = t - m_
+    if scale is None:
+        scale = float(d) ** -0.5
+    if out is None:
+        out = torch.empty((m_, h * d), dtype=torch.float16, device=q.device)
+    _require(out, torch.float16, "out")
+    if out.numel() != m_ * h * d:
+        raise ValueError("out must hold M * H * D values")
+    lib = load()
+    if workspace is None:
+        need = int(lib.m4q_attention_workspace_bytes(h, hkv, m_, t, d))
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.m4q_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), kv_codec, h, hkv, m_, t, d,
+                             q_offset, int(bool(causal)), float(scale), out.data_ptr(), ws_ptr, ws_bytes,
+                             _stream_ptr(stream)), "m4q_attention")
     return out
 
 

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libm4q.so")
-SOURCES = ["api.cu", "misc.cu", "gemv.cu", "tc_q4_0.cu", "tc_q8_0.cu", "tc_q2_0.cu", "tc_mlx4.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "misc.cu", "gemv.cu", "tc_q4_0.cu", "tc_q8_0.cu", "tc_q2_0.cu", "tc_mlx4.cu", "noalloc.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -314,6 +314,107 @@ int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int
              : M4Q_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ attention
+
+}  // extern "C"
+
+namespace {
+
+// Key split of an attention call: CTAs = row tiles x KV heads; when that
+// leaves the GPU under two CTAs per SM, split the keys (tiles of 64) so the
+// grid reaches about that, each split keeping at least two tiles.
+struct AttnSplit {
+  int rtiles, nsplit, tsplit;
+  size_t ws_bytes;
+};
+
+AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, int sms) {
+  AttnSplit a;
+  const int64_t R = M * (H / Hkv);
+  a.rtiles = (int)((R + 63) / 64);
+  const int64_t ctas = (int64_t)a.rtiles * Hkv;
+  const int64_t ktiles = (T + 63) / 64;
+  int64_t ns = 1;
+  if (ctas < 2 * (int64_t)sms) {
+    ns = (2 * (int64_t)sms + ctas - 1) / ctas;
+    const int64_t most = ktiles / 2 > 1 ? ktiles / 2 : 1;
+    if (ns > most) ns = most;
+  }
+  const int64_t per = (ktiles + ns - 1) / ns;     // key tiles per split
+  a.tsplit = (int)(per * 64);
+  a.nsplit = (int)((ktiles + per - 1) / per);
+  a.ws_bytes = a.nsplit > 1 ? (size_t)a.nsplit * Hkv * a.rtiles * 64 * (size_t)(D * 4 + 8) : 0;
+  return a;
+}
+
+int check_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
+                    int64_t M, int64_t T, int64_t D, int64_t q_offset, float scale, const void* O) {
+  if (!Q || !K || !V || !O) return M4Q_ERR_INVALID_ARG;
+  if (kv_codec != M4Q_KV_F16 && kv_codec != M4Q_Q8_0) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (H < 1 || Hkv < 1 || M < 1 || T < 1 || q_offset < 0) return M4Q_ERR_INVALID_ARG;
+  if (H > 65535 || M > INT32_MAX || T > INT32_MAX || q_offset > INT32_MAX || M * H > INT32_MAX)
+    return M4Q_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return M4Q_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || (D != 64 && D != 128)) return M4Q_ERR_BAD_SHAPE;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return M4Q_ERR_MISALIGNED;
+  return M4Q_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D) {
+  if (H < 1 || Hkv < 1 || M < 1 || T < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
+  DevInfo dev;
+  if (current_device_info(&dev) != M4Q_OK) return 0;
+  return attn_split(H, Hkv, M, T, D, dev.sms).ws_bytes;
+}
+
+int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
+                  int64_t M, int64_t T, int64_t D, int64_t q_offset, int causal, float scale, void* O,
+                  void* workspace, size_t workspace_bytes, m4q_stream_t stream) {
+  int rc = check_attention(Q, K, V, kv_codec, H, Hkv, M, T, D, q_offset, scale, O);
+  if (rc != M4Q_OK) return rc;
+  if (workspace && !aligned16(workspace)) return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+  AttnSplit a = attn_split(H, Hkv, M, T, D, dev.sms);
+  if (a.nsplit > 1 && (!workspace || workspace_bytes < a.ws_bytes)) {
+    a.nsplit = 1;   // no room for partial results: one CTA walks all keys
+    a.tsplit = (int)(((T + 63) / 64) * 64);
+  }
+  m4q::AttnParams p{};
+  p.q = static_cast<const __half*>(Q);
+  p.k = static_cast<const uint8_t*>(K);
+  p.v = static_cast<const uint8_t*>(V);
+  p.o = static_cast<__half*>(O);
+  p.H = (int)H;
+  p.Hkv = (int)Hkv;
+  p.G = (int)(H / Hkv);
+  p.M = (int)M;
+  p.T = (int)T;
+  p.D = (int)D;
+  p.kv_row_bytes = kv_codec == M4Q_KV_F16 ? 2 * D : (D / 32) * 34;
+  p.q_offset = (int)q_offset;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.rtiles = a.rtiles;
+  p.nsplit = a.nsplit;
+  p.tsplit = a.tsplit;
+  if (a.nsplit > 1) {
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                         (size_t)a.nsplit * Hkv * a.rtiles * 64 * D * 4);
+  }
+  return m4q::launch_attention(p, kv_codec == M4Q_Q8_0, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? M4Q_OK
+             : M4Q_ERR_CUDA;
+}
+
 int m4q_check_finite(const void* x, int64_t n, m4q_stream_t stream) {
   if (!x || n < 0) return M4Q_ERR_INVALID_ARG;
   if (!aligned16(x)) return M4Q_ERR_MISALIGNED;

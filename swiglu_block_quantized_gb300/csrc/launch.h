@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,6 +52,25 @@ cudaError_t launch_tc_q8_0(const ProjLaunch& L);
 cudaError_t launch_tc_q2_0(const ProjLaunch& L);
 cudaError_t launch_tc_mlx4(const ProjLaunch& L);
 cudaError_t launch_gemv(int codec, const ProjLaunch& L);
+
+// attention.cu: attention of fp16 Q [H][M][D] over a KV cache [Hkv][T] of
+// rows of D values (fp16, or Q8_0 blocks along D); O fp16 [M][H * D].
+struct AttnParams {
+  const __half* q;
+  const uint8_t* k;
+  const uint8_t* v;
+  __half* o;
+  float* ws_o;            // key splits: unnormalised O [nsplit][Hkv][rtiles * 64][D]
+  float2* ws_ml;          // key splits: (max, sum) per row, same order
+  int H, Hkv, G, M, T, D;
+  long long kv_row_bytes; // bytes of one key row (2 D, or D / 32 * 34)
+  int q_offset;           // causal: query i sees keys j <= q_offset + i
+  int causal;
+  float scale_log2;       // softmax scale * log2(e)
+  int rtiles;             // ceil(M * G / 64) row tiles per KV head
+  int nsplit, tsplit;     // key splits and keys per split (a multiple of 64)
+};
+cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 
 // misc.cu
 uint32_t* status_words();  // [0] wait status, [1] non-finite flag; per current device

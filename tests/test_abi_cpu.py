@@ -97,6 +97,18 @@ def test_argument_errors_return_before_any_cuda_call(lib):
     assert lib.m4q_mlx4_pack(P(good), P(good), P(good + 3), 8, 32, P(good), s) == m.ERR_MISALIGNED
     assert lib.m4q_mlx4_pack(P(good), P(good), P(good), 8, 32, P(good + 4), s) == m.ERR_MISALIGNED
     assert lib.m4q_check_finite(None, 10, s) == m.ERR_INVALID_ARG
+    att = lambda q, k, v, codec, H, Hkv, M, T, D, off, sc, o, ws=None, wsb=0: lib.m4q_attention(
+        q, k, v, codec, H, Hkv, M, T, D, off, 1, sc, o, ws, wsb, s)
+    assert att(None, P(good), P(good), m.KV_F16, 4, 2, 8, 8, 64, 0, 0.125, P(good)) == m.ERR_INVALID_ARG
+    assert att(P(good), P(good), P(good), m.Q4_0, 4, 2, 8, 8, 64, 0, 0.125, P(good)) == m.ERR_UNSUPPORTED_CODEC
+    assert att(P(good), P(good), P(good), m.KV_F16, 4, 3, 8, 8, 64, 0, 0.125, P(good)) == m.ERR_BAD_SHAPE
+    assert att(P(good), P(good), P(good), m.Q8_0, 4, 2, 8, 8, 96, 0, 0.125, P(good)) == m.ERR_BAD_SHAPE
+    assert att(P(good), P(good), P(good), m.Q8_0, 4, 2, 0, 8, 64, 0, 0.125, P(good)) == m.ERR_INVALID_ARG
+    assert att(P(good), P(good), P(good), m.Q8_0, 4, 2, 8, 8, 64, -1, 0.125, P(good)) == m.ERR_INVALID_ARG
+    assert att(P(good), P(good), P(good), m.Q8_0, 4, 2, 8, 8, 64, 0, float("nan"), P(good)) == m.ERR_INVALID_ARG
+    assert att(P(good), P(good + 2), P(good), m.Q8_0, 4, 2, 8, 8, 64, 0, 0.125, P(good)) == m.ERR_MISALIGNED
+    assert att(P(good), P(good), P(good), m.Q8_0, 4, 2, 8, 8, 64, 0, 0.125, P(good + 8)) == m.ERR_MISALIGNED
+    assert lib.m4q_attention_workspace_bytes(4, 3, 8, 8, 64) == 0
     assert lib.m4q_selftest_wait_timeout(10, s) == m.ERR_INVALID_ARG
 
 

@@ -1,0 +1,102 @@
+"""GPU parity of m4q_attention (fp16 or Q8_0 KV cache) against the oracle.
+
+Tolerance as for the projections: per element |gpu - ref| <= 1e-2 *
+max(1, |ref|), ref the binary64 oracle.  The GPU computes scores and the
+softmax in fp32 and rounds the probabilities to fp16 for the P V product.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import swiglu_block_quantized_gb300 as m
+from _helpers import assert_close, dev, host, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+F16, Q8 = synth.KV_F16, synth.Q8_0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.build()
+    m.load()
+    yield
+    assert m.check_device_status() == m.OK
+
+
+def run(codec, H, Hkv, M, T, D, q_offset, causal, seed=0, workspace="auto", rows=None):
+    Q = synth.queries(H, M, D, seed=seed)
+    K = synth.kv_cache(codec, Hkv, T, D, seed=seed + 1, name="K")
+    V = synth.kv_cache(codec, Hkv, T, D, seed=seed + 1, name="V")
+    kw = {} if workspace == "auto" else {"workspace": workspace}
+    O = host(m.attention(dev(Q), dev(K), dev(V), codec, Hkv, T, q_offset=q_offset, causal=causal, **kw))
+    ref = oracle.attention(Q, K, V, codec, H, Hkv, M, T, D, q_offset, causal, rows=rows)
+    return (O if rows is None else O[rows]), ref
+
+
+@pytest.mark.parametrize("codec", [F16, Q8])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("M,T", [(1, 1), (1, 200), (5, 63), (64, 64), (130, 1000), (77, 77)])
+def test_attention_parity(codec, D, H, Hkv, M, T):
+    for causal in (True, False):
+        O, ref = run(codec, H, Hkv, M, T, D, T - M, causal, seed=M + T)
+        assert_close(O, ref, "attn codec=%d D=%d H=%d/%d M=%d T=%d causal=%d" % (codec, D, H, Hkv, M, T, causal))
+
+
+@pytest.mark.parametrize("codec", [F16, Q8])
+def test_attention_offsets(codec):
+    # queries past the end of the cache (q_offset + i >= T see every key) and
+    # a zero offset (query i sees keys 0..i)
+    for M, T, off in ((9, 4, 0), (40, 100, 0), (3, 50, 10)):
+        O, ref = run(codec, 4, 2, M, T, 64, off, True, seed=M)
+        assert_close(O, ref, "offset M=%d T=%d off=%d" % (M, T, off))
+
+
+@pytest.mark.parametrize("codec", [F16, Q8])
+def test_key_split_matches_single_pass(codec):
+    # M = 1 over a long cache: the key range is split across CTAs and merged;
+    # without a workspace one CTA per row tile walks every key.
+    import torch
+    H, Hkv, M, T, D = 8, 2, 1, 4096, 128
+    assert m.load().m4q_attention_workspace_bytes(H, Hkv, M, T, D) > 0
+    Osplit, ref = run(codec, H, Hkv, M, T, D, T - M, True, seed=3)
+    Oone, _ = run(codec, H, Hkv, M, T, D, T - M, True, seed=3, workspace=None)
+    assert_close(Osplit, ref, "split")
+    assert_close(Oone, ref, "single pass")
+    assert np.abs(Osplit.astype(np.float64) - Oone.astype(np.float64)).max() < 2e-3
+
+
+def test_8b_prefill_sampled_rows():
+    # The 8B layer's attention at the prefill size: H = 32, 8 KV heads,
+    # D = 128, M = T = 2048, causal, Q8_0 cache; sampled query rows.
+    H, Hkv, M, T, D = 32, 8, 2048, 2048, 128
+    rows = sample_rows(M)
+    O, ref = run(Q8, H, Hkv, M, T, D, 0, True, seed=7, rows=rows)
+    assert_close(O, ref, "8b prefill")
+
+
+@pytest.mark.parametrize("codec", [F16, Q8])
+def test_decode_long_context(codec):
+    # one new token over a 32K cache (split keys), 8B shape
+    H, Hkv, M, T, D = 32, 8, 1, 32768, 128
+    O, ref = run(codec, H, Hkv, M, T, D, T - 1, True, seed=11)
+    assert_close(O, ref, "decode 32K")
+
+
+def test_direct_head_q_feeds_attention():
+    # Q projected straight into [H, M, D] by m4q_gemm_heads feeds attention
+    # without a transpose; O [M, H * D] feeds the o-projection.
+    K_, hd, H, Hkv, M, T = 256, 64, 4, 2, 40, 40
+    W = synth.weights(synth.Q4_0, H * hd, K_, seed=50, name="Wq")
+    X = synth.activations(M, K_, seed=51)
+    q = m.gemm_heads(dev(X), dev(W), synth.Q4_0, H * hd, K_, hd)
+    Kc = synth.kv_cache(Q8, Hkv, T, hd, seed=52, name="K")
+    Vc = synth.kv_cache(Q8, Hkv, T, hd, seed=52, name="V")
+    O = host(m.attention(q, dev(Kc), dev(Vc), Q8, Hkv, T))
+    ref = oracle.attention(host(q), Kc, Vc, Q8, H, Hkv, M, T, hd, 0, True)
+    assert_close(O, ref, "heads -> attention")
