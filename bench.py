@@ -486,6 +486,20 @@ def run_profile_case(case, local):
     import swiglu_block_quantized_gb300 as m
     torch.cuda.set_device(local)
     m.build()
+    if case.startswith("attn_"):
+        import synth
+        H, Hkv, D = 32, 8, 128
+        codec = synth.Q8_0 if case.endswith("q8_0") else synth.KV_F16
+        M, T = (2048, 2048) if "prefill" in case else (1, 32768)
+        q = torch.from_numpy(synth.queries(H, M, D, seed=1)).cuda()
+        k = torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=2, name="K")).cuda()
+        v = torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=2, name="V")).cuda()
+        for _ in range(3):
+            m.attention(q, k, v, codec, Hkv, T, q_offset=T - M)
+        torch.cuda.synchronize()
+        assert m.check_device_status() == m.OK
+        print("profile case %s: 3 launches done" % case)
+        return
     X, Wg, Wu = make_inputs()
     codec = m.Q4_0
     if "mlx4" in case:
@@ -514,7 +528,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", default=None,
-                    choices=["swiglu_m2048", "swiglu_m1", "swiglu_mlx4_m2048", "swiglu_mlx4_m1"],
+                    choices=["swiglu_m2048", "swiglu_m1", "swiglu_mlx4_m2048", "swiglu_mlx4_m1",
+                             "attn_prefill_q8_0", "attn_decode_q8_0", "attn_prefill_f16", "attn_decode_f16"],
                     help="only run 3 launches of one case (for ncu)")
     args = ap.parse_args(argv)
     if args.profile_case:

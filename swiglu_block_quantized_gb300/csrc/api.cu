@@ -321,8 +321,9 @@ int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int
 namespace {
 
 // Key split of an attention call: CTAs = row tiles x KV heads; when that
-// leaves the GPU under two CTAs per SM, split the keys (tiles of 64) so the
-// grid reaches about that, each split keeping at least two tiles.
+// leaves the GPU under two CTAs per SM (three for the at-most-16-row decode
+// kernel, which fits three per SM), split the keys (tiles of 64) so the grid
+// reaches about that, each split keeping at least two tiles.
 struct AttnSplit {
   int rtiles, nsplit, tsplit;
   size_t ws_bytes;
@@ -334,9 +335,10 @@ AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, in
   a.rtiles = (int)((R + 63) / 64);
   const int64_t ctas = (int64_t)a.rtiles * Hkv;
   const int64_t ktiles = (T + 63) / 64;
+  const int64_t target = (R <= 16 ? 3 : 2) * (int64_t)sms;
   int64_t ns = 1;
-  if (ctas < 2 * (int64_t)sms) {
-    ns = (2 * (int64_t)sms + ctas - 1) / ctas;
+  if (ctas < target) {
+    ns = (target + ctas - 1) / ctas;
     const int64_t most = ktiles / 2 > 1 ? ktiles / 2 : 1;
     if (ns > most) ns = most;
   }
@@ -398,6 +400,7 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   p.T = (int)T;
   p.D = (int)D;
   p.kv_row_bytes = kv_codec == M4Q_KV_F16 ? 2 * D : (D / 32) * 34;
+  p.kv_vec16 = (T * p.kv_row_bytes) % 16 == 0;   // K and V are 16-byte aligned (checked above)
   p.q_offset = (int)q_offset;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;

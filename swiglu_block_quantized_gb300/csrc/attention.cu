@@ -66,70 +66,129 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Decode keys [k0, k0 + 64) of one KV head into dst[64][D + 8] (fp16); keys
-// at or past `kend` are written as zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <int D, bool Q8>
-__device__ __forceinline__ void load_kv_tile(__half (*dst)[D + 8], const uint8_t* __restrict__ head,
-                                             long long row_bytes, int k0, int kend) {
+struct AttnCfg {
+  static constexpr int kRowBytes = Q8 ? D / 32 * 34 : 2 * D;   // one key row in the cache
+  static constexpr int kPitch = (D + 8) * 2;                   // padded fp16 row in shared memory
+  static constexpr int kTile = kKeys * kPitch;                 // one padded fp16 tile
+  static constexpr int kRaw = kKeys * kRowBytes;               // one packed Q8_0 tile
+  // Q8_0: packed K and V tiles, double-buffered, then the decoded K and V
+  // tiles.  fp16: the padded K and V tiles, double-buffered.
+  static constexpr int kSmem = Q8 ? 4 * kRaw + 2 * kTile : 4 * kTile;
+};
+
+// Start the asynchronous copy of keys [k0, min(k0 + 64, T)) of one KV head:
+// packed rows as they are (Q8_0), or fp16 rows into the padded tile, whose
+// rows past T are zeroed (they are masked, but V enters P V, where 0 * NaN
+// would be NaN).  vec16: every tile start and the cache end are 16-byte
+// aligned, so 16-byte copies; otherwise 4-byte copies (Q8_0 rows are 4-byte
+// multiples).
+template <int D, bool Q8>
+__device__ __forceinline__ void issue_tile(uint8_t* kdst, uint8_t* vdst, const uint8_t* khead,
+                                           const uint8_t* vhead, int k0, int T, bool vec16) {
+  using Cfg = AttnCfg<D, Q8>;
+  const int rows = min(kKeys, T - k0);
+  const uint8_t* ks = khead + (long long)k0 * Cfg::kRowBytes;
+  const uint8_t* vs = vhead + (long long)k0 * Cfg::kRowBytes;
   if constexpr (Q8) {
-    constexpr int kBlk = D / 32;                  // Q8_0 blocks per key row
-    constexpr int kUnits = kKeys * kBlk / 128;    // (row, block) units per thread
-#pragma unroll
-    for (int u = 0; u < kUnits; ++u) {
-      const int unit = threadIdx.x + 128 * u;
-      const int rr = unit / kBlk, blk = unit % kBlk;
-      uint4* out = reinterpret_cast<uint4*>(&dst[rr][32 * blk]);
-      if (k0 + rr < kend) {
-        const unsigned short* src =
-            reinterpret_cast<const unsigned short*>(head + (long long)(k0 + rr) * row_bytes + 34 * blk);
-        uint32_t w[9];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = (uint32_t)__ldg(src + 2 * i) | ((uint32_t)__ldg(src + 2 * i + 1) << 16);
-        w[8] = __ldg(src + 16);
-        const uint32_t d2 = dup_scale(u16_at(w, 0));
-        uint32_t v[16];
-#pragma unroll
-        for (int p = 0; p < 16; ++p) v[p] = q8_pair(spread_pair(w, 2 + 2 * p), d2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[i] = make_uint4(0, 0, 0, 0);
+    const int bytes = rows * Cfg::kRowBytes;
+    if (vec16) {
+      for (int c = threadIdx.x; c < bytes / 16; c += 128) {
+        cp_async16(kdst + 16 * c, ks + 16 * c);
+        cp_async16(vdst + 16 * c, vs + 16 * c);
+      }
+    } else {
+      for (int c = threadIdx.x; c < bytes / 4; c += 128) {
+        cp_async4(kdst + 4 * c, ks + 4 * c);
+        cp_async4(vdst + 4 * c, vs + 4 * c);
       }
     }
   } else {
-    constexpr int kChunks = D / 8;                 // 16-byte chunks per key row
-    constexpr int kUnits = kKeys * kChunks / 128;
+    constexpr int kChunks = D / 8;
+    for (int c = threadIdx.x; c < kKeys * kChunks; c += 128) {
+      const int r = c / kChunks, ch = c % kChunks;
+      uint8_t* kd = kdst + r * Cfg::kPitch + 16 * ch;
+      uint8_t* vd = vdst + r * Cfg::kPitch + 16 * ch;
+      if (r < rows) {
+        cp_async16(kd, ks + (long long)r * Cfg::kRowBytes + 16 * ch);
+        cp_async16(vd, vs + (long long)r * Cfg::kRowBytes + 16 * ch);
+      } else {
+        *reinterpret_cast<uint4*>(kd) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  cp_async_commit();
+}
+
+// Decode a packed Q8_0 tile (rows of D / 32 blocks) into the padded fp16
+// tile: RNE(q * d) per value, the weights' exact decode.  Rows at or past
+// `valid` are written as zeros.
+template <int D>
+__device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw, int valid) {
+  using Cfg = AttnCfg<D, true>;
+  constexpr int kBlk = D / 32;
+  constexpr int kUnits = kKeys * kBlk / 128;
 #pragma unroll
-    for (int u = 0; u < kUnits; ++u) {
-      const int unit = threadIdx.x + 128 * u;
-      const int rr = unit / kChunks, c = unit % kChunks;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (k0 + rr < kend) val = __ldg(reinterpret_cast<const uint4*>(head + (long long)(k0 + rr) * row_bytes) + c);
-      *reinterpret_cast<uint4*>(&dst[rr][8 * c]) = val;
+  for (int u = 0; u < kUnits; ++u) {
+    const int unit = threadIdx.x + 128 * u;
+    const int rr = unit / kBlk, blk = unit % kBlk;
+    uint4* out = reinterpret_cast<uint4*>(dst + rr * Cfg::kPitch + 64 * blk);
+    if (rr < valid) {
+      const unsigned short* src = reinterpret_cast<const unsigned short*>(raw + rr * Cfg::kRowBytes + 34 * blk);
+      uint32_t w[9];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = (uint32_t)src[2 * i] | ((uint32_t)src[2 * i + 1] << 16);
+      w[8] = src[16];
+      const uint32_t d2 = dup_scale(u16_at(w, 0));
+      uint32_t v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = q8_pair(spread_pair(w, 2 + 2 * q), d2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[i] = make_uint4(0, 0, 0, 0);
     }
   }
 }
 
-template <int D, bool Q8>
-__global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
-  constexpr int NT = kKeys / 8;   // score n8 tiles per key tile
+// KS (at most 16 query rows, decode): the 4 warps share rows 0..15 of the
+// tile and split every key tile, warp w taking keys 16 w .. 16 w + 15; their
+// partial (max, sum, O) are merged through shared memory at the end.
+template <int D, bool Q8, bool KS>
+__global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams p) {
+  using Cfg = AttnCfg<D, Q8>;
+  constexpr int NT = KS ? 2 : kKeys / 8;   // score n8 tiles per warp and key tile
   constexpr int DK = D / 16;      // k16 steps over the head dim
   constexpr int DN = D / 8;       // output n8 tiles
-  __shared__ alignas(128) __half Ks[kKeys][D + 8];
-  __shared__ alignas(128) __half Vs[kKeys][D + 8];
+  extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int rt = blockIdx.x, hk = blockIdx.y, split = blockIdx.z;
+  // Row tiles in reverse order: under a causal mask the last tiles see the
+  // most keys, so they start first.
+  const int rt = (int)gridDim.x - 1 - (int)blockIdx.x, hk = blockIdx.y, split = blockIdx.z;
   const int R = p.M * p.G;
+  const int wrow = KS ? 0 : 16 * warp;           // first row of this warp in the tile
+  const int kw = KS ? 16 * warp : 0;             // first key of this warp in a key tile
+  const bool active = rt * kRows + wrow < R;     // this warp has a row to compute
 
   // This thread's two rows (g and g + 8 of the warp's 16).
   int qi[2], qh[2], lim[2];
   bool rok[2];
 #pragma unroll
   for (int h2 = 0; h2 < 2; ++h2) {
-    const int r = rt * kRows + 16 * warp + g + 8 * h2;
+    const int r = rt * kRows + wrow + g + 8 * h2;
     rok[h2] = r < R;
     qi[h2] = rok[h2] ? r / p.G : 0;
     qh[h2] = hk * p.G + (rok[h2] ? r % p.G : 0);
@@ -167,13 +226,34 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
   for (int dn = 0; dn < DN; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
-  const uint8_t* khead = p.k + (long long)hk * p.T * p.kv_row_bytes;
-  const uint8_t* vhead = p.v + (long long)hk * p.T * p.kv_row_bytes;
-  for (int k0 = kbeg; k0 < kend; k0 += kKeys) {
-    __syncthreads();   // the previous tile's fragments have been read
-    load_kv_tile<D, Q8>(Ks, khead, p.kv_row_bytes, k0, kend);
-    load_kv_tile<D, Q8>(Vs, vhead, p.kv_row_bytes, k0, kend);
-    __syncthreads();
+  const uint8_t* khead = p.k + (long long)hk * p.T * Cfg::kRowBytes;
+  const uint8_t* vhead = p.v + (long long)hk * p.T * Cfg::kRowBytes;
+  // stage s: Q8_0 packed K at 2 s * kRaw, V at (2 s + 1) * kRaw; fp16 padded
+  // K at 2 s * kTile, V at (2 s + 1) * kTile
+  constexpr int kStage = Q8 ? Cfg::kRaw : Cfg::kTile;
+  uint8_t* dec = smem + 4 * Cfg::kRaw;   // Q8_0: decoded K, then V
+  if (kbeg < kend) issue_tile<D, Q8>(smem, smem + kStage, khead, vhead, kbeg, p.T, p.kv_vec16);
+  int it = 0;
+  for (int k0 = kbeg; k0 < kend; k0 += kKeys, ++it) {
+    const int st = it & 1;
+    cp_async_wait_all();
+    __syncthreads();   // this tile has landed; every warp is done with the previous one
+    if (k0 + kKeys < kend)
+      issue_tile<D, Q8>(smem + 2 * (st ^ 1) * kStage, smem + (2 * (st ^ 1) + 1) * kStage, khead, vhead,
+                        k0 + kKeys, p.T, p.kv_vec16);
+    const uint8_t* Kt;
+    const uint8_t* Vt;
+    if constexpr (Q8) {
+      decode_q8_tile<D>(dec, smem + 2 * st * kStage, kend - k0);
+      decode_q8_tile<D>(dec + Cfg::kTile, smem + (2 * st + 1) * kStage, kend - k0);
+      __syncthreads();
+      Kt = dec;
+      Vt = dec + Cfg::kTile;
+    } else {
+      Kt = smem + 2 * st * kStage;
+      Vt = smem + (2 * st + 1) * kStage;
+    }
+    if (!active) continue;
 
     // S = Q K^T (16 rows x 64 keys per warp)
     float s[NT][4];
@@ -185,7 +265,7 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
       for (int j = 0; j < NT; j += 2) {
         uint32_t b[4];
         const int mi = lane >> 3;
-        ldsm_x4(b, &Ks[8 * (j + (mi >> 1)) + (lane & 7)][16 * kk + 8 * (mi & 1)]);
+        ldsm_x4(b, Kt + (kw + 8 * (j + (mi >> 1)) + (lane & 7)) * Cfg::kPitch + 2 * (16 * kk + 8 * (mi & 1)));
         mma16816(s[j], qa[kk], b[0], b[1]);
         mma16816(s[j + 1], qa[kk], b[2], b[3]);
       }
@@ -196,7 +276,7 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int key = k0 + 8 * j + 2 * t + (c & 1);
+        const int key = k0 + kw + 8 * j + 2 * t + (c & 1);
         const float x = key < lim[c >> 1] ? s[j][c] * p.scale_log2 : -INFINITY;
         s[j][c] = x;
         mx[c >> 1] = fmaxf(mx[c >> 1], x);
@@ -231,7 +311,7 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
 
     // O += P V, P repacked from the score accumulators as the A operand
 #pragma unroll
-    for (int kk = 0; kk < kKeys / 16; ++kk) {
+    for (int kk = 0; kk < NT / 2; ++kk) {
       const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]), pack_h2(s[2 * kk][2], s[2 * kk][3]),
                               pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
                               pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
@@ -239,7 +319,7 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
       for (int dn = 0; dn < DN; dn += 2) {
         uint32_t b[4];
         const int mi = lane >> 3;
-        ldsm_x4_t(b, &Vs[16 * kk + 8 * (mi & 1) + (lane & 7)][8 * (dn + (mi >> 1))]);
+        ldsm_x4_t(b, Vt + (kw + 16 * kk + 8 * (mi & 1) + (lane & 7)) * Cfg::kPitch + 2 * (8 * (dn + (mi >> 1))));
         mma16816(o[dn], pa, b[0], b[1]);
         mma16816(o[dn + 1], pa, b[2], b[3]);
       }
@@ -251,6 +331,61 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
   for (int h2 = 0; h2 < 2; ++h2) {
     lrow[h2] += __shfl_xor_sync(0xffffffffu, lrow[h2], 1);
     lrow[h2] += __shfl_xor_sync(0xffffffffu, lrow[h2], 2);
+  }
+  if constexpr (KS) {
+    // Merge the 4 warps' partials of rows 0..15: m = max_w m_w,
+    // O = sum_w 2^(m_w - m) O_w / sum_w 2^(m_w - m) l_w.  The tile buffers
+    // are free (no copy is in flight after the last tile).
+    __syncthreads();
+    float* Ow = reinterpret_cast<float*>(smem);                   // [4 warps][16 rows][D]
+    float2* ML = reinterpret_cast<float2*>(Ow + 4 * 16 * D);      // [4 warps][16 rows]
+#pragma unroll
+    for (int dn = 0; dn < DN; ++dn)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        *reinterpret_cast<float2*>(Ow + (warp * 16 + g + 8 * h2) * D + 8 * dn + 2 * t) =
+            make_float2(o[dn][2 * h2], o[dn][2 * h2 + 1]);
+    if (t == 0)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) ML[warp * 16 + g + 8 * h2] = make_float2(mrow[h2], lrow[h2]);
+    __syncthreads();
+    const int row = threadIdx.x >> 3, seg = threadIdx.x & 7;   // 16 rows x 8 segments of D / 8
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m = fmaxf(m, ML[w * 16 + row].x);
+    const float mref = m == -INFINITY ? 0.f : m;
+    float wgt[4], L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      wgt[w] = fast_exp2(ML[w * 16 + row].x - mref);
+      L += wgt[w] * ML[w * 16 + row].y;
+    }
+    const int r = rt * kRows + row;
+    constexpr int SEG = D / 8;
+    float acc[SEG];
+#pragma unroll
+    for (int e = 0; e < SEG; ++e) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) a += wgt[w] * Ow[(w * 16 + row) * D + seg * SEG + e];
+      acc[e] = a;
+    }
+    if (p.nsplit == 1) {
+      if (r < R) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        __half* orow = p.o + (long long)(r / p.G) * p.H * D + (long long)(hk * p.G + r % p.G) * D + seg * SEG;
+#pragma unroll
+        for (int e = 0; e < SEG; e += 2)
+          *reinterpret_cast<__half2*>(orow + e) = __floats2half2_rn(acc[e] * inv, acc[e + 1] * inv);
+      }
+    } else {
+      const long long slot = ((long long)split * p.Hkv + hk) * ((long long)p.rtiles * kRows) + r;
+#pragma unroll
+      for (int e = 0; e < SEG; e += 2)
+        *reinterpret_cast<float2*>(p.ws_o + slot * D + seg * SEG + e) = make_float2(acc[e], acc[e + 1]);
+      if (seg == 0) p.ws_ml[slot] = make_float2(m, L);
+    }
+    return;
   }
   if (p.nsplit == 1) {
 #pragma unroll
@@ -267,7 +402,7 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const AttnParams p) {
     const long long rows_pad = (long long)p.rtiles * kRows;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
-      const long long r = (long long)rt * kRows + 16 * warp + g + 8 * h2;
+      const long long r = (long long)rt * kRows + wrow + g + 8 * h2;
       const long long slot = ((long long)split * p.Hkv + hk) * rows_pad + r;
       float* wrow = p.ws_o + slot * D;
 #pragma unroll
@@ -309,11 +444,24 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   for (int c = 0; c < D / 32; ++c) orow[lane + 32 * c] = __float2half_rn(acc[c] * inv);
 }
 
-template <int D, bool Q8>
-cudaError_t launch_attn_dq(const AttnParams& p, cudaStream_t s) {
+template <int D, bool Q8, bool KS>
+cudaError_t launch_attn_dqk(const AttnParams& p, cudaStream_t s) {
+  auto kern = attn_kernel<D, Q8, KS>;
+  constexpr int kSmem = AttnCfg<D, Q8>::kSmem;
+  static_assert(4 * 16 * D * 4 + 4 * 16 * 8 <= kSmem, "warp merge buffer");
+  std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 3, D, Q8, KS>>();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
   const dim3 grid((unsigned)p.rtiles, (unsigned)p.Hkv, (unsigned)p.nsplit);
-  attn_kernel<D, Q8><<<grid, 128, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  kern<<<grid, 128, kSmem, s>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
   const long long warps = (long long)p.Hkv * p.M * p.G;
   attn_combine_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
@@ -321,6 +469,12 @@ cudaError_t launch_attn_dq(const AttnParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+template <int D, bool Q8>
+cudaError_t launch_attn_dq(const AttnParams& p, cudaStream_t s) {
+  // at most 16 rows (decode): the warps split the keys instead of the rows
+  return p.M * p.G <= 16 ? launch_attn_dqk<D, Q8, true>(p, s) : launch_attn_dqk<D, Q8, false>(p, s);
+}
 
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s) {
   if (p.D == 64) return q8 ? launch_attn_dq<64, true>(p, s) : launch_attn_dq<64, false>(p, s);

@@ -69,6 +69,7 @@ struct AttnParams {
   float scale_log2;       // softmax scale * log2(e)
   int rtiles;             // ceil(M * G / 64) row tiles per KV head
   int nsplit, tsplit;     // key splits and keys per split (a multiple of 64)
+  bool kv_vec16;          // every K/V tile start and T * kv_row_bytes are 16-byte aligned
 };
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 
