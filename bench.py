@@ -425,7 +425,7 @@ def measure_attention(m, dev, reps=20):
     """Attention of the 8B layer (H = 32, 8 KV heads, D = 128) over an fp16
     and a Q8_0 KV cache: causal prefill M = T = 2048 (TFLOP/s, causal FLOPs
     4 H D sum_i (i + 1)) and one decode token over T = 32768 (GB/s of KV
-    cache read).  CUDA events around `reps` launches."""
+    cache read).  CUDA events around a graph of `reps` launches."""
     import torch
 
     import synth
@@ -436,12 +436,19 @@ def measure_attention(m, dev, reps=20):
     pk, _ = peaks()
 
     def timed(fn):
+        # `reps` launches captured in one CUDA graph, so host-side launch
+        # cost (a 10-50 us kernel here) does not enter the device time
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(reps):
-            fn()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps

@@ -132,7 +132,13 @@ __device__ __forceinline__ void issue_tile(uint8_t* kdst, uint8_t* vdst, const u
 
 // Decode a packed Q8_0 tile (rows of D / 32 blocks) into the padded fp16
 // tile: RNE(q * d) per value, the weights' exact decode.  Rows at or past
-// `valid` are written as zeros.
+// `valid` are written as zeros.  A warp takes 32 consecutive rows of one
+// block column, so the branch on the block's alignment is uniform: a block
+// at an even index starts 4-byte aligned (rows are 4-byte multiples) and is
+// read as 9 words; one at an odd index starts 2 bytes past a word and is
+// read as 10 words and shifted.  Those reads may run up to 4 bytes past the
+// block (into the next row, or the next buffer for the tile's last row);
+// the extra bytes are never used.
 template <int D>
 __device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw, int valid) {
   using Cfg = AttnCfg<D, true>;
@@ -141,14 +147,22 @@ __device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw,
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
     const int unit = threadIdx.x + 128 * u;
-    const int rr = unit / kBlk, blk = unit % kBlk;
+    const int blk = unit / kKeys, rr = unit % kKeys;
     uint4* out = reinterpret_cast<uint4*>(dst + rr * Cfg::kPitch + 64 * blk);
     if (rr < valid) {
-      const unsigned short* src = reinterpret_cast<const unsigned short*>(raw + rr * Cfg::kRowBytes + 34 * blk);
+      const int off = rr * Cfg::kRowBytes + 34 * blk;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(raw + (off & ~3));
       uint32_t w[9];
+      if ((off & 3) == 0) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = (uint32_t)src[2 * i] | ((uint32_t)src[2 * i + 1] << 16);
-      w[8] = src[16];
+        for (int i = 0; i < 9; ++i) w[i] = src[i];
+      } else {
+        uint32_t a[10];
+#pragma unroll
+        for (int i = 0; i < 10; ++i) a[i] = src[i];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = __funnelshift_r(a[i], a[i + 1], 16);
+      }
       const uint32_t d2 = dup_scale(u16_at(w, 0));
       uint32_t v[16];
 #pragma unroll
@@ -414,7 +428,9 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
 }
 
 // Merge the key splits of one row: O = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s.
-// One warp per (KV head, row); lanes over the head dim.
+// One warp per (KV head, row).  The lanes take the splits for the max and the
+// sum; the weighted sum of O has the lanes over the head dim and 8 splits'
+// loads in flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const long long rows_pad = (long long)p.rtiles * kRows;
@@ -423,20 +439,35 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int R = p.M * p.G;
   if (wid >= (long long)p.Hkv * R) return;
   const int hk = (int)(wid / R), r = (int)(wid % R);
+  const long long base = (long long)hk * rows_pad + r;          // slot of split s: base + s * stride
+  const long long stride = (long long)p.Hkv * rows_pad;
   float m = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) m = fmaxf(m, p.ws_ml[((long long)s * p.Hkv + hk) * rows_pad + r].x);
+  for (int s = lane; s < p.nsplit; s += 32) m = fmaxf(m, p.ws_ml[base + s * stride].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float mref = m == -INFINITY ? 0.f : m;
-  float acc[D / 32], l = 0.f;
+  float l = 0.f;
+  float acc[D / 32];
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const long long slot = ((long long)s * p.Hkv + hk) * rows_pad + r;
-    const float2 ml = p.ws_ml[slot];
-    const float w = fast_exp2(ml.x - mref);
-    l += w * ml.y;
+  for (int s0 = 0; s0 < p.nsplit; s0 += 32) {
+    float w = 0.f;
+    if (s0 + lane < p.nsplit) {
+      const float2 ml = p.ws_ml[base + (s0 + lane) * stride];
+      w = fast_exp2(ml.x - mref);
+      l += w * ml.y;
+    }
+    const int n = min(32, p.nsplit - s0);
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const float* src = p.ws_o + (base + (s0 + j) * stride) * D + lane;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) acc[c] += w * p.ws_o[slot * D + lane + 32 * c];
+      for (int c = 0; c < D / 32; ++c) acc[c] += wj * src[32 * c];
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const int i = r / p.G, h = hk * p.G + r % p.G;
   __half* orow = p.o + (long long)i * p.H * D + (long long)h * D;
