@@ -428,51 +428,61 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
 }
 
 // Merge the key splits of one row: O = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s.
-// One warp per (KV head, row).  The lanes take the splits for the max and the
-// sum; the weighted sum of O has the lanes over the head dim and 8 splits'
-// loads in flight at a time.
+// One CTA of 8 warps per (KV head, row): the threads take the splits for the
+// max; warp w sums splits w, w + 8, ... with its lanes over the head dim (so
+// every split's loads are in flight at once); shared memory adds the warps.
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
+  __shared__ float red_m[8], red_l[8];
+  __shared__ float red_o[8][D];
   const long long rows_pad = (long long)p.rtiles * kRows;
-  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   const int R = p.M * p.G;
-  if (wid >= (long long)p.Hkv * R) return;
-  const int hk = (int)(wid / R), r = (int)(wid % R);
+  const int hk = (int)(blockIdx.x / R), r = (int)(blockIdx.x % R);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long base = (long long)hk * rows_pad + r;          // slot of split s: base + s * stride
   const long long stride = (long long)p.Hkv * rows_pad;
   float m = -INFINITY;
-  for (int s = lane; s < p.nsplit; s += 32) m = fmaxf(m, p.ws_ml[base + s * stride].x);
+  for (int s = threadIdx.x; s < p.nsplit; s += 256) m = fmaxf(m, p.ws_ml[base + s * stride].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red_m[warp] = m;
+  __syncthreads();
+  m = red_m[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, red_m[w]);
   const float mref = m == -INFINITY ? 0.f : m;
   float l = 0.f;
   float acc[D / 32];
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
-  for (int s0 = 0; s0 < p.nsplit; s0 += 32) {
-    float w = 0.f;
-    if (s0 + lane < p.nsplit) {
-      const float2 ml = p.ws_ml[base + (s0 + lane) * stride];
-      w = fast_exp2(ml.x - mref);
-      l += w * ml.y;
-    }
-    const int n = min(32, p.nsplit - s0);
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      const float* src = p.ws_o + (base + (s0 + j) * stride) * D + lane;
+#pragma unroll 4
+  for (int s = warp; s < p.nsplit; s += 8) {
+    const float2 ml = p.ws_ml[base + s * stride];
+    const float w = fast_exp2(ml.x - mref);
+    l += w * ml.y;
+    const float* src = p.ws_o + (base + s * stride) * D + lane;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) acc[c] += wj * src[32 * c];
-    }
+    for (int c = 0; c < D / 32; ++c) acc[c] += w * src[32 * c];
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const int i = r / p.G, h = hk * p.G + r % p.G;
-  __half* orow = p.o + (long long)i * p.H * D + (long long)h * D;
+  for (int c = 0; c < D / 32; ++c) red_o[warp][lane + 32 * c] = acc[c];
+  if (lane == 0) red_l[warp] = l;
+  __syncthreads();
+  if (warp == 0) {
+    float L = 0.f;
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) orow[lane + 32 * c] = __float2half_rn(acc[c] * inv);
+    for (int w = 0; w < 8; ++w) L += red_l[w];
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int i = r / p.G, h = hk * p.G + r % p.G;
+    __half* orow = p.o + (long long)i * p.H * D + (long long)h * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += red_o[w][lane + 32 * c];
+      orow[lane + 32 * c] = __float2half_rn(v * inv);
+    }
+  }
 }
 
 template <int D, bool Q8, bool KS>
@@ -494,8 +504,7 @@ cudaError_t launch_attn_dqk(const AttnParams& p, cudaStream_t s) {
   kern<<<grid, 128, kSmem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  const long long warps = (long long)p.Hkv * p.M * p.G;
-  attn_combine_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
+  attn_combine_kernel<D><<<(unsigned)((long long)p.Hkv * p.M * p.G), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
