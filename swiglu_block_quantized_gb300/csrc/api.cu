@@ -175,8 +175,11 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     // Widest activation tile that still gives every SM a tile.
     const int64_t out_rows = swiglu ? 64 : 128;
     const int64_t ntiles = (N + out_rows - 1) / out_rows;
+    // M <= 128 with TMA-able rows and row-major output: the small-M kernel
+    // (one activation tile of 128 rows as the A operand).
+    L.small = L.wtma && head_dim == 0 && M <= 128;
     int nx = 64;
-    if (!L.wtma) {
+    if (!L.wtma || L.small) {
       nx = 128;
     } else if (((M + 255) / 256) * ntiles >= dev.sms) {
       nx = 256;
@@ -190,7 +193,12 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
       return M4Q_ERR_CUDA;
     // Y boxes: GEMM stages [32 m][128 n] chunks per warpgroup; SwiGLU stores
     // one [nx/2 m][16 n] slab per epilogue warp.
-    if (head_dim != 0) {
+    if (L.small) {
+      // [128 m][64 n] boxes in the 128-byte swizzled layout
+      if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2, 64, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return M4Q_ERR_CUDA;
+    } else if (head_dim != 0) {
       if (!encode_heads(&L.tm_y, Y, M, N, (uint32_t)head_dim)) return M4Q_ERR_CUDA;
     } else if (!encode_2d(&L.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, N, M, N * 2,
                           swiglu ? 16u : (uint32_t)out_rows, swiglu ? (uint32_t)(nx / 2) : 32u,

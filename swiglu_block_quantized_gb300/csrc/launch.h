@@ -30,6 +30,7 @@ struct ProjLaunch {
   cudaStream_t stream;
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
+  bool small;             // M <= 128 kernel (activations as the A operand, tc_small.cuh)
   int sms;                // multiprocessors (persistent grid size, both paths)
   CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path

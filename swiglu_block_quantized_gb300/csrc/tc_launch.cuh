@@ -6,6 +6,7 @@
 
 #include "launch.h"
 #include "tc_proj.cuh"
+#include "tc_small.cuh"
 
 namespace m4q {
 
@@ -66,8 +67,47 @@ cudaError_t launch_tc_glu(const ProjLaunch& L) {
   return L.act ? launch_tc_nx<C, true, WTMA, 1, 0>(L) : launch_tc_nx<C, true, WTMA, 0, 0>(L);
 }
 
+// Small M (<= 128): activations as the A operand, decoded weights as B.
+template <int C, bool SWIGLU, int ACT>
+cudaError_t launch_tcs_one(const ProjLaunch& L) {
+  using Cfg = TsCfg<C, SWIGLU>;
+  auto kern = tc_small_kernel<C, SWIGLU, ACT>;
+  std::atomic<unsigned long long>& configured =
+      attr_flag<std::integer_sequence<int, 4, C, SWIGLU, ACT>>();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  TcParams p;
+  p.w0 = static_cast<const uint8_t*>(L.w0);
+  p.w1 = static_cast<const uint8_t*>(L.w1);
+  p.M = L.M;
+  p.N = L.N;
+  p.K = L.K;
+  p.row_bytes = L.row_bytes;
+  p.m_tiles = 1;
+  p.tiles = (L.N + Cfg::kOutRows - 1) / Cfg::kOutRows;
+  p.status = L.status;
+  p.limit_ns = L.limit_ns;
+  const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
+  return cudaGetLastError();
+}
+
+template <int C>
+cudaError_t launch_tcs(const ProjLaunch& L) {
+  if (!L.swiglu) return launch_tcs_one<C, false, 0>(L);
+  return L.act ? launch_tcs_one<C, true, 1>(L) : launch_tcs_one<C, true, 0>(L);
+}
+
 template <int C>
 cudaError_t launch_tc_impl(const ProjLaunch& L) {
+  if (L.small) return launch_tcs<C>(L);
   if (L.wtma) {
     return L.swiglu ? launch_tc_glu<C, true>(L) : launch_tc_gemm<C, true>(L);
   }

@@ -1,0 +1,323 @@
+// tc_small.cuh -- tcgen05 kernel for the projection at small M (M <= 128):
+// Y = X W^T and Y = act(X Wg^T) x (X Wu^T).
+//
+// Pages: "v0.1 vs v0.2 comparison" 2.1 and 2.2 (Bricks 1-3), "Releases"
+// v0.3.0 (one linear layer for every M).  With few activation rows the MMA
+// shape of tc_proj (M = 128 weight rows read from TMEM, N = the activation
+// rows) spends most of each instruction on the weight operand: at N = 64 an
+// MMA takes about five times its share of the tensor pipe.  Here the roles
+// of the operands are swapped, so that every MMA covers 128 weight rows for
+// all activation rows at once:
+//   D[128 activation rows (TMEM lanes)][128 weight rows (columns)]
+//     += X_tile[128 x 16] * Wdec_tile[128 x 16]^T,   M = N = 128, K = 16,
+// with both operands in shared memory (128-byte swizzled, K-major).  Rows of
+// X past M are zero-filled by TMA (no memory traffic); they produce zero rows
+// of D that are never stored.
+//
+// CTA roles (512 threads), one persistent CTA per SM over output tiles of
+// 128 weight rows (64 outputs for the gated projection, gate row i and up
+// row i at B rows 2i and 2i + 1):
+//   warp 0, one lane: TMA producer of X sub-tiles [128 rows x 64 k] (the same
+//     sub-tiles for every output tile, re-read from L2).
+//   warp 2, one lane: TMA producer of packed weight stages (as tc_proj).
+//   warp 1, one lane: issues the MMAs (4 per 64-k sub-step) and owns TMEM
+//     (two D buffers of 128 columns).
+//   warps 4..11, two decode groups: thread r of a group owns B row r and
+//     decodes weights [32 g, 32 g + 32) of each 64-k sub-step (codec.cuh,
+//     bit-exact) straight into the swizzled B ring in shared memory.
+//   warps 12..15: epilogue.  Thread m owns activation row m = TMEM lane m: it
+//     reads its 128 columns of D, forms fp16 outputs (act(g) x u for column
+//     pairs), stages them in a 128-byte swizzled tile and one thread stores
+//     the tile with TMA (rows past M are clipped by the tensor map).
+// Every wait is bounded in time; on expiry the CTA records the failure,
+// drains its copies in flight, frees TMEM and returns.
+#pragma once
+
+#include "tc_proj.cuh"
+
+namespace m4q {
+
+// D[tmem] (+)= A[smem] * B[smem]^T; fp16 inputs, fp32 accumulator.
+__device__ __forceinline__ void tc_mma_ss_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int C, bool SWIGLU>
+struct TsCfg {
+  using S = Stage<C>;
+  static constexpr int kThreads = 512;
+  static constexpr int kRows = 128;                          // B rows (weight rows) per tile = MMA N
+  static constexpr int kOutRows = SWIGLU ? 64 : 128;         // outputs per tile
+  static constexpr int kXStage = 128 * 128;                  // [128 m][64 k] fp16, swizzled
+  static constexpr int kBStage = 128 * 128;                  // [128 weight rows][64 k] fp16, swizzled
+  static constexpr int kSW = S::KPB <= 160 ? 3 : 2;          // packed-W ring depth
+  static constexpr int kSX = S::KPB <= 160 ? 4 : 3;          // X ring depth
+  static constexpr int kSB = 4;                              // decoded-B ring depth
+  static constexpr int kWStage = kRows * S::KPB;
+  static constexpr int kYBytes = 128 * kOutRows * 2;         // 64-output boxes of [128 m][128 B]
+  static constexpr int kBars = 2 * kSX + 2 * kSW + 2 * kSB + 5;
+  static constexpr int kSmemBytes =
+      1024 + kSX * kXStage + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
+  static constexpr uint32_t kTmemCols = 256;                 // two D buffers
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kWStage % 128 == 0 && (64 * S::KPB) % 128 == 0, "TMA destinations 128-byte aligned");
+};
+
+template <int C, bool SWIGLU, int ACT>
+__global__ void __launch_bounds__(512, 1)
+    tc_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+                    const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
+                    const TcParams p) {
+  using Cfg = TsCfg<C, SWIGLU>;
+  using S = Stage<C>;
+  constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SB = Cfg::kSB;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* xs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* bs = xs + SX * Cfg::kXStage;
+  uint8_t* ys = bs + SB * Cfg::kBStage;
+  uint8_t* ws = ys + Cfg::kYBytes;
+  uint64_t* x_full = reinterpret_cast<uint64_t*>(ws + SW * Cfg::kWStage);
+  uint64_t* x_empty = x_full + SX;
+  uint64_t* w_full = x_empty + SX;
+  uint64_t* w_empty = w_full + SW;
+  uint64_t* b_full = w_empty + SW;
+  uint64_t* b_empty = b_full + SB;
+  uint64_t* d_full = b_empty + SB;    // [2]
+  uint64_t* d_empty = d_full + 2;     // [2]
+  uint64_t* drain = d_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nks = (p.K + 63) / 64;
+  const int npk = (p.K + S::KP - 1) / S::KP;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
+    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 256); }
+    for (int i = 0; i < SB; ++i) { mbar_init(&b_full[i], 256); mbar_init(&b_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ X producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      int xi = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        for (int ks = 0; ks < nks; ++ks) {
+          const int sx = xi % SX;
+          if (xi >= SX && !mbar_wait_idle(&x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
+          tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx], ks * 64, 0);
+          ++xi;
+        }
+      }
+      if (!ok) {
+        for (int i = (xi > SX ? xi - SX : 0); i < xi; ++i)
+          mbar_wait_drain(&x_full[i % SX], (i / SX) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ W producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w0);
+      if (SWIGLU) tma_prefetch_desc(&tm_w1);
+      int wi = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        const int n0 = tile * Cfg::kOutRows;
+        for (int pk = 0; pk < npk; ++pk) {
+          const int sp = wi % SW;
+          if (wi >= SW && !mbar_wait_idle(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
+          uint8_t* dst = ws + sp * Cfg::kWStage;
+          const int xc = pk * (S::KPB / 2);  // uint16 elements
+          tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
+          if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
+          ++wi;
+        }
+      }
+      if (!ok) {
+        for (int i = (wi > SW ? wi - SW : 0); i < wi; ++i)
+          mbar_wait_drain(&w_full[i % SW], (i / SW) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, 128);
+      int ks_g = 0, lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++lt) {
+        const int db = lt & 1;
+        // D buffer db must have been read out by the epilogue two tiles ago.
+        if (lt >= 2 && !mbar_wait(&d_empty[db], ((lt >> 1) - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        for (int ks = 0; ks < nks; ++ks, ++ks_g) {
+          const int sx = ks_g % SX, sb = ks_g % SB;
+          if (!mbar_wait(&b_full[sb], (ks_g / SB) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(&x_full[sx], (ks_g / SX) & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_sw128_kmajor(smem_u32(xs + sx * Cfg::kXStage));
+          const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(bs + sb * Cfg::kBStage));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ss_f16(tmem + 128 * db, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+          tc_commit(&x_empty[sx]);
+          tc_commit(&b_empty[sb]);
+        }
+        if (ok) tc_commit(&d_full[db]);
+      }
+      // Every MMA issued above completes before the CTA frees TMEM.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ decode
+    const int G = (warp - 4) >> 2;      // weights [32 G, 32 G + 32) of each sub-step
+    const int r = threadIdx.x & 127;    // B row
+    const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
+    bool ok = true;
+    int ks_g = 0, pk_g = 0;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      int ks = 0;
+      for (int pk = 0; pk < npk && ok; ++pk, ++pk_g) {
+        uint32_t w[S::WORDS];
+        const int sp = pk_g % SW;
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk_g / SW) & 1, ctl));
+        if (!ok) break;
+        const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + srow * S::KPB);
+#pragma unroll
+        for (int i = 0; i < S::KPB / 16; ++i) {
+          const uint4 v = src[i];
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        mbar_arrive(&w_empty[sp]);
+#pragma unroll
+        for (int j = 0; j < S::SUB; ++j) {
+          if (ks >= nks) break;
+          const int sb = ks_g % SB;
+          if (ks_g >= SB) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&b_empty[sb], ((ks_g / SB) - 1) & 1, ctl));
+            if (!ok) break;
+          }
+          uint32_t out[16];
+          if (G == 0) decode_half<C, 0>(w, j, out);
+          else decode_half<C, 1>(w, j, out);
+          // row r of the 128-byte swizzled tile: 16-byte chunk c sits at c ^ (r & 7)
+          uint8_t* row = bs + sb * Cfg::kBStage + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 4 * G + q;
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+          }
+          fence_proxy_async_smem();   // generic-proxy writes, read by the tensor core
+          mbar_arrive(&b_full[sb]);
+          ++ks;
+          ++ks_g;
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int m = 32 * q + lane;        // activation row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const bool leader = threadIdx.x == 384;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++lt) {
+      const int db = lt & 1;
+      const int n0 = tile * Cfg::kOutRows;
+      bool dok = false;
+      if (!*ctl.abort) dok = mbar_wait_idle(&d_full[db], (lt >> 1) & 1, ctl, 128);
+      if (named_bar_any(1, 128, !dok || *ctl.abort)) break;
+      // The previous tile's store has read the staging tile.
+      if (leader) bulk_wait_read<0>();
+      named_bar_sync(1, 128);
+      tc_fence_after();
+      // Staging: [box of 64 outputs][128 m][128 B], 16-byte chunk c of row m
+      // at c ^ (m & 7).  Each 32-column chunk of D is converted and written
+      // as soon as it is read.
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_base + 128 * db + 32 * ch, v);
+        constexpr int NW = SWIGLU ? 8 : 16;   // packed fp16 pairs from this chunk
+        uint32_t y2[NW];
+        if constexpr (SWIGLU) {
+          // columns 2i, 2i + 1: gate and up of output 16 ch + i
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float y[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float g = __uint_as_float(v[2 * (i + h)]), u = __uint_as_float(v[2 * (i + h) + 1]);
+              y[h] = (ACT ? gelu_f(g) : __fdividef(g, 1.0f + __expf(-g))) * u;
+            }
+            const __half2 hy = __floats2half2_rn(y[0], y[1]);
+            y2[i / 2] = *reinterpret_cast<const uint32_t*>(&hy);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const __half2 hy = __floats2half2_rn(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            y2[i / 2] = *reinterpret_cast<const uint32_t*>(&hy);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < NW / 4; ++k) {
+          const int c = (NW / 4) * ch + k;          // 16-byte chunk of this row's outputs
+          uint8_t* box = ys + (c >> 3) * (128 * 128);
+          *reinterpret_cast<uint4*>(box + m * 128 + (((c & 7) ^ (m & 7)) << 4)) =
+              make_uint4(y2[4 * k], y2[4 * k + 1], y2[4 * k + 2], y2[4 * k + 3]);
+        }
+      }
+      // Every column of D has been read: the buffer may take tile lt + 2.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[db]);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+#pragma unroll
+        for (int b = 0; b < Cfg::kOutRows / 64; ++b) tma_store_2d(&tm_y, ys + b * (128 * 128), n0 + 64 * b, 0);
+        bulk_commit();
+      }
+    }
+    if (leader) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace m4q

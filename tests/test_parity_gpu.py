@@ -147,6 +147,39 @@ def test_tc_swiglu_parity(codec, general, M):
         assert_close(Y, oracle.swiglu(X, Wg, Wu, codec, M, N, K), "tc swiglu %s M=%d K=%d" % (codec, M, K))
 
 
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("M", [1, 5, 16, 33, 100, 128])
+def test_tc_small_m_parity(codec, M):
+    # M <= 128 on the tensor-core path: the activations are the A operand and
+    # the decoded weights the B operand (N = 264: ragged last tiles).
+    K = kvals(codec, False)[-1]
+    N = 264
+    X = synth.activations(M, K, seed=M + 60)
+    W = synth.weights(codec, N, K, seed=61)
+    Wu = synth.weights(codec, N, K, seed=61, name="Wu")
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_TC))
+    assert_close(Y, oracle.gemm(X, W, codec, M, N, K), "tc small gemm %s M=%d" % (codec, M))
+    Ys = host(m.glu(dev(X), dev(W), dev(Wu), codec, N, K, m.ACT_SILU, path=m.PATH_TC))
+    assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "tc small swiglu %s M=%d" % (codec, M))
+    Yg = host(m.glu(dev(X), dev(W), dev(Wu), codec, N, K, m.ACT_GELU, path=m.PATH_TC))
+    assert_close(Yg, oracle.geglu(X, W, Wu, codec, M, N, K), "tc small geglu %s M=%d" % (codec, M))
+
+
+@pytest.mark.parametrize("codec", CODECS)
+def test_tc_small_m_one_hot_readout_bit_exact(codec):
+    # X rows are unit vectors at permuted columns: every output is one exact
+    # product 1 * w, so Y must be columns of the fp16 weights bit for bit --
+    # checks the decode, the swizzled operand layouts and the epilogue.
+    K = kvals(codec, False)[0]
+    M, N = 128, 200
+    cols = np.random.default_rng(codec).permutation(K)[:M]
+    X = np.zeros((M, K), dtype=np.float16)
+    X[np.arange(M), cols] = 1
+    W = synth.weights(codec, N, K, seed=62)
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_TC)).view(np.uint16)
+    assert np.array_equal(Y, oracle.dequant_f16(W, codec, N, K)[:, cols].T)
+
+
 def test_tc_tile_widths():
     # M large enough for 256- and 128-wide activation tiles on a full GPU.
     import torch
