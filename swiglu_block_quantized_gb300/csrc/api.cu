@@ -179,7 +179,9 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     // (one activation tile of 128 rows as the A operand).
     L.small = L.wtma && head_dim == 0 && M <= 128;
     int nx = 64;
-    if (!L.wtma || L.small) {
+    if (L.small) {
+      nx = M <= 32 ? 32 : (M <= 64 ? 64 : 128);   // X rows per stage of the small-M kernel
+    } else if (!L.wtma) {
       nx = 128;
     } else if (((M + 255) / 256) * ntiles >= dev.sms) {
       nx = 256;

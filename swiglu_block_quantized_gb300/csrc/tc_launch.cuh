@@ -68,12 +68,12 @@ cudaError_t launch_tc_glu(const ProjLaunch& L) {
 }
 
 // Small M (<= 128): activations as the A operand, decoded weights as B.
-template <int C, bool SWIGLU, int ACT>
+template <int C, bool SWIGLU, int ACT, int XR>
 cudaError_t launch_tcs_one(const ProjLaunch& L) {
-  using Cfg = TsCfg<C, SWIGLU>;
-  auto kern = tc_small_kernel<C, SWIGLU, ACT>;
+  using Cfg = TsCfg<C, SWIGLU, XR>;
+  auto kern = tc_small_kernel<C, SWIGLU, ACT, XR>;
   std::atomic<unsigned long long>& configured =
-      attr_flag<std::integer_sequence<int, 4, C, SWIGLU, ACT>>();
+      attr_flag<std::integer_sequence<int, 4, C, SWIGLU, ACT, XR>>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -99,10 +99,18 @@ cudaError_t launch_tcs_one(const ProjLaunch& L) {
   return cudaGetLastError();
 }
 
+template <int C, int XR>
+cudaError_t launch_tcs_xr(const ProjLaunch& L) {
+  if (!L.swiglu) return launch_tcs_one<C, false, 0, XR>(L);
+  return L.act ? launch_tcs_one<C, true, 1, XR>(L) : launch_tcs_one<C, true, 0, XR>(L);
+}
+
+// L.nx = X rows per stage (32, 64 or 128; the X tensor map's box height).
 template <int C>
 cudaError_t launch_tcs(const ProjLaunch& L) {
-  if (!L.swiglu) return launch_tcs_one<C, false, 0>(L);
-  return L.act ? launch_tcs_one<C, true, 1>(L) : launch_tcs_one<C, true, 0>(L);
+  if (L.nx == 32) return launch_tcs_xr<C, 32>(L);
+  if (L.nx == 64) return launch_tcs_xr<C, 64>(L);
+  return launch_tcs_xr<C, 128>(L);
 }
 
 template <int C>

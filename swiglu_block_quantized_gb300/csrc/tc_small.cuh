@@ -10,9 +10,12 @@
 // all activation rows at once:
 //   D[128 activation rows (TMEM lanes)][128 weight rows (columns)]
 //     += X_tile[128 x 16] * Wdec_tile[128 x 16]^T,   M = N = 128, K = 16,
-// with both operands in shared memory (128-byte swizzled, K-major).  Rows of
-// X past M are zero-filled by TMA (no memory traffic); they produce zero rows
-// of D that are never stored.
+// with both operands in shared memory (128-byte swizzled, K-major).  An X
+// stage holds XR = 32, 64 or 128 rows (the least multiple covering M), so a
+// 64 KB X ring has 16, 8 or 4 stages: X sub-tiles are re-read from L2 for
+// every output tile, and the ring must cover that latency.  The MMA still
+// reads a 128-row A window; rows past XR are the next stages (or a pad after
+// the ring) and only feed rows of D at or past M, which are never stored.
 //
 // CTA roles (512 threads), one persistent CTA per SM over output tiles of
 // 128 weight rows (64 outputs for the gated projection, gate row i and up
@@ -48,40 +51,43 @@ __device__ __forceinline__ void tc_mma_ss_f16(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-template <int C, bool SWIGLU>
+template <int C, bool SWIGLU, int XR>
 struct TsCfg {
   using S = Stage<C>;
   static constexpr int kThreads = 512;
   static constexpr int kRows = 128;                          // B rows (weight rows) per tile = MMA N
   static constexpr int kOutRows = SWIGLU ? 64 : 128;         // outputs per tile
-  static constexpr int kXStage = 128 * 128;                  // [128 m][64 k] fp16, swizzled
+  static constexpr int kXStage = XR * 128;                   // [XR m][64 k] fp16, swizzled
+  static constexpr int kXPad = (128 - XR) * 128;             // keeps the last stage's A window inside
   static constexpr int kBStage = 128 * 128;                  // [128 weight rows][64 k] fp16, swizzled
   static constexpr int kSW = S::KPB <= 160 ? 3 : 2;          // packed-W ring depth
-  static constexpr int kSX = S::KPB <= 160 ? 4 : 3;          // X ring depth
+  static constexpr int kSX = ((SWIGLU && S::KPB <= 160) ? 65536 : 49152) / kXStage;  // X ring depth
   static constexpr int kSB = 4;                              // decoded-B ring depth
   static constexpr int kWStage = kRows * S::KPB;
   static constexpr int kYBytes = 128 * kOutRows * 2;         // 64-output boxes of [128 m][128 B]
   static constexpr int kBars = 2 * kSX + 2 * kSW + 2 * kSB + 5;
   static constexpr int kSmemBytes =
-      1024 + kSX * kXStage + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
+      1024 + kSX * kXStage + kXPad + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
   static constexpr uint32_t kTmemCols = 256;                 // two D buffers
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(XR == 32 || XR == 64 || XR == 128, "X stage rows");
+  static_assert(kXStage % 1024 == 0, "X stages start on swizzle atoms");
   static_assert(kWStage % 128 == 0 && (64 * S::KPB) % 128 == 0, "TMA destinations 128-byte aligned");
 };
 
-template <int C, bool SWIGLU, int ACT>
+template <int C, bool SWIGLU, int ACT, int XR>
 __global__ void __launch_bounds__(512, 1)
     tc_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y,
                     const TcParams p) {
-  using Cfg = TsCfg<C, SWIGLU>;
+  using Cfg = TsCfg<C, SWIGLU, XR>;
   using S = Stage<C>;
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SB = Cfg::kSB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* xs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* bs = xs + SX * Cfg::kXStage;
+  uint8_t* bs = xs + SX * Cfg::kXStage + Cfg::kXPad;
   uint8_t* ys = bs + SB * Cfg::kBStage;
   uint8_t* ws = ys + Cfg::kYBytes;
   uint64_t* x_full = reinterpret_cast<uint64_t*>(ws + SW * Cfg::kWStage);
