@@ -516,6 +516,8 @@ def run_profile_case(case, local):
         Wu = synth.weights(synth.MLX4, N_, K_, seed=2, name="Wu")
     if case.endswith("_m1"):
         X = X[:1].copy()
+    elif case.endswith("_m64"):
+        X = X[:64].copy()
     x = torch.from_numpy(X).cuda()
     wg, wu = torch.from_numpy(Wg).cuda(), torch.from_numpy(Wu).cuda()
     y = torch.empty((X.shape[0], N_), dtype=torch.float16, device="cuda")
@@ -535,7 +537,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-case", default=None,
-                    choices=["swiglu_m2048", "swiglu_m1", "swiglu_mlx4_m2048", "swiglu_mlx4_m1",
+                    choices=["swiglu_m2048", "swiglu_m1", "swiglu_m64", "swiglu_mlx4_m2048", "swiglu_mlx4_m1",
                              "attn_prefill_q8_0", "attn_decode_q8_0", "attn_prefill_f16", "attn_decode_f16"],
                     help="only run 3 launches of one case (for ncu)")
     args = ap.parse_args(argv)
