@@ -177,7 +177,9 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     const int64_t ntiles = (N + out_rows - 1) / out_rows;
     // M <= 128 with TMA-able rows and row-major output: the small-M kernel
     // (one activation tile of 128 rows as the A operand).
-    L.small = L.wtma && head_dim == 0 && M <= 128;
+    // (Not for a plain GEMM with 272-byte packed stages above M = 64: its
+    // 128-row X stages and 128-output Y tile do not fit shared memory.)
+    L.small = L.wtma && head_dim == 0 && M <= 128 && !(kStageBytes[codec] > 160 && !swiglu && M > 64);
     int nx = 64;
     if (L.small) {
       nx = M <= 32 ? 32 : (M <= 64 ? 64 : 128);   // X rows per stage of the small-M kernel

@@ -71,6 +71,9 @@ cudaError_t launch_tc_glu(const ProjLaunch& L) {
 template <int C, bool SWIGLU, int ACT, int XR>
 cudaError_t launch_tcs_one(const ProjLaunch& L) {
   using Cfg = TsCfg<C, SWIGLU, XR>;
+  if constexpr (!Cfg::kFits) {
+    return cudaErrorInvalidConfiguration;   // not dispatched here (see api.cu)
+  } else {
   auto kern = tc_small_kernel<C, SWIGLU, ACT, XR>;
   std::atomic<unsigned long long>& configured =
       attr_flag<std::integer_sequence<int, 4, C, SWIGLU, ACT, XR>>();
@@ -97,6 +100,7 @@ cudaError_t launch_tcs_one(const ProjLaunch& L) {
   const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
   return cudaGetLastError();
+  }
 }
 
 template <int C, int XR>

@@ -61,16 +61,21 @@ struct TsCfg {
   static constexpr int kXPad = (128 - XR) * 128;             // keeps the last stage's A window inside
   static constexpr int kBStage = 128 * 128;                  // [128 weight rows][64 k] fp16, swizzled
   static constexpr int kSW = S::KPB <= 160 ? 3 : 2;          // packed-W ring depth
-  static constexpr int kSX = ((SWIGLU && S::KPB <= 160) ? 65536 : 49152) / kXStage;  // X ring depth
+  // X and decoded-B rings advance together, 4 slots = 2 pairs of sub-steps:
+  // the MMA thread consumes a pair at once and frees it with one commit.
+  static constexpr int kSX = 4;                              // X ring depth
   static constexpr int kSB = 4;                              // decoded-B ring depth
   static constexpr int kWStage = kRows * S::KPB;
   static constexpr int kYBytes = 128 * kOutRows * 2;         // 64-output boxes of [128 m][128 B]
-  static constexpr int kBars = 2 * kSX + 2 * kSW + 2 * kSB + 5;
+  static constexpr int kBars = kSX + 2 * kSW + kSB + 2 + 5;
   static constexpr int kSmemBytes =
       1024 + kSX * kXStage + kXPad + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
   static constexpr uint32_t kTmemCols = 256;                 // two D buffers
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // Q8_0 / Q2_0 GEMM with 128-row X stages does not fit; the host sends
+  // that case to tc_proj (M > 64 with 272-byte packed stages).
+  static constexpr bool kFits = kSmemBytes <= 227 * 1024;
   static_assert(XR == 32 || XR == 64 || XR == 128, "X stage rows");
+  static_assert(kSX == kSB && kSX % 2 == 0, "paired X and B rings");
   static_assert(kXStage % 1024 == 0, "X stages start on swizzle atoms");
   static_assert(kWStage % 128 == 0 && (64 * S::KPB) % 128 == 0, "TMA destinations 128-byte aligned");
 };
@@ -82,6 +87,7 @@ __global__ void __launch_bounds__(512, 1)
                     const TcParams p) {
   using Cfg = TsCfg<C, SWIGLU, XR>;
   using S = Stage<C>;
+  static_assert(Cfg::kFits, "shared memory budget");
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SB = Cfg::kSB;
 
   extern __shared__ uint8_t smem_raw[];
@@ -91,12 +97,11 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t* ys = bs + SB * Cfg::kBStage;
   uint8_t* ws = ys + Cfg::kYBytes;
   uint64_t* x_full = reinterpret_cast<uint64_t*>(ws + SW * Cfg::kWStage);
-  uint64_t* x_empty = x_full + SX;
-  uint64_t* w_full = x_empty + SX;
+  uint64_t* w_full = x_full + SX;
   uint64_t* w_empty = w_full + SW;
   uint64_t* b_full = w_empty + SW;
-  uint64_t* b_empty = b_full + SB;
-  uint64_t* d_full = b_empty + SB;    // [2]
+  uint64_t* pair_free = b_full + SB;  // [2]: X and B slots 2p, 2p + 1 consumed
+  uint64_t* d_full = pair_free + 2;   // [2]
   uint64_t* d_empty = d_full + 2;     // [2]
   uint64_t* drain = d_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -107,9 +112,10 @@ __global__ void __launch_bounds__(512, 1)
   const int npk = (p.K + S::KP - 1) / S::KP;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
+    for (int i = 0; i < SX; ++i) mbar_init(&x_full[i], 1);
     for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 256); }
-    for (int i = 0; i < SB; ++i) { mbar_init(&b_full[i], 256); mbar_init(&b_empty[i], 1); }
+    for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 256);
+    for (int i = 0; i < 2; ++i) mbar_init(&pair_free[i], 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
         for (int ks = 0; ks < nks; ++ks) {
           const int sx = xi % SX;
-          if (xi >= SX && !mbar_wait_idle(&x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+          if (xi >= SX && !mbar_wait_idle(&pair_free[sx >> 1], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
           tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx], ks * 64, 0);
           ++xi;
@@ -181,18 +187,25 @@ __global__ void __launch_bounds__(512, 1)
         // D buffer db must have been read out by the epilogue two tiles ago.
         if (lt >= 2 && !mbar_wait(&d_empty[db], ((lt >> 1) - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < nks; ++ks, ++ks_g) {
-          const int sx = ks_g % SX, sb = ks_g % SB;
-          if (!mbar_wait(&b_full[sb], (ks_g / SB) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&x_full[sx], (ks_g / SX) & 1, ctl)) { ok = false; break; }
+        // nks is even here (K is a multiple of 128 on this path)
+        for (int ks = 0; ks < nks; ks += 2, ks_g += 2) {
+          const int s0 = ks_g % SX;   // slots s0, s0 + 1 of both rings (SX == SB)
+          if (!mbar_wait(&b_full[s0], (ks_g / SB) & 1, ctl) || !mbar_wait(&x_full[s0], (ks_g / SX) & 1, ctl) ||
+              !mbar_wait(&b_full[s0 + 1], (ks_g / SB) & 1, ctl) ||
+              !mbar_wait(&x_full[s0 + 1], (ks_g / SX) & 1, ctl)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint64_t adesc = sdesc_sw128_kmajor(smem_u32(xs + sx * Cfg::kXStage));
-          const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(bs + sb * Cfg::kBStage));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ss_f16(tmem + 128 * db, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
-          tc_commit(&x_empty[sx]);
-          tc_commit(&b_empty[sb]);
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t adesc = sdesc_sw128_kmajor(smem_u32(xs + (s0 + h) * Cfg::kXStage));
+            const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(bs + (s0 + h) * Cfg::kBStage));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ss_f16(tmem + 128 * db, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | h | kk) != 0);
+          }
+          tc_commit(&pair_free[s0 >> 1]);
         }
         if (ok) tc_commit(&d_full[db]);
       }
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(512, 1)
           if (ks >= nks) break;
           const int sb = ks_g % SB;
           if (ks_g >= SB) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&b_empty[sb], ((ks_g / SB) - 1) & 1, ctl));
+            ok = __all_sync(0xffffffffu, mbar_wait(&pair_free[sb >> 1], ((ks_g / SB) - 1) & 1, ctl));
             if (!ok) break;
           }
           uint32_t out[16];
