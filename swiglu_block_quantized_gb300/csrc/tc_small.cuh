@@ -23,8 +23,11 @@
 //   warp 0, one lane: TMA producer of X sub-tiles [128 rows x 64 k] (the same
 //     sub-tiles for every output tile, re-read from L2).
 //   warp 2, one lane: TMA producer of packed weight stages (as tc_proj).
-//   warp 1, one lane: issues the MMAs (4 per 64-k sub-step) and owns TMEM
-//     (two D buffers of 128 columns).
+//   warp 1, one lane: issues the MMAs and owns TMEM (two D buffers of 128
+//     columns).  The issue loop is the serial step of this kernel, so it
+//     takes two 64-k sub-steps at a time (8 MMAs) and frees both with one
+//     commit on a per-pair barrier that the X producer and the decode
+//     warps both wait on (X and B rings advance together, 2 pairs deep).
 //   warps 4..11, two decode groups: thread r of a group owns B row r and
 //     decodes weights [32 g, 32 g + 32) of each 64-k sub-step (codec.cuh,
 //     bit-exact) straight into the swizzled B ring in shared memory.
