@@ -11,11 +11,11 @@
 //   D[128 activation rows (TMEM lanes)][128 weight rows (columns)]
 //     += X_tile[128 x 16] * Wdec_tile[128 x 16]^T,   M = N = 128, K = 16,
 // with both operands in shared memory (128-byte swizzled, K-major).  An X
-// stage holds XR = 32, 64 or 128 rows (the least multiple covering M), so a
-// 64 KB X ring has 16, 8 or 4 stages: X sub-tiles are re-read from L2 for
-// every output tile, and the ring must cover that latency.  The MMA still
-// reads a 128-row A window; rows past XR are the next stages (or a pad after
-// the ring) and only feed rows of D at or past M, which are never stored.
+// stage holds XR = 32, 64 or 128 rows (the least of them covering M): TMA
+// then moves only the rows that exist (128-row boxes that were mostly out of
+// bounds were slow).  The MMA still reads a 128-row A window; rows past XR
+// are the next stages (or a pad after the ring) and only feed rows of D at
+// or past M, which are never stored.
 //
 // CTA roles (512 threads), one persistent CTA per SM over output tiles of
 // 128 weight rows (64 outputs for the gated projection, gate row i and up
