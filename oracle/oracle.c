@@ -24,7 +24,8 @@
  *    fixes them as 32-weight blocks with an fp16 scale d, Q4_0 w = (q - 8) * d
  *    with a 4-bit q, Q8_0 w = q * d with a signed 8-bit q.
  *  - Project page, section 4 (v0.2.1, "mlx_4bit_planar") and Table B
- *    ("identical MLX 4-bit weights (block_mlx_4bit)"), and "Releases" v0.2.1
+ *    (both engines of the MLX comparison read the same block_mlx_4bit
+ *    weights), and "Releases" v0.2.1
  *    and v0.3.0 (MLX 4-bit among the affine formats of the codec registry):
  *    the MLX 4-bit block is a 20-byte struct.  The pages give its size but
  *    not its fields; this oracle reads it as MLX's affine group quantization
@@ -47,7 +48,7 @@
  *  - "v0.1 vs v0.2 comparison", section 2.2 (dual-SIMDgroup SwiGLU): the
  *    fused projection is SiLU(X * Wg^T) x (X * Wu^T), with only the final
  *    activation written out.
- *  - "Releases", v0.3.0 (TransformerBlock: "SwiGLU / GeGLU activations",
+ *  - "Releases", v0.3.0 (TransformerBlock: GeGLU listed beside SwiGLU,
  *    Gemma 2 configurations): the same gated projection with GELU in place
  *    of SiLU.  The pages do not define GELU; this oracle takes the textbook
  *    definition GELU(g) = g * Phi(g) = g/2 * erfc(-g / sqrt 2).
