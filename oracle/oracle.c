@@ -20,8 +20,8 @@
  *    q = 3 decodes to +2 * d.
  *  - "Releases", v0.3.0 / v0.2.3 and the project page's Table B: GGUF Q4_0
  *    (block_q4_0) and Q8_0 are the other two codecs.  The pages name them
- *    but do not print their formulas; the workload statement of this library
- *    fixes them as 32-weight blocks with an fp16 scale d, Q4_0 w = (q - 8) * d
+ *    but do not print their formulas; this oracle takes GGUF's public
+ *    definition: 32-weight blocks with an fp16 scale d, Q4_0 w = (q - 8) * d
  *    with a 4-bit q, Q8_0 w = q * d with a signed 8-bit q.
  *  - Project page, section 4 (v0.2.1, "mlx_4bit_planar") and Table B
  *    (both engines of the MLX comparison read the same block_mlx_4bit
