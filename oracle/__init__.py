@@ -72,6 +72,8 @@ def _bind(path: str):
     lib.oracle_gelu.restype = ctypes.c_double
     lib.oracle_mlx4_pack.argtypes = [vp, vp, vp, i64, i64, vp]
     lib.oracle_mlx4_pack.restype = i32
+    lib.oracle_repack.argtypes = [vp, i32, i64, i64, vp]
+    lib.oracle_repack.restype = i32
     lib.oracle_attention.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32,
                                      ctypes.c_double, vp, i64, vp, i32]
     lib.oracle_attention.restype = i32
@@ -203,6 +205,15 @@ def mlx4_pack(words, scales, biases, N: int, K: int) -> np.ndarray:
     b = np.ascontiguousarray(np.asarray(biases, dtype=np.float16)).view(np.uint16)
     out = np.zeros((N, (K // 32) * 20), dtype=np.uint8)
     _check(_L().oracle_mlx4_pack(_ptr(w), _ptr(s), _ptr(b), N, K, _ptr(out)), "mlx4_pack")
+    return out
+
+
+def repack(W: np.ndarray, codec: int, N: int, K: int) -> np.ndarray:
+    """Blocks -> planes, uint8 [weight bytes]: the code bytes of every block
+    in order, then the fp16 scales [N, K/B], then (MLX4) the fp16 biases."""
+    Wp = _as_packed(W)
+    out = np.zeros(Wp.size, dtype=np.uint8)
+    _check(_L().oracle_repack(_ptr(Wp), codec, N, K, _ptr(out)), "repack")
     return out
 
 

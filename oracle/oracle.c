@@ -247,6 +247,42 @@ int oracle_mlx4_pack(const uint32_t* words, const uint16_t* scales, const uint16
   return 0;
 }
 
+/* Blocks -> planes: the one-time re-layout that splits the blocks of W into
+ * separate arrays ("v0.1 vs v0.2 comparison", section 4, splits MLX 4-bit
+ * blocks this way; the same split is taken here for every codec).  P receives,
+ * back to back, with no padding:
+ *   codes:  for each row n and block b in order, the block's code bytes,
+ *           unchanged (16 bytes for Q4_0 and MLX4, 32 for Q8_0 and Q2_0);
+ *   scales: fp16 [N, K/B], the scale d of each block (MLX4: s);
+ *   biases: fp16 [N, K/B], MLX4 only, the bias b of each block.
+ * P has as many bytes as W.  For MLX4 the three arrays are MLX's planar
+ * arrays (the inverse of oracle_mlx4_pack).  Returns 0, -2 for an unknown
+ * codec, -3 for a bad shape. */
+int oracle_repack(const uint8_t* W, int codec, long long N, long long K, uint8_t* P) {
+  int rc = check_shape(codec, N, K);
+  if (rc) return rc;
+  long long nb = K / oracle_block_size(codec), BB = oracle_block_bytes(codec);
+  long long head = (codec == ORACLE_MLX4) ? 4 : 2; /* scale (and bias) bytes */
+  long long CB = BB - head;                        /* code bytes per block */
+  uint8_t* codes = P;
+  uint8_t* scales = codes + N * nb * CB;
+  uint8_t* biases = scales + 2 * N * nb;
+  for (long long n = 0; n < N; ++n) {
+    for (long long b = 0; b < nb; ++b) {
+      long long i = n * nb + b;
+      const uint8_t* blk = W + i * BB;
+      memcpy(codes + i * CB, blk + head, (size_t)CB);
+      scales[2 * i] = blk[0];
+      scales[2 * i + 1] = blk[1];
+      if (codec == ORACLE_MLX4) {
+        biases[2 * i] = blk[2];
+        biases[2 * i + 1] = blk[3];
+      }
+    }
+  }
+  return 0;
+}
+
 /* SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), in binary64. */
 double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
 

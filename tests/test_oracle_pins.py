@@ -272,6 +272,56 @@ def test_mlx4_pack():
         oracle.mlx4_pack(np.zeros((1, 2), np.uint32), np.zeros(1, np.float16), np.zeros(1, np.float16), 1, 16)
 
 
+# ------------------------------------------------------------ blocks -> planes
+
+def check_repack_golden(blocks):
+    # Hand-built blocks of one codec, laid out as two rows (the second in
+    # reverse order): the codes plane is each block's code bytes in row-major
+    # block order, then the scale bits, then (MLX4) the bias bits.
+    by_codec = {}
+    for blk in blocks:
+        by_codec.setdefault(CODEC_BY_NAME[blk["codec"]], []).append(blk)
+    for codec, blks in by_codec.items():
+        B = oracle.block_size(codec)
+        order = blks + blks[::-1]
+        nb = len(blks)
+        W = np.concatenate([golden_packed(b) for b in order])
+        P = oracle.repack(W, codec, 2, nb * B)
+        codes = [c for b in order for c in b["code_bytes"]]
+        expect = codes + [v for b in order for v in (b["d_bits"] & 0xFF, b["d_bits"] >> 8)]
+        if codec == synth.MLX4:
+            expect += [v for b in order for v in (b["b_bits"] & 0xFF, b["b_bits"] >> 8)]
+        assert P.tolist() == expect, codec
+
+
+def check_repack_planes():
+    # The scale plane is the generator's scale array; for MLX4 the three
+    # planes are the generator's own MLX planar arrays (words, scales, biases).
+    for codec in synth.CODECS:
+        for N, K in ((3, 256), (2, 1024)):
+            q = synth.codes(codec, N, K, seed=N, name="W")
+            d = synth.scales(codec, N, K, seed=N, name="W")
+            b = synth.biases(codec, N, K, seed=N, name="W", d=d)
+            W = synth.pack(codec, q, d, b)
+            P = oracle.repack(W, codec, N, K)
+            nb = K // oracle.block_size(codec)
+            cb = oracle.block_bytes(codec) - (4 if codec == synth.MLX4 else 2)
+            scales = P[N * nb * cb: N * nb * (cb + 2)].view(np.float16).reshape(N, nb)
+            assert np.array_equal(scales.view(np.uint16), d.view(np.uint16)), codec
+            if codec == synth.MLX4:
+                words, s, bb = synth.planar(q, d, b)
+                assert np.array_equal(P[:N * nb * cb].view("<u4").reshape(N, K // 8), words)
+                assert np.array_equal(P[N * nb * (cb + 2):].view(np.uint16).reshape(N, nb), bb.view(np.uint16))
+                assert np.array_equal(oracle.mlx4_pack(words, s, bb, N, K), W)
+
+
+def test_repack(golden_blocks):
+    check_repack_golden(golden_blocks)
+    check_repack_planes()
+    with pytest.raises(ValueError):
+        oracle.repack(np.zeros(18, np.uint8), synth.Q4_0, 1, 16)
+
+
 def test_mlx4_scale_zero_gives_bias():
     # s = 0: every weight equals the block's bias whatever its code.
     K = 64
@@ -444,6 +494,14 @@ MUTATIONS = {
                              "int q = (int)((words[n * (K / 8) + k / 8] >> (28 - 4 * (k % 8))) & 0xf);"),
     "mlx4_pack_bias_scale_swapped": ("uint16_t s = scales[n * nb + b], t = biases[n * nb + b];",
                                      "uint16_t t = scales[n * nb + b], s = biases[n * nb + b];"),
+    "repack_codes_with_header": ("memcpy(codes + i * CB, blk + head, (size_t)CB);",
+                                 "memcpy(codes + i * CB, blk, (size_t)CB);"),
+    "repack_blocks_column_major": ("memcpy(codes + i * CB, blk + head, (size_t)CB);",
+                                   "memcpy(codes + (b * N + n) * CB, blk + head, (size_t)CB);"),
+    "repack_scale_byte_order": ("scales[2 * i] = blk[0];\n      scales[2 * i + 1] = blk[1];",
+                                "scales[2 * i] = blk[1];\n      scales[2 * i + 1] = blk[0];"),
+    "repack_bias_from_scale": ("biases[2 * i] = blk[2];\n        biases[2 * i + 1] = blk[3];",
+                               "biases[2 * i] = blk[0];\n        biases[2 * i + 1] = blk[1];"),
 }
 
 
@@ -463,6 +521,8 @@ def all_pins_pass(golden_blocks):
         check_mlx4_affine_closed_form,
         check_mlx4_one_rounding,
         check_mlx4_pack,
+        lambda: check_repack_golden(golden_blocks),
+        check_repack_planes,
     ]
     for c in checks:
         try:
