@@ -176,6 +176,26 @@ int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* W
 int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int64_t N, int64_t K,
                   void* W, m4q_stream_t stream);
 
+/* Split packed weights into planes ("v0.1 vs v0.2 comparison", section 4:
+ * the v0.2.1 planar layout, which moves the codes of the 20-byte MLX 4-bit
+ * blocks into their own 16-byte aligned array; the same split is offered for
+ * every codec).  W: packed [N, K/B] blocks in `codec`.  Wplanar receives, back
+ * to back with no padding, m4q_weight_bytes(codec, N, K) bytes in all:
+ *   codes:  the code bytes of every block, unchanged, in row-major block
+ *           order (16 bytes per block for Q4_0 and MLX4, 32 for Q8_0 and
+ *           Q2_0), at offset 0;
+ *   scales: fp16 [N, K/B], each block's scale d (MLX4: s), right after;
+ *   biases: fp16 [N, K/B], MLX4 only, each block's bias b, after the scales.
+ * For MLX4 the three arrays are MLX's own planar arrays (the inverse of
+ * m4q_mlx4_pack).  The projections above read the packed blocks, never the
+ * planes: this is an export for callers that store or hand on weights in
+ * planar form.  Requires a known codec (else M4Q_ERR_UNSUPPORTED_CODEC),
+ * N >= 1, K >= 1 (else M4Q_ERR_INVALID_ARG) with K % B == 0 (else
+ * M4Q_ERR_BAD_SHAPE), W and Wplanar 16-byte aligned (else
+ * M4Q_ERR_MISALIGNED) and not overlapping (not checked).  Device pointers;
+ * enqueued on stream; the caller owns both buffers. */
+int m4q_repack(const void* W, int codec, int64_t N, int64_t K, void* Wplanar, m4q_stream_t stream);
+
 /* KV cache value formats for m4q_attention: fp16 values, or M4Q_Q8_0 blocks
  * along the head dimension. */
 enum m4q_kv_codec { M4Q_KV_F16 = 16 };

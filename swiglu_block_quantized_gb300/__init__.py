@@ -67,6 +67,7 @@ SIGNATURES = {
     "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_mlx4_pack": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp]),
+    "m4q_repack": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_attention": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
                              ctypes.c_float, _vp, _vp, _sz, _vp]),
     "m4q_attention_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
@@ -264,6 +265,21 @@ def mlx4_pack(words, scales, biases, n: int, k: int, out=None, stream=None):
     _packed_check(out, MLX4, n, k, "out")
     _check(load().m4q_mlx4_pack(words.data_ptr(), scales.data_ptr(), biases.data_ptr(), n, k,
                                 out.data_ptr(), _stream_ptr(stream)), "m4q_mlx4_pack")
+    return out
+
+
+def repack(w, codec: int, n: int, k: int, out=None, stream=None):
+    """Packed blocks [n, k] -> planes, uint8 [weight_bytes(codec, n, k)]: the
+    code bytes of every block in row-major block order, then the fp16 scales
+    [n, k/B], then (MLX4) the fp16 biases [n, k/B]."""
+    import torch
+    _packed_check(w, codec, n, k, "w")
+    if out is None:
+        out = torch.empty(weight_bytes(codec, n, k), dtype=torch.uint8, device=w.device)
+    _require(out, torch.uint8, "out")
+    if out.numel() != weight_bytes(codec, n, k):
+        raise ValueError("out must hold %d bytes" % weight_bytes(codec, n, k))
+    _check(load().m4q_repack(w.data_ptr(), codec, n, k, out.data_ptr(), _stream_ptr(stream)), "m4q_repack")
     return out
 
 

@@ -326,6 +326,22 @@ int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int
              : M4Q_ERR_CUDA;
 }
 
+int m4q_repack(const void* W, int codec, int64_t N, int64_t K, void* Wplanar, m4q_stream_t stream) {
+  if (!W || !Wplanar) return M4Q_ERR_INVALID_ARG;
+  if (!known_codec(codec)) return M4Q_ERR_UNSUPPORTED_CODEC;
+  if (N < 1 || K < 1 || N > INT32_MAX || K > INT32_MAX) return M4Q_ERR_INVALID_ARG;
+  if (K % kBlock[codec] != 0) return M4Q_ERR_BAD_SHAPE;
+  if (!aligned16(W) || !aligned16(Wplanar)) return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+  const long long blocks = N * (K / kBlock[codec]);
+  return m4q::launch_repack(codec, W, blocks, Wplanar, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? M4Q_OK
+             : M4Q_ERR_CUDA;
+}
+
 // ------------------------------------------------------------ attention
 
 }  // extern "C"

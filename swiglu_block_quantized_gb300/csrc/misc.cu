@@ -113,6 +113,59 @@ cudaError_t launch_mlx4_pack(const void* words, const void* scales, const void* 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- repack
+
+// Blocks -> planes: the code bytes of every block in row-major block order,
+// then the fp16 scales, then (MLX4) the fp16 biases.  One thread per block,
+// grid-stride.  A block starts on an even byte, so it is read as 16-bit
+// words; its CB code bytes (16 or 32) start on a 16-byte boundary of the
+// codes plane and are written as 16-byte stores.
+template <int C>
+__global__ void __launch_bounds__(256)
+    repack_kernel(const unsigned short* __restrict__ W, long long blocks, uint4* __restrict__ codes,
+                  unsigned short* __restrict__ scales, unsigned short* __restrict__ biases) {
+  constexpr int BB = CodecTraits<C>::BB;       // bytes per block (even)
+  constexpr int HEAD = (C == kMLX4) ? 4 : 2;   // scale (and bias) bytes
+  constexpr int CB = BB - HEAD;                // code bytes per block
+  static_assert(BB % 2 == 0 && CB % 16 == 0, "block layout");
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < blocks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const unsigned short* blk = W + i * (BB / 2);
+    scales[i] = __ldg(blk);
+    if (C == kMLX4) biases[i] = __ldg(blk + 1);
+    uint32_t w[CB / 4];
+#pragma unroll
+    for (int j = 0; j < CB / 4; ++j)
+      w[j] = (uint32_t)__ldg(blk + HEAD / 2 + 2 * j) | ((uint32_t)__ldg(blk + HEAD / 2 + 2 * j + 1) << 16);
+    uint4* dst = codes + i * (CB / 16);
+#pragma unroll
+    for (int j = 0; j < CB / 16; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
+template <int C>
+cudaError_t launch_repack_c(const void* w, long long blocks, void* out, cudaStream_t s) {
+  constexpr int CB = CodecTraits<C>::BB - ((C == kMLX4) ? 4 : 2);
+  auto* base = static_cast<uint8_t*>(out);
+  auto* scales = reinterpret_cast<unsigned short*>(base + blocks * CB);
+  auto* biases = scales + blocks;  // written for MLX4 only
+  long long grid = (blocks + 255) / 256;
+  if (grid > 152 * 16) grid = 152 * 16;
+  repack_kernel<C><<<(unsigned)grid, 256, 0, s>>>(static_cast<const unsigned short*>(w), blocks,
+                                                    reinterpret_cast<uint4*>(base), scales, biases);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(int codec, const void* w, long long blocks, void* out, cudaStream_t s) {
+  if (blocks == 0) return cudaSuccess;
+  switch (codec) {
+    case kQ4_0: return launch_repack_c<kQ4_0>(w, blocks, out, s);
+    case kQ8_0: return launch_repack_c<kQ8_0>(w, blocks, out, s);
+    case kQ2_0: return launch_repack_c<kQ2_0>(w, blocks, out, s);
+    default: return launch_repack_c<kMLX4>(w, blocks, out, s);
+  }
+}
+
 // ---------------------------------------------------------------- finite check
 
 __global__ void __launch_bounds__(256)

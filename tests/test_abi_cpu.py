@@ -96,6 +96,13 @@ def test_argument_errors_return_before_any_cuda_call(lib):
     assert lib.m4q_mlx4_pack(P(good), P(good + 1), P(good), 8, 32, P(good), s) == m.ERR_MISALIGNED
     assert lib.m4q_mlx4_pack(P(good), P(good), P(good + 3), 8, 32, P(good), s) == m.ERR_MISALIGNED
     assert lib.m4q_mlx4_pack(P(good), P(good), P(good), 8, 32, P(good + 4), s) == m.ERR_MISALIGNED
+    assert lib.m4q_repack(None, 0, 8, 32, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_repack(P(good), 0, 8, 32, None, s) == m.ERR_INVALID_ARG
+    assert lib.m4q_repack(P(good), 4, 8, 32, P(good), s) == m.ERR_UNSUPPORTED_CODEC
+    assert lib.m4q_repack(P(good), 0, 0, 32, P(good), s) == m.ERR_INVALID_ARG
+    assert lib.m4q_repack(P(good), 2, 8, 64, P(good), s) == m.ERR_BAD_SHAPE   # Q2_0 K % 128
+    assert lib.m4q_repack(P(good + 2), 0, 8, 32, P(good), s) == m.ERR_MISALIGNED
+    assert lib.m4q_repack(P(good), 3, 8, 32, P(good + 8), s) == m.ERR_MISALIGNED
     assert lib.m4q_check_finite(None, 10, s) == m.ERR_INVALID_ARG
     att = lambda q, k, v, codec, H, Hkv, M, T, D, off, sc, o, ws=None, wsb=0: lib.m4q_attention(
         q, k, v, codec, H, Hkv, M, T, D, off, 1, sc, o, ws, wsb, s)
