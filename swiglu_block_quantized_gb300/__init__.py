@@ -18,7 +18,12 @@ Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     attention(q, k, v, kv_codec, hkv, t, q_offset=None, causal=True, scale=None, out=None)
     weight_bytes(codec, n, k), check_finite(t), check_device_status(),
     selftest_wait_timeout(limit_ns), status_string(code), version()
-and ``QuantLinear`` is the layer wrapper (leading batch dimensions are
+Activations are read as M whole rows (their element count must be a multiple
+of the row length) and a caller's ``out`` must hold exactly the result's
+element count; both are checked before anything is launched.  M = 0 (an
+empty batch) returns an empty result without a launch.
+
+``QuantLinear`` is the layer wrapper (leading batch dimensions are
 flattened into M; M <= 16 streams the weights, larger M uses tcgen05), the
 analogue of the pages' M4QuantizedLinear ("Releases" v0.3.0); ``QuantGLU``
 wraps the gated gate/up projection (SwiGLU or GeGLU), ``QuantMLP`` the
@@ -149,6 +154,33 @@ def _require(t, dtype, what):
         raise ValueError("%s must be contiguous" % what)
 
 
+def _rows(x, k: int, what: str = "x") -> int:
+    """Rows M of an activation tensor read as [M, k]; its element count must
+    be a whole number of rows (M = 0 is allowed: an empty batch)."""
+    if k < 1 or x.numel() % k != 0:
+        raise ValueError("%s holds %d elements, not a whole number of rows of %d"
+                         % (what, x.numel(), k))
+    return x.numel() // k
+
+
+def _result(out, shape, device, what="out"):
+    """The caller's output tensor, checked to hold exactly prod(shape) fp16
+    values, or a new one of that shape.  A kernel writes every element of the
+    result, so a smaller buffer would be overrun and a larger one only partly
+    written: both are rejected before anything is launched."""
+    import torch
+    need = 1
+    for s in shape:
+        need *= int(s)
+    if out is None:
+        return torch.empty(tuple(int(s) for s in shape), dtype=torch.float16, device=device)
+    _require(out, torch.float16, what)
+    if out.numel() != need:
+        raise ValueError("%s holds %d elements, expected %d for shape %s"
+                         % (what, out.numel(), need, tuple(int(s) for s in shape)))
+    return out
+
+
 def _packed_check(w, codec, n, k, what):
     import torch
     _require(w, torch.uint8, what)
@@ -159,14 +191,15 @@ def _packed_check(w, codec, n, k, what):
 
 
 def gemm(x, w, codec: int, n: int, k: int, out=None, path: int = PATH_AUTO, stream=None):
-    """Y[M, n] = X[M, k] . W^T with W packed [n, k] (uint8 blocks)."""
+    """Y[M, n] = X[M, k] . W^T with W packed [n, k] (uint8 blocks).  X holds
+    M whole rows of k values; out, if given, exactly M * n values."""
     import torch
     _require(x, torch.float16, "x")
     _packed_check(w, codec, n, k, "w")
-    m = x.numel() // k
-    if out is None:
-        out = torch.empty((m, n), dtype=torch.float16, device=x.device)
-    _require(out, torch.float16, "out")
+    m = _rows(x, k)
+    out = _result(out, (m, n), x.device)
+    if m == 0:
+        return out
     _check(load().m4q_gemm_ex(x.data_ptr(), w.data_ptr(), codec, m, n, k, out.data_ptr(),
                               path, _stream_ptr(stream)), "m4q_gemm")
     return out
@@ -177,10 +210,12 @@ def gemm_heads(x, w, codec: int, n: int, k: int, head_dim: int, out=None, stream
     import torch
     _require(x, torch.float16, "x")
     _packed_check(w, codec, n, k, "w")
-    m = x.numel() // k
-    if out is None:
-        out = torch.empty((n // head_dim, m, head_dim), dtype=torch.float16, device=x.device)
-    _require(out, torch.float16, "out")
+    if head_dim < 1 or n % head_dim != 0:
+        raise ValueError("head_dim %d must divide n = %d" % (head_dim, n))
+    m = _rows(x, k)
+    out = _result(out, (n // head_dim, m, head_dim), x.device)
+    if m == 0:
+        return out
     _check(load().m4q_gemm_heads(x.data_ptr(), w.data_ptr(), codec, m, n, k, head_dim, out.data_ptr(),
                                  _stream_ptr(stream)), "m4q_gemm_heads")
     return out
@@ -192,10 +227,10 @@ def glu(x, wg, wu, codec: int, n: int, k: int, act: int, out=None, path: int = P
     _require(x, torch.float16, "x")
     _packed_check(wg, codec, n, k, "wg")
     _packed_check(wu, codec, n, k, "wu")
-    m = x.numel() // k
-    if out is None:
-        out = torch.empty((m, n), dtype=torch.float16, device=x.device)
-    _require(out, torch.float16, "out")
+    m = _rows(x, k)
+    out = _result(out, (m, n), x.device)
+    if m == 0:
+        return out
     _check(load().m4q_glu_ex(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), codec, m, n, k,
                              out.data_ptr(), act, path, _stream_ptr(stream)), "m4q_glu_ex")
     return out
@@ -220,15 +255,15 @@ def mlp(x, wg, wu, wd, codec_gu: int, codec_d: int, d: int, f: int, act: int = A
     _packed_check(wg, codec_gu, f, d, "wg")
     _packed_check(wu, codec_gu, f, d, "wu")
     _packed_check(wd, codec_d, d, f, "wd")
-    m = x.numel() // d
+    m = _rows(x, d)
+    out = _result(out, (m, d), x.device)
     if h is None:
         h = torch.empty((m, f), dtype=torch.float16, device=x.device)
-    if out is None:
-        out = torch.empty((m, d), dtype=torch.float16, device=x.device)
     _require(h, torch.float16, "h")
-    _require(out, torch.float16, "out")
     if h.numel() < m * f:
         raise ValueError("h holds %d elements, needs %d" % (h.numel(), m * f))
+    if m == 0:
+        return out
     _check(load().m4q_mlp(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), wd.data_ptr(), codec_gu, codec_d,
                           m, d, f, h.data_ptr(), out.data_ptr(), act, _stream_ptr(stream)), "m4q_mlp")
     return out
@@ -238,9 +273,7 @@ def dequant(w, codec: int, n: int, k: int, out=None, stream=None):
     """fp16 [n, k] decode of the packed weights (bit-exact test hook)."""
     import torch
     _packed_check(w, codec, n, k, "w")
-    if out is None:
-        out = torch.empty((n, k), dtype=torch.float16, device=w.device)
-    _require(out, torch.float16, "out")
+    out = _result(out, (n, k), w.device)
     _check(load().m4q_dequant(w.data_ptr(), codec, n, k, out.data_ptr(), _stream_ptr(stream)),
            "m4q_dequant")
     return out

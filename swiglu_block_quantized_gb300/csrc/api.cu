@@ -320,7 +320,7 @@ int m4q_mlx4_pack(const void* words, const void* scales, const void* biases, int
   int rc = current_device_info(&dev);
   if (rc != M4Q_OK) return rc;
   if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
-  return m4q::launch_mlx4_pack(words, scales, biases, (int)N, (int)K, W,
+  return m4q::launch_mlx4_pack(words, scales, biases, (int)N, (int)K, W, dev.sms,
                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? M4Q_OK
              : M4Q_ERR_CUDA;
@@ -337,7 +337,8 @@ int m4q_repack(const void* W, int codec, int64_t N, int64_t K, void* Wplanar, m4
   if (rc != M4Q_OK) return rc;
   if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
   const long long blocks = N * (K / kBlock[codec]);
-  return m4q::launch_repack(codec, W, blocks, Wplanar, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return m4q::launch_repack(codec, W, blocks, Wplanar, dev.sms, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? M4Q_OK
              : M4Q_ERR_CUDA;
 }

@@ -81,7 +81,7 @@ cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row
 cudaError_t launch_finite_check(const void* x, long long n, uint32_t* flag, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_mlx4_pack(const void* words, const void* scales, const void* biases, int N, int K,
-                             void* w, cudaStream_t s);
-cudaError_t launch_repack(int codec, const void* w, long long blocks, void* out, cudaStream_t s);
+                             void* w, int sms, cudaStream_t s);
+cudaError_t launch_repack(int codec, const void* w, long long blocks, void* out, int sms, cudaStream_t s);
 
 }  // namespace m4q

@@ -102,11 +102,19 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Grid of a grid-stride layout kernel: one thread per block, at most 16 CTAs
+// of 256 threads per multiprocessor (a full SM's worth of resident threads
+// is 8 such CTAs; twice that hides the tail).
+long long layout_grid(long long blocks, int sms) {
+  const long long grid = (blocks + 255) / 256;
+  const long long cap = 16ll * (sms > 0 ? sms : 1);
+  return grid < cap ? grid : cap;
+}
+
 cudaError_t launch_mlx4_pack(const void* words, const void* scales, const void* biases, int N, int K,
-                             void* w, cudaStream_t s) {
+                             void* w, int sms, cudaStream_t s) {
   const long long blocks = (long long)N * (K / 32);
-  long long grid = (blocks + 255) / 256;
-  if (grid > 152 * 16) grid = 152 * 16;
+  const long long grid = layout_grid(blocks, sms);
   mlx4_pack_kernel<<<(unsigned)grid, 256, 0, s>>>(
       static_cast<const uint4*>(words), static_cast<const unsigned short*>(scales),
       static_cast<const unsigned short*>(biases), blocks, static_cast<uint32_t*>(w));
@@ -144,25 +152,24 @@ __global__ void __launch_bounds__(256)
 }
 
 template <int C>
-cudaError_t launch_repack_c(const void* w, long long blocks, void* out, cudaStream_t s) {
+cudaError_t launch_repack_c(const void* w, long long blocks, void* out, int sms, cudaStream_t s) {
   constexpr int CB = CodecTraits<C>::BB - ((C == kMLX4) ? 4 : 2);
   auto* base = static_cast<uint8_t*>(out);
   auto* scales = reinterpret_cast<unsigned short*>(base + blocks * CB);
   auto* biases = scales + blocks;  // written for MLX4 only
-  long long grid = (blocks + 255) / 256;
-  if (grid > 152 * 16) grid = 152 * 16;
+  const long long grid = layout_grid(blocks, sms);
   repack_kernel<C><<<(unsigned)grid, 256, 0, s>>>(static_cast<const unsigned short*>(w), blocks,
                                                     reinterpret_cast<uint4*>(base), scales, biases);
   return cudaGetLastError();
 }
 
-cudaError_t launch_repack(int codec, const void* w, long long blocks, void* out, cudaStream_t s) {
+cudaError_t launch_repack(int codec, const void* w, long long blocks, void* out, int sms, cudaStream_t s) {
   if (blocks == 0) return cudaSuccess;
   switch (codec) {
-    case kQ4_0: return launch_repack_c<kQ4_0>(w, blocks, out, s);
-    case kQ8_0: return launch_repack_c<kQ8_0>(w, blocks, out, s);
-    case kQ2_0: return launch_repack_c<kQ2_0>(w, blocks, out, s);
-    default: return launch_repack_c<kMLX4>(w, blocks, out, s);
+    case kQ4_0: return launch_repack_c<kQ4_0>(w, blocks, out, sms, s);
+    case kQ8_0: return launch_repack_c<kQ8_0>(w, blocks, out, sms, s);
+    case kQ2_0: return launch_repack_c<kQ2_0>(w, blocks, out, sms, s);
+    default: return launch_repack_c<kMLX4>(w, blocks, out, sms, s);
   }
 }
 
