@@ -166,7 +166,9 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
           const uint4 v = src[i];
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
-        mbar_arrive(&sm.w_empty[sp]);
+        // Released after the sub-steps below have used the words (an
+        // arrive right after the loads could let the slot's next TMA fill
+        // overtake loads still in flight).
       } else {
         load_stage_global<C>(grow, grow_ok, p.row_bytes, pk, w);
       }
@@ -190,6 +192,9 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
         pending = sa;
         ++ks;
         ++ks_g;
+      }
+      if constexpr (WTMA) {
+        if (ok) mbar_arrive(&sm.w_empty[pk_g % SW]);
       }
     }
   }

@@ -237,7 +237,10 @@ __global__ void __launch_bounds__(512, 1)
           const uint4 v = src[i];
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
-        mbar_arrive(&w_empty[sp]);
+        // The slot is released only after the loop below has used every
+        // loaded word: an arrive issued right after the loads let the next
+        // TMA fill of the slot land before loads still in flight had read it
+        // (seen as stale weights in some rows under shared-memory load).
 #pragma unroll
         for (int j = 0; j < S::SUB; ++j) {
           if (ks >= nks) break;
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(512, 1)
           ++ks;
           ++ks_g;
         }
+        if (ok) mbar_arrive(&w_empty[sp]);
       }
     }
   } else if (warp >= 12) {
