@@ -79,33 +79,107 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Cache of encoded tensor maps.  A map is a pure function of its
+// description (element type, rank, base address, extents, pitches, box and
+// swizzle), so a map found under an equal description is the one that
+// encoding would produce, whatever happened to the memory in between; the
+// cache holds no ownership of that memory.  Eager callers repeat the same
+// few descriptions call after call (their weights and activation buffers),
+// and a lookup costs far less than cuTensorMapEncodeTiled.  Direct-mapped,
+// bounded, guarded by one mutex.
+struct MapKey {
+  uint32_t dt, rank, swz;
+  uint64_t base;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  bool operator==(const MapKey& o) const {
+    return dt == o.dt && rank == o.rank && swz == o.swz && base == o.base && dims[0] == o.dims[0] &&
+           dims[1] == o.dims[1] && dims[2] == o.dims[2] && strides[0] == o.strides[0] &&
+           strides[1] == o.strides[1] && box[0] == o.box[0] && box[1] == o.box[1] && box[2] == o.box[2];
+  }
+  uint64_t hash() const {
+    uint64_t h = 0x9E3779B97F4A7C15ull;
+    auto mix = [&h](uint64_t v) { h = (h ^ v) * 0xBF58476D1CE4E5B9ull; h ^= h >> 29; };
+    mix(dt | ((uint64_t)rank << 8) | ((uint64_t)swz << 16));
+    mix(base);
+    for (int i = 0; i < 3; ++i) mix(dims[i]);
+    for (int i = 0; i < 2; ++i) mix(strides[i]);
+    mix(box[0] | ((uint64_t)box[1] << 20) | ((uint64_t)box[2] << 40));
+    return h;
+  }
+};
+
+struct MapSlot {
+  bool used = false;
+  MapKey key;
+  CUtensorMap map;
+};
+
+constexpr int kMapSlots = 512;
+std::mutex g_map_mu;
+MapSlot g_maps[kMapSlots];
+
+bool encode_cached(CUtensorMap* map, const MapKey& k, const cuuint32_t* estr, int rank) {
+  const int slot = (int)(k.hash() % kMapSlots);
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps[slot].used && g_maps[slot].key == k) {
+      *map = g_maps[slot].map;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {k.dims[0], k.dims[1], k.dims[2]};
+  const cuuint64_t strides[2] = {k.strides[0], k.strides[1]};
+  const cuuint32_t box[3] = {k.box[0], k.box[1], k.box[2]};
+  if (fn(map, (CUtensorMapDataType)k.dt, rank, reinterpret_cast<void*>(k.base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)k.swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  g_maps[slot].used = true;
+  g_maps[slot].key = k;
+  g_maps[slot].map = *map;
+  return true;
+}
+
 // 2-D map: inner extent `inner` elements, `outer` rows, row pitch in bytes.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swz) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {pitch_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  MapKey k{};
+  k.dt = (uint32_t)dt;
+  k.rank = 2;
+  k.swz = (uint32_t)swz;
+  k.base = reinterpret_cast<uint64_t>(base);
+  k.dims[0] = inner;
+  k.dims[1] = outer;
+  k.strides[0] = pitch_bytes;
+  k.box[0] = box_inner;
+  k.box[1] = box_outer;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_cached(map, k, estr, 2);
 }
 
 // Head-major Y [N / hd][M][hd] as a 3-D tensor (d, m, head), boxes of
 // [128 / hd heads][32 m][hd] (one staged GEMM chunk of 128 outputs).
 bool encode_heads(CUtensorMap* map, const void* base, uint64_t M, uint64_t N, uint32_t hd) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {hd, M, N / hd};
-  const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)M * hd * 2};
-  const cuuint32_t box[3] = {hd, 32, 128 / hd};
+  MapKey k{};
+  k.dt = (uint32_t)CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  k.rank = 3;
+  k.swz = (uint32_t)CU_TENSOR_MAP_SWIZZLE_NONE;
+  k.base = reinterpret_cast<uint64_t>(base);
+  k.dims[0] = hd;
+  k.dims[1] = M;
+  k.dims[2] = N / hd;
+  k.strides[0] = (uint64_t)hd * 2;
+  k.strides[1] = (uint64_t)M * hd * 2;
+  k.box[0] = hd;
+  k.box[1] = 32;
+  k.box[2] = 128 / hd;
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(map, k, estr, 3);
 }
 
 // ------------------------------------------------------------ validation
