@@ -153,11 +153,14 @@ int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int c
  * device array of the library, 1 << 20 elements (2 MiB, held on every GPU
  * that loads the library until the process exits).  M * F above that returns
  * M4Q_ERR_SCRATCH_LIMIT before anything is enqueued.  The call allocates
- * nothing.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and should come before any stream capture on that
- * device.  All calls share the array: each one overwrites the part it uses
- * before reading it, but calls whose work overlaps on the GPU (no stream
- * order between them) race. */
+ * nothing.  The first call on a device checks that it is an sm_103 part
+ * (else M4Q_ERR_UNSUPPORTED_DEVICE), looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; it should
+ * come before any stream capture on that device.  cudaDeviceReset() on a
+ * device makes the kept address stale: do not call this entry point on that
+ * device afterwards.  All calls share the array: each one overwrites the part
+ * it uses before reading it, but calls whose work overlaps on the GPU (no
+ * stream order between them) race. */
 int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* Wd, int codec_gu,
                     int codec_d, int64_t M, int64_t D, int64_t F, void* Y, int act,
                     m4q_stream_t stream);

@@ -11,10 +11,13 @@
 // process exits), so the caller passes only inputs and the output.
 //
 // Set-up: the host cannot use the array's name as a device address.  The
-// first call on each device looks the address up with cudaGetSymbolAddress,
-// with that device current, and keeps it in a per-device table; later calls
+// first call on each device checks that the device is an sm_103 part, looks
+// the address up with cudaGetSymbolAddress, with that device current, and
+// keeps it in a per-device table for the life of the process; later calls
 // reuse it.  That first call should therefore be made before any stream
-// capture on that device.
+// capture on that device.  A cudaDeviceReset() destroys the array with the
+// rest of the device's context and leaves the kept address stale, so a
+// process that resets a device must not call this entry point on it again.
 //
 // Sharing: every call on a device writes the same array.  The gated
 // projection overwrites all M * F elements of H before the down projection
@@ -39,14 +42,29 @@ std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 
 // Device address of g_mlp_scratch on the current device (looked up once).
+// A device that is not sm_103 holds no image of this library's device code,
+// so it is turned away before the lookup, with the status every other entry
+// point returns for it.  A failed lookup leaves CUDA's last-error slot set;
+// it is cleared here so that a later, unrelated launch check does not report
+// it.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return M4Q_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return M4Q_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch[dev]) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return M4Q_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return M4Q_ERR_UNSUPPORTED_DEVICE;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_mlp_scratch) != cudaSuccess || !p) return M4Q_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_mlp_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return M4Q_ERR_CUDA;
+    }
     g_scratch[dev] = p;
   }
   *out = g_scratch[dev];
