@@ -139,6 +139,25 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def dist_setup(ngpus):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -193,7 +212,7 @@ def cpu_baseline(X, Wg, Wu, target_s=12.0):
         n = int(min(M_, max(2 * n, n * target_s / max(t, 1e-3))))
     flops = 2.0 * 2.0 * len(rows) * N_ * K_
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": "%d of %d activation rows of the workload (all %d outputs per row), %.1f s"
                       % (len(rows), M_, N_, t)}
 
@@ -347,8 +366,11 @@ def run_ours(args, ws, rank, local):
            "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": M_ * N_ * 2,
            "weights": "resident in HBM (model parameters)"}
 
-    mlx4 = measure_mlx4(m, X, dev, steps=max(20, min(args.steps, 200)))
-    attention = measure_attention(m, dev)
+    # The extra tables are measured after the headline; a failure in one of
+    # them is reported in its key (and on stderr) instead of losing the line.
+    mlx4 = guarded(measure_mlx4, m, X, dev, steps=max(20, min(args.steps, 200)))
+    attention = guarded(measure_attention, m, dev)
+    configs = None if args.no_configs else guarded(measure_configs, m, dev, peaks()[0], do_cpu)
 
     if rank != 0:
         return
@@ -362,11 +384,254 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs rotate through %d distinct copies (%.0f MB > L2)"
                          % (ROTATE, ROTATE * (X.nbytes + Wg.nbytes + Wu.nbytes + M_ * N_ * 2) / 1e6),
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "roofline": roofline, "m1": m1, "e2e": e2e, "mlx4": mlx4, "attention": attention,
+        "roofline": roofline, "m1": m1, "e2e": e2e, "mlx4": mlx4, "attention": attention, "configs": configs,
         "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
+
+
+def guarded(fn, *a, **kw):
+    try:
+        return fn(*a, **kw)
+    except Exception as exc:  # reported, not hidden: the key carries the error
+        import traceback
+        traceback.print_exc()
+        return {"error": "%s: %s" % (type(exc).__name__, exc)}
+
+
+# ---------------------------------------------------------------- every workload
+
+def proj_flops(kind, M, N, K):
+    return (4.0 if kind == "swiglu" else 2.0) * M * N * K
+
+
+def proj_bytes(m, kind, codec, M, N, K):
+    """Algorithmic bytes of one projection: packed weights (both for the
+    gated form), X read once, Y written once."""
+    return (2 if kind == "swiglu" else 1) * m.weight_bytes(codec, N, K) + 2 * M * K + 2 * M * N
+
+
+def roofline_of(flops, nbytes, pk):
+    """(roofline time in s, bound): the slower of the FLOPs at the dense fp16
+    tensor peak and the bytes at the HBM copy bandwidth."""
+    t_f = flops / (pk["bf16_tflops"] * 1e12)
+    t_b = nbytes / (pk["hbm_gbs"] * 1e9)
+    return (t_f, "tensor") if t_f >= t_b else (t_b, "hbm")
+
+
+class GraphTimer:
+    """Mean device time of one call: CUDA events around replays of a CUDA
+    graph that issues the calls back to back, cycling through `calls` (one
+    closure per copy of the inputs, so consecutive launches read different
+    memory).  Replays are repeated until about 3 ms of device time is timed."""
+
+    def __init__(self, stream):
+        import torch
+        self.torch, self.stream = torch, stream
+        self.e0 = torch.cuda.Event(enable_timing=True)
+        self.e1 = torch.cuda.Event(enable_timing=True)
+
+    def __call__(self, calls, min_calls=40):
+        torch = self.torch
+        for c in calls[:3]:
+            c()   # first launches outside the capture (per-kernel attributes)
+        torch.cuda.synchronize()
+        reps = len(calls) * max(1, -(-min_calls // len(calls)))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                calls[i % len(calls)]()
+        g.replay()
+        torch.cuda.synchronize()
+        self.e0.record(self.stream)
+        g.replay()
+        self.e1.record(self.stream)
+        torch.cuda.synchronize()
+        one = self.e0.elapsed_time(self.e1)
+        n = max(1, min(50, int(3.0 / max(one, 1e-3))))
+        self.e0.record(self.stream)
+        for _ in range(n):
+            g.replay()
+        self.e1.record(self.stream)
+        torch.cuda.synchronize()
+        del g
+        return self.e0.elapsed_time(self.e1) / (n * reps), reps * n
+
+
+def copies_for(set_bytes, l2_bytes, most=300):
+    """Distinct copies of a launch's inputs and outputs so that the copies
+    together exceed twice the L2: each launch then reads cold memory (the
+    tiny workload, bound by launch latency, stops at `most` copies)."""
+    return int(max(2, min(most, -(-2 * l2_bytes // max(set_bytes, 1)))))
+
+
+def oracle_rate(kind, X, W, Wu, codec, M, N, K, threads, target_s=1.5):
+    """The CPU oracle's TFLOP/s on a row sample of one projection, grown until
+    it takes about target_s seconds (or covers every row)."""
+    import numpy as np
+
+    import oracle
+    n = min(M, 4)
+    while True:
+        rows = sorted(set(np.linspace(0, M - 1, n).astype(int).tolist()))
+        t0 = time.perf_counter()
+        if kind == "swiglu":
+            oracle.swiglu(X, W, Wu, codec, M, N, K, rows=rows, nthreads=threads)
+        else:
+            oracle.gemm(X, W, codec, M, N, K, rows=rows, nthreads=threads)
+        t = time.perf_counter() - t0
+        if t >= 0.6 * target_s or len(rows) >= M:
+            break
+        n = int(min(M, max(2 * n, n * target_s / max(t, 1e-4))))
+    return {"value": proj_flops(kind, len(rows), N, K) / t / 1e12, "unit": "TFLOP/s", "threads": threads,
+            "kind": "oracle", "sample": "%d of %d activation rows, all %d outputs, %.2f s" % (len(rows), M, N, t)}
+
+
+def measure_configs(m, dev, pk, do_cpu):
+    """Every workload the pages' tables measure, one GPU: the tiny Q4_0 GEMM,
+    the 1B projections in Q4_0 and Q8_0, the Q2_0 sweep over M, and the 1B
+    layer set per projection and per layer at M in {1, 128, 512, 2048}.  Each
+    entry: time per launch, TFLOP/s, GB/s of algorithmic bytes, and the
+    fraction of its roofline (the slower of FLOPs at the dense fp16 peak and
+    bytes at HBM bandwidth, both measured).  Inputs and outputs rotate
+    through copies larger than twice the L2, so every launch reads cold
+    memory; launches are issued from CUDA graphs."""
+    import torch
+
+    import synth
+    stream = torch.cuda.current_stream()
+    timer = GraphTimer(stream)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cpu_threads = os.cpu_count() or 1
+    out = {}
+
+    def upload(a):
+        return torch.from_numpy(a).to(dev)
+
+    def entry(name, kind, codec, M, N, K, x, w, wu, flops=None, nbytes=None, calls=None, note=None):
+        nbytes = nbytes if nbytes is not None else proj_bytes(m, kind, codec, M, N, K)
+        flops = flops if flops is not None else proj_flops(kind, M, N, K)
+        if calls is None:
+            ncopy = copies_for(nbytes, l2)
+            xs = [x] + [x.clone() for _ in range(ncopy - 1)]
+            ws = [w] + [w.clone() for _ in range(ncopy - 1)]
+            wus = [wu] + [wu.clone() for _ in range(ncopy - 1)] if wu is not None else None
+            ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(ncopy)]
+            if kind == "swiglu":
+                calls = [lambda i=i: m.swiglu(xs[i], ws[i], wus[i], codec, N, K, out=ys[i]) for i in range(ncopy)]
+            else:
+                calls = [lambda i=i: m.gemm(xs[i], ws[i], codec, N, K, out=ys[i]) for i in range(ncopy)]
+        ms, launches = timer(calls)
+        t_roof, bound = roofline_of(flops, nbytes, pk)
+        e = {"M": M, "N": N, "K": K, "codec": synth.CODEC_NAMES[codec] if codec is not None else "mixed",
+             "kind": kind, "us_per_launch": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12,
+             "gbs": nbytes / (ms * 1e-3) / 1e9, "flops": flops, "bytes": nbytes, "bound": bound,
+             "roofline_us": 1e6 * t_roof, "frac": t_roof / (ms * 1e-3),
+             "timing": "CUDA graph, %d launches cycling through %d copies of inputs and outputs (%.0f MB; L2 %.0f MB)"
+                       % (launches, len(calls), len(calls) * nbytes / 1e6, l2 / 1e6)}
+        if note:
+            e["note"] = note
+        out[name] = e
+        return e
+
+    # C0: the tiny Q4_0 GEMM (a correctness case; bound by launch latency)
+    M, N, K = 64, 256, 256
+    X0 = synth.activations(M, K, seed=0)
+    W0 = synth.weights(synth.Q4_0, N, K, seed=0)
+    e = entry("c0_tiny_q4_0_m64", "gemm", synth.Q4_0, M, N, K, upload(X0), upload(W0), None)
+    e["bound"] = "launch latency (roofline %.3f us)" % e["roofline_us"]
+    if do_cpu:
+        e["cpu_baseline"] = [oracle_rate("gemm", X0, W0, None, synth.Q4_0, M, N, K, 1),
+                             oracle_rate("gemm", X0, W0, None, synth.Q4_0, M, N, K, cpu_threads)]
+
+    # C1: the 1B projection 2048 x 8192 x 2048 in Q4_0 and Q8_0
+    M, N, K = 2048, 8192, 2048
+    X1 = synth.activations(M, K, seed=1)
+    for codec in (synth.Q4_0, synth.Q8_0):
+        W1 = synth.weights(codec, N, K, seed=1)
+        e = entry("c1_1b_proj_%s_m2048" % synth.CODEC_NAMES[codec].lower(), "gemm", codec, M, N, K,
+                  upload(X1), upload(W1), None)
+        if do_cpu:
+            e["cpu_baseline"] = [oracle_rate("gemm", X1, W1, None, codec, M, N, K, 1),
+                                 oracle_rate("gemm", X1, W1, None, codec, M, N, K, cpu_threads)]
+
+    # C3: the Q2_0 ternary 4096 x 4096 over M
+    N = K = 4096
+    W3 = synth.weights(synth.Q2_0, N, K, seed=3)
+    w3 = upload(W3)
+    for M in (1, 16, 512, 2048):
+        X3 = synth.activations(M, K, seed=3)
+        e = entry("c3_q2_0_m%d" % M, "gemm", synth.Q2_0, M, N, K, upload(X3), w3, None)
+        if do_cpu and M == 2048:
+            e["cpu_baseline"] = [oracle_rate("gemm", X3, W3, None, synth.Q2_0, M, N, K, cpu_threads)]
+
+    # C4: the 1B layer set, per projection and per layer (one graph of the
+    # layer's launches: q, k, v, o, gate/up, down; and with q/k/v fused into
+    # one head-major projection)
+    layer = synth.llama1b_layer(1)
+    wts = {}
+    for i, (name, kind, codec, _, n, k) in enumerate(layer):
+        if kind == "swiglu":
+            wts[name] = (upload(synth.weights(codec, n, k, seed=40 + i, name="Wg")),
+                         upload(synth.weights(codec, n, k, seed=40 + i, name="Wu")))
+        else:
+            wts[name] = (upload(synth.weights(codec, n, k, seed=40 + i)), None)
+    wqkv = torch.cat([wts["q"][0], wts["k"][0], wts["v"][0]]).contiguous()
+    for M in (1, 128, 512, 2048):
+        xs_in = {}
+        lay_flops = lay_bytes = 0.0
+        per = {}
+        for i, (name, kind, codec, _, n, k) in enumerate(layer):
+            x = xs_in.setdefault(k, upload(synth.activations(M, k, seed=60 + k)))
+            e = entry("c4_1b_layer_m%d_%s" % (M, name), kind, codec, M, n, k, x, wts[name][0], wts[name][1])
+            per[name] = e
+            lay_flops += e["flops"]
+            lay_bytes += e["bytes"]
+        # whole layer as one chain of launches per copy of its activations
+        ncopy = copies_for(lay_bytes, l2)
+        sets = []
+        for c in range(ncopy):
+            d = {"x": xs_in[2048].clone() if c else xs_in[2048],
+                 "ao": xs_in[2048].clone(),   # stands in for the attention output (o's input)
+                 "h": torch.empty((M, 8192), dtype=torch.float16, device=dev),
+                 "q": torch.empty((M, 2048), dtype=torch.float16, device=dev),
+                 "k": torch.empty((M, 512), dtype=torch.float16, device=dev),
+                 "v": torch.empty((M, 512), dtype=torch.float16, device=dev),
+                 "qkv": torch.empty((48, M, 64), dtype=torch.float16, device=dev),
+                 "o": torch.empty((M, 2048), dtype=torch.float16, device=dev),
+                 "y": torch.empty((M, 2048), dtype=torch.float16, device=dev)}
+            if c:
+                d["w"] = {nm: (a.clone(), b.clone() if b is not None else None) for nm, (a, b) in wts.items()}
+                d["wqkv"] = wqkv.clone()
+            else:
+                d["w"], d["wqkv"] = wts, wqkv
+            sets.append(d)
+
+        def layer_call(d, fused):
+            w = d["w"]
+            if fused:
+                m.gemm_heads(d["x"], d["wqkv"], synth.Q8_0, 3072, 2048, 64, out=d["qkv"])
+            else:
+                m.gemm(d["x"], w["q"][0], synth.Q8_0, 2048, 2048, out=d["q"])
+                m.gemm(d["x"], w["k"][0], synth.Q8_0, 512, 2048, out=d["k"])
+                m.gemm(d["x"], w["v"][0], synth.Q8_0, 512, 2048, out=d["v"])
+            m.gemm(d["ao"], w["o"][0], synth.Q8_0, 2048, 2048, out=d["o"])
+            m.swiglu(d["x"], w["gate_up"][0], w["gate_up"][1], synth.Q4_0, 8192, 2048, out=d["h"])
+            m.gemm(d["h"], w["down"][0], synth.Q4_0, 2048, 8192, out=d["y"])
+
+        for fused in (False, True):
+            calls = [lambda d=d, f=fused: layer_call(d, f) for d in sets]
+            name = "c4_1b_layer_m%d_%s" % (M, "layer_fused_qkv" if fused else "layer")
+            e = entry(name, "layer", None, M, 2048, 2048, None, None, None, flops=lay_flops, nbytes=lay_bytes,
+                      calls=calls, note="%s, one graph of %d launches per layer"
+                      % ("q/k/v as one head-major projection" if fused else "q, k, v, o, gate/up, down",
+                         4 if fused else 6))
+            e["sum_of_projections_us"] = sum(v["us_per_launch"] for v in per.values())
+        del sets
+        torch.cuda.empty_cache()
+    assert m.check_device_status() == m.OK
+    return out
 
 
 def measure_mlx4(m, X, dev, steps):
@@ -507,6 +772,22 @@ def run_profile_case(case, local):
         assert m.check_device_status() == m.OK
         print("profile case %s: 3 launches done" % case)
         return
+    if case.startswith("gemm_"):
+        # gemm_<codec>_<n>x<k>_m<M>: one projection of the workload table
+        import synth
+        _, cname, shape, mtag = case.split("_")
+        codec = {"q4": synth.Q4_0, "q8": synth.Q8_0, "q2": synth.Q2_0}[cname]
+        N, K = (int(v) for v in shape.split("x"))
+        M = int(mtag[1:])
+        x = torch.from_numpy(synth.activations(M, K, seed=1)).cuda()
+        w = torch.from_numpy(synth.weights(codec, N, K, seed=1)).cuda()
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        for _ in range(3):
+            m.gemm(x, w, codec, N, K, out=y)
+        torch.cuda.synchronize()
+        assert m.check_device_status() == m.OK
+        print("profile case %s: 3 launches done" % case)
+        return
     X, Wg, Wu = make_inputs()
     codec = m.Q4_0
     if "mlx4" in case:
@@ -536,9 +817,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (every BASELINE workload, timed after the headline)")
     ap.add_argument("--profile-case", default=None,
                     choices=["swiglu_m2048", "swiglu_m1", "swiglu_m64", "swiglu_mlx4_m2048", "swiglu_mlx4_m1",
-                             "attn_prefill_q8_0", "attn_decode_q8_0", "attn_prefill_f16", "attn_decode_f16"],
+                             "attn_prefill_q8_0", "attn_decode_q8_0", "attn_prefill_f16", "attn_decode_f16",
+                             "gemm_q4_8192x2048_m2048", "gemm_q8_8192x2048_m2048", "gemm_q2_4096x4096_m1",
+                             "gemm_q2_4096x4096_m16", "gemm_q2_4096x4096_m2048"],
                     help="only run 3 launches of one case (for ncu)")
     args = ap.parse_args(argv)
     if args.profile_case:
