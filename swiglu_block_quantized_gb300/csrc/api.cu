@@ -255,8 +255,19 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     // 128-row X stages and 128-output Y tile do not fit shared memory.)
     L.small = L.wtma && head_dim == 0 && M <= 128 && !(kStageBytes[codec] > 160 && !swiglu && M > 64);
     int nx = 64;
+    L.split = 1;
     if (L.small) {
       nx = M <= 32 ? 32 : (M <= 64 ? 64 : 128);   // X rows per stage of the small-M kernel
+      // Few output tiles leave most SMs idle: split K over a cluster of up
+      // to 8 CTAs per tile, each CTA taking a whole number of packed
+      // stages, as long as every cluster of the grid can be resident at
+      // once (clusters must fit inside one GPC, so fewer clusters of 8 than
+      // SMs / 8 fit the GPU).
+      L.tiles = (N + out_rows - 1) / out_rows;
+      const int64_t npk = K / (8 * kBlock[codec]);
+      L.split = 8;
+      while (L.split > 1 && (npk % L.split != 0 || L.tiles * L.split > dev.sms)) L.split /= 2;
+      L.split_probe = true;   // the launcher lowers it to what the occupancy query allows
     } else if (!L.wtma) {
       nx = 128;
     } else if (((M + 255) / 256) * ntiles >= dev.sms) {

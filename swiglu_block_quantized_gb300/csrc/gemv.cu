@@ -22,8 +22,7 @@ cudaError_t launch_gemv_one(const ProjLaunch& L, const GemvParams& p) {
     configured.fetch_or(bit);
   }
   const unsigned grid = (unsigned)(p.units < L.sms ? p.units : L.sms);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(p);
-  return cudaGetLastError();
+  return launch_proj(kern, grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream, 1u, p);
 }
 
 template <int C, bool SWIGLU, bool WTMA>

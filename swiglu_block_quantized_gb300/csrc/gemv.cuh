@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
   }
   __syncthreads();
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+  pdl_launch_dependents();
+  pdl_wait();   // every global access below comes after the previous kernel
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

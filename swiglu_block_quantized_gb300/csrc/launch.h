@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <atomic>
 #include <utility>
@@ -31,6 +32,9 @@ struct ProjLaunch {
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
   bool small;             // M <= 128 kernel (activations as the A operand, tc_small.cuh)
+  int split;              // small-M kernel: CTAs of a cluster splitting K for one tile (1, 2, 4, 8)
+  bool split_probe;       // lower `split` until all clusters of the grid can be co-resident
+  long long tiles;        // small-M kernel: output tiles
   int sms;                // multiprocessors (persistent grid size, both paths)
   CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path
@@ -47,6 +51,47 @@ std::atomic<unsigned long long>& attr_flag() {
   return f;
 }
 }  // namespace
+
+// Programmatic dependent launch of the projection kernels (on unless the
+// environment sets M4Q_PDL=0): a kernel may be scheduled while the previous
+// kernel of the stream finishes; it waits for that kernel (griddepcontrol)
+// before its first global access.
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("M4Q_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+// Launch `kern` with the projection kernels' attributes: programmatic
+// dependent launch, and a cluster of `cluster` CTAs along x when > 1.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_proj(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                        unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_tc_q4_0(const ProjLaunch& L);
 cudaError_t launch_tc_q8_0(const ProjLaunch& L);

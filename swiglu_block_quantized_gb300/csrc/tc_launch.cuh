@@ -28,17 +28,20 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   TcParams p;
   p.w0 = static_cast<const uint8_t*>(L.w0);
   p.w1 = static_cast<const uint8_t*>(L.w1);
+  p.y = static_cast<__half*>(L.y);
   p.M = L.M;
   p.N = L.N;
   p.K = L.K;
   p.row_bytes = L.row_bytes;
+  p.split = 1;
+  p.ks_per = (L.K + 63) / 64;
   p.m_tiles = (L.M + NX - 1) / NX;
   p.tiles = p.m_tiles * ((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows);
   p.status = L.status;
   p.limit_ns = L.limit_ns;
   const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
-  return cudaGetLastError();
+  return launch_proj(kern, grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream, 1u, L.tm_x, L.tm_w0, L.tm_w1, L.tm_y,
+                     p);
 }
 
 template <int C, bool SWIGLU, bool WTMA, int ACT, int HD>
@@ -89,6 +92,7 @@ cudaError_t launch_tcs_one(const ProjLaunch& L) {
   TcParams p;
   p.w0 = static_cast<const uint8_t*>(L.w0);
   p.w1 = static_cast<const uint8_t*>(L.w1);
+  p.y = static_cast<__half*>(L.y);
   p.M = L.M;
   p.N = L.N;
   p.K = L.K;
@@ -97,9 +101,45 @@ cudaError_t launch_tcs_one(const ProjLaunch& L) {
   p.tiles = (L.N + Cfg::kOutRows - 1) / Cfg::kOutRows;
   p.status = L.status;
   p.limit_ns = L.limit_ns;
-  const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream>>>(L.tm_x, L.tm_w0, L.tm_w1, L.tm_y, p);
-  return cudaGetLastError();
+  const int npk = (L.K + Cfg::S::KP - 1) / Cfg::S::KP;
+  p.split = L.split > 1 ? L.split : 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // Largest split (a divisor of the packed stages, chosen by the host) whose
+  // clusters all fit on the GPU at once; the answer is kept per kernel,
+  // device and cluster size.
+  while (p.split > 1 && L.split_probe) {
+    static std::atomic<int> fit[64][4];   // per device ordinal, per log2 split: 0 unknown, 1 + max clusters
+    const int lg = p.split == 2 ? 1 : (p.split == 4 ? 2 : 3);
+    int known = fit[dev & 63][lg].load();
+    if (known == 0) {
+      cfg.gridDim = dim3((unsigned)(p.tiles * p.split), 1, 1);
+      attr[0].val.clusterDim.x = (unsigned)p.split;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      known = 1 + n;
+      fit[dev & 63][lg].store(known);
+    }
+    if ((long long)(known - 1) >= p.tiles) break;
+    p.split /= 2;
+  }
+  p.ks_per = (npk / p.split) * Cfg::S::SUB;   // the host picks splits that divide npk
+  // Persistent CTAs, or (K split) one cluster of p.split CTAs per output tile.
+  const unsigned grid = p.split == 1 ? (unsigned)(p.tiles < L.sms ? p.tiles : L.sms)
+                                     : (unsigned)(p.tiles * p.split);
+  return launch_proj(kern, grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream, (unsigned)p.split, L.tm_x, L.tm_w0,
+                     L.tm_w1, L.tm_y, p);
   }
 }
 

@@ -45,9 +45,12 @@ namespace m4q {
 struct TcParams {
   const uint8_t* w0;   // weights (gate rows for SwiGLU); read directly when !WTMA
   const uint8_t* w1;   // up weights for SwiGLU, else null
+  __half* y;           // output (K-split epilogue of the small-M kernel writes it directly)
   int M, N, K;
   long long row_bytes; // packed bytes per weight row
   int m_tiles, tiles;  // activation tiles, total output tiles
+  int split;           // CTAs of a cluster sharing one tile along K (1: no split)
+  int ks_per;          // 64-weight sub-steps per CTA of a split (a whole number of packed stages)
   uint32_t* status;    // device status word
   unsigned long long limit_ns;
 };
@@ -410,6 +413,8 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+  pdl_launch_dependents();
+  pdl_wait();   // every global access below comes after the previous kernel
 
   if (warp == 0) {
     // ------------------------------------------------------------ X producer

@@ -74,6 +74,10 @@ struct TsCfg {
   static constexpr int kSmemBytes =
       1024 + kSX * kXStage + kXPad + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
   static constexpr uint32_t kTmemCols = 256;                 // two D buffers
+  // K split: each CTA stages its fp32 partial D [128 m][128 cols] over the
+  // idle X and B rings; a pitch of 132 floats spreads 8 rows over all banks.
+  static constexpr int kDPitch = 132;
+  static_assert(128 * kDPitch * 4 <= kSX * kXStage + kXPad + kSB * kBStage, "D staging fits the rings");
   // Q8_0 / Q2_0 GEMM with 128-row X stages does not fit; the host sends
   // that case to tc_proj (M > 64 with 272-byte packed stages).
   static constexpr bool kFits = kSmemBytes <= 227 * 1024;
@@ -112,7 +116,15 @@ __global__ void __launch_bounds__(512, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nks = (p.K + 63) / 64;
-  const int npk = (p.K + S::KP - 1) / S::KP;
+  // K split (p.split > 1): the CTAs of a cluster share one output tile, CTA
+  // `rank` taking sub-steps [ks0, ks1) (whole packed stages [pk0, pk1)).
+  const int nsplit = p.split;
+  const int rank = nsplit > 1 ? (int)cluster_ctarank() : 0;
+  const int ks0 = rank * p.ks_per;
+  const int ks1 = min(nks, ks0 + p.ks_per);
+  const int pk0 = ks0 / S::SUB, pk1 = (ks1 + S::SUB - 1) / S::SUB;
+  const int tile0 = blockIdx.x / nsplit, tstep = gridDim.x / nsplit;
+  bool split_ok = false;   // epilogue threads: this CTA's partial D is staged
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SX; ++i) mbar_init(&x_full[i], 1);
@@ -133,6 +145,8 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.limit_ns};
+  pdl_launch_dependents();
+  pdl_wait();   // every global access below comes after the previous kernel
 
   if (warp == 0) {
     // ------------------------------------------------------------ X producer
@@ -140,8 +154,8 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tm_x);
       int xi = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-        for (int ks = 0; ks < nks; ++ks) {
+      for (int tile = tile0; tile < p.tiles && ok; tile += tstep) {
+        for (int ks = ks0; ks < ks1; ++ks) {
           const int sx = xi % SX;
           if (xi >= SX && !mbar_wait_idle(&pair_free[sx >> 1], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
@@ -161,9 +175,9 @@ __global__ void __launch_bounds__(512, 1)
       if (SWIGLU) tma_prefetch_desc(&tm_w1);
       int wi = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < p.tiles && ok; tile += tstep) {
         const int n0 = tile * Cfg::kOutRows;
-        for (int pk = 0; pk < npk; ++pk) {
+        for (int pk = pk0; pk < pk1; ++pk) {
           const int sp = wi % SW;
           if (wi >= SW && !mbar_wait_idle(&w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
@@ -185,13 +199,14 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t idesc = idesc_f16_f32(128, 128);
       int ks_g = 0, lt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++lt) {
+      for (int tile = tile0; tile < p.tiles && ok; tile += tstep, ++lt) {
         const int db = lt & 1;
         // D buffer db must have been read out by the epilogue two tiles ago.
         if (lt >= 2 && !mbar_wait(&d_empty[db], ((lt >> 1) - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        // nks is even here (K is a multiple of 128 on this path)
-        for (int ks = 0; ks < nks; ks += 2, ks_g += 2) {
+        // ks1 - ks0 is even here (K is a multiple of 128 on this path and a
+        // split takes whole packed stages)
+        for (int ks = ks0; ks < ks1; ks += 2, ks_g += 2) {
           const int s0 = ks_g % SX;   // slots s0, s0 + 1 of both rings (SX == SB)
           if (!mbar_wait(&b_full[s0], (ks_g / SB) & 1, ctl) || !mbar_wait(&x_full[s0], (ks_g / SX) & 1, ctl) ||
               !mbar_wait(&b_full[s0 + 1], (ks_g / SB) & 1, ctl) ||
@@ -206,7 +221,7 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(bs + (s0 + h) * Cfg::kBStage));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_ss_f16(tmem + 128 * db, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | h | kk) != 0);
+              tc_mma_ss_f16(tmem + 128 * db, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks != ks0) | h | kk);
           }
           tc_commit(&pair_free[s0 >> 1]);
         }
@@ -224,9 +239,9 @@ __global__ void __launch_bounds__(512, 1)
     const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
     bool ok = true;
     int ks_g = 0, pk_g = 0;
-    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      int ks = 0;
-      for (int pk = 0; pk < npk && ok; ++pk, ++pk_g) {
+    for (int tile = tile0; tile < p.tiles && ok; tile += tstep) {
+      int ks = ks0;
+      for (int pk = pk0; pk < pk1 && ok; ++pk, ++pk_g) {
         uint32_t w[S::WORDS];
         const int sp = pk_g % SW;
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk_g / SW) & 1, ctl));
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(512, 1)
         // (seen as stale weights in some rows under shared-memory load).
 #pragma unroll
         for (int j = 0; j < S::SUB; ++j) {
-          if (ks >= nks) break;
+          if (ks >= ks1) break;
           const int sb = ks_g % SB;
           if (ks_g >= SB) {
             ok = __all_sync(0xffffffffu, mbar_wait(&pair_free[sb >> 1], ((ks_g / SB) - 1) & 1, ctl));
@@ -268,6 +283,29 @@ __global__ void __launch_bounds__(512, 1)
         if (ok) mbar_arrive(&w_empty[sp]);
       }
     }
+  } else if (warp >= 12 && nsplit > 1) {
+    // ------------------------------------------------ epilogue, K split
+    // One tile per cluster.  Stage this CTA's partial D (thread m = row m)
+    // in its own shared memory; the cluster then reduces it below.
+    const int m = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const bool dok = !*ctl.abort && mbar_wait_idle(&d_full[0], 0, ctl, 128);
+    split_ok = !named_bar_any(1, 128, !dok || *ctl.abort);
+    if (split_ok) {
+      tc_fence_after();
+      float* row = reinterpret_cast<float*>(xs) + m * Cfg::kDPitch;  // X and B rings are idle
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_base + 32 * ch, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(row + 32 * ch)[i] =
+              make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                          __uint_as_float(v[4 * i + 3]));
+      }
+      tc_fence_before();
+    }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -275,7 +313,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const bool leader = threadIdx.x == 384;
     int lt = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++lt) {
+    for (int tile = tile0; tile < p.tiles; tile += tstep, ++lt) {
       const int db = lt & 1;
       const int n0 = tile * Cfg::kOutRows;
       bool dok = false;
@@ -335,6 +373,66 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     if (leader) bulk_wait_all();
+  }
+
+  if (nsplit > 1) {
+    // Every thread of the cluster: all partials are staged.
+    cluster_sync_all();
+    if (warp >= 12 && split_ok) {
+      // CTA `rank` owns columns [rank W, rank W + W) of the tile and adds
+      // them up over the cluster's CTAs in rank order (a fixed order, so the
+      // result does not depend on timing), then writes its outputs.
+      const int m = 32 * (warp & 3) + lane;
+      const int W = 128 / nsplit;
+      const int n_base = tile0 * Cfg::kOutRows + (SWIGLU ? rank * (W / 2) : rank * W);
+      const uint32_t my = smem_u32(reinterpret_cast<float*>(xs) + m * Cfg::kDPitch + rank * W);
+      for (int cc = 0; cc < W; cc += 16) {
+        float a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = 0.f;
+        for (int src = 0; src < nsplit; ++src) {
+          const uint32_t ra = mapa_shared(my + 4 * cc, (uint32_t)src);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 f = ld_dsmem_f4(ra + 16 * i);
+            a[4 * i] += f.x; a[4 * i + 1] += f.y; a[4 * i + 2] += f.z; a[4 * i + 3] += f.w;
+          }
+        }
+        if (m < p.M) {
+          if constexpr (SWIGLU) {
+            // columns 2i, 2i + 1: gate and up of output n_base + cc/2 + i
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              float y[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const float g = a[2 * (i + k)], u = a[2 * (i + k) + 1];
+                y[k] = (ACT ? gelu_f(g) : __fdividef(g, 1.0f + __expf(-g))) * u;
+              }
+              const __half2 hy = __floats2half2_rn(y[0], y[1]);
+              h[i / 2] = *reinterpret_cast<const uint32_t*>(&hy);
+            }
+            const int n = n_base + cc / 2;   // 8 outputs; N % 8 == 0: all inside or all outside
+            if (n < p.N) *reinterpret_cast<uint4*>(p.y + (size_t)m * p.N + n) = make_uint4(h[0], h[1], h[2], h[3]);
+          } else {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t h[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __half2 hy = __floats2half2_rn(a[8 * half + 2 * i], a[8 * half + 2 * i + 1]);
+                h[i] = *reinterpret_cast<const uint32_t*>(&hy);
+              }
+              const int n = n_base + cc + 8 * half;
+              if (n < p.N) *reinterpret_cast<uint4*>(p.y + (size_t)m * p.N + n) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          }
+        }
+      }
+    }
+    // No CTA leaves while a peer may still read its staged partial.
+    cluster_sync_all();
   }
 
   tc_fence_before();

@@ -180,6 +180,37 @@ def test_tc_small_m_one_hot_readout_bit_exact(codec):
     assert np.array_equal(Y, oracle.dequant_f16(W, codec, N, K)[:, cols].T)
 
 
+@pytest.mark.parametrize("codec", CODECS)
+def test_tc_small_m_k_split_one_hot_readout_bit_exact(codec):
+    # Few output tiles and a long K: the small-M kernel splits K over a
+    # cluster of CTAs and adds their partial tiles.  With one-hot X rows each
+    # output is one exact product, held by exactly one CTA of the split, so
+    # the sum is still exact: Y must be columns of the fp16 weights.
+    K = 8 * 8 * synth.BLOCK[codec]           # eight packed stages: a split of 8
+    M, N = 40, 136
+    cols = np.random.default_rng(codec + 7).permutation(K)[:M]
+    X = np.zeros((M, K), dtype=np.float16)
+    X[np.arange(M), cols] = 1
+    W = synth.weights(codec, N, K, seed=63)
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_TC)).view(np.uint16)
+    assert np.array_equal(Y, oracle.dequant_f16(W, codec, N, K)[:, cols].T)
+
+
+@pytest.mark.parametrize("N", [136, 9728])
+def test_tc_small_m_with_and_without_k_split(N):
+    # N = 136: 3 gated / 2 plain tiles, K split 8 ways over clusters.
+    # N = 9728: 152 gated tiles, a full wave with no split, and 76 plain
+    # tiles, split 2 ways.  All match the oracle.
+    M, K = 40, 2048
+    X = synth.activations(M, K, seed=64)
+    Wg = synth.weights(synth.Q4_0, N, K, seed=65, name="Wg")
+    Wu = synth.weights(synth.Q4_0, N, K, seed=65, name="Wu")
+    Y = host(m.swiglu(dev(X), dev(Wg), dev(Wu), synth.Q4_0, N, K))
+    assert_close(Y, oracle.swiglu(X, Wg, Wu, synth.Q4_0, M, N, K), "small-M swiglu N=%d" % N)
+    Yl = host(m.gemm(dev(X), dev(Wg), synth.Q4_0, N, K))
+    assert_close(Yl, oracle.gemm(X, Wg, synth.Q4_0, M, N, K), "small-M gemm N=%d" % N)
+
+
 def test_tc_tile_widths():
     # M large enough for 256- and 128-wide activation tiles on a full GPU.
     import torch
