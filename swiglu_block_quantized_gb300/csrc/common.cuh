@@ -18,6 +18,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// First byte of `base` (dynamic shared memory) aligned to `A` bytes.  The
+// pointer is advanced, not rebuilt from an integer, so the compiler still
+// knows it addresses shared memory and emits shared-memory loads and stores
+// for everything derived from it (a pointer rebuilt from an integer is
+// generic: every access then goes through a 64-bit generic address).
+template <uint32_t A>
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* base) {
+  return base + ((A - (smem_u32(base) & (A - 1))) & (A - 1));
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -229,8 +229,7 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
   const int stage_bytes = 8 * p.pp;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
+  uint8_t* ring = smem_align<128>(smem_raw);
   float* red = reinterpret_cast<float*>(ring + Cfg::kRingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
   uint64_t* empty = full + Cfg::kRingMax;

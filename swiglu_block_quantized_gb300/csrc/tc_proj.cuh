@@ -371,8 +371,7 @@ __global__ void __launch_bounds__(640, 1)
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SA = Cfg::kSA;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* base = smem_align<1024>(smem_raw);
   TcSmem sm;
   sm.xs = base;
   sm.ys = sm.xs + SX * Cfg::kXStage;

@@ -98,8 +98,7 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int SX = Cfg::kSX, SW = Cfg::kSW, SB = Cfg::kSB;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* xs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* xs = smem_align<1024>(smem_raw);
   uint8_t* bs = xs + SX * Cfg::kXStage + Cfg::kXPad;
   uint8_t* ys = bs + SB * Cfg::kBStage;
   uint8_t* ws = ys + Cfg::kYBytes;
