@@ -142,6 +142,7 @@ __device__ __forceinline__ void issue_tile(uint8_t* kdst, uint8_t* vdst, const u
 template <int D>
 __device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw, int valid) {
   using Cfg = AttnCfg<D, true>;
+  const DecK K = make_deck();
   constexpr int kBlk = D / 32;
   constexpr int kUnits = kKeys * kBlk / 128;
 #pragma unroll
@@ -166,7 +167,7 @@ __device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw,
       const uint32_t d2 = dup_scale(u16_at(w, 0));
       uint32_t v[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = q8_pair(spread_pair(w, 2 + 2 * q), d2);
+      for (int q = 0; q < 16; ++q) v[q] = q8_pair(spread_pair(w, 2 + 2 * q), d2, K);
 #pragma unroll
       for (int i = 0; i < 4; ++i) out[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     } else {

@@ -96,30 +96,110 @@ __device__ __forceinline__ uint32_t spread_byte(const uint32_t* w, int off) {
   return __byte_perm(w[off >> 2], 0u, 0x4040u | (b << 8) | b);
 }
 
-__device__ __forceinline__ uint32_t dup_scale(uint32_t dbits) { return dbits | (dbits << 16); }
+// The low half of `dbits` in both halves (a scale or bias for fp16x2 math).
+__device__ __forceinline__ uint32_t dup_scale(uint32_t dbits) { return __byte_perm(dbits, 0u, 0x1010u); }
 
-// Biased fp16x2 constants: 0x6400 = 1024 (step 1 at fraction bit 0),
-// 0x5C00 = 256 (step 1 at bit 2), 0x5400 = 64 (bit 4), 0x4C00 = 16 (bit 6).
-// Q4_0 low nibbles -> 1024 + q; high nibbles -> 64 + q.
-__device__ __forceinline__ void q4_pair(uint32_t t, uint32_t d2, uint32_t& lo, uint32_t& hi) {
-  lo = hmul2_rn(hsub2_rn((t & 0x000F000Fu) | 0x64006400u, 0x64086408u), d2);  // - 1032
-  hi = hmul2_rn(hsub2_rn((t & 0x00F000F0u) | 0x54005400u, 0x54805480u), d2);  // - 72
+// Biased fp16x2 constants of the decoders, held in registers.  Each code is
+// placed with one three-input logic operation, (x & mask) | bias, whose
+// mask is its immediate operand; the instruction takes one immediate only,
+// and a bias that the compiler sees as a constant makes it split the
+// operation in two, so the biases come from an opaque move, once per thread.
+// 0x6400 = 1024 (a fraction step of 1 at bit 0), 0x5C00 = 256 (step 1 at
+// bit 2), 0x5400 = 64 (bit 4), 0x4C00 = 16 (bit 6).
+struct DecK {
+  uint32_t b6464;  // (1024, 1024)
+  uint32_t b5454;  // (64, 64)
+  uint32_t b5c64;  // (1024, 256)  Q2_0 codes 0 and 1 of a byte
+  uint32_t b4c54;  // (64, 16)     Q2_0 codes 2 and 3
+  uint32_t b5464;  // (1024, 64)   MLX4 low and high nibble of a byte
+  uint32_t bff00;  // 0xFF00FF00: Q8_0 bytes of a whole word (see q8_word)
+};
+
+__device__ __forceinline__ DecK make_deck() {
+  DecK k;
+  asm volatile("mov.b32 %0, 0x64006400;" : "=r"(k.b6464));
+  asm volatile("mov.b32 %0, 0x54005400;" : "=r"(k.b5454));
+  asm volatile("mov.b32 %0, 0x5C006400;" : "=r"(k.b5c64));
+  asm volatile("mov.b32 %0, 0x4C005400;" : "=r"(k.b4c54));
+  asm volatile("mov.b32 %0, 0x54006400;" : "=r"(k.b5464));
+  asm volatile("mov.b32 %0, 0xFF00FF00;" : "=r"(k.bff00));
+  return k;
 }
-// Q8_0 signed byte: (q ^ 0x80) = q + 128 -> 1024 + 128 + q.
-__device__ __forceinline__ uint32_t q8_pair(uint32_t t, uint32_t d2) {
-  return hmul2_rn(hsub2_rn((t ^ 0x00800080u) | 0x64006400u, 0x64806480u), d2);  // - 1152
+
+// (a & MASK) | c in one instruction.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+// (a ^ X) | c in one instruction.
+template <uint32_t X>
+__device__ __forceinline__ uint32_t xor_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xBE;" : "=r"(d) : "r"(a), "n"(X), "r"(c));
+  return d;
+}
+
+// Q4_0 bytes [b0, 0, b1, 0]: low nibbles -> 1024 + q; high nibbles -> 64 + q.
+__device__ __forceinline__ void q4_pair(uint32_t t, uint32_t d2, const DecK& K, uint32_t& lo, uint32_t& hi) {
+  lo = hmul2_rn(hsub2_rn(and_or<0x000F000Fu>(t, K.b6464), 0x64086408u), d2);  // - 1032
+  hi = hmul2_rn(hsub2_rn(and_or<0x00F000F0u>(t, K.b5454), 0x54805480u), d2);  // - 72
+}
+// Q8_0 signed bytes [b0, 0, b1, 0]: (q ^ 0x80) = q + 128 -> 1024 + 128 + q.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t t, uint32_t d2, const DecK& K) {
+  return hmul2_rn(hsub2_rn(xor_or<0x00800080u>(t, K.b6464), 0x64806480u), d2);  // - 1152
 }
 // Q2_0 byte [v,0,v,0]: codes at bits 0-1, 2-3 -> (1024 + q0, 256 + q1);
 // bits 4-5, 6-7 -> (64 + q2, 16 + q3).
-__device__ __forceinline__ void q2_byte(uint32_t t, uint32_t d2, uint32_t& p01, uint32_t& p23) {
-  p01 = hmul2_rn(hsub2_rn((t & 0x000C0003u) | 0x5C006400u, 0x5C046401u), d2);  // -(257, 1025)
-  p23 = hmul2_rn(hsub2_rn((t & 0x00C00030u) | 0x4C005400u, 0x4C405410u), d2);  // -(17, 65)
+__device__ __forceinline__ void q2_byte(uint32_t t, uint32_t d2, const DecK& K, uint32_t& p01, uint32_t& p23) {
+  p01 = hmul2_rn(hsub2_rn(and_or<0x000C0003u>(t, K.b5c64), 0x5C046401u), d2);  // -(257, 1025)
+  p23 = hmul2_rn(hsub2_rn(and_or<0x00C00030u>(t, K.b4c54), 0x4C405410u), d2);  // -(17, 65)
 }
 
 // MLX4 byte [v,0,v,0]: low nibble -> 1024 + q0, high nibble -> 64 + q1;
 // subtract the biases exactly, then one fused q * s + b per half.
-__device__ __forceinline__ uint32_t mlx_pair(uint32_t t, uint32_t s2, uint32_t b2) {
-  return hfma2_rn(hsub2_rn((t & 0x00F0000Fu) | 0x54006400u, 0x54006400u), s2, b2);
+__device__ __forceinline__ uint32_t mlx_pair(uint32_t t, uint32_t s2, uint32_t b2, const DecK& K) {
+  return hfma2_rn(hsub2_rn(and_or<0x00F0000Fu>(t, K.b5464), 0x54006400u), s2, b2);
+}
+
+// Whole-word decoders: the four bytes [b0 b1 b2 b3] of one 32-bit word of
+// codes, without a byte permute per pair.  The fp16x2 results pair the
+// weights of bytes (0, 2) and (1, 3); the caller pairs the activations the
+// same way.
+// Q4_0: l02 = low nibbles of b0, b2; h02 = high nibbles; l13, h13 for b1, b3.
+__device__ __forceinline__ void q4_word(uint32_t w, uint32_t d2, const DecK& K, uint32_t& l02, uint32_t& l13,
+                                        uint32_t& h02, uint32_t& h13) {
+  const uint32_t v = w >> 8;
+  l02 = hmul2_rn(hsub2_rn(and_or<0x000F000Fu>(w, K.b6464), 0x64086408u), d2);
+  h02 = hmul2_rn(hsub2_rn(and_or<0x00F000F0u>(w, K.b5454), 0x54805480u), d2);
+  l13 = hmul2_rn(hsub2_rn(and_or<0x000F000Fu>(v, K.b6464), 0x64086408u), d2);
+  h13 = hmul2_rn(hsub2_rn(and_or<0x00F000F0u>(v, K.b5454), 0x54805480u), d2);
+}
+// Q8_0: p02 = signed bytes b0, b2; p13 = b1, b3.  One logic operation keeps
+// the low byte of each half, flips its bit 7 and sets the exponent:
+// ((w & 0x00FF00FF) ^ 0x00800080) | 0x64006400, written as the lookup 0x36
+// over (w, 0x9B809B80, 0xFF00FF00): where the third operand is 0 the bit is
+// w's, flipped where the second is 1; elsewhere it is the complement of the
+// second operand (which holds the complement of the exponent bits).
+__device__ __forceinline__ uint32_t q8_bytes02(uint32_t w, const DecK& K) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x36;" : "=r"(d) : "r"(w), "n"(0x9B809B80u), "r"(K.bff00));
+  return d;
+}
+__device__ __forceinline__ void q8_word(uint32_t w, uint32_t d2, const DecK& K, uint32_t& p02, uint32_t& p13) {
+  p02 = hmul2_rn(hsub2_rn(q8_bytes02(w, K), 0x64806480u), d2);
+  p13 = hmul2_rn(hsub2_rn(q8_bytes02(w >> 8, K), 0x64806480u), d2);
+}
+// MLX4: byte i holds codes 2i (low nibble) and 2i + 1; lo02 = codes of the
+// low nibbles of b0, b2, hi02 their high nibbles, lo13 / hi13 for b1, b3.
+__device__ __forceinline__ void mlx_word(uint32_t w, uint32_t s2, uint32_t b2, const DecK& K, uint32_t& lo02,
+                                         uint32_t& hi02, uint32_t& lo13, uint32_t& hi13) {
+  const uint32_t v = w >> 8;
+  lo02 = hfma2_rn(hsub2_rn(and_or<0x000F000Fu>(w, K.b6464), 0x64006400u), s2, b2);
+  hi02 = hfma2_rn(hsub2_rn(and_or<0x00F000F0u>(w, K.b5454), 0x54005400u), s2, b2);
+  lo13 = hfma2_rn(hsub2_rn(and_or<0x000F000Fu>(v, K.b6464), 0x64006400u), s2, b2);
+  hi13 = hfma2_rn(hsub2_rn(and_or<0x00F000F0u>(v, K.b5454), 0x54005400u), s2, b2);
 }
 
 // MLX4 scale and bias of the block at even byte offset bo, each duplicated
@@ -133,10 +213,11 @@ __device__ __forceinline__ void mlx_scale_bias(const uint32_t* w, int bo, uint32
 // into out[i] = fp16x2 (w[64j + 2i], w[64j + 2i + 1]).  `w` holds the row's
 // packed stage bytes; j must be a compile-time constant after unrolling.
 template <int C>
-__device__ __forceinline__ void decode_sub(const uint32_t* w, int j, uint32_t (&out)[32]);
+__device__ __forceinline__ void decode_sub(const uint32_t* w, int j, uint32_t (&out)[32], const DecK& K);
 
 template <>
-__device__ __forceinline__ void decode_sub<kQ4_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+__device__ __forceinline__ void decode_sub<kQ4_0>(const uint32_t* w, int j, uint32_t (&out)[32],
+                                              const DecK& K) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int bo = (2 * j + h) * 18;
@@ -144,7 +225,7 @@ __device__ __forceinline__ void decode_sub<kQ4_0>(const uint32_t* w, int j, uint
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       uint32_t lo, hi;
-      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, lo, hi);
+      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, K, lo, hi);
       out[16 * h + p] = lo;      // weights 2p, 2p+1 of the block
       out[16 * h + 8 + p] = hi;  // weights 16+2p, 17+2p
     }
@@ -152,37 +233,40 @@ __device__ __forceinline__ void decode_sub<kQ4_0>(const uint32_t* w, int j, uint
 }
 
 template <>
-__device__ __forceinline__ void decode_sub<kQ8_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+__device__ __forceinline__ void decode_sub<kQ8_0>(const uint32_t* w, int j, uint32_t (&out)[32],
+                                              const DecK& K) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int bo = (2 * j + h) * 34;
     const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
-    for (int p = 0; p < 16; ++p) out[16 * h + p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+    for (int p = 0; p < 16; ++p) out[16 * h + p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2, K);
   }
 }
 
 template <>
-__device__ __forceinline__ void decode_sub<kMLX4>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+__device__ __forceinline__ void decode_sub<kMLX4>(const uint32_t* w, int j, uint32_t (&out)[32],
+                                              const DecK& K) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int bo = (2 * j + h) * 20;
     uint32_t s2, b2;
     mlx_scale_bias(w, bo, s2, b2);
 #pragma unroll
-    for (int p = 0; p < 16; ++p) out[16 * h + p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2);
+    for (int p = 0; p < 16; ++p) out[16 * h + p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2, K);
   }
 }
 
 template <>
-__device__ __forceinline__ void decode_sub<kQ2_0>(const uint32_t* w, int j, uint32_t (&out)[32]) {
+__device__ __forceinline__ void decode_sub<kQ2_0>(const uint32_t* w, int j, uint32_t (&out)[32],
+                                              const DecK& K) {
   const int bo = (j >> 1) * 34;
   const int cb = bo + 2 + 16 * (j & 1);  // first code byte of this half block
   const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
     uint32_t p01, p23;
-    q2_byte(spread_byte(w, cb + c), d2, p01, p23);
+    q2_byte(spread_byte(w, cb + c), d2, K, p01, p23);
     out[2 * c] = p01;
     out[2 * c + 1] = p23;
   }
@@ -192,14 +276,14 @@ __device__ __forceinline__ void decode_sub<kQ2_0>(const uint32_t* w, int j, uint
 // w[64j + 32g + 2i + 1]), i < 16.  j and g must be compile-time constants
 // after unrolling.
 template <int C, int G>
-__device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (&out)[16]) {
+__device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (&out)[16], const DecK& K) {
   if constexpr (C == kQ4_0) {
     const int bo = (2 * j + G) * 18;  // block 2j + G
     const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       uint32_t lo, hi;
-      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, lo, hi);
+      q4_pair(spread_pair(w, bo + 2 + 2 * p), d2, K, lo, hi);
       out[p] = lo;
       out[8 + p] = hi;
     }
@@ -207,13 +291,13 @@ __device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (
     const int bo = (2 * j + G) * 34;
     const uint32_t d2 = dup_scale(u16_at(w, bo));
 #pragma unroll
-    for (int p = 0; p < 16; ++p) out[p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2);
+    for (int p = 0; p < 16; ++p) out[p] = q8_pair(spread_pair(w, bo + 2 + 2 * p), d2, K);
   } else if constexpr (C == kMLX4) {
     const int bo = (2 * j + G) * 20;
     uint32_t s2, b2;
     mlx_scale_bias(w, bo, s2, b2);
 #pragma unroll
-    for (int p = 0; p < 16; ++p) out[p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2);
+    for (int p = 0; p < 16; ++p) out[p] = mlx_pair(spread_byte(w, bo + 4 + p), s2, b2, K);
   } else {
     const int bo = (j >> 1) * 34;
     const int cb = bo + 2 + 16 * (j & 1) + 8 * G;  // 8 code bytes = 32 weights
@@ -221,7 +305,7 @@ __device__ __forceinline__ void decode_half(const uint32_t* w, int j, uint32_t (
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       uint32_t p01, p23;
-      q2_byte(spread_byte(w, cb + c), d2, p01, p23);
+      q2_byte(spread_byte(w, cb + c), d2, K, p01, p23);
       out[2 * c] = p01;
       out[2 * c + 1] = p23;
     }

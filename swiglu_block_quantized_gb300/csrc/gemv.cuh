@@ -153,17 +153,17 @@ __device__ __forceinline__ void load_xfrag(const GemvParams& p, int g, int t, in
 template <int C, int MT>
 __device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1, int t,
                                            const uint32_t (&xf)[MT][XFrag<C>::kRegs],
-                                           float (&acc)[MT][4]) {
+                                           float (&acc)[MT][4], const DecK& K) {
   const uint32_t d0 = dup_scale(lds_u16(r0)), d1 = dup_scale(lds_u16(r1));
 
   if constexpr (C == kQ4_0) {
     const uint8_t* c0 = r0 + 2 + 4 * t;
     const uint8_t* c1 = r1 + 2 + 4 * t;
     uint32_t lo00, hi00, lo01, hi01, lo10, hi10, lo11, hi11;
-    q4_pair(spread16(lds_u16(c0)), d0, lo00, hi00);
-    q4_pair(spread16(lds_u16(c0 + 2)), d0, lo01, hi01);
-    q4_pair(spread16(lds_u16(c1)), d1, lo10, hi10);
-    q4_pair(spread16(lds_u16(c1 + 2)), d1, lo11, hi11);
+    q4_pair(spread16(lds_u16(c0)), d0, K, lo00, hi00);
+    q4_pair(spread16(lds_u16(c0 + 2)), d0, K, lo01, hi01);
+    q4_pair(spread16(lds_u16(c1)), d1, K, lo10, hi10);
+    q4_pair(spread16(lds_u16(c1 + 2)), d1, K, lo11, hi11);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       mma_16816(acc[mt], lo00, lo10, lo01, lo11, xf[mt][0], xf[mt][1]);
@@ -175,8 +175,8 @@ __device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1,
     uint32_t w[2][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      w[0][i] = q8_pair(spread16(lds_u16(c0 + 2 * i)), d0);
-      w[1][i] = q8_pair(spread16(lds_u16(c1 + 2 * i)), d1);
+      w[0][i] = q8_pair(spread16(lds_u16(c0 + 2 * i)), d0, K);
+      w[1][i] = q8_pair(spread16(lds_u16(c1 + 2 * i)), d1, K);
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -193,8 +193,8 @@ __device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1,
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t sel = 0x4040u | (uint32_t)(i << 8) | (uint32_t)i;  // byte i, replicated
-      w[0][i] = mlx_pair(__byte_perm(v0, 0u, sel), d0, b0);
-      w[1][i] = mlx_pair(__byte_perm(v1, 0u, sel), d1, b1);
+      w[0][i] = mlx_pair(__byte_perm(v0, 0u, sel), d0, b0, K);
+      w[1][i] = mlx_pair(__byte_perm(v1, 0u, sel), d1, b1, K);
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -211,12 +211,119 @@ __device__ __forceinline__ void gemv_block(const uint8_t* r0, const uint8_t* r1,
     for (int c = 0; c < 8; ++c) {
       const uint32_t sel = (c & 1) ? 0x4141u : 0x4040u;  // byte c of the pair, replicated
       uint32_t a0, a1, a2, a3;
-      q2_byte(__byte_perm(v0[c >> 1], 0u, sel), d0, a0, a2);
-      q2_byte(__byte_perm(v1[c >> 1], 0u, sel), d1, a1, a3);
+      q2_byte(__byte_perm(v0[c >> 1], 0u, sel), d0, K, a0, a2);
+      q2_byte(__byte_perm(v1[c >> 1], 0u, sel), d1, K, a1, a3);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) mma_16816(acc[mt], a0, a1, a2, a3, xf[mt][2 * c], xf[mt][2 * c + 1]);
     }
   }
+}
+
+// ---------------------------------------------------------------- X resident
+// When a weight row is one stage (XH), every consumer warp works on the same
+// blocks of every unit, so its activation fragments are built once per
+// launch, in whatever k order suits the decode.  The bodies below read the
+// codes as aligned 32-bit words (the 18- and 34-byte blocks are taken in
+// pairs: the odd block of a pair starts on a word, the even one on a
+// half-word) and decode whole words (codec.cuh); activation pairs follow
+// the weight pairs of q4_word / q8_word / mlx_word.
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
+
+// In-block k of the activation in half `e` of fragment register `r` of
+// thread t, for the even (odd = false) or odd block of a pair (Q4_0, Q8_0)
+// or any block (MLX4).  Q4_0 thread t reads code bytes (c0..c3): of the odd
+// block 4t..4t+3; of the even block 4t+2..4t+5, or 0, 1, 14, 15 for t = 3
+// (from the words that straddle the block's start and end).  Registers:
+// (c0, c2), (c1, c3), then the high nibbles 16 later.  Q8_0 reads two words
+// (a0..a3), (b0..b3): odd 8t.., 8t+4..; even 8t+2.., 8t+6.., or 26..29 and
+// 30, 31, 0, 1 for t = 3; registers (a0, a2), (a1, a3), (b0, b2), (b1, b3).
+// MLX4 word 4t..4t+3 holds codes 8t..8t+7; registers (8t, 8t+4),
+// (8t+1, 8t+5), (8t+2, 8t+6), (8t+3, 8t+7).
+template <int C>
+__device__ __forceinline__ int xh_k(bool odd, int t, int r, int e) {
+  if constexpr (C == kQ4_0) {
+    int c[4];
+    for (int i = 0; i < 4; ++i) c[i] = odd ? 4 * t + i : (t < 3 ? 4 * t + 2 + i : (i < 2 ? i : 12 + i));
+    const int byte = (r & 1) + 2 * e;         // r 0: (c0, c2), r 1: (c1, c3)
+    return c[byte] + (r >= 2 ? 16 : 0);
+  } else if constexpr (C == kQ8_0) {
+    int a[8];
+    for (int i = 0; i < 8; ++i) {
+      if (odd) a[i] = 8 * t + i;
+      else if (t < 3) a[i] = 8 * t + 2 + i;
+      else a[i] = (26 + i) & 31;                 // 26..31, then 0, 1
+    }
+    const int word = r >> 1, byte = (r & 1) + 2 * e;
+    return a[4 * word + byte];
+  } else {
+    return 8 * t + r + 4 * e;
+  }
+}
+
+// Q4_0 pair of blocks at shared addresses a0 (tile row g) and a1 (row g + 8).
+__device__ __forceinline__ void xh_pair_q4(uint32_t a0, uint32_t a1, uint32_t eoff, uint32_t esel, uint32_t ooff,
+                                           const DecK& K, const uint32_t (&xe)[4], const uint32_t (&xo)[4],
+                                           float (&acc)[4]) {
+  uint32_t l02[2][2], l13[2][2], h02[2][2], h13[2][2];  // [even/odd block][row]
+  const uint32_t base[2] = {a0, a1};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t w0 = lds32(base[r]), w4 = lds32(base[r] + 16);
+    const uint32_t we = lds32(base[r] + eoff), wo = lds32(base[r] + ooff);
+    q4_word(__byte_perm(we, w4, esel), __byte_perm(w0, 0u, 0x1010u), K, l02[0][r], l13[0][r], h02[0][r],
+            h13[0][r]);
+    q4_word(wo, __byte_perm(w4, 0u, 0x3232u), K, l02[1][r], l13[1][r], h02[1][r], h13[1][r]);
+  }
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t(&x)[4] = b ? xo : xe;
+    mma_16816(acc, l02[b][0], l02[b][1], l13[b][0], l13[b][1], x[0], x[1]);
+    mma_16816(acc, h02[b][0], h02[b][1], h13[b][0], h13[b][1], x[2], x[3]);
+  }
+}
+
+// Q8_0 pair of blocks (68 bytes, 17 words) at a0 / a1.
+__device__ __forceinline__ void xh_pair_q8(uint32_t a0, uint32_t a1, uint32_t eoff_a, uint32_t eoff_b,
+                                           uint32_t esel, uint32_t ooff, const DecK& K, const uint32_t (&xe)[4],
+                                           const uint32_t (&xo)[4], float (&acc)[4]) {
+  uint32_t p[2][2][4];  // [even/odd block][row][(a02, a13, b02, b13)]
+  const uint32_t base[2] = {a0, a1};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t w0 = lds32(base[r]), w8 = lds32(base[r] + 32);
+    const uint32_t ea = lds32(base[r] + eoff_a), eb = lds32(base[r] + eoff_b);
+    const uint32_t oa = lds32(base[r] + ooff), ob = lds32(base[r] + ooff + 4);
+    const uint32_t de = __byte_perm(w0, 0u, 0x1010u), dodd = __byte_perm(w8, 0u, 0x3232u);
+    q8_word(ea, de, K, p[0][r][0], p[0][r][1]);
+    q8_word(__byte_perm(eb, w0, esel), de, K, p[0][r][2], p[0][r][3]);
+    q8_word(oa, dodd, K, p[1][r][0], p[1][r][1]);
+    q8_word(ob, dodd, K, p[1][r][2], p[1][r][3]);
+  }
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t(&x)[4] = b ? xo : xe;
+    mma_16816(acc, p[b][0][0], p[b][1][0], p[b][0][1], p[b][1][1], x[0], x[1]);
+    mma_16816(acc, p[b][0][2], p[b][1][2], p[b][0][3], p[b][1][3], x[2], x[3]);
+  }
+}
+
+// MLX4 block (20 bytes: scale, bias, 16 code bytes from byte 4) at a0 / a1.
+__device__ __forceinline__ void xh_block_mlx(uint32_t a0, uint32_t a1, uint32_t coff, const DecK& K,
+                                             const uint32_t (&x)[4], float (&acc)[4]) {
+  uint32_t lo02[2], hi02[2], lo13[2], hi13[2];
+  const uint32_t base[2] = {a0, a1};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t sb = lds32(base[r]), w = lds32(base[r] + coff);
+    mlx_word(w, __byte_perm(sb, 0u, 0x1010u), __byte_perm(sb, 0u, 0x3232u), K, lo02[r], hi02[r], lo13[r],
+             hi13[r]);
+  }
+  mma_16816(acc, lo02[0], lo02[1], hi02[0], hi02[1], x[0], x[1]);
+  mma_16816(acc, lo13[0], lo13[1], hi13[0], hi13[1], x[2], x[3]);
 }
 
 template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
@@ -259,7 +366,9 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
     // ------------------------------------------------------------ producer
     // Stage order of a unit: for each row segment s, the gate tile then (for
     // SwiGLU) the up tile.
-    int q = 0;
+    int q = 0;             // stages issued
+    int pslot = 0;         // ring slot of the next stage
+    uint32_t pphase = 0;   // parity of the ring lap being filled
     bool ok = true;
     if constexpr (WTMA) {
       // Lane g < 8 copies row pair g (weight rows n0 + 2g, n0 + 2g + 1).
@@ -272,10 +381,14 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
           const long long left = p.row_bytes - off;
           const uint32_t bytes = (uint32_t)(left < p.sb ? left : p.sb);
           for (int mat = 0; mat < NM; ++mat, ++q) {
-            const int slot = q % R;
+            const int slot = pslot;
             if (q >= R) {
-              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], pphase ^ 1u, ctl));
               if (!ok) break;
+            }
+            if (++pslot == R) {
+              pslot = 0;
+              pphase ^= 1u;
             }
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * bytes * pairs);
             __syncwarp();
@@ -304,10 +417,14 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         for (int s = 0; s < p.nst && ok; ++s) {
           for (int mat = 0; mat < NM; ++mat, ++q) {
-            const int slot = q % R;
+            const int slot = pslot;
             if (q >= R) {
-              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], ((q / R) - 1) & 1, ctl));
+              ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[slot], pphase ^ 1u, ctl));
               if (!ok) break;
+            }
+            if (++pslot == R) {
+              pslot = 0;
+              pphase ^= 1u;
             }
             uint8_t* dst = ring + slot * stage_bytes;
             const uint8_t* base = mat ? p.w1 : p.w0;
@@ -334,14 +451,34 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
     const int g = lane >> 2, t = lane & 3;
     const int bps = p.sb / S::BB;  // blocks per full stage
     constexpr int XR = XFrag<C>::kRegs;
-    // XH: one full stage per row; warp cw always handles blocks cw + 16 j.
-    uint32_t xh[XH ? Cfg::kXH : 1][MT][XR];
+    const DecK K = make_deck();
+    // XH (one stage per row, MT = 1): the activation fragments of this
+    // warp's blocks for the whole launch, in the k order of the word
+    // decoders.  Q4_0 and Q8_0 warps take block pairs cw + 16 j (blocks
+    // 2 (cw + 16 j) and the next), MLX4 warps blocks cw + 16 j.
+    constexpr bool kPairs = (C == kQ4_0 || C == kQ8_0);
+    uint32_t xh[XH ? Cfg::kXH : 1][4];
     if constexpr (XH) {
+      static_assert(MT == 1 && C != kQ2_0, "resident activations: one n8 tile, 32-weight blocks");
+      const bool ok_m = g < p.M;   // activation row g is the fragment column
+      const unsigned short* xrow = reinterpret_cast<const unsigned short*>(p.x) + (size_t)(ok_m ? g : 0) * p.K;
 #pragma unroll
-      for (int j = 0; j < Cfg::kXH; ++j) load_xfrag<C, MT>(p, g, t, (cw + NC * j) * S::B, xh[j]);
+      for (int j = 0; j < Cfg::kXH; ++j) {
+        const int blk = kPairs ? 2 * (cw + NC * (j >> 1)) + (j & 1) : cw + NC * j;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t lo = ok_m ? __ldg(xrow + blk * S::B + xh_k<C>(j & 1, t, r, 0)) : 0u;
+          const uint32_t hi = ok_m ? __ldg(xrow + blk * S::B + xh_k<C>(j & 1, t, r, 1)) : 0u;
+          xh[j][r] = lo | (hi << 16);
+        }
+      }
     }
+    // Per-thread word offsets of the XH bodies (see xh_k).
+    const uint32_t q4_eoff = t < 3 ? 4u * (1 + t) : 0u, q4_esel = t < 3 ? 0x3210u : 0x5432u;
+    const uint32_t q8_eoff_b = t < 3 ? 4u * (2 + 2 * t) : 32u, q8_esel = t < 3 ? 0x3210u : 0x7610u;
     const int row_off = g * p.pp + cw * S::BB;  // this thread's row g, this warp's first block
-    int q = 0, i = 0;
+    int slot = 0, i = 0;
+    uint32_t phase = 0;   // parity of the ring lap being consumed
     for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
       float acc[NM][MT][4], acc1[NM][MT][4];
 #pragma unroll
@@ -358,50 +495,75 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
         // The NM tiles (gate, up) of this segment are adjacent ring slots:
         // wait for both, then run them block by block (independent MMA chains
         // that share the X fragments).
-        const int slot = q % R;
         for (int mat = 0; mat < NM && ok; ++mat)
-          ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot + mat], ((q + mat) / R) & 1, ctl, 64));
+          ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot + mat], phase, ctl, 64));
         if (!ok) break;
-        const uint8_t* r0 = ring + slot * stage_bytes + row_off;  // block cw, row g, tile 0
-        const uint8_t* r1 = r0 + p.sb;                            // block cw, row g + 8
-        if (XH || nb == Cfg::kBlocks) {
-          // Full stage: every block of this warp is inside K.
+        if constexpr (XH) {
+          const uint32_t rs = smem_u32(ring) + slot * stage_bytes + g * p.pp;  // tile row g of this stage
+          if constexpr (kPairs) {
 #pragma unroll
-          for (int j = 0; j < Cfg::kXH; ++j) {
-            const int bo = NC * j * S::BB;
-            uint32_t xf[MT][XR];
-            if constexpr (XH) {
+            for (int j = 0; j < Cfg::kXH / 2; ++j) {
 #pragma unroll
-              for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int r = 0; r < XR; ++r) xf[mt][r] = xh[j][mt][r];
-            } else {
-              load_xfrag<C, MT>(p, g, t, kb0 + (cw + NC * j) * S::B, xf);
+              for (int mat = 0; mat < NM; ++mat) {
+                float(&a)[4] = (NM == 1 && (j & 1)) ? acc1[mat][0] : acc[mat][0];
+                const uint32_t a0 = rs + mat * stage_bytes + (cw + NC * j) * (2 * S::BB);
+                if constexpr (C == kQ4_0)
+                  xh_pair_q4(a0, a0 + p.sb, q4_eoff, q4_esel, 20u + 4u * t, K, xh[2 * j], xh[2 * j + 1], a);
+                else
+                  xh_pair_q8(a0, a0 + p.sb, 4u * (1 + 2 * t), q8_eoff_b, q8_esel, 36u + 8u * t, K, xh[2 * j],
+                             xh[2 * j + 1], a);
+              }
             }
+          } else {
 #pragma unroll
-            for (int mat = 0; mat < NM; ++mat) {
-              const int to = mat * stage_bytes + bo;
-              if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat]);
-              else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat]);
+            for (int j = 0; j < Cfg::kXH; ++j) {
+#pragma unroll
+              for (int mat = 0; mat < NM; ++mat) {
+                float(&a)[4] = (NM == 1 && (j & 1)) ? acc1[mat][0] : acc[mat][0];
+                const uint32_t a0 = rs + mat * stage_bytes + (cw + NC * j) * S::BB;
+                xh_block_mlx(a0, a0 + p.sb, 4u + 4u * t, K, xh[j], a);
+              }
             }
           }
         } else {
-          for (int b = cw, j = 0; b < nb; b += NC, ++j) {
-            const int bo = (b - cw) * S::BB;
-            uint32_t xf[MT][XR];
-            load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
+          const uint8_t* r0 = ring + slot * stage_bytes + row_off;  // block cw, row g, tile 0
+          const uint8_t* r1 = r0 + p.sb;                            // block cw, row g + 8
+          if (nb == Cfg::kBlocks) {
+            // Full stage: every block of this warp is inside K.
 #pragma unroll
-            for (int mat = 0; mat < NM; ++mat) {
-              const int to = mat * stage_bytes + bo;
-              if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat]);
-              else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat]);
+            for (int j = 0; j < Cfg::kXH; ++j) {
+              const int bo = NC * j * S::BB;
+              uint32_t xf[MT][XR];
+              load_xfrag<C, MT>(p, g, t, kb0 + (cw + NC * j) * S::B, xf);
+#pragma unroll
+              for (int mat = 0; mat < NM; ++mat) {
+                const int to = mat * stage_bytes + bo;
+                if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat], K);
+                else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat], K);
+              }
+            }
+          } else {
+            for (int b = cw, j = 0; b < nb; b += NC, ++j) {
+              const int bo = (b - cw) * S::BB;
+              uint32_t xf[MT][XR];
+              load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
+#pragma unroll
+              for (int mat = 0; mat < NM; ++mat) {
+                const int to = mat * stage_bytes + bo;
+                if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat], K);
+                else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat], K);
+              }
             }
           }
         }
         __syncwarp();
         if (lane == 0)
           for (int mat = 0; mat < NM; ++mat) mbar_arrive(&empty[slot + mat]);
-        q += NM;
+        slot += NM;   // the ring holds a whole number of NM-slot groups
+        if (slot == R) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
       if (!ok) break;
       const int rb = i & 1;

@@ -53,8 +53,9 @@ __global__ void __launch_bounds__(256)
     w[i] = lo | (hi << 16);
   }
   uint32_t v[32];
-  if (C == kQ2_0 && (s & 1)) decode_sub<C>(w, 1, v);
-  else decode_sub<C>(w, 0, v);
+  const DecK dk = make_deck();
+  if (C == kQ2_0 && (s & 1)) decode_sub<C>(w, 1, v, dk);
+  else decode_sub<C>(w, 0, v, dk);
 
   const int valid = (K - 64 * s) >= 64 ? 64 : (K - 64 * s);
   uint4* dst = reinterpret_cast<uint4*>(out + (long long)n * K + 64 * s);

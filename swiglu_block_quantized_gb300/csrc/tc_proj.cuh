@@ -146,6 +146,7 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
   bool ok = true;
   int pending = -1;  // A stage whose tcgen05.st is still in flight
   int ks_g = 0, pk_g = 0;
+  const DecK K = make_deck();
   for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
     const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
     const uint8_t* grow = nullptr;
@@ -185,7 +186,7 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
         }
         tc_fence_after();
         uint32_t out[16];
-        decode_half<C, G>(w, j, out);
+        decode_half<C, G>(w, j, out, K);
         if (pending >= 0) {
           tmem_wait_st();
           tc_fence_before();

@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(512, 1)
     const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
     bool ok = true;
     int ks_g = 0, pk_g = 0;
+    const DecK K = make_deck();
     for (int tile = tile0; tile < p.tiles && ok; tile += tstep) {
       int ks = ks0;
       for (int pk = pk0; pk < pk1 && ok; ++pk, ++pk_g) {
@@ -264,8 +265,8 @@ __global__ void __launch_bounds__(512, 1)
             if (!ok) break;
           }
           uint32_t out[16];
-          if (G == 0) decode_half<C, 0>(w, j, out);
-          else decode_half<C, 1>(w, j, out);
+          if (G == 0) decode_half<C, 0>(w, j, out, K);
+          else decode_half<C, 1>(w, j, out, K);
           // row r of the 128-byte swizzled tile: 16-byte chunk c sits at c ^ (r & 7)
           uint8_t* row = bs + sb * Cfg::kBStage + r * 128;
 #pragma unroll

@@ -326,6 +326,45 @@ def test_gemv_parity(codec, general, M):
         assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "gemv swiglu %s M=%d" % (codec, M))
 
 
+# Rows of exactly one streamed stage (Q4_0 K = 4096, Q8_0 K = 2048, MLX4
+# K = 4096) with M <= 8: the activation fragments stay in registers for the
+# launch and the codes are read as aligned words (Q4_0 and Q8_0 as block
+# pairs), with the activations permuted to the weight pairs' k order.
+RESIDENT_X = [(synth.Q4_0, 4096), (synth.Q8_0, 2048), (synth.MLX4, 4096)]
+
+
+@pytest.mark.parametrize("codec,K", RESIDENT_X)
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_gemv_resident_x_parity(codec, K, M):
+    N = 264
+    X = synth.activations(M, K, seed=M + 30)
+    W = synth.weights(codec, N, K, seed=K + 5)
+    Wu = synth.weights(codec, N, K, seed=K + 5, name="Wu")
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_GEMV))
+    assert_close(Y, oracle.gemm(X, W, codec, M, N, K), "gemv resident %s M=%d" % (codec, M))
+    Ys = host(m.swiglu(dev(X), dev(W), dev(Wu), codec, N, K, path=m.PATH_GEMV))
+    assert_close(Ys, oracle.swiglu(X, W, Wu, codec, M, N, K), "gemv resident swiglu %s M=%d" % (codec, M))
+
+
+@pytest.mark.parametrize("codec,K", RESIDENT_X)
+def test_gemv_resident_x_one_hot_readout_bit_exact(codec, K):
+    # Eight one-hot activation rows at spread-out columns (every k position
+    # class of a block: even and odd blocks, both halves, the straddling
+    # words): each output is one exact product, so Y must be columns of the
+    # fp16 weights bit for bit -- a wrong activation permutation or a wrong
+    # code word shows up as a wrong column.
+    N = 136
+    W = synth.weights(codec, N, K, seed=K + 6)
+    ref = oracle.dequant_f16(W, codec, N, K)
+    rng = np.random.default_rng(K)
+    for rep in range(8):
+        cols = rng.permutation(K)[:8] if rep else np.array([0, 1, 14, 15, 16, 30, 31, 32 + 26])
+        X = np.zeros((8, K), dtype=np.float16)
+        X[np.arange(8), cols] = 1
+        Y = host(m.gemm(dev(X), dev(W), codec, N, K, path=m.PATH_GEMV)).view(np.uint16)
+        assert np.array_equal(Y, ref[:, cols].T), "columns %s" % cols.tolist()
+
+
 @pytest.mark.parametrize("codec,K", [(synth.Q4_0, 4352), (synth.Q8_0, 2304), (synth.Q2_0, 5120),
                                      (synth.MLX4, 4096),
                                      (synth.Q4_0, 2400), (synth.Q8_0, 2080), (synth.Q2_0, 5248),
