@@ -7,8 +7,10 @@
 namespace m4q {
 
 template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
-cudaError_t launch_gemv_one(const ProjLaunch& L, const GemvParams& p) {
-  using Cfg = GemvCfg<C>;
+cudaError_t launch_gemv_one(const ProjLaunch& L, GemvParams p) {
+  using Cfg = GemvCfg<C, MT>;
+  const int ring = Cfg::kRingBytes / (8 * p.pp);
+  p.ring = ring < Cfg::kRingMax ? ring : Cfg::kRingMax;
   auto kern = gemv_kernel<C, SWIGLU, MT, WTMA, XH>;
   std::atomic<unsigned long long>& configured =
       attr_flag<std::integer_sequence<int, 2, C, SWIGLU, MT, WTMA, XH>>();
@@ -27,7 +29,7 @@ cudaError_t launch_gemv_one(const ProjLaunch& L, const GemvParams& p) {
 
 template <int C, bool SWIGLU, bool WTMA>
 cudaError_t launch_gemv_mt(const ProjLaunch& L) {
-  using Cfg = GemvCfg<C>;
+  using Cfg = GemvCfg<C, 1>;   // stage sizes do not depend on MT
   GemvParams p;
   p.x = static_cast<const __half*>(L.x);
   p.w0 = static_cast<const uint8_t*>(L.w0);
@@ -42,9 +44,6 @@ cudaError_t launch_gemv_mt(const ProjLaunch& L) {
   p.sb = (int)(L.row_bytes <= Cfg::kSBMax ? L.row_bytes : Cfg::kSBMax);
   p.nst = (int)((L.row_bytes + p.sb - 1) / p.sb);
   p.pp = 2 * p.sb + 16;
-  const int ring = Cfg::kRingBytes / (8 * p.pp);
-  p.ring = ring < Cfg::kRingMax ? ring : Cfg::kRingMax;
-  if (SWIGLU) p.ring &= ~1;  // gate and up tiles of a segment sit in adjacent slots
   p.units = (L.N + 15) / 16;
   p.act = L.act;
   p.head_dim = L.head_dim;

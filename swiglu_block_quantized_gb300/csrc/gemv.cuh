@@ -60,7 +60,7 @@ struct GemvParams {
   unsigned long long limit_ns;
 };
 
-template <int C>
+template <int C, int MT>
 struct GemvCfg {
   using S = Stage<C>;
   static constexpr int kConsumers = 16;
@@ -73,10 +73,13 @@ struct GemvCfg {
   static constexpr int kSBMax = C == kMLX4 ? 2560 : (2400 / (16 * S::BB)) * 16 * S::BB;
   static constexpr int kBlocks = kSBMax / S::BB;             // blocks of a full stage
   static constexpr int kXH = kBlocks / kConsumers;           // blocks per warp of a full stage
-  static constexpr int kRingBytes = 160 * 1024;
   static constexpr int kRingMax = 16;
-  static constexpr int kRedFloats = 2 * kConsumers * 32 * 16; // [buf][warp][lane][2 mats x MT x 4]
+  static constexpr int kLaneFloats = 2 * MT * 4;                    // [2 mats][MT][4] accumulators
+  static constexpr int kRedFloats = 2 * kConsumers * 32 * kLaneFloats;  // [buf][warp][lane][...]
   static constexpr int kBars = 2 * kRingMax + 4;
+  // The ring takes all the shared memory the rest leaves: the deeper it is,
+  // the more weight bytes are in flight while the consumers work.
+  static constexpr int kRingBytes = (227 * 1024 - kRedFloats * 4 - kBars * 8 - 16 - 128) / 128 * 128;
   static constexpr int kSmemBytes = kRingBytes + kRedFloats * 4 + kBars * 8 + 16 + 128;
   static_assert(kXH * kConsumers == kBlocks, "blocks split evenly over the consumers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -327,8 +330,8 @@ __device__ __forceinline__ void xh_block_mlx(uint32_t a0, uint32_t a1, uint32_t 
 }
 
 template <int C, bool SWIGLU, int MT, bool WTMA, bool XH>
-__global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const GemvParams p) {
-  using Cfg = GemvCfg<C>;
+__global__ void __launch_bounds__(GemvCfg<C, MT>::kThreads, 1) gemv_kernel(const GemvParams p) {
+  using Cfg = GemvCfg<C, MT>;
   using S = Stage<C>;
   constexpr int NC = Cfg::kConsumers;
   constexpr int NM = SWIGLU ? 2 : 1;  // tiles (matrices) per unit
@@ -495,18 +498,27 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
         // The NM tiles (gate, up) of this segment are adjacent ring slots:
         // wait for both, then run them block by block (independent MMA chains
         // that share the X fragments).
+        // The NM stages of this segment are consecutive in the ring (with an
+        // odd ring the second may wrap to slot 0 of the next lap).
+        int sl[NM];
+        uint32_t ph[NM];
+        sl[0] = slot;
+        ph[0] = phase;
+        if constexpr (NM == 2) {
+          sl[1] = slot + 1 == R ? 0 : slot + 1;
+          ph[1] = slot + 1 == R ? phase ^ 1u : phase;
+        }
         for (int mat = 0; mat < NM && ok; ++mat)
-          ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[slot + mat], phase, ctl, 64));
+          ok = __all_sync(0xffffffffu, mbar_wait_idle(&full[sl[mat]], ph[mat], ctl, 64));
         if (!ok) break;
         if constexpr (XH) {
-          const uint32_t rs = smem_u32(ring) + slot * stage_bytes + g * p.pp;  // tile row g of this stage
           if constexpr (kPairs) {
 #pragma unroll
             for (int j = 0; j < Cfg::kXH / 2; ++j) {
 #pragma unroll
               for (int mat = 0; mat < NM; ++mat) {
                 float(&a)[4] = (NM == 1 && (j & 1)) ? acc1[mat][0] : acc[mat][0];
-                const uint32_t a0 = rs + mat * stage_bytes + (cw + NC * j) * (2 * S::BB);
+                const uint32_t a0 = smem_u32(ring) + sl[mat] * stage_bytes + g * p.pp + (cw + NC * j) * (2 * S::BB);
                 if constexpr (C == kQ4_0)
                   xh_pair_q4(a0, a0 + p.sb, q4_eoff, q4_esel, 20u + 4u * t, K, xh[2 * j], xh[2 * j + 1], a);
                 else
@@ -520,14 +532,14 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
 #pragma unroll
               for (int mat = 0; mat < NM; ++mat) {
                 float(&a)[4] = (NM == 1 && (j & 1)) ? acc1[mat][0] : acc[mat][0];
-                const uint32_t a0 = rs + mat * stage_bytes + (cw + NC * j) * S::BB;
+                const uint32_t a0 = smem_u32(ring) + sl[mat] * stage_bytes + g * p.pp + (cw + NC * j) * S::BB;
                 xh_block_mlx(a0, a0 + p.sb, 4u + 4u * t, K, xh[j], a);
               }
             }
           }
         } else {
-          const uint8_t* r0 = ring + slot * stage_bytes + row_off;  // block cw, row g, tile 0
-          const uint8_t* r1 = r0 + p.sb;                            // block cw, row g + 8
+          const uint8_t* r0 = ring + row_off;   // block cw, row g (plus the stage of each tile)
+          const uint8_t* r1 = r0 + p.sb;         // block cw, row g + 8
           if (nb == Cfg::kBlocks) {
             // Full stage: every block of this warp is inside K.
 #pragma unroll
@@ -537,7 +549,7 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
               load_xfrag<C, MT>(p, g, t, kb0 + (cw + NC * j) * S::B, xf);
 #pragma unroll
               for (int mat = 0; mat < NM; ++mat) {
-                const int to = mat * stage_bytes + bo;
+                const int to = sl[mat] * stage_bytes + bo;
                 if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat], K);
                 else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat], K);
               }
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
               load_xfrag<C, MT>(p, g, t, kb0 + b * S::B, xf);
 #pragma unroll
               for (int mat = 0; mat < NM; ++mat) {
-                const int to = mat * stage_bytes + bo;
+                const int to = sl[mat] * stage_bytes + bo;
                 if (NM == 1 && (j & 1)) gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc1[mat], K);
                 else gemv_block<C, MT>(r0 + to, r1 + to, t, xf, acc[mat], K);
               }
@@ -558,17 +570,17 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
         }
         __syncwarp();
         if (lane == 0)
-          for (int mat = 0; mat < NM; ++mat) mbar_arrive(&empty[slot + mat]);
-        slot += NM;   // the ring holds a whole number of NM-slot groups
-        if (slot == R) {
-          slot = 0;
-          phase ^= 1u;
-        }
+          for (int mat = 0; mat < NM; ++mat) mbar_arrive(&empty[sl[mat]]);
+        for (int mat = 0; mat < NM; ++mat)
+          if (++slot == R) {
+            slot = 0;
+            phase ^= 1u;
+          }
       }
       if (!ok) break;
       const int rb = i & 1;
       if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_idle(&red_empty[rb], ((i >> 1) - 1) & 1, ctl))) break;
-      float4* dst = reinterpret_cast<float4*>(red + ((rb * NC + cw) * 32 + lane) * 16);
+      float4* dst = reinterpret_cast<float4*>(red + ((rb * NC + cw) * 32 + lane) * Cfg::kLaneFloats);
 #pragma unroll
       for (int mat = 0; mat < NM; ++mat)
 #pragma unroll
@@ -594,7 +606,7 @@ __global__ void __launch_bounds__(GemvCfg<C>::kThreads, 1) gemv_kernel(const Gem
           for (int c = 0; c < 4; ++c) v[mat][mt][c] = 0.f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float4* src = reinterpret_cast<const float4*>(red + ((rb * NC + w) * 32 + lane) * 16);
+        const float4* src = reinterpret_cast<const float4*>(red + ((rb * NC + w) * 32 + lane) * Cfg::kLaneFloats);
 #pragma unroll
         for (int mat = 0; mat < NM; ++mat)
 #pragma unroll
