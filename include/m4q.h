@@ -165,6 +165,35 @@ int m4q_mlp_noalloc(const void* X, const void* Wg, const void* Wu, const void* W
                     int codec_d, int64_t M, int64_t D, int64_t F, void* Y, int act,
                     m4q_stream_t stream);
 
+/* The projection of m4q_gemm (W1 == NULL) or the gated projection of
+ * m4q_glu_ex (W1 != NULL, activation `act`) with the activations in host
+ * memory and the result written to host memory: the end-to-end call of a
+ * caller whose inputs arrive from the host.  M is cut into chunks of
+ * `chunk_rows` rows (0: about a quarter of M, rounded up to 128 rows); each
+ * chunk's activations are copied to the device on `h2d_stream`, projected on
+ * `stream` (the dispatch of m4q_gemm / m4q_glu_ex with path AUTO) and
+ * copied back on `d2h_stream`, so the copies of one chunk overlap the
+ * kernels of its neighbours.  The copies overlap only if X_host and Y_host
+ * are page-locked (cudaHostAlloc / pinned); otherwise the result is the same
+ * and the copies serialize.
+ *  - X_host: fp16 [M, K]; Y_host: fp16 [M, N] (host memory).
+ *  - X_dev, Y_dev: device staging buffers of M * K and M * N fp16, 16-byte
+ *    aligned, owned by the caller (the library allocates no memory).
+ *  - W0, W1: packed device weights as for m4q_gemm / m4q_glu_ex.
+ *  - Ordering: the copies start after the work already enqueued on
+ *    `stream`, and `stream` waits for the last copy back, so work enqueued
+ *    on `stream` after this call, and a synchronization of `stream`, see
+ *    Y_host complete.  The three streams should be distinct for overlap.
+ *  - The call records CUDA events of a per-device pool, created by the first
+ *    call on a device; calls from several host threads are serialized while
+ *    they enqueue.
+ * Errors: those of m4q_gemm / m4q_glu_ex (checked before anything is
+ * enqueued), M4Q_ERR_INVALID_ARG for a null host or staging pointer or a
+ * negative chunk_rows, M4Q_ERR_MISALIGNED for unaligned staging buffers. */
+int m4q_project_host(const void* X_host, const void* W0, const void* W1, int codec, int act, int64_t M,
+                     int64_t N, int64_t K, void* Y_host, void* X_dev, void* Y_dev, int64_t chunk_rows,
+                     m4q_stream_t stream, m4q_stream_t h2d_stream, m4q_stream_t d2h_stream);
+
 /* Repack MLX 4-bit weights from MLX's planar arrays into MLX4 blocks
  * (project page, section 4: the deinterleaved "mlx_4bit_planar" layout of
  * the 20-byte block_mlx_4bit).  words: uint32 [N, K/8], code k of row n at

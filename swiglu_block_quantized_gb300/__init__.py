@@ -13,6 +13,7 @@ Functions mirror the C ABI (same names without the ``m4q_`` prefix):
     geglu(x, wg, wu, codec, n, k, out=None, path=PATH_AUTO)
     glu(x, wg, wu, codec, n, k, act, out=None, path=PATH_AUTO)
     mlp(x, wg, wu, wd, codec_gu, codec_d, d, f, act=ACT_SILU, h=None, out=None)
+    project_host(x_host, w, codec, n, k, wu=None, act=ACT_SILU, out=None, ...)
     dequant(w, codec, n, k, out=None)
     mlx4_pack(words, scales, biases, n, k, out=None)
     attention(q, k, v, kv_codec, hkv, t, q_offset=None, causal=True, scale=None, out=None)
@@ -70,6 +71,8 @@ SIGNATURES = {
     "m4q_glu_ex": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _i32, _vp]),
     "m4q_mlp": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp]),
     "m4q_mlp_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "m4q_project_host": (_i32, [_vp, _vp, _vp, _i32, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp,
+                                _vp]),
     "m4q_dequant": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "m4q_mlx4_pack": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "m4q_repack": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
@@ -266,6 +269,51 @@ def mlp(x, wg, wu, wd, codec_gu: int, codec_d: int, d: int, f: int, act: int = A
         return out
     _check(load().m4q_mlp(x.data_ptr(), wg.data_ptr(), wu.data_ptr(), wd.data_ptr(), codec_gu, codec_d,
                           m, d, f, h.data_ptr(), out.data_ptr(), act, _stream_ptr(stream)), "m4q_mlp")
+    return out
+
+
+_host_streams_by_device = {}
+
+
+def _host_streams(device):
+    """Two copy streams per device, created once, for project_host."""
+    import torch
+    key = torch.device(device).index
+    if key not in _host_streams_by_device:
+        _host_streams_by_device[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _host_streams_by_device[key]
+
+
+def project_host(x, w, codec: int, n: int, k: int, wu=None, act: int = ACT_SILU, out=None, x_dev=None,
+                 y_dev=None, chunk_rows: int = 0, stream=None):
+    """Y = X W^T (wu None) or act(X W^T) * (X Wu^T) with X and Y in host
+    memory: chunks of rows are copied in, projected and copied back with the
+    copies overlapping the kernels (m4q_project_host).  x: CPU fp16 [..., k]
+    (page-locked for overlap); out: CPU fp16 [M, n], page-locked when
+    allocated here.  x_dev / y_dev: device staging [M, k] / [M, n], allocated
+    if not given.  The result is complete once the current stream (or
+    `stream`) has reached this point: synchronize it before reading out."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.is_cuda or x.dtype != torch.float16 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous fp16 host tensor")
+    _packed_check(w, codec, n, k, "w")
+    if wu is not None:
+        _packed_check(wu, codec, n, k, "wu")
+    m = _rows(x, k)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float16, pin_memory=True)
+    elif (not isinstance(out, torch.Tensor) or out.is_cuda or out.dtype != torch.float16
+          or not out.is_contiguous() or out.numel() != m * n):
+        raise ValueError("out must be a contiguous fp16 host tensor of %d elements" % (m * n))
+    x_dev = _result(x_dev, (m, k), w.device, "x_dev")
+    y_dev = _result(y_dev, (m, n), w.device, "y_dev")
+    if m == 0:
+        return out
+    s_in, s_out = _host_streams(w.device)
+    _check(load().m4q_project_host(x.data_ptr(), w.data_ptr(), wu.data_ptr() if wu is not None else None, codec,
+                                   act, m, n, k, out.data_ptr(), x_dev.data_ptr(), y_dev.data_ptr(), chunk_rows,
+                                   _stream_ptr(stream), ctypes.c_void_p(s_in.cuda_stream),
+                                   ctypes.c_void_p(s_out.cuda_stream)), "m4q_project_host")
     return out
 
 

@@ -196,6 +196,19 @@ int check_shape(int codec, int64_t M, int64_t N, int64_t K) {
   return M4Q_OK;
 }
 
+// ------------------------------------------------------------ host pipeline
+
+// Events of m4q_project_host: per device, recorded and waited in stream
+// order, so one pool serves every call; calls enqueue one at a time.
+constexpr int kHostChunks = 16;
+constexpr int kMaxEventDevices = 64;
+struct HostEvents {
+  bool ready = false;
+  cudaEvent_t e[2 * kHostChunks + 2];
+};
+HostEvents g_host_events[kMaxEventDevices];
+std::mutex g_host_mu[kMaxEventDevices];
+
 // ------------------------------------------------------------ dispatch
 
 int project(const void* X, const void* W0, const void* W1, int codec, int64_t M, int64_t N,
@@ -369,6 +382,66 @@ int m4q_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, int c
   rc = project(X, Wg, Wu, codec_gu, M, F, D, H, M4Q_PATH_AUTO, true, act, stream);
   if (rc != M4Q_OK) return rc;
   return project(H, Wd, nullptr, codec_d, M, D, F, Y, M4Q_PATH_AUTO, false, M4Q_ACT_SILU, stream);
+}
+
+int m4q_project_host(const void* X_host, const void* W0, const void* W1, int codec, int act, int64_t M,
+                     int64_t N, int64_t K, void* Y_host, void* X_dev, void* Y_dev, int64_t chunk_rows,
+                     m4q_stream_t stream, m4q_stream_t h2d_stream, m4q_stream_t d2h_stream) {
+  if (!X_host || !Y_host || !X_dev || !Y_dev || !W0 || chunk_rows < 0) return M4Q_ERR_INVALID_ARG;
+  if (act != M4Q_ACT_SILU && act != M4Q_ACT_GELU) return M4Q_ERR_INVALID_ARG;
+  int rc = check_shape(codec, M, N, K);
+  if (rc != M4Q_OK) return rc;
+  if (!aligned16(X_dev) || !aligned16(Y_dev) || !aligned16(W0) || (W1 && !aligned16(W1)))
+    return M4Q_ERR_MISALIGNED;
+  DevInfo dev;
+  rc = current_device_info(&dev);
+  if (rc != M4Q_OK) return rc;
+  if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
+  int64_t rows = chunk_rows ? chunk_rows : ((M + 3) / 4 + 127) / 128 * 128;
+  if (rows > M) rows = M;
+  const int64_t chunks = (M + rows - 1) / rows;
+  if (chunks > kHostChunks) rows = (M + kHostChunks - 1) / kHostChunks;   // at most kHostChunks chunks
+  int dev_id = 0;
+  if (cudaGetDevice(&dev_id) != cudaSuccess || dev_id < 0 || dev_id >= kMaxEventDevices) return M4Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mu[dev_id]);
+  HostEvents& ev = g_host_events[dev_id];
+  if (!ev.ready) {
+    for (int i = 0; i < 2 * kHostChunks + 2; ++i)
+      if (cudaEventCreateWithFlags(&ev.e[i], cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return M4Q_ERR_CUDA;
+      }
+    ev.ready = true;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t sin = reinterpret_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t sout = reinterpret_cast<cudaStream_t>(d2h_stream);
+  auto fail = [] { return M4Q_ERR_CUDA; };
+  // Both copy streams start after the work already on `stream`.
+  if (cudaEventRecord(ev.e[0], s) != cudaSuccess || cudaStreamWaitEvent(sin, ev.e[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(sout, ev.e[0], 0) != cudaSuccess)
+    return fail();
+  const uint8_t* xh = static_cast<const uint8_t*>(X_host);
+  uint8_t* yh = static_cast<uint8_t*>(Y_host);
+  uint8_t* xd = static_cast<uint8_t*>(X_dev);
+  uint8_t* yd = static_cast<uint8_t*>(Y_dev);
+  int c = 0;
+  for (int64_t r0 = 0; r0 < M; r0 += rows, ++c) {
+    const int64_t n = (M - r0) < rows ? (M - r0) : rows;
+    const size_t xoff = (size_t)(r0 * K * 2), yoff = (size_t)(r0 * N * 2);
+    cudaEvent_t in = ev.e[1 + 2 * c], done = ev.e[2 + 2 * c];
+    if (cudaMemcpyAsync(xd + xoff, xh + xoff, (size_t)(n * K * 2), cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+        cudaEventRecord(in, sin) != cudaSuccess || cudaStreamWaitEvent(s, in, 0) != cudaSuccess)
+      return fail();
+    rc = project(xd + xoff, W0, W1, codec, n, N, K, yd + yoff, M4Q_PATH_AUTO, W1 != nullptr, act, stream);
+    if (rc != M4Q_OK) return rc;
+    if (cudaEventRecord(done, s) != cudaSuccess || cudaStreamWaitEvent(sout, done, 0) != cudaSuccess ||
+        cudaMemcpyAsync(yh + yoff, yd + yoff, (size_t)(n * N * 2), cudaMemcpyDeviceToHost, sout) != cudaSuccess)
+      return fail();
+  }
+  cudaEvent_t last = ev.e[2 * kHostChunks + 1];
+  if (cudaEventRecord(last, sout) != cudaSuccess || cudaStreamWaitEvent(s, last, 0) != cudaSuccess) return fail();
+  return M4Q_OK;
 }
 
 size_t m4q_weight_bytes(int codec, int64_t N, int64_t K) {

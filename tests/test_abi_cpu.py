@@ -130,3 +130,21 @@ def test_python_binding_rejects_non_cuda_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         m.load(str(tmp_path / "nope.so"))
+
+
+def test_project_host_argument_errors(lib):
+    good = 0x100000
+    s = None
+    # null host or staging pointers, negative chunk
+    assert lib.m4q_project_host(None, P(good), None, 0, 0, 4, 8, 32, P(good), P(good), P(good), 0, s, s, s) \
+        == m.ERR_INVALID_ARG
+    assert lib.m4q_project_host(P(good), P(good), None, 0, 0, 4, 8, 32, P(good), None, P(good), 0, s, s, s) \
+        == m.ERR_INVALID_ARG
+    assert lib.m4q_project_host(P(good), P(good), None, 0, 0, 4, 8, 32, P(good), P(good), P(good), -1, s, s, s) \
+        == m.ERR_INVALID_ARG
+    assert lib.m4q_project_host(P(good), P(good), P(good), 0, 5, 4, 8, 32, P(good), P(good), P(good), 0, s, s, s) \
+        == m.ERR_INVALID_ARG   # activation
+    assert lib.m4q_project_host(P(good), P(good), None, 0, 0, 4, 12, 32, P(good), P(good), P(good), 0, s, s, s) \
+        == m.ERR_BAD_SHAPE
+    assert lib.m4q_project_host(P(good), P(good), None, 0, 0, 4, 8, 32, P(good), P(good + 8), P(good), 0, s, s, s) \
+        == m.ERR_MISALIGNED
