@@ -276,17 +276,28 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
       // stages, as long as every cluster of the grid can be resident at
       // once (clusters must fit inside one GPC, so fewer clusters of 8 than
       // SMs / 8 fit the GPU).
-      L.tiles = (N + out_rows - 1) / out_rows;
-      const int64_t npk = K / (8 * kBlock[codec]);
+      const int64_t tiles = (N + out_rows - 1) / out_rows;
+      const int64_t npk = (K + 8 * kBlock[codec] - 1) / (8 * kBlock[codec]);   // packed stages
       L.split = 8;
-      while (L.split > 1 && (npk % L.split != 0 || L.tiles * L.split > dev.sms)) L.split /= 2;
-      L.split_probe = true;   // the launcher lowers it to what the occupancy query allows
+      while (L.split > 1 && (npk % L.split != 0 || tiles * L.split > dev.sms)) L.split /= 2;
     } else if (!L.wtma) {
       nx = 128;
     } else if (((M + 255) / 256) * ntiles >= dev.sms) {
       nx = 256;
     } else if (((M + 127) / 128) * ntiles >= dev.sms) {
       nx = 128;
+    } else if (head_dim == 0) {
+      // Fewer 128-row tiles than SMs: keep the 128-wide MMA (narrower ones
+      // cost more than their share of the tensor pipe) and split K over a
+      // cluster per tile when that fills the GPU better than 64-wide tiles.
+      const int64_t tiles = ((M + 127) / 128) * ntiles;
+      const int64_t npk = (K + 8 * kBlock[codec] - 1) / (8 * kBlock[codec]);   // packed stages
+      int s = 8;
+      while (s > 1 && (npk % s != 0 || tiles * s > dev.sms)) s /= 2;
+      if (s > 1) {
+        nx = 128;
+        L.split = s;
+      }
     }
     L.nx = nx;
     L.sms = dev.sms;

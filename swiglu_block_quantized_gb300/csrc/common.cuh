@@ -361,12 +361,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 
 // 16-byte load from a peer CTA's shared memory (distributed shared memory).
+// No memory clobber: the loads of a reduction are independent and are meant
+// to be in flight together (they stay after the cluster barrier, whose
+// volatile statement they follow).
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t caddr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(caddr)
-               : "memory");
+               : "r"(caddr));
   return v;
 }
 

@@ -32,9 +32,8 @@ struct ProjLaunch {
   // tcgen05 path
   int nx;                 // activation rows per tile: 64, 128 or 256
   bool small;             // M <= 128 kernel (activations as the A operand, tc_small.cuh)
-  int split;              // small-M kernel: CTAs of a cluster splitting K for one tile (1, 2, 4, 8)
-  bool split_probe;       // lower `split` until all clusters of the grid can be co-resident
-  long long tiles;        // small-M kernel: output tiles
+  int split;              // CTAs of a cluster splitting K for one tile (1, 2, 4, 8); the launcher
+                          // lowers it until all clusters of the grid can be co-resident
   int sms;                // multiprocessors (persistent grid size, both paths)
   CUtensorMap tm_x, tm_w0, tm_w1, tm_y;
   // GEMV path

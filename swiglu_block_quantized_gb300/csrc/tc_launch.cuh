@@ -10,6 +10,41 @@
 
 namespace m4q {
 
+// Largest K split, from `split` down by halves, whose clusters (one per
+// output tile) can all be resident on the device at once; the occupancy
+// answer is kept per kernel, device and cluster size.
+template <typename Kern>
+int fit_split(Kern kern, int split, long long tiles, unsigned threads, size_t smem, int dev,
+              std::atomic<int> (&fit)[64][4]) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  while (split > 1) {
+    const int lg = split == 2 ? 1 : (split == 4 ? 2 : 3);
+    int known = fit[dev & 63][lg].load();
+    if (known == 0) {
+      cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
+      attr[0].val.clusterDim.x = (unsigned)split;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      known = 1 + n;
+      fit[dev & 63][lg].store(known);
+    }
+    if ((long long)(known - 1) >= tiles) break;
+    split /= 2;
+  }
+  return split;
+}
+
 template <int C, bool SWIGLU, int NX, bool WTMA, int ACT, int HD>
 cudaError_t launch_tc_one(const ProjLaunch& L) {
   using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
@@ -33,15 +68,24 @@ cudaError_t launch_tc_one(const ProjLaunch& L) {
   p.N = L.N;
   p.K = L.K;
   p.row_bytes = L.row_bytes;
-  p.split = 1;
-  p.ks_per = (L.K + 63) / 64;
   p.m_tiles = (L.M + NX - 1) / NX;
   p.tiles = p.m_tiles * ((L.N + Cfg::kOutRows - 1) / Cfg::kOutRows);
   p.status = L.status;
   p.limit_ns = L.limit_ns;
-  const unsigned grid = (unsigned)(p.tiles < L.sms ? p.tiles : L.sms);  // persistent CTAs
-  return launch_proj(kern, grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream, 1u, L.tm_x, L.tm_w0, L.tm_w1, L.tm_y,
-                     p);
+  p.split = 1;
+  if constexpr (NX <= 128 && HD == 0 && WTMA) {   // the K-split epilogue exists for these
+    if (L.split > 1) {
+      static std::atomic<int> fit[64][4];
+      p.split = fit_split(kern, L.split, p.tiles, Cfg::kThreads, Cfg::kSmemBytes, dev, fit);
+    }
+  }
+  const int npk = (L.K + Cfg::S::KP - 1) / Cfg::S::KP;
+  p.ks_per = (npk / p.split) * Cfg::S::SUB;   // the host picks splits that divide npk
+  // Persistent CTAs, or (K split) one cluster of p.split CTAs per output tile.
+  const unsigned grid = p.split == 1 ? (unsigned)(p.tiles < L.sms ? p.tiles : L.sms)
+                                     : (unsigned)(p.tiles * p.split);
+  return launch_proj(kern, grid, Cfg::kThreads, Cfg::kSmemBytes, L.stream, (unsigned)p.split, L.tm_x, L.tm_w0,
+                     L.tm_w1, L.tm_y, p);
 }
 
 template <int C, bool SWIGLU, bool WTMA, int ACT, int HD>
@@ -102,37 +146,10 @@ cudaError_t launch_tcs_one(const ProjLaunch& L) {
   p.status = L.status;
   p.limit_ns = L.limit_ns;
   const int npk = (L.K + Cfg::S::KP - 1) / Cfg::S::KP;
-  p.split = L.split > 1 ? L.split : 1;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-  cfg.stream = L.stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  // Largest split (a divisor of the packed stages, chosen by the host) whose
-  // clusters all fit on the GPU at once; the answer is kept per kernel,
-  // device and cluster size.
-  while (p.split > 1 && L.split_probe) {
+  p.split = 1;
+  if (L.split > 1) {
     static std::atomic<int> fit[64][4];   // per device ordinal, per log2 split: 0 unknown, 1 + max clusters
-    const int lg = p.split == 2 ? 1 : (p.split == 4 ? 2 : 3);
-    int known = fit[dev & 63][lg].load();
-    if (known == 0) {
-      cfg.gridDim = dim3((unsigned)(p.tiles * p.split), 1, 1);
-      attr[0].val.clusterDim.x = (unsigned)p.split;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        n = 0;
-      }
-      known = 1 + n;
-      fit[dev & 63][lg].store(known);
-    }
-    if ((long long)(known - 1) >= p.tiles) break;
-    p.split /= 2;
+    p.split = fit_split(kern, L.split, p.tiles, Cfg::kThreads, Cfg::kSmemBytes, dev, fit);
   }
   p.ks_per = (npk / p.split) * Cfg::S::SUB;   // the host picks splits that divide npk
   // Persistent CTAs, or (K split) one cluster of p.split CTAs per output tile.

@@ -128,6 +128,27 @@ struct TcSmem {
   uint64_t *d_full, *d_empty, *drain;
 };
 
+// The part of the K loop a CTA runs.  Without a split (p.split == 1) every
+// CTA walks all sub-steps of its tiles (persistent: tiles tile0, tile0 +
+// tstep, ...).  With a split the CTAs of a cluster share one tile and CTA
+// `rank` takes sub-steps [ks0, ks1), whole packed stages [pk0, pk1).
+struct KRange {
+  int ks0, ks1, pk0, pk1, tile0, tstep, rank;
+};
+template <int SUB>
+__device__ __forceinline__ KRange k_range(const TcParams& p) {
+  KRange r;
+  const int nks = (p.K + 63) / 64;
+  r.rank = p.split > 1 ? (int)cluster_ctarank() : 0;
+  r.ks0 = r.rank * p.ks_per;
+  r.ks1 = min(nks, r.ks0 + p.ks_per);
+  r.pk0 = r.ks0 / SUB;
+  r.pk1 = (r.ks1 + SUB - 1) / SUB;
+  r.tile0 = blockIdx.x / p.split;
+  r.tstep = gridDim.x / p.split;
+  return r;
+}
+
 // Decode role of group G (0 or 1): every tile, every sub-step, weights
 // [32G, 32G+32) of this thread's row.
 template <int C, bool SWIGLU, int NX, bool WTMA, int G>
@@ -141,13 +162,12 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
       tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + Cfg::kACol0 + 16 * G;
   // SwiGLU: lane 2i decodes gate row n0+i, lane 2i+1 the up row n0+i.
   const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
-  const int nks = (p.K + 63) / 64;
-  const int npk = (p.K + S::KP - 1) / S::KP;
+  const KRange kr = k_range<S::SUB>(p);
   bool ok = true;
   int pending = -1;  // A stage whose tcgen05.st is still in flight
   int ks_g = 0, pk_g = 0;
   const DecK K = make_deck();
-  for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+  for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep) {
     const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
     const uint8_t* grow = nullptr;
     bool grow_ok = false;
@@ -157,8 +177,8 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
       const uint8_t* base = (SWIGLU && (r & 1)) ? p.w1 : p.w0;
       grow = base + (grow_ok ? (long long)n * p.row_bytes : 0);
     }
-    int ks = 0;
-    for (int pk = 0; pk < npk && ok; ++pk, ++pk_g) {
+    int ks = kr.ks0;
+    for (int pk = kr.pk0; pk < kr.pk1 && ok; ++pk, ++pk_g) {
       uint32_t w[S::WORDS];
       if constexpr (WTMA) {
         const int sp = pk_g % SW;
@@ -178,7 +198,7 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
       }
 #pragma unroll
       for (int j = 0; j < S::SUB; ++j) {
-        if (ks >= nks) break;
+        if (ks >= kr.ks1) break;
         const int sa = ks_g % SA;
         if (ks_g >= SA) {
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.a_empty[sa], ((ks_g / SA) - 1) & 1, ctl));
@@ -360,6 +380,87 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
   if (leader) bulk_wait_all();
 }
 
+// K split.  Slice q of the staged partial tile holds the W = NX / split
+// activation columns CTA q of the cluster owns, column-major: column c's
+// 128 weight rows are contiguous.  The staging writes of 32 consecutive rows
+// are then conflict-free, an owner reads a peer's slice as contiguous runs
+// (distributed shared memory requests that touch scattered rows were an
+// order of magnitude slower), and 4 consecutive weight rows of one column
+// are 4 consecutive outputs of one activation row: one vector store.
+__device__ __forceinline__ int split_slot(int r, int c, int W) {   // float index of (row r, column c)
+  return ((c / W) * W + (c % W)) * 128 + r;
+}
+
+// K split, epilogue warps (group E of two, lane quadrant warp & 3): stage
+// this CTA's partial D [128 weight rows][NX activation columns] in its own,
+// now idle, X ring.  Returns false if the tile's accumulator never arrived
+// (the CTA gave up).
+template <int C, bool SWIGLU, int NX, bool WTMA>
+__device__ __forceinline__ bool split_stage_role(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                                 const WaitCtl& ctl, int warp, int E) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  static_assert(128 * NX * 4 <= Cfg::kSX * Cfg::kXStage, "staged partial fits the X ring");
+  const int r = threadIdx.x & 127;
+  const int W = NX / p.split;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const bool dok = !*ctl.abort && mbar_wait_idle(sm.d_full, 0, ctl, 128);
+  if (named_bar_any(5, 256, !dok || *ctl.abort)) return false;
+  tc_fence_after();
+  float* stg = reinterpret_cast<float*>(sm.xs);
+#pragma unroll
+  for (int ch = 0; ch < NX / 64; ++ch) {
+    const int c0 = E * (NX / 2) + 32 * ch;
+    uint32_t v[32];
+    tmem_ld32_wait(tmem + lane_base + c0, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) stg[split_slot(r, c0 + i, W)] = __uint_as_float(v[i]);
+  }
+  tc_fence_before();
+  return true;
+}
+
+// K split, after the cluster barrier: CTA `rank` owns activation columns
+// [rank W, rank W + W).  The 256 epilogue threads walk its slice a float4
+// (4 consecutive weight rows of one column) each, add the slices of the
+// cluster's CTAs in rank order and write the outputs: 4 outputs of one
+// activation row (GEMM), or 2 (gated: rows 2i, 2i + 1 are gate and up).
+template <int C, bool SWIGLU, int NX, bool WTMA, int ACT>
+__device__ __forceinline__ void split_reduce_role(const TcSmem& sm, const TcParams& p, const KRange& kr) {
+  using Cfg = TcCfg<C, SWIGLU, NX, WTMA>;
+  const int t = threadIdx.x - 384;               // 0 .. 255
+  const int W = NX / p.split;
+  const int m0 = (kr.tile0 % p.m_tiles) * NX + kr.rank * W;
+  const int n0 = (kr.tile0 / p.m_tiles) * Cfg::kOutRows;
+  const uint32_t slice = smem_u32(reinterpret_cast<float*>(sm.xs) + kr.rank * W * 128);
+  for (int e = t; e < 32 * W; e += 256) {
+    const int c = e >> 5, r = 4 * (e & 31);      // column c, weight rows r .. r + 3
+    const uint32_t a = slice + 4u * (uint32_t)(c * 128 + r);
+    float4 f[8];
+#pragma unroll
+    for (int src = 0; src < 8; ++src)
+      if (src < p.split) f[src] = ld_dsmem_f4(mapa_shared(a, (uint32_t)src));
+    float4 s4 = f[0];
+#pragma unroll
+    for (int src = 1; src < 8; ++src)
+      if (src < p.split) { s4.x += f[src].x; s4.y += f[src].y; s4.z += f[src].z; s4.w += f[src].w; }
+    const int m = m0 + c;
+    if (m >= p.M) continue;
+    if constexpr (SWIGLU) {
+      const int n = n0 + r / 2;                  // 2 outputs, n even
+      const float y0 = (ACT ? gelu_f(s4.x) : __fdividef(s4.x, 1.0f + __expf(-s4.x))) * s4.y;
+      const float y1 = (ACT ? gelu_f(s4.z) : __fdividef(s4.z, 1.0f + __expf(-s4.z))) * s4.w;
+      if (n < p.N) *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
+    } else {
+      const int n = n0 + r;                      // 4 outputs; N % 8 == 0: all in or all out
+      if (n < p.N) {
+        const __half2 h0 = __floats2half2_rn(s4.x, s4.y), h1 = __floats2half2_rn(s4.z, s4.w);
+        *reinterpret_cast<uint2*>(p.y + (size_t)m * p.N + n) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      }
+    }
+  }
+}
+
 // ACT (gated projections): 0 SiLU, 1 GELU.  HD (GEMM): 0 row-major Y, else
 // the head dim of the direct-head output.
 template <int C, bool SWIGLU, int NX, bool WTMA, int ACT, int HD>
@@ -391,8 +492,8 @@ __global__ void __launch_bounds__(640, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nks = (p.K + 63) / 64;            // 64-weight sub-steps per tile
-  const int npk = (p.K + S::KP - 1) / S::KP;  // packed stages per tile
+  const KRange kr = k_range<S::SUB>(p);      // sub-steps and packed stages of this CTA
+  bool staged = false;                       // K split: this CTA's partial tile is staged
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SX; ++i) { mbar_init(&sm.x_full[i], 1); mbar_init(&sm.x_empty[i], 1); }
@@ -422,9 +523,9 @@ __global__ void __launch_bounds__(640, 1)
       tma_prefetch_desc(&tm_x);
       int xi = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep) {
         const int m0 = (tile % p.m_tiles) * NX;
-        for (int ks = 0; ks < nks; ++ks) {
+        for (int ks = kr.ks0; ks < kr.ks1; ++ks) {
           const int sx = xi % SX;
           if (xi >= SX && !mbar_wait_idle(&sm.x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.x_full[sx], Cfg::kXStage);
@@ -446,9 +547,9 @@ __global__ void __launch_bounds__(640, 1)
         if (SWIGLU) tma_prefetch_desc(&tm_w1);
         int wi = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep) {
           const int n0 = (tile / p.m_tiles) * Cfg::kOutRows;
-          for (int pk = 0; pk < npk; ++pk) {
+          for (int pk = kr.pk0; pk < kr.pk1; ++pk) {
             const int sp = wi % SW;
             if (wi >= SW && !mbar_wait_idle(&sm.w_empty[sp], ((wi / SW) - 1) & 1, ctl)) { ok = false; break; }
             mbar_arrive_expect_tx(&sm.w_full[sp], Cfg::kWStage);
@@ -471,11 +572,11 @@ __global__ void __launch_bounds__(640, 1)
       constexpr uint32_t idesc = idesc_f16_f32(128, NX);
       int ks_g = 0, lt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++lt) {
+      for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep, ++lt) {
         // D must have been read out by the epilogue of the previous tile.
         if (lt > 0 && !mbar_wait(sm.d_empty, (lt - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < nks; ++ks, ++ks_g) {
+        for (int ks = kr.ks0; ks < kr.ks1; ++ks, ++ks_g) {
           const int sx = ks_g % SX, sa = ks_g % SA;
           if (!mbar_wait(&sm.a_full[sa], (ks_g / SA) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(&sm.x_full[sx], (ks_g / SX) & 1, ctl)) { ok = false; break; }
@@ -484,7 +585,7 @@ __global__ void __launch_bounds__(640, 1)
           const uint32_t acol = tmem + Cfg::kACol0 + sa * 32;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+            tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks != kr.ks0) | kk);
           tc_commit(&sm.x_empty[sx]);
           tc_commit(&sm.a_empty[sa]);
         }
@@ -500,7 +601,23 @@ __global__ void __launch_bounds__(640, 1)
   } else if (warp >= 8 && warp < 12) {
     decode_role<C, SWIGLU, NX, WTMA, 1>(sm, p, tmem, ctl, warp);
   } else if (warp >= 12) {
-    epilogue_role<C, SWIGLU, NX, WTMA, ACT, HD>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
+    if constexpr (NX <= 128 && HD == 0 && WTMA) {
+      if (p.split > 1) staged = split_stage_role<C, SWIGLU, NX, WTMA>(sm, p, tmem, ctl, warp, (warp - 12) >> 2);
+      else epilogue_role<C, SWIGLU, NX, WTMA, ACT, HD>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
+    } else {
+      epilogue_role<C, SWIGLU, NX, WTMA, ACT, HD>(sm, p, tmem, ctl, &tm_y, warp, (warp - 12) >> 2);
+    }
+  }
+
+  if constexpr (NX <= 128 && HD == 0 && WTMA) {
+    if (p.split > 1) {
+      // Every thread of the cluster: all partial tiles are staged; then each
+      // CTA reduces its columns; no CTA leaves while a peer may still read
+      // its staged partial.
+      cluster_sync_all();
+      if (warp >= 12 && staged) split_reduce_role<C, SWIGLU, NX, WTMA, ACT>(sm, p, kr);
+      cluster_sync_all();
+    }
   }
 
   tc_fence_before();

@@ -54,6 +54,17 @@ __device__ __forceinline__ void tc_mma_ss_f16(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// K split of this kernel: slice q of a staged partial tile holds the W =
+// 128 / split weight columns CTA q owns, for every activation row, rows
+// W + 4 floats apart (the pad spreads the writes of 32 consecutive rows
+// over all banks).  An owner reads a peer's slice as nearly contiguous runs
+// (distributed shared memory requests that touch scattered rows were an
+// order of magnitude slower), and 4 columns of a row are 4 consecutive
+// outputs.
+__device__ __forceinline__ int small_split_slot(int m, int c, int W) {
+  return ((c / W) * 128 + m) * (W + 4) + (c % W);
+}
+
 template <int C, bool SWIGLU, int XR>
 struct TsCfg {
   using S = Stage<C>;
@@ -75,9 +86,8 @@ struct TsCfg {
       1024 + kSX * kXStage + kXPad + kSB * kBStage + kYBytes + kSW * kWStage + kBars * 8 + 16;
   static constexpr uint32_t kTmemCols = 256;                 // two D buffers
   // K split: each CTA stages its fp32 partial D [128 m][128 cols] over the
-  // idle X and B rings; a pitch of 132 floats spreads 8 rows over all banks.
-  static constexpr int kDPitch = 132;
-  static_assert(128 * kDPitch * 4 <= kSX * kXStage + kXPad + kSB * kBStage, "D staging fits the rings");
+  // idle X and B rings, slice-major (small_split_slot).
+  static_assert(128 * (128 + 32) * 4 <= kSX * kXStage + kXPad + kSB * kBStage, "D staging fits the rings");
   // Q8_0 / Q2_0 GEMM with 128-row X stages does not fit; the host sends
   // that case to tc_proj (M > 64 with 272-byte packed stages).
   static constexpr bool kFits = kSmemBytes <= 227 * 1024;
@@ -293,14 +303,15 @@ __global__ void __launch_bounds__(512, 1)
     split_ok = !named_bar_any(1, 128, !dok || *ctl.abort);
     if (split_ok) {
       tc_fence_after();
-      float* row = reinterpret_cast<float*>(xs) + m * Cfg::kDPitch;  // X and B rings are idle
+      float* stg = reinterpret_cast<float*>(xs);   // X and B rings are idle
+      const int W = 128 / nsplit;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
         tmem_ld32_wait(tmem + lane_base + 32 * ch, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(row + 32 * ch)[i] =
+          *reinterpret_cast<float4*>(stg + small_split_slot(m, 32 * ch + 4 * i, W)) =
               make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
                           __uint_as_float(v[4 * i + 3]));
       }
@@ -379,54 +390,38 @@ __global__ void __launch_bounds__(512, 1)
     // Every thread of the cluster: all partials are staged.
     cluster_sync_all();
     if (warp >= 12 && split_ok) {
-      // CTA `rank` owns columns [rank W, rank W + W) of the tile and adds
-      // them up over the cluster's CTAs in rank order (a fixed order, so the
-      // result does not depend on timing), then writes its outputs.
-      const int m = 32 * (warp & 3) + lane;
-      const int W = 128 / nsplit;
-      const int n_base = tile0 * Cfg::kOutRows + (SWIGLU ? rank * (W / 2) : rank * W);
-      const uint32_t my = smem_u32(reinterpret_cast<float*>(xs) + m * Cfg::kDPitch + rank * W);
-      for (int cc = 0; cc < W; cc += 16) {
-        float a[16];
+      // CTA `rank` owns weight columns [rank W, rank W + W) of the tile for
+      // every activation row; the 128 epilogue threads walk its slice a
+      // float4 (4 columns of one row) each, add the slices of the cluster's
+      // CTAs in rank order (a fixed order: the result does not depend on
+      // timing) and write the outputs.
+      const int t = threadIdx.x - 384;
+      const int W = 128 / nsplit, Q = W / 4;
+      const uint32_t slice = smem_u32(reinterpret_cast<float*>(xs) + rank * 128 * (W + 4));
+      for (int e = t; e < 128 * Q; e += 128) {
+        const int m = e / Q, c = 4 * (e % Q);
+        const uint32_t a = slice + 4u * (uint32_t)(m * (W + 4) + c);
+        float4 f[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) a[i] = 0.f;
-        for (int src = 0; src < nsplit; ++src) {
-          const uint32_t ra = mapa_shared(my + 4 * cc, (uint32_t)src);
+        for (int src = 0; src < 8; ++src)
+          if (src < nsplit) f[src] = ld_dsmem_f4(mapa_shared(a, (uint32_t)src));
+        float4 s4 = f[0];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 f = ld_dsmem_f4(ra + 16 * i);
-            a[4 * i] += f.x; a[4 * i + 1] += f.y; a[4 * i + 2] += f.z; a[4 * i + 3] += f.w;
-          }
-        }
-        if (m < p.M) {
-          if constexpr (SWIGLU) {
-            // columns 2i, 2i + 1: gate and up of output n_base + cc/2 + i
-            uint32_t h[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              float y[2];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const float g = a[2 * (i + k)], u = a[2 * (i + k) + 1];
-                y[k] = (ACT ? gelu_f(g) : __fdividef(g, 1.0f + __expf(-g))) * u;
-              }
-              const __half2 hy = __floats2half2_rn(y[0], y[1]);
-              h[i / 2] = *reinterpret_cast<const uint32_t*>(&hy);
-            }
-            const int n = n_base + cc / 2;   // 8 outputs; N % 8 == 0: all inside or all outside
-            if (n < p.N) *reinterpret_cast<uint4*>(p.y + (size_t)m * p.N + n) = make_uint4(h[0], h[1], h[2], h[3]);
-          } else {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t h[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const __half2 hy = __floats2half2_rn(a[8 * half + 2 * i], a[8 * half + 2 * i + 1]);
-                h[i] = *reinterpret_cast<const uint32_t*>(&hy);
-              }
-              const int n = n_base + cc + 8 * half;
-              if (n < p.N) *reinterpret_cast<uint4*>(p.y + (size_t)m * p.N + n) = make_uint4(h[0], h[1], h[2], h[3]);
-            }
+        for (int src = 1; src < 8; ++src)
+          if (src < nsplit) { s4.x += f[src].x; s4.y += f[src].y; s4.z += f[src].z; s4.w += f[src].w; }
+        if (m >= p.M) continue;
+        if constexpr (SWIGLU) {
+          // columns c, c + 1 (c + 2, c + 3): gate and up of one output
+          const int n = tile0 * Cfg::kOutRows + (rank * W + c) / 2;   // 2 outputs, n even
+          const float y0 = (ACT ? gelu_f(s4.x) : __fdividef(s4.x, 1.0f + __expf(-s4.x))) * s4.y;
+          const float y1 = (ACT ? gelu_f(s4.z) : __fdividef(s4.z, 1.0f + __expf(-s4.z))) * s4.w;
+          if (n < p.N) *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
+        } else {
+          const int n = tile0 * Cfg::kOutRows + rank * W + c;   // 4 outputs; N % 8 == 0: all in or all out
+          if (n < p.N) {
+            const __half2 h0 = __floats2half2_rn(s4.x, s4.y), h1 = __floats2half2_rn(s4.z, s4.w);
+            *reinterpret_cast<uint2*>(p.y + (size_t)m * p.N + n) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
           }
         }
       }

@@ -211,6 +211,40 @@ def test_tc_small_m_with_and_without_k_split(N):
     assert_close(Yl, oracle.gemm(X, Wg, synth.Q4_0, M, N, K), "small-M gemm N=%d" % N)
 
 
+@pytest.mark.parametrize("M", [40, 200, 600])
+def test_k_split_with_a_partial_last_stage(M):
+    # MLX4 with K % 256 == 128: the last packed stage of a row is half past
+    # the row end, and a K split must still cover every sub-step (both
+    # tensor-core kernels split K here: few output tiles).
+    K, N = 2176, 136
+    X = synth.activations(M, K, seed=90 + M)
+    W = synth.weights(synth.MLX4, N, K, seed=91, name="Wg")
+    Wu = synth.weights(synth.MLX4, N, K, seed=91, name="Wu")
+    rows = sample_rows(M)
+    Y = host(m.gemm(dev(X), dev(W), synth.MLX4, N, K))
+    assert_close(Y[rows], oracle.gemm(X, W, synth.MLX4, M, N, K, rows=rows), "split mlx4 gemm M=%d" % M)
+    Ys = host(m.swiglu(dev(X), dev(W), dev(Wu), synth.MLX4, N, K))
+    assert_close(Ys[rows], oracle.swiglu(X, W, Wu, synth.MLX4, M, N, K, rows=rows), "split mlx4 swiglu M=%d" % M)
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("M,N", [(300, 512), (1000, 136), (512, 2048)])
+def test_prefill_k_split_parity(codec, M, N):
+    # M > 128 with few 128-row output tiles: the prefill kernel splits K
+    # over a cluster per tile (GEMM and SwiGLU), against the oracle on
+    # sampled rows, every column.
+    K = 2048 if codec != synth.Q2_0 else 4096
+    X = synth.activations(M, K, seed=92 + M)
+    W = synth.weights(codec, N, K, seed=93, name="Wg")
+    Wu = synth.weights(codec, N, K, seed=93, name="Wu")
+    rows = sample_rows(M)
+    Y = host(m.gemm(dev(X), dev(W), codec, N, K))
+    assert_close(Y[rows], oracle.gemm(X, W, codec, M, N, K, rows=rows), "prefill split gemm M=%d N=%d" % (M, N))
+    Ys = host(m.swiglu(dev(X), dev(W), dev(Wu), codec, N, K))
+    assert_close(Ys[rows], oracle.swiglu(X, W, Wu, codec, M, N, K, rows=rows),
+                 "prefill split swiglu M=%d N=%d" % (M, N))
+
+
 def test_tc_tile_widths():
     # M large enough for 256- and 128-wide activation tiles on a full GPU.
     import torch
