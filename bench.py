@@ -826,7 +826,8 @@ def main(argv=None):
                     choices=["swiglu_m2048", "swiglu_m1", "swiglu_m64", "swiglu_mlx4_m2048", "swiglu_mlx4_m1",
                              "attn_prefill_q8_0", "attn_decode_q8_0", "attn_prefill_f16", "attn_decode_f16",
                              "gemm_q4_8192x2048_m2048", "gemm_q8_8192x2048_m2048", "gemm_q2_4096x4096_m1",
-                             "gemm_q2_4096x4096_m16", "gemm_q2_4096x4096_m2048"],
+                             "gemm_q2_4096x4096_m16", "gemm_q2_4096x4096_m2048", "gemm_q8_512x2048_m128",
+                             "gemm_q4_2048x8192_m128"],
                     help="only run 3 launches of one case (for ncu)")
     args = ap.parse_args(argv)
     if args.profile_case:
