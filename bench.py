@@ -371,7 +371,7 @@ def run_ours(args, ws, rank, local):
     # them is reported in its key (and on stderr) instead of losing the line.
     mlx4 = guarded(measure_mlx4, m, X, dev, steps=max(20, min(args.steps, 200)))
     attention = guarded(measure_attention, m, dev)
-    configs = None if args.no_configs else guarded(measure_configs, m, dev, peaks()[0], do_cpu)
+    configs = None if args.no_configs else guarded(measure_configs, m, dev, peaks()[0], do_cpu, (wgs[0], wus[0]))
 
     if rank != 0:
         return
@@ -489,7 +489,7 @@ def oracle_rate(kind, X, W, Wu, codec, M, N, K, threads, target_s=1.5):
             "kind": "oracle", "sample": "%d of %d activation rows, all %d outputs, %.2f s" % (len(rows), M, N, t)}
 
 
-def measure_configs(m, dev, pk, do_cpu):
+def measure_configs(m, dev, pk, do_cpu, c2w=None):
     """Every workload the pages' tables measure, one GPU: the tiny Q4_0 GEMM,
     the 1B projections in Q4_0 and Q8_0, the Q2_0 sweep over M, and the 1B
     layer set per projection and per layer at M in {1, 128, 512, 2048}.  Each
@@ -556,6 +556,15 @@ def measure_configs(m, dev, pk, do_cpu):
         if do_cpu:
             e["cpu_baseline"] = [oracle_rate("gemm", X1, W1, None, codec, M, N, K, 1),
                                  oracle_rate("gemm", X1, W1, None, codec, M, N, K, cpu_threads)]
+
+    # C2 over M: the 8B fused gate/up below the headline's M = 2048 (the
+    # GEMV for M <= 16, the small-M tcgen05 kernel up to 128, the prefill
+    # kernel above), on the headline's weights
+    if c2w is not None:
+        N2, K2 = 14336, 4096
+        for M in (1, 16, 64, 128, 512):
+            X2 = synth.activations(M, K2, seed=2)
+            entry("c2_8b_swiglu_q4_0_m%d" % M, "swiglu", synth.Q4_0, M, N2, K2, upload(X2), c2w[0], c2w[1])
 
     # C3: the Q2_0 ternary 4096 x 4096 over M
     N = K = 4096

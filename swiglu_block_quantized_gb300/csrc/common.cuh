@@ -53,6 +53,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// One arrival per warp: the lanes meet at a warp barrier first, so every
+// lane's earlier writes (and, after a proxy fence, its async-proxy-visible
+// shared-memory writes) are ordered before the arrival.  Barriers that a
+// whole warp signals count warps, not threads: per-thread arrivals on one
+// barrier serialize in shared memory.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),

@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(512, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SX; ++i) mbar_init(&x_full[i], 1);
-    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 256); }
-    for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 256);
+    for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 8); }
+    for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 8);
     for (int i = 0; i < 2; ++i) mbar_init(&pair_free[i], 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
     mbar_init(drain, 1);
@@ -286,11 +286,11 @@ __global__ void __launch_bounds__(512, 1)
                 make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
           }
           fence_proxy_async_smem();   // generic-proxy writes, read by the tensor core
-          mbar_arrive(&b_full[sb]);
+          mbar_arrive_warp(&b_full[sb]);
           ++ks;
           ++ks_g;
         }
-        if (ok) mbar_arrive(&w_empty[sp]);
+        if (ok) mbar_arrive_warp(&w_empty[sp]);
       }
     }
   } else if (warp >= 12 && nsplit > 1) {
