@@ -16,11 +16,16 @@
 //     blocks].  Independent rings; both run ahead across tile boundaries.
 //   * warp 1, one lane: issues tcgen05.mma (4 per 64-k sub-step), commits
 //     ring releases to mbarriers.  Warp 1 also owns the TMEM allocation.
+//     The A ring is handed over in pairs of sub-steps (64 columns): one
+//     a_full wait and one a_empty commit per pair.  Each handover costs the
+//     issuing thread a fixed time in which the tensor pipe runs dry, so
+//     halving their number gave 5% at the 8B shape (M = 2048) and 8% at
+//     M = 64.
 //   * warps 4..11, two decode warpgroups.  Thread r of a group owns weight
 //     row r = TMEM lane r; group g decodes weights [32g, 32g+32) of every
 //     64-k sub-step (codec.cuh) and writes them with tcgen05.st into a TMEM
-//     ring of A sub-tiles (32 columns each).  Each store completes while the
-//     thread decodes the next one.
+//     ring of A sub-tiles (32 columns each, taken in pairs): after the
+//     second store of a pair the thread waits for its stores and arrives.
 //   * warps 12..19, two epilogue warpgroups, each on half of the activation
 //     columns: tcgen05.ld of D (D is released to the next tile as soon as it
 //     is read), fp16 rounding or SiLU(g)*u, staging in shared memory and TMA
@@ -164,7 +169,11 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
   const int srow = SWIGLU ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;  // row in the W stage
   const KRange kr = k_range<S::SUB>(p);
   bool ok = true;
-  int pending = -1;  // A stage whose tcgen05.st is still in flight
+  // Pairs of sub-steps share one slot pair of 64 columns (PA of them);
+  // pairs start at the CTA's first sub-step of each tile, and the last
+  // pair of a tile holds one sub-step if the tile has an odd number.
+  constexpr int PA = SA / 2;
+  int pg = 0;                  // pairs stored so far
   int ks_g = 0, pk_g = 0;
   const DecK K = make_deck();
   for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep) {
@@ -199,21 +208,24 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
 #pragma unroll
       for (int j = 0; j < S::SUB; ++j) {
         if (ks >= kr.ks1) break;
-        const int sa = ks_g % SA;
-        if (ks_g >= SA) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&sm.a_empty[sa], ((ks_g / SA) - 1) & 1, ctl));
-          if (!ok) break;
-        }
-        tc_fence_after();
+        const int h = (ks - kr.ks0) & 1;
+        const int slot = pg % PA;
         uint32_t out[16];
         decode_half<C, G>(w, j, out, K);
-        if (pending >= 0) {
+        if (h == 0) {
+          if (pg >= PA) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.a_empty[slot], ((pg / PA) - 1) & 1, ctl));
+            if (!ok) break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(lane_addr + slot * 64 + h * 32, out);
+        if (h == 1 || ks + 1 == kr.ks1) {
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&sm.a_full[pending]);
+          mbar_arrive(&sm.a_full[slot]);
+          ++pg;
         }
-        tmem_st16(lane_addr + sa * 32, out);
-        pending = sa;
         ++ks;
         ++ks_g;
       }
@@ -221,11 +233,6 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
         if (ok) mbar_arrive(&sm.w_empty[pk_g % SW]);
       }
     }
-  }
-  if (pending >= 0) {
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&sm.a_full[pending]);
   }
 }
 
@@ -571,23 +578,45 @@ __global__ void __launch_bounds__(640, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, NX);
       int ks_g = 0, lt = 0;
+      constexpr int PA = SA / 2;
+      int pg = 0;
       bool ok = true;
       for (int tile = kr.tile0; tile < p.tiles && ok; tile += kr.tstep, ++lt) {
         // D must have been read out by the epilogue of the previous tile.
         if (lt > 0 && !mbar_wait(sm.d_empty, (lt - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = kr.ks0; ks < kr.ks1; ++ks, ++ks_g) {
-          const int sx = ks_g % SX, sa = ks_g % SA;
-          if (!mbar_wait(&sm.a_full[sa], (ks_g / SA) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(&sm.x_full[sx], (ks_g / SX) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(sm.xs + sx * Cfg::kXStage));
-          const uint32_t acol = tmem + Cfg::kACol0 + sa * 32;
+        for (int ks = kr.ks0; ks < kr.ks1; ks += 2) {
+          const int n = kr.ks1 - ks < 2 ? 1 : 2;
+          const int slot = pg % PA;
+          if (!mbar_wait(&sm.a_full[slot], (pg / PA) & 1, ctl)) { ok = false; break; }
+          // With four or more X stages both of the pair are waited for
+          // first, so its 8 MMAs issue back to back (5% at the 8B shape);
+          // a ring of three stages must not be held two at a time, so
+          // there each stage is waited for just before its MMAs.
+          if constexpr (SX >= 4) {
+            if (!mbar_wait(&sm.x_full[ks_g % SX], (ks_g / SX) & 1, ctl) ||
+                (n == 2 && !mbar_wait(&sm.x_full[(ks_g + 1) % SX], ((ks_g + 1) / SX) & 1, ctl))) {
+              ok = false;
+              break;
+            }
+          }
+          for (int h = 0; h < n; ++h) {
+            const int sx = (ks_g + h) % SX;
+            if constexpr (SX < 4) {
+              if (!mbar_wait(&sm.x_full[sx], ((ks_g + h) / SX) & 1, ctl)) { ok = false; break; }
+            }
+            tc_fence_after();
+            const uint64_t bdesc = sdesc_sw128_kmajor(smem_u32(sm.xs + sx * Cfg::kXStage));
+            const uint32_t acol = tmem + Cfg::kACol0 + slot * 64 + h * 32;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks != kr.ks0) | kk);
-          tc_commit(&sm.x_empty[sx]);
-          tc_commit(&sm.a_empty[sa]);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ts_f16(tmem, acol + kk * 8, bdesc + 2 * kk, idesc, (ks + h != kr.ks0) | kk);
+            tc_commit(&sm.x_empty[sx]);
+          }
+          if (!ok) break;
+          tc_commit(&sm.a_empty[slot]);
+          ks_g += n;
+          ++pg;
         }
         if (ok) tc_commit(sm.d_full);
       }

@@ -27,7 +27,9 @@
 //     columns).  The issue loop is the serial step of this kernel, so it
 //     takes two 64-k sub-steps at a time (8 MMAs) and frees both with one
 //     commit on a per-pair barrier that the X producer and the decode
-//     warps both wait on (X and B rings advance together, 2 pairs deep).
+//     warps both wait on (X and B rings advance together, 2 pairs deep);
+//     the X stages and decoded-B slots of a pair are likewise signalled on
+//     one barrier each, so the thread waits twice per 8 MMAs.
 //   warps 4..11, two decode groups: thread r of a group owns B row r and
 //     decodes weights [32 g, 32 g + 32) of each 64-k sub-step (codec.cuh,
 //     bit-exact) straight into the swizzled B ring in shared memory.
@@ -136,9 +138,9 @@ __global__ void __launch_bounds__(512, 1)
   bool split_ok = false;   // epilogue threads: this CTA's partial D is staged
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) mbar_init(&x_full[i], 1);
+    for (int i = 0; i < SX; ++i) mbar_init(&x_full[i], 1);   // [0], [1]: stage pairs
     for (int i = 0; i < SW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 8); }
-    for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 8);
+    for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 8);   // [0], [1]: slot pairs, one arrival per decode warp
     for (int i = 0; i < 2; ++i) mbar_init(&pair_free[i], 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
     mbar_init(drain, 1);
@@ -165,16 +167,21 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       for (int tile = tile0; tile < p.tiles && ok; tile += tstep) {
         for (int ks = ks0; ks < ks1; ++ks) {
+          // Stages 2p and 2p + 1 land on one barrier (the MMA thread takes
+          // them together); every CTA runs an even number of sub-steps here.
           const int sx = xi % SX;
-          if (xi >= SX && !mbar_wait_idle(&pair_free[sx >> 1], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(&x_full[sx], Cfg::kXStage);
-          tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx], ks * 64, 0);
+          if ((sx & 1) == 0) {
+            if (xi >= SX && !mbar_wait_idle(&pair_free[sx >> 1], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
+            mbar_arrive_expect_tx(&x_full[sx >> 1], 2 * Cfg::kXStage);
+          }
+          tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx >> 1], ks * 64, 0);
           ++xi;
         }
       }
       if (!ok) {
-        for (int i = (xi > SX ? xi - SX : 0); i < xi; ++i)
-          mbar_wait_drain(&x_full[i % SX], (i / SX) & 1, 100000000ull);
+        // (the loop stops only before the first stage of a pair)
+        for (int i = (xi > SX ? xi - SX : 0); i < xi; i += 2)
+          mbar_wait_drain(&x_full[(i % SX) >> 1], (i / SX) & 1, 100000000ull);
       }
     }
   } else if (warp == 2) {
@@ -217,9 +224,8 @@ __global__ void __launch_bounds__(512, 1)
         // split takes whole packed stages)
         for (int ks = ks0; ks < ks1; ks += 2, ks_g += 2) {
           const int s0 = ks_g % SX;   // slots s0, s0 + 1 of both rings (SX == SB)
-          if (!mbar_wait(&b_full[s0], (ks_g / SB) & 1, ctl) || !mbar_wait(&x_full[s0], (ks_g / SX) & 1, ctl) ||
-              !mbar_wait(&b_full[s0 + 1], (ks_g / SB) & 1, ctl) ||
-              !mbar_wait(&x_full[s0 + 1], (ks_g / SX) & 1, ctl)) {
+          if (!mbar_wait(&b_full[s0 >> 1], (ks_g / SB) & 1, ctl) ||
+              !mbar_wait(&x_full[s0 >> 1], (ks_g / SX) & 1, ctl)) {
             ok = false;
             break;
           }
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int j = 0; j < S::SUB; ++j) {
           if (ks >= ks1) break;
           const int sb = ks_g % SB;
-          if (ks_g >= SB) {
+          if (ks_g >= SB && (sb & 1) == 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(&pair_free[sb >> 1], ((ks_g / SB) - 1) & 1, ctl));
             if (!ok) break;
           }
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(512, 1)
                 make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
           }
           fence_proxy_async_smem();   // generic-proxy writes, read by the tensor core
-          mbar_arrive_warp(&b_full[sb]);
+          if (sb & 1) mbar_arrive_warp(&b_full[sb >> 1]);   // the pair's second slot is written
           ++ks;
           ++ks_g;
         }
