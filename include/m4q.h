@@ -87,7 +87,8 @@ enum m4q_status {
   M4Q_ERR_NONFINITE = -6,          /* m4q_check_finite found NaN/Inf */
   M4Q_ERR_TIMEOUT = -7,            /* a device pipeline wait gave up */
   M4Q_ERR_UNSUPPORTED_DEVICE = -8, /* the current device is not sm_103 */
-  M4Q_ERR_SCRATCH_LIMIT = -9       /* m4q_mlp_noalloc: M * F above its fixed scratch */
+  M4Q_ERR_SCRATCH_LIMIT = -9,      /* m4q_mlp_noalloc: M * F above its fixed scratch */
+  M4Q_ERR_BOUNDS = -10             /* bounds-checked build: an access was out of range */
 };
 
 /* Y = X * W^T.  Dispatch: M <= 16 takes the GEMV path, else the tcgen05
@@ -280,9 +281,25 @@ size_t m4q_weight_bytes(int codec, int64_t N, int64_t K);
 int m4q_check_finite(const void* x, int64_t n, m4q_stream_t stream);
 
 /* Synchronize `stream`, read and clear the current device's status word.
- * Returns M4Q_ERR_TIMEOUT if a kernel's bounded pipeline wait gave up since
- * the last check, M4Q_OK otherwise. */
+ * Returns M4Q_ERR_BOUNDS if, in a bounds-checked build, a kernel found an
+ * index out of range since the last check (the site stays readable through
+ * m4q_bounds_site until then), else M4Q_ERR_TIMEOUT if a kernel's bounded
+ * pipeline wait gave up, else M4Q_OK. */
 int m4q_check_device_status(m4q_stream_t stream);
+
+/* Bounds-checked build (compiled with -DM4Q_BOUNDS=1, for tests): every
+ * computed global access, every TMA coordinate and every computed
+ * shared-memory staging offset of the projection and attention kernels is
+ * tested against the extents the kernel was given before it is made; a
+ * failing access is skipped and reported (M4Q_ERR_BOUNDS above) instead of
+ * faulting.  m4q_build_flags() returns M4Q_BUILD_BOUNDS for such a build,
+ * 0 for the normal one.  m4q_bounds_site() synchronizes `stream` and returns
+ * the site number of the first failed check since the previous call (0: none;
+ * the numbers are listed in the library source), clearing it; it returns
+ * M4Q_ERR_CUDA (negative) if the status word cannot be read. */
+#define M4Q_BUILD_BOUNDS 1
+int m4q_build_flags(void);
+int m4q_bounds_site(m4q_stream_t stream);
 
 /* Self-test of the bounded wait: launches one block that waits on a barrier
  * nothing will complete, with a limit of `limit_ns` nanoseconds; the kernel

@@ -55,9 +55,12 @@ ERR_NONFINITE = -6
 ERR_TIMEOUT = -7
 ERR_UNSUPPORTED_DEVICE = -8
 ERR_SCRATCH_LIMIT = -9
+ERR_BOUNDS = -10
+BUILD_BOUNDS = 1
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libm4q.so")
+LIB_BOUNDS_PATH = os.path.join(HERE, "_build", "libm4q_bounds.so")   # bounds-checked build
 
 # Every symbol declared in include/m4q.h, with its ctypes signature.
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -82,6 +85,8 @@ SIGNATURES = {
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
     "m4q_check_device_status": (_i32, [_vp]),
+    "m4q_build_flags": (_i32, []),
+    "m4q_bounds_site": (_i32, [_vp]),
     "m4q_selftest_wait_timeout": (_i32, [_i64, _vp]),
     "m4q_status_string": (ctypes.c_char_p, [_i32]),
     "m4q_version": (_i32, []),
@@ -116,9 +121,9 @@ def load(path: str | None = None):
         return lib
 
 
-def build(force: bool = False) -> str:
+def build(force: bool = False, bounds: bool = False) -> str:
     from . import buildlib
-    return buildlib.build(force=force)
+    return buildlib.build(force=force, bounds=bounds)
 
 
 def status_string(code: int) -> str:
@@ -414,8 +419,22 @@ def check_finite(t, stream=None) -> bool:
 
 
 def check_device_status(stream=None) -> int:
-    """Synchronize and return (and clear) the device status: OK or ERR_TIMEOUT."""
+    """Synchronize and return (and clear) the device status: OK, ERR_BOUNDS or ERR_TIMEOUT."""
     return int(load().m4q_check_device_status(_stream_ptr(stream)))
+
+
+def build_flags() -> int:
+    """BUILD_BOUNDS for the bounds-checked build, else 0."""
+    return int(load().m4q_build_flags())
+
+
+def bounds_site(stream=None) -> int:
+    """Synchronize and return (and clear) the site of the first failed bounds
+    check (0: none; bounds-checked build only)."""
+    rc = int(load().m4q_bounds_site(_stream_ptr(stream)))
+    if rc < 0:
+        _check(rc, "m4q_bounds_site")
+    return rc
 
 
 def selftest_wait_timeout(limit_ns: int, stream=None):

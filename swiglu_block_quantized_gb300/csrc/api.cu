@@ -605,6 +605,8 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   p.rtiles = a.rtiles;
   p.nsplit = a.nsplit;
   p.tsplit = a.tsplit;
+  p.status = m4q::status_words();
+  if (!p.status) return M4Q_ERR_CUDA;
   if (a.nsplit > 1) {
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
@@ -640,9 +642,29 @@ int m4q_check_device_status(m4q_stream_t stream) {
     return M4Q_ERR_CUDA;
   if (st) {
     if (cudaMemset(words, 0, sizeof(uint32_t)) != cudaSuccess) return M4Q_ERR_CUDA;
-    return M4Q_ERR_TIMEOUT;
+    return (st & m4q::kErrBoundsBit) ? M4Q_ERR_BOUNDS : M4Q_ERR_TIMEOUT;
   }
   return M4Q_OK;
+}
+
+int m4q_build_flags(void) {
+#if M4Q_BOUNDS
+  return M4Q_BUILD_BOUNDS;
+#else
+  return 0;
+#endif
+}
+
+int m4q_bounds_site(m4q_stream_t stream) {
+  uint32_t* words = m4q::status_words();
+  if (!words) return M4Q_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t site = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(&site, words + 2, sizeof(site), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(words + 2, 0, sizeof(uint32_t)) != cudaSuccess)
+    return M4Q_ERR_CUDA;
+  return (int)site;
 }
 
 int m4q_selftest_wait_timeout(int64_t limit_ns, m4q_stream_t stream) {
@@ -667,6 +689,7 @@ const char* m4q_status_string(int status) {
     case M4Q_ERR_TIMEOUT: return "a device pipeline wait gave up";
     case M4Q_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
     case M4Q_ERR_SCRATCH_LIMIT: return "M * F exceeds the fixed scratch of m4q_mlp_noalloc (1 << 20 fp16)";
+    case M4Q_ERR_BOUNDS: return "an access was out of range (bounds-checked build)";
     default: return "unknown status";
   }
 }

@@ -94,9 +94,14 @@ struct AttnCfg {
 // multiples).
 template <int D, bool Q8>
 __device__ __forceinline__ void issue_tile(uint8_t* kdst, uint8_t* vdst, const uint8_t* khead,
-                                           const uint8_t* vhead, int k0, int T, bool vec16) {
+                                           const uint8_t* vhead, int k0, int T, bool vec16, uint32_t* status) {
   using Cfg = AttnCfg<D, Q8>;
   const int rows = min(kKeys, T - k0);
+  // keys [k0, k0 + rows) of the head, and whole 16-byte copies when vec16
+  if (!in_bounds(k0 >= 0 && rows >= 1 && (!vec16 || (rows * Cfg::kRowBytes) % 16 == 0), status, kSiteAttnKV)) {
+    cp_async_commit();
+    return;
+  }
   const uint8_t* ks = khead + (long long)k0 * Cfg::kRowBytes;
   const uint8_t* vs = vhead + (long long)k0 * Cfg::kRowBytes;
   if constexpr (Q8) {
@@ -232,8 +237,9 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
     for (int h2 = 0; h2 < 2; ++h2) {
       const uint32_t* qrow =
           reinterpret_cast<const uint32_t*>(p.q + ((long long)qh[h2] * p.M + qi[h2]) * D + 16 * kk + 2 * t);
-      qa[kk][h2] = rok[h2] ? __ldg(qrow) : 0u;
-      qa[kk][2 + h2] = rok[h2] ? __ldg(qrow + 4) : 0u;
+      const bool qok = rok[h2] && in_bounds(qh[h2] < p.H && qi[h2] < p.M, p.status, kSiteAttnQ);
+      qa[kk][h2] = qok ? __ldg(qrow) : 0u;
+      qa[kk][2 + h2] = qok ? __ldg(qrow + 4) : 0u;
     }
 
   float o[DN][4];
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   // K at 2 s * kTile, V at (2 s + 1) * kTile
   constexpr int kStage = Q8 ? Cfg::kRaw : Cfg::kTile;
   uint8_t* dec = smem + 4 * Cfg::kRaw;   // Q8_0: decoded K, then V
-  if (kbeg < kend) issue_tile<D, Q8>(smem, smem + kStage, khead, vhead, kbeg, p.T, p.kv_vec16);
+  if (kbeg < kend) issue_tile<D, Q8>(smem, smem + kStage, khead, vhead, kbeg, p.T, p.kv_vec16, p.status);
   int it = 0;
   for (int k0 = kbeg; k0 < kend; k0 += kKeys, ++it) {
     const int st = it & 1;
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
     __syncthreads();   // this tile has landed; every warp is done with the previous one
     if (k0 + kKeys < kend)
       issue_tile<D, Q8>(smem + 2 * (st ^ 1) * kStage, smem + (2 * (st ^ 1) + 1) * kStage, khead, vhead,
-                        k0 + kKeys, p.T, p.kv_vec16);
+                        k0 + kKeys, p.T, p.kv_vec16, p.status);
     const uint8_t* Kt;
     const uint8_t* Vt;
     if constexpr (Q8) {
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
       acc[e] = a;
     }
     if (p.nsplit == 1) {
-      if (r < R) {
+      if (r < R && in_bounds(hk * p.G + r % p.G < p.H, p.status, kSiteAttnO)) {
         const float inv = L > 0.f ? 1.f / L : 0.f;
         __half* orow = p.o + (long long)(r / p.G) * p.H * D + (long long)(hk * p.G + r % p.G) * D + seg * SEG;
 #pragma unroll
@@ -395,6 +401,9 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
       }
     } else {
       const long long slot = ((long long)split * p.Hkv + hk) * ((long long)p.rtiles * kRows) + r;
+      if (!in_bounds(split < p.nsplit && slot < (long long)p.nsplit * p.Hkv * p.rtiles * kRows, p.status,
+                     kSiteAttnWs))
+        return;
 #pragma unroll
       for (int e = 0; e < SEG; e += 2)
         *reinterpret_cast<float2*>(p.ws_o + slot * D + seg * SEG + e) = make_float2(acc[e], acc[e + 1]);
@@ -405,7 +414,7 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   if (p.nsplit == 1) {
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
-      if (!rok[h2]) continue;
+      if (!rok[h2] || !in_bounds(qi[h2] < p.M && qh[h2] < p.H, p.status, kSiteAttnO)) continue;
       const float inv = lrow[h2] > 0.f ? 1.f / lrow[h2] : 0.f;
       __half* orow = p.o + (long long)qi[h2] * p.H * D + (long long)qh[h2] * D;
 #pragma unroll
@@ -419,6 +428,7 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
     for (int h2 = 0; h2 < 2; ++h2) {
       const long long r = (long long)rt * kRows + wrow + g + 8 * h2;
       const long long slot = ((long long)split * p.Hkv + hk) * rows_pad + r;
+      if (!in_bounds(split < p.nsplit && r < rows_pad, p.status, kSiteAttnWs)) continue;
       float* wrow = p.ws_o + slot * D;
 #pragma unroll
       for (int dn = 0; dn < DN; ++dn)
@@ -475,6 +485,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
     for (int w = 0; w < 8; ++w) L += red_l[w];
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int i = r / p.G, h = hk * p.G + r % p.G;
+    if (!in_bounds(i < p.M && h < p.H, p.status, kSiteAttnO)) return;
     __half* orow = p.o + (long long)i * p.H * D + (long long)h * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {

@@ -11,12 +11,70 @@ namespace m4q {
 // Codec ids (same values as enum m4q_codec in include/m4q.h).
 enum : int { kQ4_0 = 0, kQ8_0 = 1, kQ2_0 = 2, kMLX4 = 3 };
 
-// Status-word bits written by kernels whose bounded waits gave up.
-enum : uint32_t { kErrWaitTimeout = 1u, kErrAborted = 2u };
+// Status-word bits: a bounded wait gave up; a bounds check failed (only in
+// the bounds-checked build, below).
+enum : uint32_t { kErrWaitTimeout = 1u, kErrAborted = 2u, kErrBounds = 4u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// ------------------------------------------------------------------ bounds
+//
+// The bounds-checked build (-DM4Q_BOUNDS=1) tests each computed global
+// access, each TMA coordinate and each computed shared-memory staging offset
+// against the extents the kernel knows, before making the access.  A failed
+// test sets kErrBounds in status word 0, records its site number in word 2
+// (the first failure only) and the access is skipped, so a wrong index is
+// reported instead of faulting.  (A skipped copy leaves its barrier short:
+// the bounded wait behind it then gives up and is reported as well.)  In the
+// normal build every test is the constant true.
+#ifndef M4Q_BOUNDS
+#define M4Q_BOUNDS 0
+#endif
+
+enum : uint32_t {
+  kSiteGemvW = 1,        // GEMV: bulk copy of a weight row pair
+  kSiteGemvWHalf = 2,    // GEMV: 2-byte weight copy into the ring
+  kSiteGemvX = 3,        // GEMV: activation fragment load
+  kSiteGemvY = 4,        // GEMV: output store
+  kSiteTcX = 5,          // tcgen05 kernels: X tile coordinates
+  kSiteTcW = 6,          // tcgen05 kernels: packed-W tile coordinates
+  kSiteTcY = 7,          // tcgen05 kernels: Y tile coordinates
+  kSiteTcWRow = 8,       // tcgen05 kernels: packed row read from the W ring
+  kSiteTcStage = 9,      // tcgen05 kernels: Y staging offset
+  kSiteTcSplitSlot = 10, // K split: staged partial offset
+  kSiteTcSplitY = 11,    // K split: output store
+  kSiteTcBRing = 12,     // small-M kernel: decoded-B ring offset
+  kSiteAttnQ = 20,       // attention: Q fragment load
+  kSiteAttnKV = 21,      // attention: K/V tile copy
+  kSiteAttnO = 22,       // attention: output store
+  kSiteAttnWs = 23,      // attention: key-split workspace
+};
+
+__device__ __forceinline__ bool in_bounds(bool cond, uint32_t* status, uint32_t site) {
+#if M4Q_BOUNDS
+  if (!cond) {
+    atomicOr(status, kErrBounds);
+    atomicCAS(status + 2, 0u, site);
+  }
+  return cond;
+#else
+  (void)status;
+  (void)site;
+  return true;
+#endif
+}
+
+// [off, off + bytes) inside [0, size)
+__device__ __forceinline__ bool span_ok(long long off, long long bytes, long long size) {
+  return off >= 0 && bytes >= 0 && off + bytes <= size;
+}
+
+// A tiled TMA copy starts on a 16-byte boundary: the innermost coordinate
+// times the element size is a multiple of 16; no coordinate of a store may
+// be negative.
+__device__ __forceinline__ bool tma_x_ok(int x, int elem_bytes) { return x >= 0 && (x * elem_bytes) % 16 == 0; }
 
 // First byte of `base` (dynamic shared memory) aligned to `A` bytes.  The
 // pointer is advanced, not rebuilt from an integer, so the compiler still

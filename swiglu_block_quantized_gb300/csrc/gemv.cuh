@@ -137,7 +137,8 @@ __device__ __forceinline__ void load_xfrag(const GemvParams& p, int g, int t, in
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const int m = g + 8 * mt;
-    const bool ok = m < p.M;
+    constexpr int kSpan = C == kQ2_0 ? 128 : 32;   // k values of one block
+    const bool ok = m < p.M && in_bounds(kb + kSpan <= p.K, p.status, kSiteGemvX);
     const __half* xr = p.x + (size_t)(ok ? m : 0) * p.K + kb;
     if constexpr (C == kQ4_0) {
       ldx<8>(&xf[mt][0], xr + 4 * t, ok);
@@ -395,7 +396,10 @@ __global__ void __launch_bounds__(GemvCfg<C, MT>::kThreads, 1) gemv_kernel(const
             }
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * bytes * pairs);
             __syncwarp();
-            if (mine) {
+            if (mine && in_bounds(n + 1 < p.N && span_ok(off, bytes, p.row_bytes) &&
+                                      span_ok((long long)lane * p.pp, (long long)p.sb + bytes, stage_bytes) &&
+                                      (p.nst > 1 || (long long)bytes == p.sb),
+                                  p.status, kSiteGemvW)) {
               const uint8_t* src = (mat ? p.w1 : p.w0) + (long long)n * p.row_bytes + off;
               uint8_t* dst = ring + slot * stage_bytes + lane * p.pp;
               if (p.nst == 1) {
@@ -441,7 +445,9 @@ __global__ void __launch_bounds__(GemvCfg<C, MT>::kThreads, 1) gemv_kernel(const
               unsigned short v = 0;
               if (n < p.N && o < p.row_bytes)
                 v = __ldg(reinterpret_cast<const unsigned short*>(base + (long long)n * p.row_bytes + o));
-              *reinterpret_cast<unsigned short*>(dst + gg * p.pp + hi * p.sb + 2 * c2) = v;
+              if (in_bounds(span_ok((long long)gg * p.pp + hi * p.sb + 2 * c2, 2, stage_bytes), p.status,
+                            kSiteGemvWHalf))
+                *reinterpret_cast<unsigned short*>(dst + gg * p.pp + hi * p.sb + 2 * c2) = v;
             }
             mbar_arrive(&full[slot]);
           }
@@ -463,7 +469,8 @@ __global__ void __launch_bounds__(GemvCfg<C, MT>::kThreads, 1) gemv_kernel(const
     uint32_t xh[XH ? Cfg::kXH : 1][4];
     if constexpr (XH) {
       static_assert(MT == 1 && C != kQ2_0, "resident activations: one n8 tile, 32-weight blocks");
-      const bool ok_m = g < p.M;   // activation row g is the fragment column
+      const bool ok_m = g < p.M &&  // activation row g is the fragment column
+                        in_bounds(p.sb == (int)p.row_bytes && bps * S::B == p.K, p.status, kSiteGemvX);
       const unsigned short* xrow = reinterpret_cast<const unsigned short*>(p.x) + (size_t)(ok_m ? g : 0) * p.K;
 #pragma unroll
       for (int j = 0; j < Cfg::kXH; ++j) {
@@ -635,7 +642,8 @@ __global__ void __launch_bounds__(GemvCfg<C, MT>::kThreads, 1) gemv_kernel(const
             // outputs n, n + 1 (same head: n is even and head_dim is too)
             const size_t off = p.head_dim == 0 ? (size_t)m * p.N + n
                                                : ((size_t)(n / p.head_dim) * p.M + m) * p.head_dim + n % p.head_dim;
-            *reinterpret_cast<__half2*>(p.y + off) = __floats2half2_rn(a, b);
+            if (in_bounds(off + 2 <= (size_t)p.M * p.N && (n + 1 < p.N), p.status, kSiteGemvY))
+              *reinterpret_cast<__half2*>(p.y + off) = __floats2half2_rn(a, b);
           }
       }
     }

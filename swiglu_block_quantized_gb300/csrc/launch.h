@@ -115,11 +115,18 @@ struct AttnParams {
   int rtiles;             // ceil(M * G / 64) row tiles per KV head
   int nsplit, tsplit;     // key splits and keys per split (a multiple of 64)
   bool kv_vec16;          // every K/V tile start and T * kv_row_bytes are 16-byte aligned
+  uint32_t* status;       // device status word (bounds-checked build)
 };
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 
 // misc.cu
-uint32_t* status_words();  // [0] wait status, [1] non-finite flag; per current device
+// Status bit of a failed bounds check (the kernels' kErrBounds), and the
+// bounds-checked build switch (-DM4Q_BOUNDS=1).
+constexpr uint32_t kErrBoundsBit = 4u;
+#ifndef M4Q_BOUNDS
+#define M4Q_BOUNDS 0
+#endif
+uint32_t* status_words();  // [0] wait/bounds status, [1] non-finite flag, [2] first bounds site; per current device
 cudaError_t launch_dequant(int codec, const void* w, int N, int K, long long row_bytes, void* out,
                            cudaStream_t s);
 cudaError_t launch_finite_check(const void* x, long long n, uint32_t* flag, cudaStream_t s);

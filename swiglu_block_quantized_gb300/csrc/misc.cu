@@ -7,8 +7,10 @@
 
 namespace m4q {
 
-// [0]: bits set by kernels whose bounded waits gave up; [1]: non-finite flag.
-__device__ uint32_t g_status_words[2];
+// [0]: bits set by kernels whose bounded waits gave up (or, in the
+// bounds-checked build, whose bounds check failed); [1]: non-finite flag;
+// [2]: site of the first failed bounds check (0: none); [3]: unused.
+__device__ uint32_t g_status_words[4];
 
 uint32_t* status_words() {
   static std::mutex mu;

@@ -194,9 +194,10 @@ __device__ __forceinline__ void decode_role(const TcSmem& sm, const TcParams& p,
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.w_full[sp], (pk_g / SW) & 1, ctl));
         if (!ok) break;
         const uint4* src = reinterpret_cast<const uint4*>(sm.ws + sp * Cfg::kWStage + srow * S::KPB);
+        const bool rok = in_bounds(span_ok((long long)srow * S::KPB, S::KPB, Cfg::kWStage), p.status, kSiteTcWRow);
 #pragma unroll
         for (int i = 0; i < S::KPB / 16; ++i) {
-          const uint4 v = src[i];
+          const uint4 v = rok ? src[i] : make_uint4(0, 0, 0, 0);
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
         // Released after the sub-steps below have used the words (an
@@ -306,6 +307,7 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
         for (int k = 0; k < 8; ++k) {
           const uint32_t w = y2[ch][k];
           const int m = 32 * ch + 4 * k + odd;  // columns 2jj + odd for jj = 2k, 2k + 1
+          if (!in_bounds(span_ok((long long)m * 32, 3 * 32, Cfg::kYSlab), p.status, kSiteTcStage)) continue;
           __half* row0 = reinterpret_cast<__half*>(slab + m * 32);
           __half* row1 = reinterpret_cast<__half*>(slab + (m + 2) * 32);
           row0[lane >> 1] = __ushort_as_half((unsigned short)(w & 0xFFFFu));
@@ -314,7 +316,8 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tm_y, slab, n0 + 16 * q, m0 + c_begin);
+        if (in_bounds(tma_x_ok(n0 + 16 * q, 2) && m0 + c_begin >= 0, p.status, kSiteTcY))
+          tma_store_2d(tm_y, slab, n0 + 16 * q, m0 + c_begin);
         bulk_commit();
       }
     }
@@ -354,10 +357,14 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
           const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
           const __half2 h = odd ? __floats2half2_rn(recv, b) : __floats2half2_rn(a, recv);
           if constexpr (HD == 0) {
-            *reinterpret_cast<__half2*>(stg + (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2) = h;
+            const int o = (j + odd) * (Cfg::kOutRows * 2) + (r - odd) * 2;
+            if (in_bounds(span_ok(o, 4, Cfg::kYStage), p.status, kSiteTcStage))
+              *reinterpret_cast<__half2*>(stg + o) = h;
           } else {  // [head][32 m][HD]: n and n+1 are in the same head
             const int nl = r - odd;
-            *reinterpret_cast<__half2*>(stg + ((nl / HD) * 32 + j + odd) * (HD * 2) + (nl % HD) * 2) = h;
+            const int o = ((nl / HD) * 32 + j + odd) * (HD * 2) + (nl % HD) * 2;
+            if (in_bounds(span_ok(o, 4, Cfg::kYStage), p.status, kSiteTcStage))
+              *reinterpret_cast<__half2*>(stg + o) = h;
           }
         }
       } else {
@@ -370,15 +377,18 @@ __device__ __forceinline__ void epilogue_role(const TcSmem& sm, const TcParams& 
           const float g = odd ? recv : a;
           const float u = odd ? b : recv;
           const float y = __fdividef(g, 1.0f + __expf(-g)) * u;
-          *reinterpret_cast<__half*>(stg + (2 * jj + odd) * (Cfg::kOutRows * 2) + (r >> 1) * 2) =
-              __float2half_rn(y);
+          const int o = (2 * jj + odd) * (Cfg::kOutRows * 2) + (r >> 1) * 2;
+          if (in_bounds(span_ok(o, 2, Cfg::kYStage), p.status, kSiteTcStage))
+            *reinterpret_cast<__half*>(stg + o) = __float2half_rn(y);
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       if (leader) {
-        if constexpr (HD == 0) tma_store_2d(tm_y, stg, n0, m0 + c0);
-        else tma_store_3d(tm_y, stg, 0, m0 + c0, n0 / HD);
+        if (in_bounds(tma_x_ok(n0, 2) && m0 + c0 >= 0, p.status, kSiteTcY)) {
+          if constexpr (HD == 0) tma_store_2d(tm_y, stg, n0, m0 + c0);
+          else tma_store_3d(tm_y, stg, 0, m0 + c0, n0 / HD);
+        }
         bulk_commit();
       }
       ++it;
@@ -420,7 +430,9 @@ __device__ __forceinline__ bool split_stage_role(const TcSmem& sm, const TcParam
     uint32_t v[32];
     tmem_ld32_wait(tmem + lane_base + c0, v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) stg[split_slot(r, c0 + i, W)] = __uint_as_float(v[i]);
+    for (int i = 0; i < 32; ++i)
+      if (in_bounds(split_slot(r, c0 + i, W) < Cfg::kSX * Cfg::kXStage / 4, p.status, kSiteTcSplitSlot))
+        stg[split_slot(r, c0 + i, W)] = __uint_as_float(v[i]);
   }
   tc_fence_before();
   return true;
@@ -442,6 +454,9 @@ __device__ __forceinline__ void split_reduce_role(const TcSmem& sm, const TcPara
   for (int e = t; e < 32 * W; e += 256) {
     const int c = e >> 5, r = 4 * (e & 31);      // column c, weight rows r .. r + 3
     const uint32_t a = slice + 4u * (uint32_t)(c * 128 + r);
+    if (!in_bounds(span_ok(4ll * ((kr.rank * W + c) * 128 + r), 16, (long long)Cfg::kSX * Cfg::kXStage), p.status,
+                   kSiteTcSplitSlot))
+      continue;
     float4 f[8];
 #pragma unroll
     for (int src = 0; src < 8; ++src)
@@ -456,10 +471,11 @@ __device__ __forceinline__ void split_reduce_role(const TcSmem& sm, const TcPara
       const int n = n0 + r / 2;                  // 2 outputs, n even
       const float y0 = (ACT ? gelu_f(s4.x) : __fdividef(s4.x, 1.0f + __expf(-s4.x))) * s4.y;
       const float y1 = (ACT ? gelu_f(s4.z) : __fdividef(s4.z, 1.0f + __expf(-s4.z))) * s4.w;
-      if (n < p.N) *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
+      if (n < p.N && in_bounds(n + 2 <= p.N, p.status, kSiteTcSplitY))
+        *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
     } else {
       const int n = n0 + r;                      // 4 outputs; N % 8 == 0: all in or all out
-      if (n < p.N) {
+      if (n < p.N && in_bounds(n + 4 <= p.N, p.status, kSiteTcSplitY)) {
         const __half2 h0 = __floats2half2_rn(s4.x, s4.y), h1 = __floats2half2_rn(s4.z, s4.w);
         *reinterpret_cast<uint2*>(p.y + (size_t)m * p.N + n) =
             make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
@@ -536,7 +552,8 @@ __global__ void __launch_bounds__(640, 1)
           const int sx = xi % SX;
           if (xi >= SX && !mbar_wait_idle(&sm.x_empty[sx], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.x_full[sx], Cfg::kXStage);
-          tma_load_2d(sm.xs + sx * Cfg::kXStage, &tm_x, &sm.x_full[sx], ks * 64, m0);
+          if (in_bounds(tma_x_ok(ks * 64, 2) && m0 >= 0, p.status, kSiteTcX))
+            tma_load_2d(sm.xs + sx * Cfg::kXStage, &tm_x, &sm.x_full[sx], ks * 64, m0);
           ++xi;
         }
       }
@@ -562,8 +579,10 @@ __global__ void __launch_bounds__(640, 1)
             mbar_arrive_expect_tx(&sm.w_full[sp], Cfg::kWStage);
             uint8_t* dst = sm.ws + sp * Cfg::kWStage;
             const int xc = pk * (S::KPB / 2);  // uint16 elements
-            tma_load_2d(dst, &tm_w0, &sm.w_full[sp], xc, n0);
-            if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &sm.w_full[sp], xc, n0);
+            if (in_bounds(tma_x_ok(xc, 2) && 2ll * xc < p.row_bytes && n0 >= 0, p.status, kSiteTcW)) {
+              tma_load_2d(dst, &tm_w0, &sm.w_full[sp], xc, n0);
+              if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &sm.w_full[sp], xc, n0);
+            }
             ++wi;
           }
         }

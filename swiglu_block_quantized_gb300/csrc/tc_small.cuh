@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(512, 1)
             if (xi >= SX && !mbar_wait_idle(&pair_free[sx >> 1], ((xi / SX) - 1) & 1, ctl)) { ok = false; break; }
             mbar_arrive_expect_tx(&x_full[sx >> 1], 2 * Cfg::kXStage);
           }
-          tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx >> 1], ks * 64, 0);
+          if (in_bounds(tma_x_ok(ks * 64, 2), p.status, kSiteTcX))
+            tma_load_2d(xs + sx * Cfg::kXStage, &tm_x, &x_full[sx >> 1], ks * 64, 0);
           ++xi;
         }
       }
@@ -199,8 +200,10 @@ __global__ void __launch_bounds__(512, 1)
           mbar_arrive_expect_tx(&w_full[sp], Cfg::kWStage);
           uint8_t* dst = ws + sp * Cfg::kWStage;
           const int xc = pk * (S::KPB / 2);  // uint16 elements
-          tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
-          if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
+          if (in_bounds(tma_x_ok(xc, 2) && 2ll * xc < p.row_bytes && n0 >= 0, p.status, kSiteTcW)) {
+            tma_load_2d(dst, &tm_w0, &w_full[sp], xc, n0);
+            if (SWIGLU) tma_load_2d(dst + 64 * S::KPB, &tm_w1, &w_full[sp], xc, n0);
+          }
           ++wi;
         }
       }
@@ -263,9 +266,10 @@ __global__ void __launch_bounds__(512, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sp], (pk_g / SW) & 1, ctl));
         if (!ok) break;
         const uint4* src = reinterpret_cast<const uint4*>(ws + sp * Cfg::kWStage + srow * S::KPB);
+        const bool rok = in_bounds(span_ok((long long)srow * S::KPB, S::KPB, Cfg::kWStage), p.status, kSiteTcWRow);
 #pragma unroll
         for (int i = 0; i < S::KPB / 16; ++i) {
-          const uint4 v = src[i];
+          const uint4 v = rok ? src[i] : make_uint4(0, 0, 0, 0);
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
         // The slot is released only after the loop below has used every
@@ -288,8 +292,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = 4 * G + q;
-            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
-                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+            if (in_bounds(span_ok((long long)r * 128 + ((c ^ (r & 7)) << 4), 16, Cfg::kBStage), p.status,
+                          kSiteTcBRing))
+              *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                  make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
           }
           fence_proxy_async_smem();   // generic-proxy writes, read by the tensor core
           if (sb & 1) mbar_arrive_warp(&b_full[sb >> 1]);   // the pair's second slot is written
@@ -317,9 +323,12 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld32_wait(tmem + lane_base + 32 * ch, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(stg + small_split_slot(m, 32 * ch + 4 * i, W)) =
-              make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                          __uint_as_float(v[4 * i + 3]));
+          if (in_bounds(span_ok(4ll * small_split_slot(m, 32 * ch + 4 * i, W), 16,
+                                (long long)SX * Cfg::kXStage + Cfg::kXPad + SB * Cfg::kBStage),
+                        p.status, kSiteTcSplitSlot))
+            *reinterpret_cast<float4*>(stg + small_split_slot(m, 32 * ch + 4 * i, W)) =
+                make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
       }
       tc_fence_before();
     }
@@ -373,8 +382,11 @@ __global__ void __launch_bounds__(512, 1)
         for (int k = 0; k < NW / 4; ++k) {
           const int c = (NW / 4) * ch + k;          // 16-byte chunk of this row's outputs
           uint8_t* box = ys + (c >> 3) * (128 * 128);
-          *reinterpret_cast<uint4*>(box + m * 128 + (((c & 7) ^ (m & 7)) << 4)) =
-              make_uint4(y2[4 * k], y2[4 * k + 1], y2[4 * k + 2], y2[4 * k + 3]);
+          if (in_bounds(span_ok((long long)(c >> 3) * (128 * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4), 16,
+                                Cfg::kYBytes),
+                        p.status, kSiteTcStage))
+            *reinterpret_cast<uint4*>(box + m * 128 + (((c & 7) ^ (m & 7)) << 4)) =
+                make_uint4(y2[4 * k], y2[4 * k + 1], y2[4 * k + 2], y2[4 * k + 3]);
         }
       }
       // Every column of D has been read: the buffer may take tile lt + 2.
@@ -385,7 +397,9 @@ __global__ void __launch_bounds__(512, 1)
       named_bar_sync(1, 128);
       if (leader) {
 #pragma unroll
-        for (int b = 0; b < Cfg::kOutRows / 64; ++b) tma_store_2d(&tm_y, ys + b * (128 * 128), n0 + 64 * b, 0);
+        for (int b = 0; b < Cfg::kOutRows / 64; ++b)
+          if (in_bounds(tma_x_ok(n0 + 64 * b, 2), p.status, kSiteTcY))
+            tma_store_2d(&tm_y, ys + b * (128 * 128), n0 + 64 * b, 0);
         bulk_commit();
       }
     }
@@ -407,6 +421,10 @@ __global__ void __launch_bounds__(512, 1)
       for (int e = t; e < 128 * Q; e += 128) {
         const int m = e / Q, c = 4 * (e % Q);
         const uint32_t a = slice + 4u * (uint32_t)(m * (W + 4) + c);
+        if (!in_bounds(span_ok(4ll * (rank * 128 * (W + 4) + m * (W + 4) + c), 16,
+                               (long long)SX * Cfg::kXStage + Cfg::kXPad + SB * Cfg::kBStage),
+                       p.status, kSiteTcSplitSlot))
+          continue;
         float4 f[8];
 #pragma unroll
         for (int src = 0; src < 8; ++src)
@@ -421,10 +439,11 @@ __global__ void __launch_bounds__(512, 1)
           const int n = tile0 * Cfg::kOutRows + (rank * W + c) / 2;   // 2 outputs, n even
           const float y0 = (ACT ? gelu_f(s4.x) : __fdividef(s4.x, 1.0f + __expf(-s4.x))) * s4.y;
           const float y1 = (ACT ? gelu_f(s4.z) : __fdividef(s4.z, 1.0f + __expf(-s4.z))) * s4.w;
-          if (n < p.N) *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
+          if (n < p.N && in_bounds(n + 2 <= p.N, p.status, kSiteTcSplitY))
+            *reinterpret_cast<__half2*>(p.y + (size_t)m * p.N + n) = __floats2half2_rn(y0, y1);
         } else {
           const int n = tile0 * Cfg::kOutRows + rank * W + c;   // 4 outputs; N % 8 == 0: all in or all out
-          if (n < p.N) {
+          if (n < p.N && in_bounds(n + 4 <= p.N, p.status, kSiteTcSplitY)) {
             const __half2 h0 = __floats2half2_rn(s4.x, s4.y), h1 = __floats2half2_rn(s4.z, s4.w);
             *reinterpret_cast<uint2*>(p.y + (size_t)m * p.N + n) =
                 make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));

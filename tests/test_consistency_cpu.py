@@ -34,6 +34,7 @@ def test_header_enums_match_the_binding():
         "M4Q_ERR_MISALIGNED": m.ERR_MISALIGNED, "M4Q_ERR_CUDA": m.ERR_CUDA,
         "M4Q_ERR_NONFINITE": m.ERR_NONFINITE, "M4Q_ERR_TIMEOUT": m.ERR_TIMEOUT,
         "M4Q_ERR_UNSUPPORTED_DEVICE": m.ERR_UNSUPPORTED_DEVICE, "M4Q_ERR_SCRATCH_LIMIT": m.ERR_SCRATCH_LIMIT,
+        "M4Q_ERR_BOUNDS": m.ERR_BOUNDS,
     }
     assert set(pairs) == set(e), sorted(set(pairs) ^ set(e))
     for name, v in pairs.items():
