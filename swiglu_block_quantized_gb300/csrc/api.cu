@@ -259,7 +259,7 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
     L.sms = dev.sms;
     e = m4q::launch_gemv(codec, L);
   } else {
-    // Widest activation tile that still gives every SM a tile.
+    // Output tiles along N (64 outputs per tile for the gated projections).
     const int64_t out_rows = swiglu ? 64 : 128;
     const int64_t ntiles = (N + out_rows - 1) / out_rows;
     // M <= 128 with TMA-able rows and row-major output: the small-M kernel
@@ -282,21 +282,31 @@ int project(const void* X, const void* W0, const void* W1, int codec, int64_t M,
       while (L.split > 1 && (npk % L.split != 0 || tiles * L.split > dev.sms)) L.split /= 2;
     } else if (!L.wtma) {
       nx = 128;
-    } else if (((M + 255) / 256) * ntiles >= dev.sms) {
-      nx = 256;
-    } else if (((M + 127) / 128) * ntiles >= dev.sms) {
-      nx = 128;
-    } else if (head_dim == 0) {
-      // Fewer 128-row tiles than SMs: keep the 128-wide MMA (narrower ones
-      // cost more than their share of the tensor pipe) and split K over a
-      // cluster per tile when that fills the GPU better than 64-wide tiles.
-      const int64_t tiles = ((M + 127) / 128) * ntiles;
+    } else {
+      // Tile width and K split with the least estimated time.  The
+      // persistent CTAs take ceil(tiles / SMs) tiles each; a tile costs its
+      // 64-k sub-steps (divided by the split) times a width factor, since a
+      // sub-step costs about the same at every width except 256, about 12%
+      // more (measured on the 8B, 1B and Q2_0 shapes); a split adds its
+      // cross-CTA reduction, about 2.5 sub-steps.  Ties go to the wider tile
+      // (less decode per FLOP).  A split needs every cluster of the grid
+      // resident at once: tiles * split <= SMs here, and the launcher halves
+      // it further if clusters of that size do not all fit.
+      const int64_t nks = (K + 63) / 64;
       const int64_t npk = (K + 8 * kBlock[codec] - 1) / (8 * kBlock[codec]);   // packed stages
-      int s = 8;
-      while (s > 1 && (npk % s != 0 || tiles * s > dev.sms)) s /= 2;
-      if (s > 1) {
-        nx = 128;
-        L.split = s;
+      double best = 1e300;
+      for (int w = 256; w >= 64; w /= 2) {
+        const int64_t t = ((M + w - 1) / w) * ntiles;
+        for (int sp = 1; sp <= 8; sp *= 2) {
+          if (sp > 1 && (w > 128 || head_dim != 0 || npk % sp != 0 || t * sp > dev.sms)) continue;
+          const double waves = (double)((t * sp + dev.sms - 1) / dev.sms);
+          const double est = waves * (double)nks / sp * (w == 256 ? 1.12 : 1.0) + (sp > 1 ? 2.5 : 0.0);
+          if (est < best - 1e-9) {
+            best = est;
+            nx = w;
+            L.split = sp;
+          }
+        }
       }
     }
     L.nx = nx;
