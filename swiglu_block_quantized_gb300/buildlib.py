@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libm4q.so")
 LIB_BOUNDS = os.path.join(OUT_DIR, "libm4q_bounds.so")
-SOURCES = ["api.cu", "misc.cu", "gemv.cu", "tc_q4_0.cu", "tc_q8_0.cu", "tc_q2_0.cu", "tc_mlx4.cu", "noalloc.cu", "attention.cu"]
+SOURCES = ["api.cu", "misc.cu", "gemv.cu", "tc_q4_0.cu", "tc_q8_0.cu", "tc_q2_0.cu", "tc_mlx4.cu", "noalloc.cu", "attention.cu", "attention_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

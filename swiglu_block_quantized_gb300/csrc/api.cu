@@ -557,6 +557,27 @@ AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, in
   return a;
 }
 
+// KV cache [Hkv][T][D] fp16 as a 3-D tensor (d, key, head), boxes of
+// [1][128 keys][64 d] with the 128-byte swizzle (the tcgen05 attention's
+// K and V tiles; keys past T read as zeros).
+bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uint64_t D) {
+  MapKey k{};
+  k.dt = (uint32_t)CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  k.rank = 3;
+  k.swz = (uint32_t)CU_TENSOR_MAP_SWIZZLE_128B;
+  k.base = reinterpret_cast<uint64_t>(base);
+  k.dims[0] = D;
+  k.dims[1] = T;
+  k.dims[2] = Hkv;
+  k.strides[0] = D * 2;
+  k.strides[1] = T * D * 2;
+  k.box[0] = 64;
+  k.box[1] = 128;
+  k.box[2] = 1;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_cached(map, k, estr, 3);
+}
+
 int check_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
                     int64_t M, int64_t T, int64_t D, int64_t q_offset, float scale, const void* O) {
   if (!Q || !K || !V || !O) return M4Q_ERR_INVALID_ARG;
@@ -622,10 +643,13 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
                                          (size_t)a.nsplit * Hkv * a.rtiles * 64 * D * 4);
   }
-  return m4q::launch_attention(p, kv_codec == M4Q_Q8_0, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? M4Q_OK
-             : M4Q_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (m4q::attention_tc_applies(p, kv_codec == M4Q_Q8_0)) {
+    CUtensorMap tm_k, tm_v;
+    if (!encode_kv(&tm_k, K, Hkv, T, D) || !encode_kv(&tm_v, V, Hkv, T, D)) return M4Q_ERR_CUDA;
+    return m4q::launch_attention_tc(p, tm_k, tm_v, s) == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
+  }
+  return m4q::launch_attention(p, kv_codec == M4Q_Q8_0, s) == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
 }
 
 int m4q_check_finite(const void* x, int64_t n, m4q_stream_t stream) {

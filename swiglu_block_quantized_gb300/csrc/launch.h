@@ -118,6 +118,12 @@ struct AttnParams {
   uint32_t* status;       // device status word (bounds-checked build)
 };
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
+// attention_tc.cu: the tcgen05 kernel for prefill-sized calls on an fp16 cache
+// (tm_k, tm_v: 3-D tensor maps [Hkv][T][D] of the caches, 128-byte swizzle,
+// boxes of [1][128 keys][64 d])
+bool attention_tc_applies(const AttnParams& p, bool q8);
+cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                cudaStream_t s);
 
 // misc.cu
 // Status bit of a failed bounds check (the kernels' kErrBounds), and the
