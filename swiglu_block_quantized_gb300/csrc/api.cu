@@ -557,10 +557,10 @@ AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, in
   return a;
 }
 
-// KV cache [Hkv][T][D] fp16 as a 3-D tensor (d, key, head), boxes of
-// [1][128 keys][64 d] with the 128-byte swizzle (the tcgen05 attention's
-// K and V tiles; keys past T read as zeros).
-bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uint64_t D) {
+// [heads][rows][D] fp16 as a 3-D tensor (d, row, head), boxes of
+// [1][box_rows][64 d] with the 128-byte swizzle: the tcgen05 attention's Q,
+// K and V tiles (rows past the extent read as zeros).
+bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uint64_t D, uint32_t box_rows = 128) {
   MapKey k{};
   k.dt = (uint32_t)CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   k.rank = 3;
@@ -572,7 +572,7 @@ bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uin
   k.strides[0] = D * 2;
   k.strides[1] = T * D * 2;
   k.box[0] = 64;
-  k.box[1] = 128;
+  k.box[1] = box_rows;
   k.box[2] = 1;
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode_cached(map, k, estr, 3);
@@ -645,9 +645,13 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (m4q::attention_tc_applies(p, kv_codec == M4Q_Q8_0)) {
-    CUtensorMap tm_k, tm_v;
-    if (!encode_kv(&tm_k, K, Hkv, T, D) || !encode_kv(&tm_v, V, Hkv, T, D)) return M4Q_ERR_CUDA;
-    return m4q::launch_attention_tc(p, tm_k, tm_v, s) == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
+    // Q [H][M][D] takes the same form as the caches, in boxes of the
+    // 128 / G queries a CTA takes of each head
+    CUtensorMap tm_q, tm_k, tm_v;
+    if (!encode_kv(&tm_q, Q, H, M, D, (uint32_t)(128 / p.G)) || !encode_kv(&tm_k, K, Hkv, T, D) ||
+        !encode_kv(&tm_v, V, Hkv, T, D))
+      return M4Q_ERR_CUDA;
+    return m4q::launch_attention_tc(p, tm_q, tm_k, tm_v, s) == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
   }
   return m4q::launch_attention(p, kv_codec == M4Q_Q8_0, s) == cudaSuccess ? M4Q_OK : M4Q_ERR_CUDA;
 }

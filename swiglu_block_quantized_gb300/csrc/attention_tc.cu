@@ -7,9 +7,10 @@
 // online softmax) and "Releases" v0.3.0 (GQA, causal mask with a sequence
 // offset, head dims 64 and 128).
 //
-// One CTA takes 128 rows (query i, group head g; row = i G + g as in
-// attention.cu) of one KV head and walks the key tiles of 128 keys its rows
-// can see:
+// One CTA takes 128 rows of one KV head, 128 / G consecutive queries of each
+// of its G query heads (row = g (128 / G) + i - q0, head-major, so that each
+// head's rows arrive as one TMA box), and walks the key tiles of 128 keys
+// its rows can see:
 //   S_j = Q K_j^T          tcgen05 MMA, both operands K-major in 128-byte
 //                          swizzled shared memory, S_j in TMEM (fp32).
 //   softmax warps          two threads per row, 64 keys each: read S_j,
@@ -34,7 +35,8 @@
 //
 // Warps: 0 MMA (one lane) and TMEM owner; 1 and 2 TMA producers of the K and
 // the V tiles (one lane each; 3-D tensor maps [Hkv][T][D], so keys past T
-// arrive as zeros); 1-3 copy Q once (cp.async); 4-11 softmax, two threads
+// arrive as zeros); 3 the TMA producer of Q (one box per head and 64-wide
+// panel from a 3-D map [H][M][D], rows past M zero); 4-11 softmax, two threads
 // per row (warps w and w + 4: keys 0-63 and 64-127 of each tile), which
 // exchange their partial row maxima through shared memory; 12-19 correction
 // (two groups of four, D/2 columns each).  Every wait is bounded in time; on
@@ -57,7 +59,6 @@ struct TaCfg {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 640;
-  static constexpr int kLoaders = 96;                // threads of warps 1-3 (Q copy)
   static constexpr int kAlphaBytes = 4 * kTR * 4;    // alpha ring of 4 tiles
   static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 2 + 2 + 2 + 4 + 2 + 2 + 1 + 1;
   static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kAlphaBytes +
@@ -97,11 +98,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-// 3-D tile load (x = d, y = key, z = KV head) completing on `bar`.
+// 3-D tile load (x = d, y = row, z = head) completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
@@ -124,14 +121,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128_nmajor(uint32_t saddr, uint32_t 
   return d;
 }
 
-// Byte offset of 16-byte chunk c of row r in a [rows][128 B] panel with the
-// 128-byte swizzle (chunk c of row r sits at c ^ (r & 7)).
-__device__ __forceinline__ int swz(int r, int c) { return r * 128 + (((c ^ (r & 7)) & 7) << 4); }
-
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(640, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const AttnParams p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using Cfg = TaCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* qs = smem_align<1024>(smem_raw);
@@ -158,19 +151,18 @@ __global__ void __launch_bounds__(640, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = (int)gridDim.x - 1 - (int)blockIdx.x, hk = blockIdx.y;   // heaviest row tiles first
-  const int R = p.M * p.G;
-  const int r0 = rt * kTR;
+  const int QPT = kTR / p.G;             // queries per tile (G divides 128)
+  const int q0 = rt * QPT;
   // keys [0, kend) are visible to some row of this tile
   int kend = p.T;
   if (CAUSAL) {
-    const int rlast = min(R - 1, r0 + kTR - 1);
-    const long long vis = (long long)p.q_offset + rlast / p.G + 1;
+    const long long vis = (long long)p.q_offset + min(p.M, q0 + QPT);
     if (vis < kend) kend = (int)vis;
   }
   const int nk = (kend + kTK - 1) / kTK;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 3);
+    mbar_init(q_full, 1);
     for (int i = 0; i < 3; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -256,21 +248,18 @@ __global__ void __launch_bounds__(640, 1)
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------------------ loaders
-    const int lt = threadIdx.x - 32;   // 0 .. 95
-    constexpr int CH = D / 8;          // 16-byte chunks of a row of D values
-    // Q rows (query i, head hk G + g), zero past R, copied once
-    for (int idx = lt; idx < kTR * CH; idx += Cfg::kLoaders) {
-      const int r = idx / CH, c = idx % CH, gr = r0 + r;
-      uint8_t* dst = qs + (c >> 3) * (kTR * 128) + swz(r, c);
-      const int i = gr / p.G, h = hk * p.G + gr % p.G;
-      if (gr < R && in_bounds(i < p.M && h < p.H, p.status, kSiteAttnQ))
-        cp_async16(dst, p.q + ((long long)h * p.M + i) * D + 8 * c);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    if (warp == 3 && lane == 0) {
+      // Q: rows g QPT .. g QPT + QPT - 1 of each 64-wide panel from head
+      // hk G + g, queries q0 .. (boxes start on 1024-byte swizzle atoms:
+      // QPT is a multiple of 8)
+      tma_prefetch_desc(&tm_q);
+      mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
+      for (int g = 0; g < p.G; ++g)
+#pragma unroll
+        for (int pn = 0; pn < D / 64; ++pn)
+          if (in_bounds(q0 >= 0 && hk * p.G + g < p.H, p.status, kSiteAttnQ))
+            tma_load_3d(qs + pn * (kTR * 128) + g * QPT * 128, &tm_q, q_full, 64 * pn, q0, hk * p.G + g);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async_smem();   // generic-proxy and cp.async writes, read by the tensor core
-    mbar_arrive_warp(q_full);
     if ((warp == 1 || warp == 2) && lane == 0) {
       // warp 1: K_j into stage j % 3 after S_{j-3}; warp 2: V_j into stage
       // j % 2 after P_{j-2} V_{j-2}.  D / 64 boxes of [128 keys][64 d] each.
@@ -300,9 +289,9 @@ __global__ void __launch_bounds__(640, 1)
   } else if (warp < 12) {
     // ------------------------------------------------------------ softmax
     const int half = (warp - 4) >> 2;   // keys [64 half, 64 half + 64) of each tile
-    const int r = 32 * (warp & 3) + lane, gr = r0 + r;
-    const bool valid = gr < R;
-    const int i = valid ? gr / p.G : 0;
+    const int r = 32 * (warp & 3) + lane;
+    const int i = q0 + r % QPT;          // query of this row
+    const bool valid = i < p.M;
     // last key this row sees (-1: none), one 32-bit bound for validity, the
     // causal limit and T together
     long long lastl = CAUSAL ? (long long)p.q_offset + i : (long long)p.T - 1;
@@ -319,15 +308,33 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_after();
       const uint32_t scol = tmem + lanes + 128 * st + 64 * half;
       const int kbase = j * kTK + 64 * half;
+      const float sc = p.scale_log2;
+      // keys e <= cut of chunk c are visible; a chunk with cut >= 31 needs
+      // no mask (the warp agrees on it, so the loops below stay uniform)
+      const bool full = __all_sync(0xffffffffu, lastk - (kbase + 32) >= 31);
+      // row maximum of sc * s over the visible keys: the max of s when
+      // sc >= 0, the min when sc < 0 (scaled after)
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32_wait(scol + 32 * c, v);
-        const int cut = lastk - (kbase + 32 * c);   // keys e <= cut of this chunk are visible
+        const int cut = lastk - (kbase + 32 * c);
+        float t = sc >= 0.f ? -INFINITY : INFINITY;
+        if (full) {
+          if (sc >= 0.f) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e <= cut) mx = fmaxf(mx, __uint_as_float(v[e]) * p.scale_log2);   // any sign of scale
+            for (int e = 0; e < 32; ++e) t = fmaxf(t, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) t = fminf(t, __uint_as_float(v[e]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e <= cut) t = sc >= 0.f ? fmaxf(t, __uint_as_float(v[e])) : fminf(t, __uint_as_float(v[e]));
+        }
+        if (t != INFINITY && t != -INFINITY) mx = fmaxf(mx, t * sc);
       }
       // the row maximum over both halves (buffers by tile parity: a thread
       // rewrites its slot two tiles later, after its partner has passed the
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(640, 1)
       const float mnew = fmaxf(m, mx);
       const float muse = mnew == -INFINITY ? 0.f : mnew;
       const float a = ex2(m - muse);   // 0 while m = -inf
-      float sum = 0.f;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
@@ -348,9 +355,14 @@ __global__ void __launch_bounds__(640, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = e <= cut ? ex2(__uint_as_float(v[e]) * p.scale_log2 - muse) : 0.f;
-          const float p1 = e + 1 <= cut ? ex2(__uint_as_float(v[e + 1]) * p.scale_log2 - muse) : 0.f;
-          sum += p0 + p1;
+          float p0 = ex2(fmaf(__uint_as_float(v[e]), sc, -muse));
+          float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sc, -muse));
+          if (!full) {
+            p0 = e <= cut ? p0 : 0.f;
+            p1 = e + 1 <= cut ? p1 : 0.f;
+          }
+          sum0 += p0;
+          sum1 += p1;
           const __half2 h = __floats2half2_rn(p0, p1);
           w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
@@ -360,6 +372,7 @@ __global__ void __launch_bounds__(640, 1)
         // its first half, and P chunk 1 lands on the rest of it
         tmem_st16(scol + 16 * c, w);
       }
+      const float sum = sum0 + sum1;
       l = l * a + sum;
       m = mnew;
       if (half == 0) alpha[(j & 3) * kTR + r] = a;
@@ -373,7 +386,8 @@ __global__ void __launch_bounds__(640, 1)
   } else {
     // ------------------------------------------------------------ correction
     const int e = (warp - 12) >> 2;    // columns [e D / 2, (e + 1) D / 2) of O
-    const int r = 32 * (warp & 3) + lane, gr = r0 + r;
+    const int r = 32 * (warp & 3) + lane;
+    const int i = q0 + r % QPT, h = hk * p.G + r / QPT;   // query and head of this row
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     constexpr int HC = D / 2;
     float o[HC];
@@ -397,11 +411,10 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_before();
       mbar_arrive_warp(&o_free[st]);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 64)) && gr < R) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 64)) && i < p.M) {
       const float l = lfin[r] + lfin[kTR + r];
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int i = gr / p.G, h = hk * p.G + gr % p.G;
-      if (in_bounds(i < p.M && h < p.H, p.status, kSiteAttnO)) {
+      if (in_bounds(h < p.H, p.status, kSiteAttnO)) {
         __half* orow = p.o + (long long)i * p.H * D + (long long)h * D + e * HC;
 #pragma unroll
         for (int c = 0; c < HC; c += 8) {
@@ -427,7 +440,8 @@ __global__ void __launch_bounds__(640, 1)
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t s) {
+cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                      cudaStream_t s) {
   using Cfg = TaCfg<D>;
   auto kern = attn_tc_kernel<D, CAUSAL>;
   std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 4, D, CAUSAL>>();
@@ -440,23 +454,26 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_k, const CUtens
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const int R = p.M * p.G;
-  const dim3 grid((unsigned)((R + kTR - 1) / kTR), (unsigned)p.Hkv, 1);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tm_k, tm_v, p);
+  const int qpt = kTR / p.G;
+  const dim3 grid((unsigned)((p.M + qpt - 1) / qpt), (unsigned)p.Hkv, 1);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// fp16 KV cache, more than 16 rows per KV head, one key split.
+// fp16 KV cache, more than 16 rows per KV head, one key split, a group size
+// that divides 128 rows into whole swizzle atoms per head (G <= 16).
 bool attention_tc_applies(const AttnParams& p, bool q8) {
-  return !q8 && p.M * p.G > 16 && p.nsplit == 1 && (p.D == 64 || p.D == 128) && (p.kv_row_bytes % 16) == 0;
+  return !q8 && p.M * p.G > 16 && p.nsplit == 1 && (p.D == 64 || p.D == 128) && (p.kv_row_bytes % 16) == 0 &&
+         p.G <= 16 && kTR % p.G == 0;
 }
 
-cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                cudaStream_t s) {
-  if (p.D == 64) return p.causal ? launch_tc<64, true>(p, tm_k, tm_v, s) : launch_tc<64, false>(p, tm_k, tm_v, s);
-  return p.causal ? launch_tc<128, true>(p, tm_k, tm_v, s) : launch_tc<128, false>(p, tm_k, tm_v, s);
+cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t s) {
+  if (p.D == 64)
+    return p.causal ? launch_tc<64, true>(p, tm_q, tm_k, tm_v, s) : launch_tc<64, false>(p, tm_q, tm_k, tm_v, s);
+  return p.causal ? launch_tc<128, true>(p, tm_q, tm_k, tm_v, s) : launch_tc<128, false>(p, tm_q, tm_k, tm_v, s);
 }
 
 }  // namespace m4q

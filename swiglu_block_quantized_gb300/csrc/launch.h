@@ -119,11 +119,12 @@ struct AttnParams {
 };
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 // attention_tc.cu: the tcgen05 kernel for prefill-sized calls on an fp16 cache
-// (tm_k, tm_v: 3-D tensor maps [Hkv][T][D] of the caches, 128-byte swizzle,
-// boxes of [1][128 keys][64 d])
+// (tm_q: 3-D tensor map [H][M][D] of Q, boxes of [1][128 / G queries][64 d];
+// tm_k, tm_v: [Hkv][T][D] of the caches, boxes of [1][128 keys][64 d]; all
+// with the 128-byte swizzle)
 bool attention_tc_applies(const AttnParams& p, bool q8);
-cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                cudaStream_t s);
+cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                const CUtensorMap& tm_v, cudaStream_t s);
 
 // misc.cu
 // Status bit of a failed bounds check (the kernels' kErrBounds), and the
