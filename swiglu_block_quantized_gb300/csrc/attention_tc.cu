@@ -98,6 +98,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// OR of `pred` over the `count` threads of named barrier `id` (all of them
+// arrive; every one gets the result).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 // 3-D tile load (x = d, y = row, z = head) completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
   asm volatile(
@@ -303,7 +318,10 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
       const int st = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (j >> 1) & 1, ctl));
+      // one decision for both warps of these rows, which meet at a named
+      // barrier below (it has no time limit)
+      const bool got = mbar_wait(&s_full[st], (j >> 1) & 1, ctl);
+      ok = !bar_red_or(7 + (warp & 3), 64, !got);
       if (!ok) break;
       tc_fence_after();
       const uint32_t scol = tmem + lanes + 128 * st + 64 * half;
