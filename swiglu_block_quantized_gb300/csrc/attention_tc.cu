@@ -13,34 +13,41 @@
 // its rows can see:
 //   S_j = Q K_j^T          tcgen05 MMA, both operands K-major in 128-byte
 //                          swizzled shared memory, S_j in TMEM (fp32).
-//   softmax warps          two threads per row, 64 keys each: read S_j,
-//                          form the running row max m (partial maxima
-//                          exchanged), P_j = exp2(S_j scale log2 e - m)
+//   softmax warps          two teams, one per S buffer (tiles j even and
+//                          odd), thread = row, all 128 keys of the tile:
+//                          the tile's own row max mu_j of the scaled
+//                          scores, P_j = exp2(S_j scale log2 e - mu_j)
 //                          rounded to fp16 and written back over the
-//                          thread's own S_j columns in TMEM (keys 64 h ..
-//                          64 h + 63 at columns 64 h .. 64 h + 31), the
-//                          running sums and the rescale factor alpha_j of
-//                          the previous accumulation.
+//                          thread's own S_j columns in TMEM (key k at
+//                          column k / 2), and l_j = sum P_j.
 //   O_j = P_j V_j          tcgen05 MMA with P_j as the TMEM operand and the
 //                          V_j tile as it lies in the cache ([key][D], the
 //                          N-major B operand: D contiguous) in shared
-//                          memory, into a fresh TMEM buffer per tile.
-//   correction warps       thread = row, half of D each: O = alpha_j O + O_j
-//                          in registers; at the end O / l is written.
-// Fresh per-tile O buffers keep the online-softmax rescale out of the MMA's
-// way: no accumulator is rescaled while the tensor core may still add to it.
-// Two S/P and two O buffers (TMEM: 2 x 128 + 2 x D columns), three K and
-// two V stages let S_{j+1} and P_j V_j run while the softmax of tile j+1 and
-// the correction of tile j proceed.
+//                          memory, into a fresh accumulation per tile.
+//   correction warps       thread = row, half of D each: the running max
+//                          m' = max(m, mu_j), O = 2^(m - m') O +
+//                          2^(mu_j - m') O_j and l the same way, in
+//                          registers; at the end O / l is written.
+// A per-tile max (instead of the running one) frees the softmax of tile j+1
+// from waiting for tile j, so the two teams overlap; the running max is
+// formed once per tile by the correction warps.  A fresh O per tile keeps
+// the rescale out of the MMA's way: no accumulator is rescaled while the
+// tensor core may still add to it.  Three S/P buffers and one O (TMEM:
+// 3 x 128 + D columns), three K and two V stages: S_{j+2} needs only
+// P_{j-1} V_{j-1} done, so the scores run two tiles ahead of the softmax.
+// The score and the P V MMAs come from two issuing threads, each waiting
+// only for its own operands: one thread's waits and issue overlap the other
+// thread's MMAs in the tensor pipe (a tcgen05.mma is accepted about once per
+// MMA duration, so a single issuer's waits leave the pipe idle).
 //
-// Warps: 0 MMA (one lane) and TMEM owner; 1 and 2 TMA producers of the K and
-// the V tiles (one lane each; 3-D tensor maps [Hkv][T][D], so keys past T
-// arrive as zeros); 3 the TMA producer of Q (one box per head and 64-wide
-// panel from a 3-D map [H][M][D], rows past M zero); 4-11 softmax, two threads
-// per row (warps w and w + 4: keys 0-63 and 64-127 of each tile), which
-// exchange their partial row maxima through shared memory; 12-19 correction
-// (two groups of four, D/2 columns each).  Every wait is bounded in time; on
-// expiry the CTA records the failure in the status word and returns.
+// Warps: 0 the score-MMA issuer (one lane) and TMEM owner; 1 and 2 TMA
+// producers of the K and the V tiles (one lane each; 3-D tensor maps
+// [Hkv][T][D], so keys past T arrive as zeros); 3 the TMA producer of Q (one
+// box per head and 64-wide panel from a 3-D map [H][M][D], rows past M zero),
+// then the P V issuer; 4-7 and 8-11 the softmax teams of the even and the
+// odd tiles; 12-19 correction (two groups of four, D/2 columns each).  CTAs run heaviest row tiles first across all
+// KV heads.  Every wait is bounded in time; on expiry the CTA records the
+// failure in the status word and returns.
 #include "codec.cuh"
 #include "launch.h"
 
@@ -59,13 +66,12 @@ struct TaCfg {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 640;
-  static constexpr int kAlphaBytes = 4 * kTR * 4;    // alpha ring of 4 tiles
-  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 2 + 2 + 2 + 4 + 2 + 2 + 1 + 1;
-  static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kAlphaBytes +
-                               2 * kTR * 4 + 4 * kTR * 4 + kBars * 8 + 16;
-  static constexpr uint32_t kOCol = 256;             // O buffers after the two S/P buffers
+  static constexpr int kMlBytes = 4 * kTR * 8;       // (mu_j, l_j) ring of 4 tiles
+  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 4 + 1 + 1 + 1;
+  static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kMlBytes + kBars * 8 + 16;
+  static constexpr uint32_t kOCol = 384;             // O after the three S/P buffers
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(kOCol + 2 * D <= 512, "TMEM budget");
+  static_assert(kOCol + D <= 512, "TMEM budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0 && kVBytes % 1024 == 0, "swizzle atoms");
 };
@@ -92,25 +98,33 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&v)[16]
       : "memory");
 }
 
+// Largest (hi) or smallest (!hi) of v[e] over e <= cut (all 32 when cut >=
+// 31), four independent chains; +-inf when none.
+__device__ __forceinline__ float extreme32(const uint32_t* v, int cut, bool hi) {
+  const float init = hi ? -INFINITY : INFINITY;
+  float t[4] = {init, init, init, init};
+  if (cut >= 31) {
+    if (hi) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) t[e & 3] = fmaxf(t[e & 3], __uint_as_float(v[e]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) t[e & 3] = fminf(t[e & 3], __uint_as_float(v[e]));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float x = e <= cut ? __uint_as_float(v[e]) : init;
+      t[e & 3] = hi ? fmaxf(t[e & 3], x) : fminf(t[e & 3], x);
+    }
+  }
+  return hi ? fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) : fminf(fminf(t[0], t[1]), fminf(t[2], t[3]));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// OR of `pred` over the `count` threads of named barrier `id` (all of them
-// arrive; every one gets the result).
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %3, 0;\n\t"
-      "bar.red.or.pred q, %1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"(count), "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
 }
 
 // 3-D tile load (x = d, y = row, z = head) completing on `bar`.
@@ -145,28 +159,28 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t* qs = smem_align<1024>(smem_raw);
   uint8_t* kst = qs + Cfg::kQBytes;                                 // K stages
   uint8_t* vst = kst + Cfg::kKStages * Cfg::kKBytes;                // V stages
-  float* alpha = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128]
-  float* lfin = alpha + 4 * kTR;                                    // [2][128] partial row sums
-  float* pmax = lfin + 2 * kTR;                                     // [2 tiles][2][128] partial row maxima
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmax + 4 * kTR);
+  float2* ml = reinterpret_cast<float2*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128] (mu_j, l_j)
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(ml + 4 * kTR);
   uint64_t* k_full = q_full + 1;      // [3] producer: K_j in stage j % 3
   uint64_t* k_empty = k_full + 3;     // [3] MMA: S_j done with stage j % 3
   uint64_t* v_full = k_empty + 3;     // [2] producer: V_j in stage j % 2
   uint64_t* v_empty = v_full + 2;     // [2] MMA: P_j V_j done with stage j % 2
-  uint64_t* s_full = v_empty + 2;     // [2] MMA: S_j in TMEM buffer j % 2
-  uint64_t* s_free = s_full + 2;      // [2] MMA: P_j read from buffer j % 2
-  uint64_t* p_full = s_free + 2;      // [2] softmax: P_j written
-  uint64_t* a_rdy = p_full + 2;       // [4] softmax: alpha_j written
-  uint64_t* o_full = a_rdy + 4;       // [2] MMA: O_j in TMEM
-  uint64_t* o_free = o_full + 2;      // [2] correction: O_j consumed
-  uint64_t* l_rdy = o_free + 2;       // softmax: final row sums written
-  uint64_t* drain = l_rdy + 1;
+  uint64_t* s_full = v_empty + 2;     // [3] MMA: S_j in TMEM buffer j % 3
+  uint64_t* s_free = s_full + 3;      // [3] MMA: P_j read from buffer j % 3
+  uint64_t* p_full = s_free + 3;      // [3] softmax: P_j written
+  uint64_t* a_rdy = p_full + 3;       // [4] softmax: (mu_j, l_j) written
+  uint64_t* o_full = a_rdy + 4;       // MMA: O_j in TMEM
+  uint64_t* o_free = o_full + 1;      // correction: O_j consumed
+  uint64_t* drain = o_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rt = (int)gridDim.x - 1 - (int)blockIdx.x, hk = blockIdx.y;   // heaviest row tiles first
   const int QPT = kTR / p.G;             // queries per tile (G divides 128)
+  // row tiles in decreasing order of their key count, every KV head at once
+  const int rtiles = (p.M + QPT - 1) / QPT;
+  const int hk = (int)(blockIdx.x % (unsigned)p.Hkv);
+  const int rt = rtiles - 1 - (int)(blockIdx.x / (unsigned)p.Hkv);
   const int q0 = rt * QPT;
   // keys [0, kend) are visible to some row of this tile
   int kend = p.T;
@@ -181,19 +195,18 @@ __global__ void __launch_bounds__(640, 1)
     for (int i = 0; i < 3; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 1);
+      mbar_init(&p_full[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 1);
-      mbar_init(&p_full[i], 8);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 8);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&a_rdy[i], 4);
-    mbar_init(l_rdy, 8);
-    mbar_init(drain, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 8);
+    mbar_init(drain, 2);   // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -207,62 +220,11 @@ __global__ void __launch_bounds__(640, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, 2000000000ull};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ MMA
-    if (lane == 0 && nk > 0) {
-      constexpr uint32_t idesc_s = idesc_f16_f32(128, kTK);
-      constexpr uint32_t idesc_o = idesc_f16_f32(128, D) | (1u << 16);   // B (V) N-major
-      bool ok = mbar_wait(q_full, 0, ctl);
-      auto issue_s = [&](int j) {
-        const int st = j & 1, sk = j % 3;
-        ok = ok && mbar_wait(&k_full[sk], (j / 3) & 1, ctl);
-        if (j >= 2) ok = ok && mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, ctl);
-        if (!ok) return;
-        tc_fence_after();
-        const uint8_t* ks = kst + sk * Cfg::kKBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int panel = kk >> 2;
-          const uint64_t a = sdesc_sw128_kmajor(smem_u32(qs + panel * (kTR * 128))) + 2 * (kk & 3);
-          const uint64_t b = sdesc_sw128_kmajor(smem_u32(ks + panel * (kTK * 128))) + 2 * (kk & 3);
-          mma_ss_f16(tmem + 128 * st, a, b, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[st]);
-        tc_commit(&k_empty[sk]);
-      };
-      auto issue_pv = [&](int j) {
-        const int st = j & 1;
-        ok = ok && mbar_wait(&v_full[st], (j >> 1) & 1, ctl);
-        ok = ok && mbar_wait(&p_full[st], (j >> 1) & 1, ctl);
-        if (j >= 2) ok = ok && mbar_wait(&o_free[st], ((j >> 1) - 1) & 1, ctl);
-        if (!ok) return;
-        tc_fence_after();
-        const uint8_t* vs = vst + st * Cfg::kVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTK / 16; ++kk) {
-          // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each panel
-          const uint64_t b = sdesc_sw128_nmajor(smem_u32(vs + kk * 2048), kTK * 128);
-          // P keys 16 kk .. 16 kk + 15: columns 64 (kk / 4) + 8 (kk % 4) of the S/P buffer
-          tc_mma_ts_f16(tmem + Cfg::kOCol + D * st, tmem + 128 * st + 64 * (kk >> 2) + 8 * (kk & 3), b, idesc_o,
-                        kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&o_full[st]);
-        tc_commit(&v_empty[st]);
-        tc_commit(&s_free[st]);
-      };
-      issue_s(0);
-      for (int j = 1; j < nk && ok; ++j) {
-        issue_s(j);
-        issue_pv(j - 1);
-      }
-      issue_pv(nk - 1);
-      // Every MMA issued above completes before the CTA frees TMEM.
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0, 200000000ull);
-    }
-    __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ loaders
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads: warp 0 the score MMAs, warp 3 (after the Q copy)
+    // the P V MMAs.  Each waits only for its own operands, so the waits and
+    // the issue of one overlap the MMAs of the other in the tensor pipe.
     if (warp == 3 && lane == 0) {
       // Q: rows g QPT .. g QPT + QPT - 1 of each 64-wide panel from head
       // hk G + g, queries q0 .. (boxes start on 1024-byte swizzle atoms:
@@ -275,6 +237,68 @@ __global__ void __launch_bounds__(640, 1)
           if (in_bounds(q0 >= 0 && hk * p.G + g < p.H, p.status, kSiteAttnQ))
             tma_load_3d(qs + pn * (kTR * 128) + g * QPT * 128, &tm_q, q_full, 64 * pn, q0, hk * p.G + g);
     }
+    if (lane == 0 && nk > 0) {
+      if (warp == 0) {
+        // S_j = Q K_j^T into buffer j % 3 once K_j has landed and
+        // P_{j-3} V_{j-3} has read that buffer
+        constexpr uint32_t idesc_s = idesc_f16_f32(128, kTK);
+        // Operand descriptors, formed once: a descriptor is (address / 16)
+        // in its low 14 bits, so that of a later slice or stage is a fixed
+        // offset from the first.
+        const uint64_t qd = sdesc_sw128_kmajor(smem_u32(qs));
+        const uint64_t kd = sdesc_sw128_kmajor(smem_u32(kst));
+        bool ok = mbar_wait(q_full, 0, ctl);
+        for (int j = 0; j < nk && ok; ++j) {
+          const int sb = j % 3, sk = j % 3;   // S buffer and K stage
+          ok = mbar_wait(&k_full[sk], (j / 3) & 1, ctl);
+          if (j >= 3) ok = ok && mbar_wait(&s_free[sb], ((j / 3) - 1) & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kds = kd + (uint64_t)(sk * (Cfg::kKBytes >> 4));
+          const uint32_t dst = tmem + 128 * sb;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // 16-element slice kk: panel kk / 4, 32 bytes per slice inside it
+            constexpr int kPanelA = kTR * 128 >> 4, kPanelB = kTK * 128 >> 4;
+            const uint32_t off_a = (kk >> 2) * kPanelA + 2 * (kk & 3);
+            const uint32_t off_b = (kk >> 2) * kPanelB + 2 * (kk & 3);
+            mma_ss_f16(dst, qd + off_a, kds + off_b, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[sb]);
+          tc_commit(&k_empty[sk]);
+        }
+      } else {
+        // O_j = P_j V_j once P_j is written, V_j has landed and the
+        // correction warps have read O_{j-1}
+        constexpr uint32_t idesc_o = idesc_f16_f32(128, D) | (1u << 16);   // B (V) N-major
+        const uint64_t vd = sdesc_sw128_nmajor(smem_u32(vst), kTK * 128);
+        bool ok = true;
+        for (int j = 0; j < nk && ok; ++j) {
+          const int st = j & 1, sb = j % 3;   // V stage and S/P buffer
+          ok = mbar_wait(&v_full[st], (j >> 1) & 1, ctl) && mbar_wait(&p_full[sb], (j / 3) & 1, ctl);
+          if (j >= 1) ok = ok && mbar_wait(o_free, (j - 1) & 1, ctl);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vds = vd + (uint64_t)(st * (Cfg::kVBytes >> 4));
+          const uint32_t dst = tmem + Cfg::kOCol, pcol = tmem + 128 * sb;
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk) {
+            // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each V
+            // panel; their P at columns 8 kk .. 8 kk + 7 of the S/P buffer
+            tc_mma_ts_f16(dst, pcol + 8 * kk, vds + (uint32_t)(kk * (2048 >> 4)), idesc_o, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(o_full);
+          tc_commit(&v_empty[st]);
+          tc_commit(&s_free[sb]);
+        }
+      }
+      // Every MMA of both issuers completes before the CTA frees TMEM.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 3) {
+    // ------------------------------------------------------------ loaders
     if ((warp == 1 || warp == 2) && lane == 0) {
       // warp 1: K_j into stage j % 3 after S_{j-3}; warp 2: V_j into stage
       // j % 2 after P_{j-2} V_{j-2}.  D / 64 boxes of [128 keys][64 d] each.
@@ -303,7 +327,7 @@ __global__ void __launch_bounds__(640, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ softmax
-    const int half = (warp - 4) >> 2;   // keys [64 half, 64 half + 64) of each tile
+    const int team = (warp - 4) >> 2;  // tiles j = team, team + 2, ... (S buffer j % 3)
     const int r = 32 * (warp & 3) + lane;
     const int i = q0 + r % QPT;          // query of this row
     const bool valid = i < p.M;
@@ -313,60 +337,32 @@ __global__ void __launch_bounds__(640, 1)
     if (lastl > (long long)p.T - 1) lastl = p.T - 1;
     const int lastk = valid ? (int)lastl : -1;
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t bar_id = 1 + (warp & 3);   // the two warps of these rows
-    float m = -INFINITY, l = 0.f;
+    const float sc = p.scale_log2;
+    const bool hi = sc >= 0.f;           // the max of sc s is sc max s, or sc min s when sc < 0
     bool ok = true;
-    for (int j = 0; j < nk && ok; ++j) {
-      const int st = j & 1;
-      // one decision for both warps of these rows, which meet at a named
-      // barrier below (it has no time limit)
-      const bool got = mbar_wait(&s_full[st], (j >> 1) & 1, ctl);
-      ok = !bar_red_or(7 + (warp & 3), 64, !got);
+    for (int j = team; j < nk && ok; j += 2) {
+      const int sb = j % 3;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / 3) & 1, ctl));
       if (!ok) break;
+      const uint32_t scol = tmem + lanes + 128 * sb;
       tc_fence_after();
-      const uint32_t scol = tmem + lanes + 128 * st + 64 * half;
-      const int kbase = j * kTK + 64 * half;
-      const float sc = p.scale_log2;
-      // keys e <= cut of chunk c are visible; a chunk with cut >= 31 needs
-      // no mask (the warp agrees on it, so the loops below stay uniform)
-      const bool full = __all_sync(0xffffffffu, lastk - (kbase + 32) >= 31);
-      // row maximum of sc * s over the visible keys: the max of s when
-      // sc >= 0, the min when sc < 0 (scaled after)
-      float mx = -INFINITY;
+      const int kbase = j * kTK;
+      // every key of the tile visible to every row of the warp: no masks
+      const bool full = __all_sync(0xffffffffu, lastk - kbase >= kTK - 1);
+      float t = hi ? -INFINITY : INFINITY;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32_wait(scol + 32 * c, v);
-        const int cut = lastk - (kbase + 32 * c);
-        float t = sc >= 0.f ? -INFINITY : INFINITY;
-        if (full) {
-          if (sc >= 0.f) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) t = fmaxf(t, __uint_as_float(v[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) t = fminf(t, __uint_as_float(v[e]));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e <= cut) t = sc >= 0.f ? fmaxf(t, __uint_as_float(v[e])) : fminf(t, __uint_as_float(v[e]));
-        }
-        if (t != INFINITY && t != -INFINITY) mx = fmaxf(mx, t * sc);
+        const float tc = extreme32(v, full ? 31 : lastk - (kbase + 32 * c), hi);
+        t = hi ? fmaxf(t, tc) : fminf(t, tc);
       }
-      // the row maximum over both halves (buffers by tile parity: a thread
-      // rewrites its slot two tiles later, after its partner has passed the
-      // next tile's barrier, hence after it has read this value)
-      float* pm = pmax + (j & 1) * (2 * kTR);
-      pm[half * kTR + r] = mx;
-      named_bar_sync(bar_id, 64);
-      mx = fmaxf(mx, pm[(half ^ 1) * kTR + r]);
-      const float mnew = fmaxf(m, mx);
-      const float muse = mnew == -INFINITY ? 0.f : mnew;
-      const float a = ex2(m - muse);   // 0 while m = -inf
+      // mu_j: -inf when the row sees no key of this tile
+      const float mu = (t == INFINITY || t == -INFINITY) ? -INFINITY : t * sc;
+      const float muse = mu == -INFINITY ? 0.f : mu;
       float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32_wait(scol + 32 * c, v);
         const int cut = lastk - (kbase + 32 * c);
@@ -384,23 +380,16 @@ __global__ void __launch_bounds__(640, 1)
           const __half2 h = __floats2half2_rn(p0, p1);
           w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        // P keys 64 half + 32 c .. + 31 go to columns 64 half + 16 c, inside
-        // this thread's own S columns and behind its reads: chunk 0 of S
-        // (columns 64 half .. + 31) is read before P chunk 0 overwrites
-        // its first half, and P chunk 1 lands on the rest of it
+        // keys 32 c .. 32 c + 31 go to columns 16 c .. 16 c + 15: S columns
+        // this thread has already read
         tmem_st16(scol + 16 * c, w);
       }
-      const float sum = sum0 + sum1;
-      l = l * a + sum;
-      m = mnew;
-      if (half == 0) alpha[(j & 3) * kTR + r] = a;
+      ml[(j & 3) * kTR + r] = make_float2(mu, sum0 + sum1);
       tmem_wait_st();
       tc_fence_before();
-      if (half == 0) mbar_arrive_warp(&a_rdy[j & 3]);
-      mbar_arrive_warp(&p_full[st]);
+      mbar_arrive_warp(&a_rdy[j & 3]);
+      mbar_arrive_warp(&p_full[sb]);
     }
-    lfin[half * kTR + r] = l;
-    mbar_arrive_warp(l_rdy);
   } else {
     // ------------------------------------------------------------ correction
     const int e = (warp - 12) >> 2;    // columns [e D / 2, (e + 1) D / 2) of O
@@ -411,26 +400,33 @@ __global__ void __launch_bounds__(640, 1)
     float o[HC];
 #pragma unroll
     for (int c = 0; c < HC; ++c) o[c] = 0.f;
+    float m = -INFINITY, l = 0.f;        // running max of the scaled scores and row sum
     bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
-      const int st = j & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_idle(&a_rdy[j & 3], (j >> 2) & 1, ctl, 64) &&
-                                       mbar_wait_idle(&o_full[st], (j >> 1) & 1, ctl, 64));
+                                       mbar_wait_idle(o_full, j & 1, ctl, 64));
       if (!ok) break;
       tc_fence_after();
-      const float a = alpha[(j & 3) * kTR + r];
+      // O = 2^(m - m') O + 2^(mu_j - m') O_j, l likewise (2^-inf = 0: the
+      // first visible tile drops the zeros before it, a tile the row does
+      // not see adds nothing)
+      const float2 mlj = ml[(j & 3) * kTR + r];
+      const float mnew = fmaxf(m, mlj.x);
+      const float a = mnew == -INFINITY ? 0.f : ex2(m - mnew);
+      const float b = mnew == -INFINITY ? 0.f : ex2(mlj.x - mnew);
+      l = l * a + mlj.y * b;
+      m = mnew;
 #pragma unroll
       for (int c = 0; c < HC / 16; ++c) {
         uint32_t v[16];
-        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + D * st + e * HC + 16 * c, v);
+        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + e * HC + 16 * c, v);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) o[16 * c + q] = o[16 * c + q] * a + __uint_as_float(v[q]);
+        for (int q = 0; q < 16; ++q) o[16 * c + q] = fmaf(__uint_as_float(v[q]), b, o[16 * c + q] * a);
       }
       tc_fence_before();
-      mbar_arrive_warp(&o_free[st]);
+      mbar_arrive_warp(o_free);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 64)) && i < p.M) {
-      const float l = lfin[r] + lfin[kTR + r];
+    if (ok && i < p.M) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (in_bounds(h < p.H, p.status, kSiteAttnO)) {
         __half* orow = p.o + (long long)i * p.H * D + (long long)h * D + e * HC;
@@ -473,7 +469,7 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtens
     configured.fetch_or(bit);
   }
   const int qpt = kTR / p.G;
-  const dim3 grid((unsigned)((p.M + qpt - 1) / qpt), (unsigned)p.Hkv, 1);
+  const dim3 grid((unsigned)((p.M + qpt - 1) / qpt) * (unsigned)p.Hkv, 1, 1);
   kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
