@@ -57,6 +57,7 @@ namespace {
 
 constexpr int kTR = 128;   // rows per CTA
 constexpr int kTK = 128;   // keys per tile
+constexpr float kLazy = 8.f;   // reference kept while the row max stays within 2^8 of it
 
 template <int D>
 struct TaCfg {
@@ -66,8 +67,8 @@ struct TaCfg {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 640;
-  static constexpr int kMlBytes = 4 * kTR * 8;       // (mu_j, l_j) ring of 4 tiles
-  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 4 + 1 + 1 + 1;
+  static constexpr int kMlBytes = 2 * kTR * 4 + 2 * kTR * 8 + 4 * 2 * kTR * 4;   // references, final (l, m), partial maxima
+  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 2 + 4 + 1 + 1;
   static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kMlBytes + kBars * 8 + 16;
   static constexpr uint32_t kOCol = 384;             // O after the three S/P buffers
   static_assert(D == 64 || D == 128, "head dim");
@@ -121,6 +122,27 @@ __device__ __forceinline__ float extreme32(const uint32_t* v, int cut, bool hi) 
   return hi ? fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) : fminf(fminf(t[0], t[1]), fminf(t[2], t[3]));
 }
 
+// Two fp32 values in one 64-bit register, for the packed f32x2 FMA and add
+// (one instruction for both).
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long x, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -159,8 +181,10 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t* qs = smem_align<1024>(smem_raw);
   uint8_t* kst = qs + Cfg::kQBytes;                                 // K stages
   uint8_t* vst = kst + Cfg::kKStages * Cfg::kKBytes;                // V stages
-  float2* ml = reinterpret_cast<float2*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128] (mu_j, l_j)
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(ml + 4 * kTR);
+  float* mref = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [2][128] reference of tile j
+  float2* lfin = reinterpret_cast<float2*>(mref + 2 * kTR);         // [2][128] (l, m) of each team
+  float* pmx = reinterpret_cast<float*>(lfin + 2 * kTR);            // [4][2][128] partial extremes of S_j
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmx + 4 * 2 * kTR);
   uint64_t* k_full = q_full + 1;      // [3] producer: K_j in stage j % 3
   uint64_t* k_empty = k_full + 3;     // [3] MMA: S_j done with stage j % 3
   uint64_t* v_full = k_empty + 3;     // [2] producer: V_j in stage j % 2
@@ -168,10 +192,10 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* s_full = v_empty + 2;     // [3] MMA: S_j in TMEM buffer j % 3
   uint64_t* s_free = s_full + 3;      // [3] MMA: P_j read from buffer j % 3
   uint64_t* p_full = s_free + 3;      // [3] softmax: P_j written
-  uint64_t* a_rdy = p_full + 3;       // [4] softmax: (mu_j, l_j) written
-  uint64_t* o_full = a_rdy + 4;       // MMA: O_j in TMEM
-  uint64_t* o_free = o_full + 1;      // correction: O_j consumed
-  uint64_t* drain = o_free + 1;
+  uint64_t* r_rdy = p_full + 3;       // [2] softmax: reference of tile j written (slot j % 2)
+  uint64_t* x_rdy = r_rdy + 2;        // [4] max warps: partial extremes of S_j written (slot j % 4)
+  uint64_t* l_rdy = x_rdy + 4;        // softmax: final (l, m) of both teams written
+  uint64_t* drain = l_rdy + 1;        // both issuers: every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -203,9 +227,10 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&a_rdy[i], 4);
-    mbar_init(o_full, 1);
-    mbar_init(o_free, 8);
+    mbar_init(&r_rdy[0], 4);
+    mbar_init(&r_rdy[1], 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&x_rdy[i], 8);
+    mbar_init(l_rdy, 8);
     mbar_init(drain, 2);   // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
@@ -268,15 +293,14 @@ __global__ void __launch_bounds__(640, 1)
           tc_commit(&k_empty[sk]);
         }
       } else {
-        // O_j = P_j V_j once P_j is written, V_j has landed and the
-        // correction warps have read O_{j-1}
+        // O += P_j V_j once P_j is written and V_j has landed (a rescale of
+        // O, when tile j raised the reference, precedes P_j)
         constexpr uint32_t idesc_o = idesc_f16_f32(128, D) | (1u << 16);   // B (V) N-major
         const uint64_t vd = sdesc_sw128_nmajor(smem_u32(vst), kTK * 128);
         bool ok = true;
         for (int j = 0; j < nk && ok; ++j) {
           const int st = j & 1, sb = j % 3;   // V stage and S/P buffer
           ok = mbar_wait(&v_full[st], (j >> 1) & 1, ctl) && mbar_wait(&p_full[sb], (j / 3) & 1, ctl);
-          if (j >= 1) ok = ok && mbar_wait(o_free, (j - 1) & 1, ctl);
           if (!ok) break;
           tc_fence_after();
           const uint64_t vds = vd + (uint64_t)(st * (Cfg::kVBytes >> 4));
@@ -285,9 +309,8 @@ __global__ void __launch_bounds__(640, 1)
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each V
             // panel; their P at columns 8 kk .. 8 kk + 7 of the S/P buffer
-            tc_mma_ts_f16(dst, pcol + 8 * kk, vds + (uint32_t)(kk * (2048 >> 4)), idesc_o, kk > 0 ? 1u : 0u);
+            tc_mma_ts_f16(dst, pcol + 8 * kk, vds + (uint32_t)(kk * (2048 >> 4)), idesc_o, (j | kk) > 0 ? 1u : 0u);
           }
-          tc_commit(o_full);
           tc_commit(&v_empty[st]);
           tc_commit(&s_free[sb]);
         }
@@ -339,6 +362,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc = p.scale_log2;
     const bool hi = sc >= 0.f;           // the max of sc s is sc max s, or sc min s when sc < 0
+    float lsum = 0.f, lref = -INFINITY;  // this team's row sum and the reference it is relative to
     bool ok = true;
     for (int j = team; j < nk && ok; j += 2) {
       const int sb = j % 3;
@@ -349,18 +373,47 @@ __global__ void __launch_bounds__(640, 1)
       const int kbase = j * kTK;
       // every key of the tile visible to every row of the warp: no masks
       const bool full = __all_sync(0xffffffffu, lastk - kbase >= kTK - 1);
-      float t = hi ? -INFINITY : INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32_wait(scol + 32 * c, v);
-        const float tc = extreme32(v, full ? 31 : lastk - (kbase + 32 * c), hi);
-        t = hi ? fmaxf(t, tc) : fminf(t, tc);
-      }
+      // the row's extreme raw score over the visible keys of the tile, from
+      // the two halves the max warps formed
+      ok = __all_sync(0xffffffffu, mbar_wait(&x_rdy[j & 3], (j >> 2) & 1, ctl));
+      if (!ok) break;
+      const float x0 = pmx[(j & 3) * 2 * kTR + r], x1 = pmx[((j & 3) * 2 + 1) * kTR + r];
+      const float t = hi ? fmaxf(x0, x1) : fminf(x0, x1);
       // mu_j: -inf when the row sees no key of this tile
       const float mu = (t == INFINITY || t == -INFINITY) ? -INFINITY : t * sc;
-      const float muse = mu == -INFINITY ? 0.f : mu;
-      float sum0 = 0.f, sum1 = 0.f;
+      // Reference of tile j: that of tile j - 1 unless mu_j exceeds it by
+      // more than kLazy (P stays below 2^kLazy); tile j - 1 belongs to the
+      // other team, whose reference arrives through shared memory.
+      float mprev = -INFINITY;
+      if (j >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&r_rdy[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl));
+        if (!ok) break;
+        mprev = mref[((j - 1) & 1) * kTR + r];
+      }
+      const float mj = mu > mprev + kLazy ? mu : mprev;
+      mref[(j & 1) * kTR + r] = mj;
+      mbar_arrive_warp(&r_rdy[j & 1]);
+      // A raised reference rescales O (P_i V_i of the tiles before j,
+      // relative to mprev) by 2^(mprev - mj), after P_{j-1} V_{j-1} is done
+      // and before P_j is published (so before P_j V_j is issued).
+      const bool resc = mj > mprev && mprev != -INFINITY;
+      if (__any_sync(0xffffffffu, resc)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_free[(j - 1) % 3], ((j - 1) / 3) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        const float a = resc ? ex2(mprev - mj) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32_wait(tmem + lanes + Cfg::kOCol + 32 * c, v);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * a);
+          tmem_st32(tmem + lanes + Cfg::kOCol + 32 * c, v);
+        }
+      }
+      const float muse = mj == -INFINITY ? 0.f : mj;
+      const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(-muse, -muse);
+      unsigned long long s2 = 0ull;          // the two lanes' partial row sums
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -369,14 +422,15 @@ __global__ void __launch_bounds__(640, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(v[e]), sc, -muse));
-          float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sc, -muse));
+          float a0, a1;
+          unpack2(fma2(pack2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2), a0, a1);
+          float p0 = ex2(a0);
+          float p1 = ex2(a1);
           if (!full) {
             p0 = e <= cut ? p0 : 0.f;
             p1 = e + 1 <= cut ? p1 : 0.f;
           }
-          sum0 += p0;
-          sum1 += p1;
+          s2 = add2(s2, pack2(p0, p1));
           const __half2 h = __floats2half2_rn(p0, p1);
           w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
@@ -384,61 +438,81 @@ __global__ void __launch_bounds__(640, 1)
         // this thread has already read
         tmem_st16(scol + 16 * c, w);
       }
-      ml[(j & 3) * kTR + r] = make_float2(mu, sum0 + sum1);
+      float sum0, sum1;
+      unpack2(s2, sum0, sum1);
+      // this team's row sum, kept relative to the latest reference it used
+      if (mj != -INFINITY) {
+        lsum = lsum * ex2(lref - mj) + (sum0 + sum1);
+        lref = mj;
+      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&a_rdy[j & 3]);
       mbar_arrive_warp(&p_full[sb]);
     }
+    lfin[team * kTR + r] = make_float2(lsum, lref);
+    mbar_arrive_warp(l_rdy);
   } else {
-    // ------------------------------------------------------------ correction
-    const int e = (warp - 12) >> 2;    // columns [e D / 2, (e + 1) D / 2) of O
+    // ------------------------------------------------------------ max, epilogue
+    const int e = (warp - 12) >> 2;    // keys [64 e, 64 e + 64) of a tile; columns [e D / 2, (e + 1) D / 2) of O
     const int r = 32 * (warp & 3) + lane;
     const int i = q0 + r % QPT, h = hk * p.G + r / QPT;   // query and head of this row
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     constexpr int HC = D / 2;
-    float o[HC];
+    // Per tile: the extreme raw score of this row over the visible keys of
+    // one half of S_j (the max when the scale is >= 0, else the min), for
+    // the softmax team, which then makes one pass over S_j.
+    {
+      long long lastl = CAUSAL ? (long long)p.q_offset + i : (long long)p.T - 1;
+      if (lastl > (long long)p.T - 1) lastl = p.T - 1;
+      const int lastk = i < p.M ? (int)lastl : -1;
+      const bool hi = p.scale_log2 >= 0.f;
+      bool mok = true;
+      for (int j = 0; j < nk && mok; ++j) {
+        const int sb = j % 3;
+        mok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / 3) & 1, ctl));
+        if (!mok) break;
+        tc_fence_after();
+        const int kb = j * kTK + 64 * e;
+        const bool full = __all_sync(0xffffffffu, lastk - kb >= 63);
+        float t = hi ? -INFINITY : INFINITY;
 #pragma unroll
-    for (int c = 0; c < HC; ++c) o[c] = 0.f;
-    float m = -INFINITY, l = 0.f;        // running max of the scaled scores and row sum
-    bool ok = true;
-    for (int j = 0; j < nk && ok; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait_idle(&a_rdy[j & 3], (j >> 2) & 1, ctl, 64) &&
-                                       mbar_wait_idle(o_full, j & 1, ctl, 64));
-      if (!ok) break;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32_wait(tmem + lanes + 128 * sb + 64 * e + 32 * c, v);
+          const float tc = extreme32(v, full ? 31 : lastk - (kb + 32 * c), hi);
+          t = hi ? fmaxf(t, tc) : fminf(t, tc);
+        }
+        pmx[((j & 3) * 2 + e) * kTR + r] = t;
+        tc_fence_before();
+        mbar_arrive_warp(&x_rdy[j & 3]);
+      }
+    }
+    // O (relative to the last tile's reference M) / l, l = sum over the
+    // teams of l_t 2^(m_t - M), once every MMA is done
+    const bool ok = nk > 0 && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 256) &&
+                                                            mbar_wait_idle(drain, 0, ctl, 256));
+    if (ok) {
       tc_fence_after();
-      // O = 2^(m - m') O + 2^(mu_j - m') O_j, l likewise (2^-inf = 0: the
-      // first visible tile drops the zeros before it, a tile the row does
-      // not see adds nothing)
-      const float2 mlj = ml[(j & 3) * kTR + r];
-      const float mnew = fmaxf(m, mlj.x);
-      const float a = mnew == -INFINITY ? 0.f : ex2(m - mnew);
-      const float b = mnew == -INFINITY ? 0.f : ex2(mlj.x - mnew);
-      l = l * a + mlj.y * b;
-      m = mnew;
+      const float M = mref[((nk - 1) & 1) * kTR + r];
+      const float2 f0 = lfin[r], f1 = lfin[kTR + r];
+      const float l = (f0.y == -INFINITY ? 0.f : f0.x * ex2(f0.y - M)) +
+                      (f1.y == -INFINITY ? 0.f : f1.x * ex2(f1.y - M));
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = i < p.M && in_bounds(h < p.H, p.status, kSiteAttnO);
+      __half* orow = p.o + (long long)(store ? i : 0) * p.H * D + (long long)(store ? h : 0) * D + e * HC;
 #pragma unroll
       for (int c = 0; c < HC / 16; ++c) {
         uint32_t v[16];
         tmem_ld16_wait(tmem + lanes + Cfg::kOCol + e * HC + 16 * c, v);
+        uint32_t w[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) o[16 * c + q] = fmaf(__uint_as_float(v[q]), b, o[16 * c + q] * a);
-      }
-      tc_fence_before();
-      mbar_arrive_warp(o_free);
-    }
-    if (ok && i < p.M) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (in_bounds(h < p.H, p.status, kSiteAttnO)) {
-        __half* orow = p.o + (long long)i * p.H * D + (long long)h * D + e * HC;
-#pragma unroll
-        for (int c = 0; c < HC; c += 8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const __half2 hh = __floats2half2_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
-            w[q] = *reinterpret_cast<const uint32_t*>(&hh);
-          }
-          *reinterpret_cast<uint4*>(orow + c) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int q = 0; q < 8; ++q) {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
+          w[q] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        if (store) {
+          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
     }

@@ -100,3 +100,33 @@ def test_direct_head_q_feeds_attention():
     O = host(m.attention(q, dev(Kc), dev(Vc), Q8, Hkv, T))
     ref = oracle.attention(host(q), Kc, Vc, Q8, H, Hkv, M, T, hd, 0, True)
     assert_close(O, ref, "heads -> attention")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("scale", [None, -0.2])
+def test_attention_growing_scores(D, scale):
+    # Key rows scaled up along the sequence (x1 .. x13), so the scaled row
+    # maximum grows by far more than 2^8 across the key tiles: a kernel that
+    # keeps a reference maximum per row must raise it, and rescale what it
+    # has accumulated, several times within a row.  A negative scale makes
+    # the smallest raw scores the largest scaled ones.
+    H, Hkv, M, T = 8, 2, 300, 700
+    Q = synth.queries(H, M, D, seed=21)
+    ramp = (1.0 + 12.0 * np.arange(T) / T).astype(np.float32)
+    K = (synth.kv_cache(F16, Hkv, T, D, seed=22, name="K").astype(np.float32) * ramp[None, :, None]).astype(np.float16)
+    V = synth.kv_cache(F16, Hkv, T, D, seed=22, name="V")
+    for causal in (True, False):
+        O = host(m.attention(dev(Q), dev(K), dev(V), F16, Hkv, T, q_offset=T - M, causal=causal, scale=scale))
+        ref = oracle.attention(Q, K, V, F16, H, Hkv, M, T, D, T - M, causal, scale=scale)
+        assert_close(O, ref, "growing scores D=%d scale=%s causal=%d" % (D, scale, causal))
+
+
+@pytest.mark.parametrize("G", [1, 2, 8, 16])
+def test_attention_group_sizes(G):
+    # prefill-sized calls for each query group size the tensor-core path
+    # takes (rows of G heads per KV head), with ragged M and T
+    Hkv, D, M, T = 2, 128, 83, 451
+    H = G * Hkv
+    for causal in (True, False):
+        O, ref = run(F16, H, Hkv, M, T, D, T - M, causal, seed=G)
+        assert_close(O, ref, "G=%d causal=%d" % (G, causal))
