@@ -12,42 +12,52 @@
 // head's rows arrive as one TMA box), and walks the key tiles of 128 keys
 // its rows can see:
 //   S_j = Q K_j^T          tcgen05 MMA, both operands K-major in 128-byte
-//                          swizzled shared memory, S_j in TMEM (fp32).
-//   softmax warps          two teams, one per S buffer (tiles j even and
-//                          odd), thread = row, all 128 keys of the tile:
-//                          the tile's own row max mu_j of the scaled
-//                          scores, P_j = exp2(S_j scale log2 e - mu_j)
+//                          swizzled shared memory, S_j in TMEM (fp32), in
+//                          buffer j % 3.
+//   max warps              two threads per row (64 keys each): the row's
+//                          extreme raw score over its visible keys (the
+//                          max, the min for a negative scale), whose
+//                          scaled value is mu_j.
+//   softmax warps          two teams (tiles j even and odd), thread = row,
+//                          all 128 keys of the tile: the reference m_j =
+//                          m_{j-1} unless mu_j > m_{j-1} + 8, then mu_j (the
+//                          teams hand m_j on through shared memory);
+//                          P_j = exp2(S_j scale log2 e - m_j) <= 2^8,
 //                          rounded to fp16 and written back over the
-//                          thread's own S_j columns in TMEM (key k at
-//                          column k / 2), and l_j = sum P_j.
-//   O_j = P_j V_j          tcgen05 MMA with P_j as the TMEM operand and the
+//                          thread's own S_j columns (key k at column k / 2);
+//                          the team's row sum l, kept relative to the last
+//                          reference it used.
+//   O += P_j V_j           tcgen05 MMA with P_j as the TMEM operand and the
 //                          V_j tile as it lies in the cache ([key][D], the
 //                          N-major B operand: D contiguous) in shared
-//                          memory, into a fresh accumulation per tile.
-//   correction warps       thread = row, half of D each: the running max
-//                          m' = max(m, mu_j), O = 2^(m - m') O +
-//                          2^(mu_j - m') O_j and l the same way, in
-//                          registers; at the end O / l is written.
-// A per-tile max (instead of the running one) frees the softmax of tile j+1
-// from waiting for tile j, so the two teams overlap; the running max is
-// formed once per tile by the correction warps.  A fresh O per tile keeps
-// the rescale out of the MMA's way: no accumulator is rescaled while the
-// tensor core may still add to it.  Three S/P buffers and one O (TMEM:
-// 3 x 128 + D columns), three K and two V stages: S_{j+2} needs only
-// P_{j-1} V_{j-1} done, so the scores run two tiles ahead of the softmax.
-// The score and the P V MMAs come from two issuing threads, each waiting
-// only for its own operands: one thread's waits and issue overlap the other
-// thread's MMAs in the tensor pipe (a tcgen05.mma is accepted about once per
-// MMA duration, so a single issuer's waits leave the pipe idle).
+//                          memory; O stays in TMEM for the whole walk.
+//   rescale                when m_j > m_{j-1}, the team of tile j scales O
+//                          by 2^(m_{j-1} - m_j) in TMEM after P_{j-1} V_{j-1}
+//                          and before it publishes P_j (rare: the reference
+//                          moves only when a row maximum jumps by 2^8).
+//   epilogue               O / l, l = the teams' sums brought to the last
+//                          reference, written as fp16.
+// The lazily raised reference keeps O accumulating in the tensor core's
+// TMEM with no per-tile read-out, and frees the softmax of tile j+1 from the
+// exponentials of tile j: only the reference, known right after the max,
+// passes from one team to the next.  Three S/P buffers and one O (TMEM:
+// 3 x 128 + D columns), three K and two V stages: S_{j+3} needs only
+// P_j V_j done, so the scores run ahead of the softmax.  The score and the
+// P V MMAs come from two issuing threads, each waiting only for its own
+// operands: one thread's waits and issue overlap the other thread's MMAs in
+// the tensor pipe (a tcgen05.mma is accepted about once per MMA duration, so
+// a single issuer's waits leave the pipe idle).
 //
 // Warps: 0 the score-MMA issuer (one lane) and TMEM owner; 1 and 2 TMA
 // producers of the K and the V tiles (one lane each; 3-D tensor maps
 // [Hkv][T][D], so keys past T arrive as zeros); 3 the TMA producer of Q (one
 // box per head and 64-wide panel from a 3-D map [H][M][D], rows past M zero),
 // then the P V issuer; 4-7 and 8-11 the softmax teams of the even and the
-// odd tiles; 12-19 correction (two groups of four, D/2 columns each).  CTAs run heaviest row tiles first across all
-// KV heads.  Every wait is bounded in time; on expiry the CTA records the
-// failure in the status word and returns.
+// odd tiles; 12-19 the max warps, then the epilogue (two groups of four:
+// keys 0-63 and 64-127 of a tile, columns 0 .. D/2 - 1 and D/2 .. D - 1 of
+// O).  CTAs run heaviest row tiles first across all KV heads.  Every wait
+// is bounded in time; on expiry the CTA records the failure in the status
+// word and returns.
 #include "codec.cuh"
 #include "launch.h"
 
@@ -97,6 +107,37 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&v)[16]
         "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr)
       : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane, not waited for:
+// v is valid after tmem_wait_ld_tied(v).
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+               : "r"(taddr)
+               : "memory");
+}
+
+// Wait for this thread's TMEM loads; v passes through the wait, so that no
+// use of it is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]) : : "memory");
+}
+
+// 64 consecutive 32-bit TMEM columns of this thread's lane, waited for.
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&v)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+               : "r"(taddr)
+               : "memory");
+}
+
+// Store 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // Largest (hi) or smallest (!hi) of v[e] over e <= cut (all 32 when cut >=
@@ -366,17 +407,16 @@ __global__ void __launch_bounds__(640, 1)
     bool ok = true;
     for (int j = team; j < nk && ok; j += 2) {
       const int sb = j % 3;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / 3) & 1, ctl));
+      // the row's extreme raw score over the visible keys of the tile, from
+      // the two halves the max warps formed (they read S_j after its MMA
+      // completed, so S_j is complete here too)
+      ok = __all_sync(0xffffffffu, mbar_wait(&x_rdy[j & 3], (j >> 2) & 1, ctl));
       if (!ok) break;
       const uint32_t scol = tmem + lanes + 128 * sb;
       tc_fence_after();
       const int kbase = j * kTK;
       // every key of the tile visible to every row of the warp: no masks
       const bool full = __all_sync(0xffffffffu, lastk - kbase >= kTK - 1);
-      // the row's extreme raw score over the visible keys of the tile, from
-      // the two halves the max warps formed
-      ok = __all_sync(0xffffffffu, mbar_wait(&x_rdy[j & 3], (j >> 2) & 1, ctl));
-      if (!ok) break;
       const float x0 = pmx[(j & 3) * 2 * kTR + r], x1 = pmx[((j & 3) * 2 + 1) * kTR + r];
       const float t = hi ? fmaxf(x0, x1) : fminf(x0, x1);
       // mu_j: -inf when the row sees no key of this tile
@@ -414,16 +454,22 @@ __global__ void __launch_bounds__(640, 1)
       const float muse = mj == -INFINITY ? 0.f : mj;
       const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(-muse, -muse);
       unsigned long long s2 = 0ull;          // the two lanes' partial row sums
+      // 16-key chunks, the load of chunk c + 1 in flight while chunk c is
+      // computed; P of keys 16 c .. 16 c + 15 goes to columns 8 c .. 8 c + 7,
+      // S columns this thread has already read
+      uint32_t v[2][16];
+      tmem_ld16_async(scol, v[0]);
+      tmem_wait_ld_tied(v[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32_wait(scol + 32 * c, v);
-        const int cut = lastk - (kbase + 32 * c);
-        uint32_t w[16];
+      for (int c = 0; c < 8; ++c) {
+        if (c < 7) tmem_ld16_async(scol + 16 * (c + 1), v[(c + 1) & 1]);
+        const uint32_t (&x)[16] = v[c & 1];
+        const int cut = lastk - (kbase + 16 * c);
+        uint32_t w[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 16; e += 2) {
           float a0, a1;
-          unpack2(fma2(pack2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2), a0, a1);
+          unpack2(fma2(pack2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc2, nm2), a0, a1);
           float p0 = ex2(a0);
           float p1 = ex2(a1);
           if (!full) {
@@ -434,9 +480,8 @@ __global__ void __launch_bounds__(640, 1)
           const __half2 h = __floats2half2_rn(p0, p1);
           w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        // keys 32 c .. 32 c + 31 go to columns 16 c .. 16 c + 15: S columns
-        // this thread has already read
-        tmem_st16(scol + 16 * c, w);
+        tmem_st8(scol + 8 * c, w);
+        if (c < 7) tmem_wait_ld_tied(v[(c + 1) & 1]);
       }
       float sum0, sum1;
       unpack2(s2, sum0, sum1);
@@ -474,14 +519,11 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         const int kb = j * kTK + 64 * e;
         const bool full = __all_sync(0xffffffffu, lastk - kb >= 63);
-        float t = hi ? -INFINITY : INFINITY;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32_wait(tmem + lanes + 128 * sb + 64 * e + 32 * c, v);
-          const float tc = extreme32(v, full ? 31 : lastk - (kb + 32 * c), hi);
-          t = hi ? fmaxf(t, tc) : fminf(t, tc);
-        }
+        uint32_t v[64];
+        tmem_ld64_wait(tmem + lanes + 128 * sb + 64 * e, v);
+        const int cut = full ? 63 : lastk - kb;
+        const float t0 = extreme32(v, cut, hi), t1 = extreme32(v + 32, cut - 32, hi);
+        const float t = hi ? fmaxf(t0, t1) : fminf(t0, t1);
         pmx[((j & 3) * 2 + e) * kTR + r] = t;
         tc_fence_before();
         mbar_arrive_warp(&x_rdy[j & 3]);
