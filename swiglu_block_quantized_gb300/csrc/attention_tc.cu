@@ -14,29 +14,30 @@
 //   S_j = Q K_j^T          tcgen05 MMA, both operands K-major in 128-byte
 //                          swizzled shared memory, S_j in TMEM (fp32), in
 //                          buffer j % 3.
-//   max warps              two threads per row (64 keys each): the row's
-//                          extreme raw score over its visible keys (the
-//                          max, the min for a negative scale), whose
-//                          scaled value is mu_j.
-//   softmax warps          two teams (tiles j even and odd), thread = row,
-//                          all 128 keys of the tile: the reference m_j =
-//                          m_{j-1} unless mu_j > m_{j-1} + 8, then mu_j (the
-//                          teams hand m_j on through shared memory);
+//   softmax warps          two teams (tiles j even and odd) of two
+//                          threads per row (keys 0-63 and 64-127): each
+//                          forms its half's extreme raw score (max, or min
+//                          for a negative scale), the pair exchanges them
+//                          (shared memory and a named barrier), giving
+//                          mu_j; the reference m_j = m_{j-1} unless
+//                          mu_j > m_{j-1} + 8, then mu_j (m_{j-1} comes from
+//                          the other team through shared memory);
 //                          P_j = exp2(S_j scale log2 e - m_j) <= 2^8,
 //                          rounded to fp16 and written back over the
-//                          thread's own S_j columns (key k at column k / 2);
-//                          the team's row sum l, kept relative to the last
-//                          reference it used.
+//                          thread's own S_j columns (keys 64 h + k at
+//                          column 64 h + k / 2); the thread's row sum l,
+//                          kept relative to the last reference it used.
 //   O += P_j V_j           tcgen05 MMA with P_j as the TMEM operand and the
 //                          V_j tile as it lies in the cache ([key][D], the
 //                          N-major B operand: D contiguous) in shared
 //                          memory; O stays in TMEM for the whole walk.
-//   rescale                when m_j > m_{j-1}, the team of tile j scales O
-//                          by 2^(m_{j-1} - m_j) in TMEM after P_{j-1} V_{j-1}
-//                          and before it publishes P_j (rare: the reference
-//                          moves only when a row maximum jumps by 2^8).
-//   epilogue               O / l, l = the teams' sums brought to the last
-//                          reference, written as fp16.
+//   rescale                when m_j > m_{j-1}, the threads of tile j scale
+//                          their half of O by 2^(m_{j-1} - m_j) in TMEM
+//                          after P_{j-1} V_{j-1} and before they publish P_j
+//                          (rare: the reference moves only when a row
+//                          maximum jumps by 2^8).
+//   epilogue               O / l, l = the four threads' sums of a row
+//                          brought to the last reference, written as fp16.
 // The lazily raised reference keeps O accumulating in the tensor core's
 // TMEM with no per-tile read-out, and frees the softmax of tile j+1 from the
 // exponentials of tile j: only the reference, known right after the max,
@@ -52,12 +53,13 @@
 // producers of the K and the V tiles (one lane each; 3-D tensor maps
 // [Hkv][T][D], so keys past T arrive as zeros); 3 the TMA producer of Q (one
 // box per head and 64-wide panel from a 3-D map [H][M][D], rows past M zero),
-// then the P V issuer; 4-7 and 8-11 the softmax teams of the even and the
-// odd tiles; 12-19 the max warps, then the epilogue (two groups of four:
-// keys 0-63 and 64-127 of a tile, columns 0 .. D/2 - 1 and D/2 .. D - 1 of
-// O).  CTAs run heaviest row tiles first across all KV heads.  Every wait
-// is bounded in time; on expiry the CTA records the failure in the status
-// word and returns.
+// then the P V issuer; 4-11 and 12-19 the softmax teams of the even and the
+// odd tiles (warps w and w + 4 of a team: the two halves of the same rows),
+// which also write the output (a quarter of D each).  CTAs run heaviest row
+// tiles first across all KV heads.  Every wait is bounded in time; on
+// expiry the CTA records the failure in the status word and returns, and
+// the two halves of a row leave their loop together (a named barrier has no
+// time limit).
 #include "codec.cuh"
 #include "launch.h"
 
@@ -77,8 +79,8 @@ struct TaCfg {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 640;
-  static constexpr int kMlBytes = 2 * kTR * 4 + 2 * kTR * 8 + 4 * 2 * kTR * 4;   // references, final (l, m), partial maxima
-  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 2 + 4 + 1 + 1;
+  static constexpr int kMlBytes = 4 * kTR * 4 + 4 * kTR * 8 + 8 * kTR * 4;   // references, final (l, m), partial maxima
+  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 2 + 1 + 1;
   static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kMlBytes + kBars * 8 + 16;
   static constexpr uint32_t kOCol = 384;             // O after the three S/P buffers
   static_assert(D == 64 || D == 128, "head dim");
@@ -138,6 +140,22 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
+}
+
+// OR of `pred` over the `count` threads of named barrier `id` (all of them
+// arrive; every one gets the result).  A named barrier has no time limit,
+// so every decision to leave a loop that holds one is taken through it.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
 
 // Largest (hi) or smallest (!hi) of v[e] over e <= cut (all 32 when cut >=
@@ -222,10 +240,10 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t* qs = smem_align<1024>(smem_raw);
   uint8_t* kst = qs + Cfg::kQBytes;                                 // K stages
   uint8_t* vst = kst + Cfg::kKStages * Cfg::kKBytes;                // V stages
-  float* mref = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [2][128] reference of tile j
-  float2* lfin = reinterpret_cast<float2*>(mref + 2 * kTR);         // [2][128] (l, m) of each team
-  float* pmx = reinterpret_cast<float*>(lfin + 2 * kTR);            // [4][2][128] partial extremes of S_j
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmx + 4 * 2 * kTR);
+  float* mref = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128] reference of tile j
+  float2* lfin = reinterpret_cast<float2*>(mref + 4 * kTR);         // [team][half][128] final (l, m)
+  float* pmx = reinterpret_cast<float*>(lfin + 4 * kTR);            // [team][tile parity][half][128] partial extremes
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmx + 8 * kTR);
   uint64_t* k_full = q_full + 1;      // [3] producer: K_j in stage j % 3
   uint64_t* k_empty = k_full + 3;     // [3] MMA: S_j done with stage j % 3
   uint64_t* v_full = k_empty + 3;     // [2] producer: V_j in stage j % 2
@@ -233,9 +251,8 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* s_full = v_empty + 2;     // [3] MMA: S_j in TMEM buffer j % 3
   uint64_t* s_free = s_full + 3;      // [3] MMA: P_j read from buffer j % 3
   uint64_t* p_full = s_free + 3;      // [3] softmax: P_j written
-  uint64_t* r_rdy = p_full + 3;       // [2] softmax: reference of tile j written (slot j % 2)
-  uint64_t* x_rdy = r_rdy + 2;        // [4] max warps: partial extremes of S_j written (slot j % 4)
-  uint64_t* l_rdy = x_rdy + 4;        // softmax: final (l, m) of both teams written
+  uint64_t* r_rdy = p_full + 3;       // [2] softmax: reference of tile j written (barrier j % 2)
+  uint64_t* l_rdy = r_rdy + 2;        // softmax: final (l, m) of every thread written
   uint64_t* drain = l_rdy + 1;        // both issuers: every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -262,7 +279,7 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
@@ -270,8 +287,7 @@ __global__ void __launch_bounds__(640, 1)
     }
     mbar_init(&r_rdy[0], 4);
     mbar_init(&r_rdy[1], 4);
-    for (int i = 0; i < 4; ++i) mbar_init(&x_rdy[i], 8);
-    mbar_init(l_rdy, 8);
+    mbar_init(l_rdy, 16);
     mbar_init(drain, 2);   // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
@@ -349,8 +365,10 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each V
-            // panel; their P at columns 8 kk .. 8 kk + 7 of the S/P buffer
-            tc_mma_ts_f16(dst, pcol + 8 * kk, vds + (uint32_t)(kk * (2048 >> 4)), idesc_o, (j | kk) > 0 ? 1u : 0u);
+            // panel; their P at columns 64 (kk / 4) + 8 (kk % 4) of the S/P
+            // buffer (each half of the keys written by its own threads)
+            tc_mma_ts_f16(dst, pcol + 64 * (kk >> 2) + 8 * (kk & 3), vds + (uint32_t)(kk * (2048 >> 4)), idesc_o,
+                          (j | kk) > 0 ? 1u : 0u);
           }
           tc_commit(&v_empty[st]);
           tc_commit(&s_free[sb]);
@@ -389,11 +407,12 @@ __global__ void __launch_bounds__(640, 1)
           mbar_wait_drain(&full[i % ns], (i / ns) & 1, 100000000ull);
       }
     }
-  } else if (warp < 12) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int team = (warp - 4) >> 2;  // tiles j = team, team + 2, ... (S buffer j % 3)
+    const int team = (warp - 4) >> 3;  // tiles j = team, team + 2, ... (S buffer j % 3)
+    const int half = (warp >> 2) & 1;  // keys [64 half, 64 half + 64) of each tile
     const int r = 32 * (warp & 3) + lane;
-    const int i = q0 + r % QPT;          // query of this row
+    const int i = q0 + r % QPT, h = hk * p.G + r / QPT;   // query and head of this row
     const bool valid = i < p.M;
     // last key this row sees (-1: none), one 32-bit bound for validity, the
     // causal limit and T together
@@ -401,68 +420,84 @@ __global__ void __launch_bounds__(640, 1)
     if (lastl > (long long)p.T - 1) lastl = p.T - 1;
     const int lastk = valid ? (int)lastl : -1;
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t bar_id = 1 + 4 * team + (warp & 3);   // the two warps (halves) of these rows
     const float sc = p.scale_log2;
     const bool hi = sc >= 0.f;           // the max of sc s is sc max s, or sc min s when sc < 0
-    float lsum = 0.f, lref = -INFINITY;  // this team's row sum and the reference it is relative to
-    bool ok = true;
-    for (int j = team; j < nk && ok; j += 2) {
+    float lsum = 0.f, lref = -INFINITY;  // this thread's row sum and the reference it is relative to
+    bool bad = false;                    // a wait ran out since the last pair barrier
+    for (int j = team; j < nk; j += 2) {
       const int sb = j % 3;
-      // the row's extreme raw score over the visible keys of the tile, from
-      // the two halves the max warps formed (they read S_j after its MMA
-      // completed, so S_j is complete here too)
-      ok = __all_sync(0xffffffffu, mbar_wait(&x_rdy[j & 3], (j >> 2) & 1, ctl));
-      if (!ok) break;
-      const uint32_t scol = tmem + lanes + 128 * sb;
-      tc_fence_after();
-      const int kbase = j * kTK;
-      // every key of the tile visible to every row of the warp: no masks
-      const bool full = __all_sync(0xffffffffu, lastk - kbase >= kTK - 1);
-      const float x0 = pmx[(j & 3) * 2 * kTR + r], x1 = pmx[((j & 3) * 2 + 1) * kTR + r];
-      const float t = hi ? fmaxf(x0, x1) : fminf(x0, x1);
+      const uint32_t scol = tmem + lanes + 128 * sb + 64 * half;
+      const int kbase = j * kTK + 64 * half;
+      // S_j and the previous tile's reference (from the other team)
+      const bool got = mbar_wait(&s_full[sb], (j / 3) & 1, ctl) &&
+                       (j == 0 || mbar_wait(&r_rdy[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl));
+      const bool okw = __all_sync(0xffffffffu, got && !bad);
+      // this half's extreme raw score over its visible keys
+      float t = hi ? -INFINITY : INFINITY;
+      if (okw) {
+        tc_fence_after();
+        const bool fullm = __all_sync(0xffffffffu, lastk - kbase >= 63);
+        uint32_t v[64];
+        tmem_ld64_wait(scol, v);
+        const int cut = fullm ? 63 : lastk - kbase;
+        const float t0 = extreme32(v, cut, hi), t1 = extreme32(v + 32, cut - 32, hi);
+        t = hi ? fmaxf(t0, t1) : fminf(t0, t1);
+      }
+      float* pm = pmx + (team * 2 + ((j >> 1) & 1)) * 2 * kTR;   // by tile parity: rewritten two tiles later
+      pm[half * kTR + r] = t;
+      // both halves leave together or go on together (the barrier has no
+      // time limit, so no half may stop short of it)
+      if (bar_red_or(bar_id, 64, !okw)) break;
+      const float tp = pm[(half ^ 1) * kTR + r];
+      t = hi ? fmaxf(t, tp) : fminf(t, tp);
       // mu_j: -inf when the row sees no key of this tile
       const float mu = (t == INFINITY || t == -INFINITY) ? -INFINITY : t * sc;
       // Reference of tile j: that of tile j - 1 unless mu_j exceeds it by
-      // more than kLazy (P stays below 2^kLazy); tile j - 1 belongs to the
-      // other team, whose reference arrives through shared memory.
-      float mprev = -INFINITY;
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&r_rdy[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl));
-        if (!ok) break;
-        mprev = mref[((j - 1) & 1) * kTR + r];
-      }
+      // more than kLazy (P stays below 2^kLazy).
+      // (4 slots: tile j + 4 rewrites slot j % 4 only after both halves of
+      // tile j + 1 have passed their pair barrier of tile j + 3)
+      const float mprev = j >= 1 ? mref[((j - 1) & 3) * kTR + r] : -INFINITY;
       const float mj = mu > mprev + kLazy ? mu : mprev;
-      mref[(j & 1) * kTR + r] = mj;
-      mbar_arrive_warp(&r_rdy[j & 1]);
-      // A raised reference rescales O (P_i V_i of the tiles before j,
-      // relative to mprev) by 2^(mprev - mj), after P_{j-1} V_{j-1} is done
-      // and before P_j is published (so before P_j V_j is issued).
+      if (half == 0) {
+        mref[(j & 3) * kTR + r] = mj;
+        mbar_arrive_warp(&r_rdy[j & 1]);
+      }
+      // A raised reference rescales this half of O (P_i V_i of the tiles
+      // before j, relative to mprev) by 2^(mprev - mj), after P_{j-1} V_{j-1}
+      // is done and before P_j is published (so before P_j V_j is issued).
       const bool resc = mj > mprev && mprev != -INFINITY;
       if (__any_sync(0xffffffffu, resc)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_free[(j - 1) % 3], ((j - 1) / 3) & 1, ctl));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_free[(j - 1) % 3], ((j - 1) / 3) & 1, ctl))) {
+          bad = true;
+          continue;
+        }
         tc_fence_after();
         const float a = resc ? ex2(mprev - mj) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld32_wait(tmem + lanes + Cfg::kOCol + 32 * c, v);
+          const uint32_t oc = tmem + lanes + Cfg::kOCol + (D / 2) * half + 32 * c;
+          tmem_ld32_wait(oc, v);
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * a);
-          tmem_st32(tmem + lanes + Cfg::kOCol + 32 * c, v);
+          tmem_st32(oc, v);
         }
       }
       const float muse = mj == -INFINITY ? 0.f : mj;
       const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(-muse, -muse);
       unsigned long long s2 = 0ull;          // the two lanes' partial row sums
+      // every key of this half visible to every row of the warp: no masks
+      const bool full = __all_sync(0xffffffffu, lastk - kbase >= 63);
       // 16-key chunks, the load of chunk c + 1 in flight while chunk c is
-      // computed; P of keys 16 c .. 16 c + 15 goes to columns 8 c .. 8 c + 7,
-      // S columns this thread has already read
+      // computed; P of keys 64 half + 16 c .. + 15 goes to columns
+      // 64 half + 8 c .. + 7, S columns this thread has already read
       uint32_t v[2][16];
       tmem_ld16_async(scol, v[0]);
       tmem_wait_ld_tied(v[0]);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        if (c < 7) tmem_ld16_async(scol + 16 * (c + 1), v[(c + 1) & 1]);
+      for (int c = 0; c < 4; ++c) {
+        if (c < 3) tmem_ld16_async(scol + 16 * (c + 1), v[(c + 1) & 1]);
         const uint32_t (&x)[16] = v[c & 1];
         const int cut = lastk - (kbase + 16 * c);
         uint32_t w[8];
@@ -477,15 +512,15 @@ __global__ void __launch_bounds__(640, 1)
             p1 = e + 1 <= cut ? p1 : 0.f;
           }
           s2 = add2(s2, pack2(p0, p1));
-          const __half2 h = __floats2half2_rn(p0, p1);
-          w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+          const __half2 hh = __floats2half2_rn(p0, p1);
+          w[e >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
         }
         tmem_st8(scol + 8 * c, w);
-        if (c < 7) tmem_wait_ld_tied(v[(c + 1) & 1]);
+        if (c < 3) tmem_wait_ld_tied(v[(c + 1) & 1]);
       }
       float sum0, sum1;
       unpack2(s2, sum0, sum1);
-      // this team's row sum, kept relative to the latest reference it used
+      // this half's row sum, kept relative to the latest reference it used
       if (mj != -INFINITY) {
         lsum = lsum * ex2(lref - mj) + (sum0 + sum1);
         lref = mj;
@@ -494,58 +529,32 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_before();
       mbar_arrive_warp(&p_full[sb]);
     }
-    lfin[team * kTR + r] = make_float2(lsum, lref);
+    lfin[(team * 2 + half) * kTR + r] = make_float2(lsum, lref);
     mbar_arrive_warp(l_rdy);
-  } else {
-    // ------------------------------------------------------------ max, epilogue
-    const int e = (warp - 12) >> 2;    // keys [64 e, 64 e + 64) of a tile; columns [e D / 2, (e + 1) D / 2) of O
-    const int r = 32 * (warp & 3) + lane;
-    const int i = q0 + r % QPT, h = hk * p.G + r / QPT;   // query and head of this row
-    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
-    constexpr int HC = D / 2;
-    // Per tile: the extreme raw score of this row over the visible keys of
-    // one half of S_j (the max when the scale is >= 0, else the min), for
-    // the softmax team, which then makes one pass over S_j.
-    {
-      long long lastl = CAUSAL ? (long long)p.q_offset + i : (long long)p.T - 1;
-      if (lastl > (long long)p.T - 1) lastl = p.T - 1;
-      const int lastk = i < p.M ? (int)lastl : -1;
-      const bool hi = p.scale_log2 >= 0.f;
-      bool mok = true;
-      for (int j = 0; j < nk && mok; ++j) {
-        const int sb = j % 3;
-        mok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j / 3) & 1, ctl));
-        if (!mok) break;
-        tc_fence_after();
-        const int kb = j * kTK + 64 * e;
-        const bool full = __all_sync(0xffffffffu, lastk - kb >= 63);
-        uint32_t v[64];
-        tmem_ld64_wait(tmem + lanes + 128 * sb + 64 * e, v);
-        const int cut = full ? 63 : lastk - kb;
-        const float t0 = extreme32(v, cut, hi), t1 = extreme32(v + 32, cut - 32, hi);
-        const float t = hi ? fmaxf(t0, t1) : fminf(t0, t1);
-        pmx[((j & 3) * 2 + e) * kTR + r] = t;
-        tc_fence_before();
-        mbar_arrive_warp(&x_rdy[j & 3]);
-      }
-    }
-    // O (relative to the last tile's reference M) / l, l = sum over the
-    // teams of l_t 2^(m_t - M), once every MMA is done
+    // ---------------------------------------------------------- epilogue
+    // O (relative to the last tile's reference M) / l, l = the sum over the
+    // four (team, half) threads of the row of l_t 2^(m_t - M), once every
+    // MMA is done; this thread writes columns [g D / 4, (g + 1) D / 4)
+    constexpr int QC = D / 4;
+    const int g = team * 2 + half;
     const bool ok = nk > 0 && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 256) &&
                                                             mbar_wait_idle(drain, 0, ctl, 256));
     if (ok) {
       tc_fence_after();
-      const float M = mref[((nk - 1) & 1) * kTR + r];
-      const float2 f0 = lfin[r], f1 = lfin[kTR + r];
-      const float l = (f0.y == -INFINITY ? 0.f : f0.x * ex2(f0.y - M)) +
-                      (f1.y == -INFINITY ? 0.f : f1.x * ex2(f1.y - M));
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool store = i < p.M && in_bounds(h < p.H, p.status, kSiteAttnO);
-      __half* orow = p.o + (long long)(store ? i : 0) * p.H * D + (long long)(store ? h : 0) * D + e * HC;
+      const float M = mref[((nk - 1) & 3) * kTR + r];
+      float l = 0.f;
 #pragma unroll
-      for (int c = 0; c < HC / 16; ++c) {
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = lfin[q * kTR + r];
+        if (f.y != -INFINITY) l += f.x * ex2(f.y - M);
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = valid && in_bounds(h < p.H, p.status, kSiteAttnO);
+      __half* orow = p.o + (long long)(store ? i : 0) * p.H * D + (long long)(store ? h : 0) * D + g * QC;
+#pragma unroll
+      for (int c = 0; c < QC / 16; ++c) {
         uint32_t v[16];
-        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + e * HC + 16 * c, v);
+        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + g * QC + 16 * c, v);
         uint32_t w[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
