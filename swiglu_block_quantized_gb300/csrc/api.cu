@@ -638,6 +638,7 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   p.tsplit = a.tsplit;
   p.status = m4q::status_words();
   if (!p.status) return M4Q_ERR_CUDA;
+  p.nsm = dev.sms;
   if (a.nsplit > 1) {
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +

@@ -7,10 +7,13 @@
 // online softmax) and "Releases" v0.3.0 (GQA, causal mask with a sequence
 // offset, head dims 64 and 128).
 //
-// One CTA takes 128 rows of one KV head, 128 / G consecutive queries of each
-// of its G query heads (row = g (128 / G) + i - q0, head-major, so that each
-// head's rows arrive as one TMA box), and walks the key tiles of 128 keys
-// its rows can see:
+// The work items are (128 rows of one KV head: 128 / G consecutive queries
+// of each of its G query heads, row = g (128 / G) + i - q0, head-major, so
+// that each head's rows arrive as one TMA box).  One persistent CTA per SM
+// walks its items one after another, and within an item the key tiles of
+// 128 keys its rows can see; the pipeline runs on across items (the next
+// item's Q loads once the scores of the last are done, its first P V waits
+// until the last item's O is read out):
 //   S_j = Q K_j^T          tcgen05 MMA, both operands K-major in 128-byte
 //                          swizzled shared memory, S_j in TMEM (fp32), in
 //                          buffer j % 3.
@@ -49,14 +52,15 @@
 // the tensor pipe (a tcgen05.mma is accepted about once per MMA duration, so
 // a single issuer's waits leave the pipe idle).
 //
-// Warps: 0 the score-MMA issuer (one lane) and TMEM owner; 1 and 2 TMA
-// producers of the K and the V tiles (one lane each; 3-D tensor maps
-// [Hkv][T][D], so keys past T arrive as zeros); 3 the TMA producer of Q (one
-// box per head and 64-wide panel from a 3-D map [H][M][D], rows past M zero),
-// then the P V issuer; 4-11 and 12-19 the softmax teams of the even and the
+// Warps: 0 the score-MMA issuer (one lane) and TMEM owner; 1 the TMA
+// producer of each item's Q (one box per head and 64-wide panel from a 3-D
+// map [H][M][D], rows past M zero) and of the K tiles, 2 of the V tiles (one
+// lane each; 3-D tensor maps [Hkv][T][D], so keys past T arrive as zeros);
+// 3 the P V issuer; 4-11 and 12-19 the softmax teams of the even and the
 // odd tiles (warps w and w + 4 of a team: the two halves of the same rows),
-// which also write the output (a quarter of D each).  CTAs run heaviest row
-// tiles first across all KV heads.  Every wait is bounded in time; on
+// which also write each item's output (a quarter of D each).  Items go out
+// heaviest first (every head's last row tile, then the one before, ...) in
+// a zigzag over the CTAs.  Every wait is bounded in time; on
 // expiry the CTA records the failure in the status word and returns, and
 // the two halves of a row leave their loop together (a named barrier has no
 // time limit).
@@ -79,8 +83,8 @@ struct TaCfg {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
   static constexpr int kThreads = 640;
-  static constexpr int kMlBytes = 4 * kTR * 4 + 4 * kTR * 8 + 8 * kTR * 4;   // references, final (l, m), partial maxima
-  static constexpr int kBars = 1 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 2 + 1 + 1;
+  static constexpr int kMlBytes = 4 * kTR * 4 + 8 * kTR * 8 + 8 * kTR * 4;   // references, final (l, m), partial maxima
+  static constexpr int kBars = 2 + 3 + 3 + 2 + 2 + 3 + 3 + 3 + 2 + 1 + 1 + 1 + 1;
   static constexpr int kSmem = 1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kMlBytes + kBars * 8 + 16;
   static constexpr uint32_t kOCol = 384;             // O after the three S/P buffers
   static_assert(D == 64 || D == 128, "head dim");
@@ -231,6 +235,33 @@ __device__ __forceinline__ uint64_t sdesc_sw128_nmajor(uint32_t saddr, uint32_t 
   return d;
 }
 
+// Work items: (row tile, KV head) in decreasing order of key count (the
+// row tile rt of every head, then rt - 1, ...), handed to the persistent
+// CTAs in a zigzag: CTA b takes items b, 2 G - 1 - b, 2 G + b, ..., so that
+// the heavy and the light items of successive rounds even out.
+struct TaItem {
+  int q0, hk, nk;
+};
+
+__device__ __forceinline__ int ta_item_index(int round, int G) {
+  return round * G + ((round & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ TaItem ta_item(const AttnParams& p, int n, int QPT, int rtiles) {
+  TaItem it;
+  it.hk = n % p.Hkv;
+  it.q0 = (rtiles - 1 - n / p.Hkv) * QPT;
+  // keys [0, kend) are visible to some row of the tile (at least key 0)
+  int kend = p.T;
+  if (CAUSAL) {
+    const long long vis = (long long)p.q_offset + min(p.M, it.q0 + QPT);
+    if (vis < kend) kend = (int)vis;
+  }
+  it.nk = (kend + kTK - 1) / kTK;
+  return it;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(640, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -240,40 +271,35 @@ __global__ void __launch_bounds__(640, 1)
   uint8_t* qs = smem_align<1024>(smem_raw);
   uint8_t* kst = qs + Cfg::kQBytes;                                 // K stages
   uint8_t* vst = kst + Cfg::kKStages * Cfg::kKBytes;                // V stages
-  float* mref = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128] reference of tile j
-  float2* lfin = reinterpret_cast<float2*>(mref + 4 * kTR);         // [team][half][128] final (l, m)
-  float* pmx = reinterpret_cast<float*>(lfin + 4 * kTR);            // [team][tile parity][half][128] partial extremes
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmx + 8 * kTR);
-  uint64_t* k_full = q_full + 1;      // [3] producer: K_j in stage j % 3
-  uint64_t* k_empty = k_full + 3;     // [3] MMA: S_j done with stage j % 3
-  uint64_t* v_full = k_empty + 3;     // [2] producer: V_j in stage j % 2
-  uint64_t* v_empty = v_full + 2;     // [2] MMA: P_j V_j done with stage j % 2
-  uint64_t* s_full = v_empty + 2;     // [3] MMA: S_j in TMEM buffer j % 3
-  uint64_t* s_free = s_full + 3;      // [3] MMA: P_j read from buffer j % 3
-  uint64_t* p_full = s_free + 3;      // [3] softmax: P_j written
-  uint64_t* r_rdy = p_full + 3;       // [2] softmax: reference of tile j written (barrier j % 2)
-  uint64_t* l_rdy = r_rdy + 2;        // softmax: final (l, m) of every thread written
-  uint64_t* drain = l_rdy + 1;        // both issuers: every MMA complete
+  float* mref = reinterpret_cast<float*>(vst + Cfg::kVStages * Cfg::kVBytes);   // [4][128] reference of tile g
+  float2* lfin = reinterpret_cast<float2*>(mref + 4 * kTR);         // [item parity][team][half][128] final (l, m)
+  float* pmx = reinterpret_cast<float*>(lfin + 8 * kTR);            // [team][tile parity][half][128] partial extremes
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(pmx + 8 * kTR);   // K producer: Q of item w
+  uint64_t* q_empty = q_full + 1;     // score issuer: the scores of item w are done with Q
+  uint64_t* k_full = q_empty + 1;     // [3] producer: K of tile g in stage g % 3
+  uint64_t* k_empty = k_full + 3;     // [3] MMA: S_g done with stage g % 3
+  uint64_t* v_full = k_empty + 3;     // [2] producer: V of tile g in stage g % 2
+  uint64_t* v_empty = v_full + 2;     // [2] MMA: P_g V_g done with stage g % 2
+  uint64_t* s_full = v_empty + 2;     // [3] MMA: S_g in TMEM buffer g % 3
+  uint64_t* s_free = s_full + 3;      // [3] MMA: P_g read from buffer g % 3
+  uint64_t* p_full = s_free + 3;      // [3] softmax: P_g written
+  uint64_t* r_rdy = p_full + 3;       // [2] softmax: reference of tile g written (barrier g % 2)
+  uint64_t* l_rdy = r_rdy + 2;        // softmax: final (l, m) of item w written by every thread
+  uint64_t* o_done = l_rdy + 1;       // P V issuer: every P V of item w done
+  uint64_t* o_free = o_done + 1;      // softmax: O of item w read out
+  uint64_t* drain = o_free + 1;       // both issuers: every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int QPT = kTR / p.G;             // queries per tile (G divides 128)
-  // row tiles in decreasing order of their key count, every KV head at once
   const int rtiles = (p.M + QPT - 1) / QPT;
-  const int hk = (int)(blockIdx.x % (unsigned)p.Hkv);
-  const int rt = rtiles - 1 - (int)(blockIdx.x / (unsigned)p.Hkv);
-  const int q0 = rt * QPT;
-  // keys [0, kend) are visible to some row of this tile
-  int kend = p.T;
-  if (CAUSAL) {
-    const long long vis = (long long)p.q_offset + min(p.M, q0 + QPT);
-    if (vis < kend) kend = (int)vis;
-  }
-  const int nk = (kend + kTK - 1) / kTK;
+  const int NI = rtiles * p.Hkv;         // work items
+  const int G = (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < 3; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -288,6 +314,8 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&r_rdy[0], 4);
     mbar_init(&r_rdy[1], 4);
     mbar_init(l_rdy, 16);
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 16);
     mbar_init(drain, 2);   // one commit from each MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
@@ -304,74 +332,81 @@ __global__ void __launch_bounds__(640, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads: warp 0 the score MMAs, warp 3 (after the Q copy)
-    // the P V MMAs.  Each waits only for its own operands, so the waits and
-    // the issue of one overlap the MMAs of the other in the tensor pipe.
-    if (warp == 3 && lane == 0) {
-      // Q: rows g QPT .. g QPT + QPT - 1 of each 64-wide panel from head
-      // hk G + g, queries q0 .. (boxes start on 1024-byte swizzle atoms:
-      // QPT is a multiple of 8)
-      tma_prefetch_desc(&tm_q);
-      mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
-      for (int g = 0; g < p.G; ++g)
-#pragma unroll
-        for (int pn = 0; pn < D / 64; ++pn)
-          if (in_bounds(q0 >= 0 && hk * p.G + g < p.H, p.status, kSiteAttnQ))
-            tma_load_3d(qs + pn * (kTR * 128) + g * QPT * 128, &tm_q, q_full, 64 * pn, q0, hk * p.G + g);
-    }
-    if (lane == 0 && nk > 0) {
+    // Two issuing threads: warp 0 the score MMAs, warp 3 the P V MMAs.  Each
+    // waits only for its own operands, so the waits and the issue of one
+    // overlap the other's MMAs in the tensor pipe.  Tiles are numbered g
+    // across the items of this CTA; every ring follows g.
+    if (lane == 0) {
       if (warp == 0) {
-        // S_j = Q K_j^T into buffer j % 3 once K_j has landed and
-        // P_{j-3} V_{j-3} has read that buffer
+        // S_g = Q K_g^T into buffer g % 3 once K_g has landed and P_{g-3}
+        // V_{g-3} has read that buffer
         constexpr uint32_t idesc_s = idesc_f16_f32(128, kTK);
         // Operand descriptors, formed once: a descriptor is (address / 16)
         // in its low 14 bits, so that of a later slice or stage is a fixed
         // offset from the first.
         const uint64_t qd = sdesc_sw128_kmajor(smem_u32(qs));
         const uint64_t kd = sdesc_sw128_kmajor(smem_u32(kst));
-        bool ok = mbar_wait(q_full, 0, ctl);
-        for (int j = 0; j < nk && ok; ++j) {
-          const int sb = j % 3, sk = j % 3;   // S buffer and K stage
-          ok = mbar_wait(&k_full[sk], (j / 3) & 1, ctl);
-          if (j >= 3) ok = ok && mbar_wait(&s_free[sb], ((j / 3) - 1) & 1, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kds = kd + (uint64_t)(sk * (Cfg::kKBytes >> 4));
-          const uint32_t dst = tmem + 128 * sb;
+        bool ok = true;
+        int g = 0;
+        for (int w = 0; ok; ++w) {
+          const int n = ta_item_index(w, G);
+          if (n >= NI) break;
+          const TaItem it = ta_item<CAUSAL>(p, n, QPT, rtiles);
+          ok = mbar_wait(q_full, w & 1, ctl);
+          for (int j = 0; j < it.nk && ok; ++j, ++g) {
+            const int sb = g % 3;   // S buffer and K stage
+            ok = mbar_wait(&k_full[sb], (g / 3) & 1, ctl);
+            if (g >= 3) ok = ok && mbar_wait(&s_free[sb], ((g / 3) - 1) & 1, ctl);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kds = kd + (uint64_t)(sb * (Cfg::kKBytes >> 4));
+            const uint32_t dst = tmem + 128 * sb;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // 16-element slice kk: panel kk / 4, 32 bytes per slice inside it
-            constexpr int kPanelA = kTR * 128 >> 4, kPanelB = kTK * 128 >> 4;
-            const uint32_t off_a = (kk >> 2) * kPanelA + 2 * (kk & 3);
-            const uint32_t off_b = (kk >> 2) * kPanelB + 2 * (kk & 3);
-            mma_ss_f16(dst, qd + off_a, kds + off_b, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // 16-element slice kk: panel kk / 4, 32 bytes per slice inside it
+              constexpr int kPanelA = kTR * 128 >> 4, kPanelB = kTK * 128 >> 4;
+              const uint32_t off_a = (kk >> 2) * kPanelA + 2 * (kk & 3);
+              const uint32_t off_b = (kk >> 2) * kPanelB + 2 * (kk & 3);
+              mma_ss_f16(dst, qd + off_a, kds + off_b, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&s_full[sb]);
+            tc_commit(&k_empty[sb]);
           }
-          tc_commit(&s_full[sb]);
-          tc_commit(&k_empty[sk]);
+          if (ok) tc_commit(q_empty);   // Q may be replaced once these MMAs are done
         }
       } else {
-        // O += P_j V_j once P_j is written and V_j has landed (a rescale of
-        // O, when tile j raised the reference, precedes P_j)
+        // O (+)= P_g V_g once P_g is written and V_g has landed; the first
+        // tile of an item also waits until the previous item's O is read
+        // out (a rescale of O, when tile g raised the reference, precedes
+        // P_g)
         constexpr uint32_t idesc_o = idesc_f16_f32(128, D) | (1u << 16);   // B (V) N-major
         const uint64_t vd = sdesc_sw128_nmajor(smem_u32(vst), kTK * 128);
         bool ok = true;
-        for (int j = 0; j < nk && ok; ++j) {
-          const int st = j & 1, sb = j % 3;   // V stage and S/P buffer
-          ok = mbar_wait(&v_full[st], (j >> 1) & 1, ctl) && mbar_wait(&p_full[sb], (j / 3) & 1, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vds = vd + (uint64_t)(st * (Cfg::kVBytes >> 4));
-          const uint32_t dst = tmem + Cfg::kOCol, pcol = tmem + 128 * sb;
+        int g = 0;
+        for (int w = 0; ok; ++w) {
+          const int n = ta_item_index(w, G);
+          if (n >= NI) break;
+          const TaItem it = ta_item<CAUSAL>(p, n, QPT, rtiles);
+          for (int j = 0; j < it.nk && ok; ++j, ++g) {
+            const int st = g & 1, sb = g % 3;   // V stage and S/P buffer
+            ok = mbar_wait(&v_full[st], (g >> 1) & 1, ctl) && mbar_wait(&p_full[sb], (g / 3) & 1, ctl);
+            if (j == 0 && w >= 1) ok = ok && mbar_wait(o_free, (w - 1) & 1, ctl);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vds = vd + (uint64_t)(st * (Cfg::kVBytes >> 4));
+            const uint32_t dst = tmem + Cfg::kOCol, pcol = tmem + 128 * sb;
 #pragma unroll
-          for (int kk = 0; kk < kTK / 16; ++kk) {
-            // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each V
-            // panel; their P at columns 64 (kk / 4) + 8 (kk % 4) of the S/P
-            // buffer (each half of the keys written by its own threads)
-            tc_mma_ts_f16(dst, pcol + 64 * (kk >> 2) + 8 * (kk & 3), vds + (uint32_t)(kk * (2048 >> 4)), idesc_o,
-                          (j | kk) > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTK / 16; ++kk) {
+              // keys 16 kk .. 16 kk + 15: two 8-key atoms, 2 KB into each V
+              // panel; their P at columns 64 (kk / 4) + 8 (kk % 4) of the S/P
+              // buffer (each half of the keys written by its own threads)
+              tc_mma_ts_f16(dst, pcol + 64 * (kk >> 2) + 8 * (kk & 3), vds + (uint32_t)(kk * (2048 >> 4)), idesc_o,
+                            (j | kk) > 0 ? 1u : 0u);
+            }
+            tc_commit(&v_empty[st]);
+            tc_commit(&s_free[sb]);
           }
-          tc_commit(&v_empty[st]);
-          tc_commit(&s_free[sb]);
+          if (ok) tc_commit(o_done);   // O of item w complete once these MMAs are done
         }
       }
       // Every MMA of both issuers completes before the CTA frees TMEM.
@@ -381,9 +416,11 @@ __global__ void __launch_bounds__(640, 1)
     __syncwarp();
   } else if (warp < 3) {
     // ------------------------------------------------------------ loaders
-    if ((warp == 1 || warp == 2) && lane == 0) {
-      // warp 1: K_j into stage j % 3 after S_{j-3}; warp 2: V_j into stage
-      // j % 2 after P_{j-2} V_{j-2}.  D / 64 boxes of [128 keys][64 d] each.
+    if (lane == 0) {
+      // warp 1: per item Q (after the previous item's scores), then K of
+      // tile g into stage g % 3 after S_{g-3}; warp 2: V of tile g into
+      // stage g % 2 after P_{g-2} V_{g-2}.  D / 64 boxes of [128 keys][64 d]
+      // each; Q in one box per head and panel.
       const bool isk = warp == 1;
       const CUtensorMap* map = isk ? &tm_k : &tm_v;
       const int ns = isk ? 3 : 2;
@@ -391,181 +428,223 @@ __global__ void __launch_bounds__(640, 1)
       uint64_t* empty = isk ? k_empty : v_empty;
       uint8_t* ring = isk ? kst : vst;
       tma_prefetch_desc(map);
+      if (isk) tma_prefetch_desc(&tm_q);
       bool ok = true;
-      int issued = 0;
-      for (int j = 0; j < nk && ok; ++j, ++issued) {
-        const int sl = j % ns, k0 = j * kTK;
-        if (j >= ns && !mbar_wait_idle(&empty[sl], ((j / ns) - 1) & 1, ctl, 128)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[sl], Cfg::kKBytes);
+      int g = 0, wq = -1;   // tiles issued; the last item whose Q was issued
+      for (int w = 0; ok; ++w) {
+        const int n = ta_item_index(w, G);
+        if (n >= NI) break;
+        const TaItem it = ta_item<CAUSAL>(p, n, QPT, rtiles);
+        if (isk) {
+          // Q: rows g QPT .. g QPT + QPT - 1 of each 64-wide panel from head
+          // hk G + g, queries q0 .. (boxes start on 1024-byte swizzle atoms:
+          // QPT is a multiple of 8)
+          if (w >= 1 && !mbar_wait_idle(q_empty, (w - 1) & 1, ctl, 128)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
+          for (int gq = 0; gq < p.G; ++gq)
 #pragma unroll
-        for (int pn = 0; pn < D / 64; ++pn)
-          if (in_bounds(k0 >= 0, p.status, kSiteAttnKV))
-            tma_load_3d(ring + sl * Cfg::kKBytes + pn * (kTK * 128), map, &full[sl], 64 * pn, k0, hk);
+            for (int pn = 0; pn < D / 64; ++pn)
+              if (in_bounds(it.q0 >= 0 && it.hk * p.G + gq < p.H, p.status, kSiteAttnQ))
+                tma_load_3d(qs + pn * (kTR * 128) + gq * QPT * 128, &tm_q, q_full, 64 * pn, it.q0,
+                            it.hk * p.G + gq);
+          wq = w;
+        }
+        for (int j = 0; j < it.nk; ++j, ++g) {
+          const int sl = g % ns, k0 = j * kTK;
+          if (g >= ns && !mbar_wait_idle(&empty[sl], ((g / ns) - 1) & 1, ctl, 128)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[sl], Cfg::kKBytes);
+#pragma unroll
+          for (int pn = 0; pn < D / 64; ++pn)
+            if (in_bounds(k0 >= 0, p.status, kSiteAttnKV))
+              tma_load_3d(ring + sl * Cfg::kKBytes + pn * (kTK * 128), map, &full[sl], 64 * pn, k0, it.hk);
+        }
       }
       if (!ok) {
-        for (int i = (issued > ns ? issued - ns : 0); i < issued; ++i)
-          mbar_wait_drain(&full[i % ns], (i / ns) & 1, 100000000ull);
+        // wait for the copies in flight before the CTA can leave
+        for (int i = (g > ns ? g - ns : 0); i < g; ++i) mbar_wait_drain(&full[i % ns], (i / ns) & 1, 100000000ull);
+        if (isk && wq >= 0) mbar_wait_drain(q_full, wq & 1, 100000000ull);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int team = (warp - 4) >> 3;  // tiles j = team, team + 2, ... (S buffer j % 3)
+    const int team = (warp - 4) >> 3;  // tiles g = team, team + 2, ... (S buffer g % 3)
     const int half = (warp >> 2) & 1;  // keys [64 half, 64 half + 64) of each tile
     const int r = 32 * (warp & 3) + lane;
-    const int i = q0 + r % QPT, h = hk * p.G + r / QPT;   // query and head of this row
-    const bool valid = i < p.M;
-    // last key this row sees (-1: none), one 32-bit bound for validity, the
-    // causal limit and T together
-    long long lastl = CAUSAL ? (long long)p.q_offset + i : (long long)p.T - 1;
-    if (lastl > (long long)p.T - 1) lastl = p.T - 1;
-    const int lastk = valid ? (int)lastl : -1;
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t bar_id = 1 + 4 * team + (warp & 3);   // the two warps (halves) of these rows
     const float sc = p.scale_log2;
     const bool hi = sc >= 0.f;           // the max of sc s is sc max s, or sc min s when sc < 0
-    float lsum = 0.f, lref = -INFINITY;  // this thread's row sum and the reference it is relative to
+    constexpr int QC = D / 4;            // output columns of this thread: [gq QC, (gq + 1) QC)
+    const int gq = team * 2 + half;
     bool bad = false;                    // a wait ran out since the last pair barrier
-    for (int j = team; j < nk; j += 2) {
-      const int sb = j % 3;
-      const uint32_t scol = tmem + lanes + 128 * sb + 64 * half;
-      const int kbase = j * kTK + 64 * half;
-      // S_j and the previous tile's reference (from the other team)
-      const bool got = mbar_wait(&s_full[sb], (j / 3) & 1, ctl) &&
-                       (j == 0 || mbar_wait(&r_rdy[(j - 1) & 1], ((j - 1) >> 1) & 1, ctl));
-      const bool okw = __all_sync(0xffffffffu, got && !bad);
-      // this half's extreme raw score over its visible keys
-      float t = hi ? -INFINITY : INFINITY;
-      if (okw) {
-        tc_fence_after();
-        const bool fullm = __all_sync(0xffffffffu, lastk - kbase >= 63);
-        uint32_t v[64];
-        tmem_ld64_wait(scol, v);
-        const int cut = fullm ? 63 : lastk - kbase;
-        const float t0 = extreme32(v, cut, hi), t1 = extreme32(v + 32, cut - 32, hi);
-        t = hi ? fmaxf(t0, t1) : fminf(t0, t1);
-      }
-      float* pm = pmx + (team * 2 + ((j >> 1) & 1)) * 2 * kTR;   // by tile parity: rewritten two tiles later
-      pm[half * kTR + r] = t;
-      // both halves leave together or go on together (the barrier has no
-      // time limit, so no half may stop short of it)
-      if (bar_red_or(bar_id, 64, !okw)) break;
-      const float tp = pm[(half ^ 1) * kTR + r];
-      t = hi ? fmaxf(t, tp) : fminf(t, tp);
-      // mu_j: -inf when the row sees no key of this tile
-      const float mu = (t == INFINITY || t == -INFINITY) ? -INFINITY : t * sc;
-      // Reference of tile j: that of tile j - 1 unless mu_j exceeds it by
-      // more than kLazy (P stays below 2^kLazy).
-      // (4 slots: tile j + 4 rewrites slot j % 4 only after both halves of
-      // tile j + 1 have passed their pair barrier of tile j + 3)
-      const float mprev = j >= 1 ? mref[((j - 1) & 3) * kTR + r] : -INFINITY;
-      const float mj = mu > mprev + kLazy ? mu : mprev;
-      if (half == 0) {
-        mref[(j & 3) * kTR + r] = mj;
-        mbar_arrive_warp(&r_rdy[j & 1]);
-      }
-      // A raised reference rescales this half of O (P_i V_i of the tiles
-      // before j, relative to mprev) by 2^(mprev - mj), after P_{j-1} V_{j-1}
-      // is done and before P_j is published (so before P_j V_j is issued).
-      const bool resc = mj > mprev && mprev != -INFINITY;
-      if (__any_sync(0xffffffffu, resc)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_free[(j - 1) % 3], ((j - 1) / 3) & 1, ctl))) {
-          bad = true;
-          continue;
+    bool stop = false;
+    int g = 0;
+    for (int w = 0; !stop; ++w) {
+      const int n = ta_item_index(w, G);
+      if (n >= NI) break;
+      const TaItem it = ta_item<CAUSAL>(p, n, QPT, rtiles);
+      const int i = it.q0 + r % QPT, h = it.hk * p.G + r / QPT;   // query and head of this row
+      const bool valid = i < p.M;
+      // last key this row sees (-1: none), one 32-bit bound for validity, the
+      // causal limit and T together
+      long long lastl = CAUSAL ? (long long)p.q_offset + i : (long long)p.T - 1;
+      if (lastl > (long long)p.T - 1) lastl = p.T - 1;
+      const int lastk = valid ? (int)lastl : -1;
+      float lsum = 0.f, lref = -INFINITY;  // this thread's row sum and the reference it is relative to
+      const int g0 = g;
+      // this team's tiles of the item: those with g = g0 + j of its parity
+      for (int j = (team - g0) & 1; j < it.nk; j += 2) {
+        const int gt = g0 + j, sb = gt % 3;
+        const uint32_t scol = tmem + lanes + 128 * sb + 64 * half;
+        const int kbase = j * kTK + 64 * half;
+        // S_g and the previous tile's reference (from the other team; also
+        // across items, which keeps the hand-off one phase apart)
+        const bool got = mbar_wait(&s_full[sb], (gt / 3) & 1, ctl) &&
+                         (gt == 0 || mbar_wait(&r_rdy[(gt - 1) & 1], ((gt - 1) >> 1) & 1, ctl));
+        const bool okw = __all_sync(0xffffffffu, got && !bad);
+        // this half's extreme raw score over its visible keys
+        float t = hi ? -INFINITY : INFINITY;
+        if (okw) {
+          tc_fence_after();
+          const bool fullm = __all_sync(0xffffffffu, lastk - kbase >= 63);
+          uint32_t v[64];
+          tmem_ld64_wait(scol, v);
+          const int cut = fullm ? 63 : lastk - kbase;
+          const float t0 = extreme32(v, cut, hi), t1 = extreme32(v + 32, cut - 32, hi);
+          t = hi ? fmaxf(t0, t1) : fminf(t0, t1);
         }
-        tc_fence_after();
-        const float a = resc ? ex2(mprev - mj) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          const uint32_t oc = tmem + lanes + Cfg::kOCol + (D / 2) * half + 32 * c;
-          tmem_ld32_wait(oc, v);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * a);
-          tmem_st32(oc, v);
+        float* pm = pmx + (team * 2 + ((gt >> 1) & 1)) * 2 * kTR;   // by tile parity: rewritten two tiles later
+        pm[half * kTR + r] = t;
+        // both halves leave together or go on together (the barrier has no
+        // time limit, so no half may stop short of it)
+        if (bar_red_or(bar_id, 64, !okw)) {
+          stop = true;
+          break;
         }
-      }
-      const float muse = mj == -INFINITY ? 0.f : mj;
-      const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(-muse, -muse);
-      unsigned long long s2 = 0ull;          // the two lanes' partial row sums
-      // every key of this half visible to every row of the warp: no masks
-      const bool full = __all_sync(0xffffffffu, lastk - kbase >= 63);
-      // 16-key chunks, the load of chunk c + 1 in flight while chunk c is
-      // computed; P of keys 64 half + 16 c .. + 15 goes to columns
-      // 64 half + 8 c .. + 7, S columns this thread has already read
-      uint32_t v[2][16];
-      tmem_ld16_async(scol, v[0]);
-      tmem_wait_ld_tied(v[0]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < 3) tmem_ld16_async(scol + 16 * (c + 1), v[(c + 1) & 1]);
-        const uint32_t (&x)[16] = v[c & 1];
-        const int cut = lastk - (kbase + 16 * c);
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float a0, a1;
-          unpack2(fma2(pack2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc2, nm2), a0, a1);
-          float p0 = ex2(a0);
-          float p1 = ex2(a1);
-          if (!full) {
-            p0 = e <= cut ? p0 : 0.f;
-            p1 = e + 1 <= cut ? p1 : 0.f;
+        const float tp = pm[(half ^ 1) * kTR + r];
+        t = hi ? fmaxf(t, tp) : fminf(t, tp);
+        // mu: -inf when the row sees no key of this tile
+        const float mu = (t == INFINITY || t == -INFINITY) ? -INFINITY : t * sc;
+        // Reference of the tile: that of the item's previous tile unless mu
+        // exceeds it by more than kLazy (P stays below 2^kLazy).  4 slots:
+        // tile g + 4 rewrites slot g % 4 only after both halves of tile g + 1
+        // have passed their pair barrier of tile g + 3.
+        const float mprev = j >= 1 ? mref[((gt - 1) & 3) * kTR + r] : -INFINITY;
+        const float mj = mu > mprev + kLazy ? mu : mprev;
+        if (half == 0) {
+          mref[(gt & 3) * kTR + r] = mj;
+          mbar_arrive_warp(&r_rdy[gt & 1]);
+        }
+        // A raised reference rescales this half of O (P V of the item's
+        // earlier tiles, relative to mprev) by 2^(mprev - mj), after the
+        // previous tile's P V is done and before P_g is published.
+        const bool resc = mj > mprev && mprev != -INFINITY;
+        if (__any_sync(0xffffffffu, resc)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&s_free[(gt - 1) % 3], ((gt - 1) / 3) & 1, ctl))) {
+            bad = true;
+            continue;
           }
-          s2 = add2(s2, pack2(p0, p1));
-          const __half2 hh = __floats2half2_rn(p0, p1);
-          w[e >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          tc_fence_after();
+          const float a = resc ? ex2(mprev - mj) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[32];
+            const uint32_t oc = tmem + lanes + Cfg::kOCol + (D / 2) * half + 32 * c;
+            tmem_ld32_wait(oc, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * a);
+            tmem_st32(oc, v);
+          }
         }
-        tmem_st8(scol + 8 * c, w);
-        if (c < 3) tmem_wait_ld_tied(v[(c + 1) & 1]);
+        const float muse = mj == -INFINITY ? 0.f : mj;
+        const unsigned long long sc2 = pack2(sc, sc), nm2 = pack2(-muse, -muse);
+        unsigned long long s2 = 0ull;          // the two lanes' partial row sums
+        // every key of this half visible to every row of the warp: no masks
+        const bool full = __all_sync(0xffffffffu, lastk - kbase >= 63);
+        // 16-key chunks, the load of chunk c + 1 in flight while chunk c is
+        // computed; P of keys 64 half + 16 c .. + 15 goes to columns
+        // 64 half + 8 c .. + 7, S columns this thread has already read
+        uint32_t v[2][16];
+        tmem_ld16_async(scol, v[0]);
+        tmem_wait_ld_tied(v[0]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) tmem_ld16_async(scol + 16 * (c + 1), v[(c + 1) & 1]);
+          const uint32_t (&x)[16] = v[c & 1];
+          const int cut = lastk - (kbase + 16 * c);
+          uint32_t wv[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float a0, a1;
+            unpack2(fma2(pack2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), sc2, nm2), a0, a1);
+            float p0 = ex2(a0);
+            float p1 = ex2(a1);
+            if (!full) {
+              p0 = e <= cut ? p0 : 0.f;
+              p1 = e + 1 <= cut ? p1 : 0.f;
+            }
+            s2 = add2(s2, pack2(p0, p1));
+            const __half2 hh = __floats2half2_rn(p0, p1);
+            wv[e >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+          tmem_st8(scol + 8 * c, wv);
+          if (c < 3) tmem_wait_ld_tied(v[(c + 1) & 1]);
+        }
+        float sum0, sum1;
+        unpack2(s2, sum0, sum1);
+        // this half's row sum, kept relative to the latest reference it used
+        if (mj != -INFINITY) {
+          lsum = lsum * ex2(lref - mj) + (sum0 + sum1);
+          lref = mj;
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive_warp(&p_full[sb]);
       }
-      float sum0, sum1;
-      unpack2(s2, sum0, sum1);
-      // this half's row sum, kept relative to the latest reference it used
-      if (mj != -INFINITY) {
-        lsum = lsum * ex2(lref - mj) + (sum0 + sum1);
-        lref = mj;
+      if (stop) break;
+      g = g0 + it.nk;
+      // ---------------------------------------------------------- epilogue
+      // O (relative to the item's last reference M) / l, l = the sum over
+      // the four (team, half) threads of the row of l_t 2^(m_t - M), once
+      // every P V of the item is done.  Entries by item parity: item w + 2
+      // rewrites them only after every thread has passed l_rdy of item
+      // w + 1, i.e. after its epilogue of item w.
+      lfin[((w & 1) * 4 + gq) * kTR + r] = make_float2(lsum, lref);
+      mbar_arrive_warp(l_rdy);
+      const bool oke = !bad && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, w & 1, ctl, 256) &&
+                                                            mbar_wait_idle(o_done, w & 1, ctl, 256));
+      if (!oke) {
+        bad = true;   // leaves at the next pair barrier, with the other half
+        continue;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive_warp(&p_full[sb]);
-    }
-    lfin[(team * 2 + half) * kTR + r] = make_float2(lsum, lref);
-    mbar_arrive_warp(l_rdy);
-    // ---------------------------------------------------------- epilogue
-    // O (relative to the last tile's reference M) / l, l = the sum over the
-    // four (team, half) threads of the row of l_t 2^(m_t - M), once every
-    // MMA is done; this thread writes columns [g D / 4, (g + 1) D / 4)
-    constexpr int QC = D / 4;
-    const int g = team * 2 + half;
-    const bool ok = nk > 0 && __all_sync(0xffffffffu, mbar_wait_idle(l_rdy, 0, ctl, 256) &&
-                                                            mbar_wait_idle(drain, 0, ctl, 256));
-    if (ok) {
       tc_fence_after();
-      const float M = mref[((nk - 1) & 3) * kTR + r];
+      const float M = mref[((g - 1) & 3) * kTR + r];
       float l = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float2 f = lfin[q * kTR + r];
+        const float2 f = lfin[((w & 1) * 4 + q) * kTR + r];
         if (f.y != -INFINITY) l += f.x * ex2(f.y - M);
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool store = valid && in_bounds(h < p.H, p.status, kSiteAttnO);
-      __half* orow = p.o + (long long)(store ? i : 0) * p.H * D + (long long)(store ? h : 0) * D + g * QC;
+      __half* orow = p.o + (long long)(store ? i : 0) * p.H * D + (long long)(store ? h : 0) * D + gq * QC;
 #pragma unroll
       for (int c = 0; c < QC / 16; ++c) {
         uint32_t v[16];
-        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + g * QC + 16 * c, v);
-        uint32_t w[8];
+        tmem_ld16_wait(tmem + lanes + Cfg::kOCol + gq * QC + 16 * c, v);
+        uint32_t wv[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const __half2 hh = __floats2half2_rn(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
-          w[q] = *reinterpret_cast<const uint32_t*>(&hh);
+          wv[q] = *reinterpret_cast<const uint32_t*>(&hh);
         }
         if (store) {
-          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
         }
       }
+      tc_fence_before();
+      mbar_arrive_warp(o_free);
     }
   }
 
@@ -593,8 +672,10 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtens
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
+  // one persistent CTA per SM (fewer when there are fewer work items)
   const int qpt = kTR / p.G;
-  const dim3 grid((unsigned)((p.M + qpt - 1) / qpt) * (unsigned)p.Hkv, 1, 1);
+  const long long items = (long long)((p.M + qpt - 1) / qpt) * p.Hkv;
+  const dim3 grid((unsigned)std::min<long long>(items, std::max(p.nsm, 1)), 1, 1);
   kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }

@@ -116,6 +116,7 @@ struct AttnParams {
   int nsplit, tsplit;     // key splits and keys per split (a multiple of 64)
   bool kv_vec16;          // every K/V tile start and T * kv_row_bytes are 16-byte aligned
   uint32_t* status;       // device status word (bounds-checked build)
+  int nsm;                // SMs of the device (persistent grids)
 };
 cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 // attention_tc.cu: the tcgen05 kernel for prefill-sized calls on an fp16 cache

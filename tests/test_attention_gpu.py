@@ -130,3 +130,30 @@ def test_attention_group_sizes(G):
     for causal in (True, False):
         O, ref = run(F16, H, Hkv, M, T, D, T - M, causal, seed=G)
         assert_close(O, ref, "G=%d causal=%d" % (G, causal))
+
+
+@pytest.mark.parametrize("G,D", [(1, 64), (4, 128)])
+def test_attention_many_row_tiles(G, D):
+    # More (row tile, KV head) work items than SMs, so that a CTA walks
+    # several items in turn (a persistent grid): rows spread over every row
+    # tile, causal and not, and with key rows scaled up along the sequence
+    # (the reference maximum raised within an item after a previous item
+    # of the same CTA ended high).
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv = 16 if G == 1 else 8
+    H = G * Hkv
+    rows_per_tile = 128 // G
+    M = ((2 * sms + 40) // Hkv + 1) * rows_per_tile - 37     # > 2 items per SM, ragged last tile
+    T = M + 90
+    rows = list(range(0, M, 19)) + [M - 1]
+    Q = synth.queries(H, M, D, seed=41)
+    Kf = synth.kv_cache(F16, Hkv, T, D, seed=42, name="K")
+    V = synth.kv_cache(F16, Hkv, T, D, seed=42, name="V")
+    ramp = (1.0 + 6.0 * np.arange(T) / T).astype(np.float32)
+    Kr = (Kf.astype(np.float32) * ramp[None, :, None]).astype(np.float16)
+    for K, tag in ((Kf, "plain"), (Kr, "growing")):
+        for causal in (True, False):
+            O = host(m.attention(dev(Q), dev(K), dev(V), F16, Hkv, T, q_offset=T - M, causal=causal))
+            ref = oracle.attention(Q, K, V, F16, H, Hkv, M, T, D, T - M, causal, rows=rows)
+            assert_close(O[rows], ref, "many tiles G=%d D=%d %s causal=%d" % (G, D, tag, causal))
