@@ -251,18 +251,30 @@ enum m4q_kv_codec { M4Q_KV_F16 = 16 };
  *    is 1 / sqrt(D)); Q, K, V, O and workspace 16-byte aligned.
  *  - Scores and the softmax are fp32; the probabilities are rounded to fp16
  *    for the P V product, which accumulates in fp32; O is rounded once.
- *  - workspace: when the query rows alone would leave SMs idle (decode), the
- *    keys are split across CTAs and merged by a second kernel, which needs
- *    m4q_attention_workspace_bytes() bytes of device memory.  NULL (or a
- *    smaller size) runs without the split: same result up to fp32 rounding,
- *    slower at small M.  The library allocates nothing. */
+ *  - workspace (m4q_attention_workspace() bytes of device memory, owned by
+ *    the caller): when the query rows alone would leave SMs idle (decode),
+ *    the keys are split across CTAs and merged by a second kernel, which
+ *    keeps its partial results there; for a Q8_0 cache under a prefill-sized
+ *    call (more than 16 rows per KV head) both caches are first decoded to
+ *    fp16 there (RNE(q * d), as above), since every key tile is read by each
+ *    row tile of its KV head, and the fp16 tensor-core path runs on them.
+ *    NULL (or a smaller size) runs without either: the same result up to
+ *    fp32 rounding, slower.  The library allocates nothing. */
 int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
                   int64_t M, int64_t T, int64_t D, int64_t q_offset, int causal, float scale, void* O,
                   void* workspace, size_t workspace_bytes, m4q_stream_t stream);
 
-/* Workspace bytes m4q_attention uses for this shape on the current device
- * (0: no key split; also 0 for an invalid shape). */
+/* Bytes of the key split's partial results m4q_attention keeps in its
+ * workspace for this shape on the current device (0: no key split; also 0
+ * for an invalid shape).  m4q_attention_workspace covers the Q8_0 staging
+ * as well. */
 size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D);
+
+/* Workspace bytes m4q_attention uses for this cache format and shape on the
+ * current device: the key split's partial results, or for a Q8_0 cache
+ * under a prefill-sized call 2 Hkv T D fp16 values (the decoded caches);
+ * 0 when it uses none, or for an invalid shape. */
+size_t m4q_attention_workspace(int kv_codec, int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D);
 
 /* Decode W [N, K] to fp16 Wf16 [N, K] (row-major): each weight (q - z) * d
  * (MLX4: q * s + b) rounded once to nearest even.  The test hook for

@@ -82,6 +82,7 @@ SIGNATURES = {
     "m4q_attention": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i32,
                              ctypes.c_float, _vp, _vp, _sz, _vp]),
     "m4q_attention_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "m4q_attention_workspace": (_sz, [_i32, _i64, _i64, _i64, _i64, _i64]),
     "m4q_weight_bytes": (_sz, [_i32, _i64, _i64]),
     "m4q_check_finite": (_i32, [_vp, _i64, _vp]),
     "m4q_check_device_status": (_i32, [_vp]),
@@ -374,8 +375,10 @@ def attention(q, k, v, kv_codec: int, hkv: int, t: int, q_offset: int | None = N
     """O fp16 [M, H * D] = attention of q fp16 [H, M, D] over the KV cache k,
     v [hkv, t, D] (fp16 for KV_F16; uint8 Q8_0 blocks [hkv, t, D / 32 * 34]
     for Q8_0).  q_offset defaults to t - M (the queries are the last M
-    positions); scale to 1 / sqrt(D).  The key-split workspace is allocated
-    here when not given."""
+    positions); scale to 1 / sqrt(D).  The workspace (the key split's
+    partial results, or the Q8_0 caches decoded to fp16 for a prefill-sized
+    call) is allocated here when not given; workspace=False runs without
+    one."""
     import torch
     _require(q, torch.float16, "q")
     if q.dim() != 3:
@@ -397,8 +400,10 @@ def attention(q, k, v, kv_codec: int, hkv: int, t: int, q_offset: int | None = N
         raise ValueError("out must hold M * H * D values")
     lib = load()
     if workspace is None:
-        need = int(lib.m4q_attention_workspace_bytes(h, hkv, m_, t, d))
+        need = int(lib.m4q_attention_workspace(kv_codec, h, hkv, m_, t, d))
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    elif workspace is False:
+        workspace = None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.m4q_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), kv_codec, h, hkv, m_, t, d,

@@ -578,6 +578,29 @@ bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uin
   return encode_cached(map, k, estr, 3);
 }
 
+// A Q8_0 cache under a prefill-sized call takes the tcgen05 path after both
+// caches are decoded to fp16 once (each key tile is read by every row tile
+// of its KV head, so one decode replaces many): the staging needs
+// 2 Hkv T D fp16 values.  False when the shape does not take that path.
+bool q8_staging_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, size_t* bytes) {
+  if (H < 1 || Hkv < 1 || M < 1 || T < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return false;
+  if (Hkv * T > INT32_MAX || M * (H / Hkv) > INT32_MAX) return false;
+  DevInfo dev;
+  if (current_device_info(&dev) != M4Q_OK) return false;
+  const AttnSplit a = attn_split(H, Hkv, M, T, D, dev.sms);
+  m4q::AttnParams p{};
+  p.H = (int)H;
+  p.Hkv = (int)Hkv;
+  p.G = (int)(H / Hkv);
+  p.M = (int)M;
+  p.D = (int)D;
+  p.nsplit = a.nsplit;
+  p.kv_row_bytes = 2 * D;
+  if (!m4q::attention_tc_applies(p, false)) return false;
+  *bytes = (size_t)2 * Hkv * T * D * 2;
+  return true;
+}
+
 int check_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
                     int64_t M, int64_t T, int64_t D, int64_t q_offset, float scale, const void* O) {
   if (!Q || !K || !V || !O) return M4Q_ERR_INVALID_ARG;
@@ -600,6 +623,13 @@ size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t 
   DevInfo dev;
   if (current_device_info(&dev) != M4Q_OK) return 0;
   return attn_split(H, Hkv, M, T, D, dev.sms).ws_bytes;
+}
+
+size_t m4q_attention_workspace(int kv_codec, int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D) {
+  const size_t split = m4q_attention_workspace_bytes(H, Hkv, M, T, D);
+  if (kv_codec != M4Q_Q8_0 || split != 0 || M * (H / Hkv) <= 16) return split;
+  size_t stage = 0;
+  return q8_staging_bytes(H, Hkv, M, T, D, &stage) ? stage : 0;
 }
 
 int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
@@ -645,6 +675,21 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
                                          (size_t)a.nsplit * Hkv * a.rtiles * 64 * D * 4);
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  size_t stage = 0;
+  if (kv_codec == M4Q_Q8_0 && a.nsplit == 1 && workspace && q8_staging_bytes(H, Hkv, M, T, D, &stage) &&
+      workspace_bytes >= stage) {
+    // decode both caches to fp16 in the workspace, then the fp16 path
+    __half* kf = static_cast<__half*>(workspace);
+    __half* vf = kf + (size_t)Hkv * T * D;
+    if (m4q::launch_kv_q8_stage(K, V, (long long)Hkv * T, (int)D, kf, vf, s) != cudaSuccess) return M4Q_ERR_CUDA;
+    K = kf;
+    V = vf;
+    p.k = reinterpret_cast<const uint8_t*>(kf);
+    p.v = reinterpret_cast<const uint8_t*>(vf);
+    p.kv_row_bytes = 2 * D;
+    p.kv_vec16 = true;
+    kv_codec = M4Q_KV_F16;
+  }
   if (m4q::attention_tc_applies(p, kv_codec == M4Q_Q8_0)) {
     // Q [H][M][D] takes the same form as the caches, in boxes of the
     // 128 / G queries a CTA takes of each head

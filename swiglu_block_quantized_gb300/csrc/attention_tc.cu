@@ -329,6 +329,8 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, 2000000000ull};
+  pdl_launch_dependents();
+  pdl_wait();   // every global access below comes after the previous kernel
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
@@ -657,6 +659,41 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
+// Q8_0 KV cache -> fp16, the staging of the tensor-core path: one thread per
+// 16 values of a row (half of a 32-value block), K for blockIdx.y == 0 and V
+// for 1.  Each value is RNE(q d): q is exact in fp16, so one fp16 multiply
+// rounds the exact product once.  Blocks start on 2-byte boundaries (34-byte
+// blocks), so the codes are read in 2-byte words.
+__global__ void __launch_bounds__(256)
+    kv_q8_stage_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v, long long rows, int D,
+                       __half* __restrict__ kf, __half* __restrict__ vf) {
+  pdl_wait();   // the caches may come from the previous kernel
+  pdl_launch_dependents();
+  const uint8_t* src = blockIdx.y ? v : k;
+  __half* dst = blockIdx.y ? vf : kf;
+  const int per_row = D / 16;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const long long n = idx / per_row;
+  const int c = (int)(idx % per_row);
+  const uint8_t* blk = src + n * (D / 32) * 34 + (long long)(c >> 1) * 34;
+  const __half2 d2 = __half2half2(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(blk))));
+  const unsigned short* q = reinterpret_cast<const unsigned short*>(blk + 2 + 16 * (c & 1));
+  uint32_t out[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int two = __ldg(q + e);
+    int q0 = two & 0xff, q1 = (two >> 8) & 0xff;
+    q0 -= (q0 & 0x80) << 1;   // the codes are signed bytes
+    q1 -= (q1 & 0x80) << 1;
+    const __half2 h = __hmul2(__halves2half2(__int2half_rn(q0), __int2half_rn(q1)), d2);
+    out[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  uint4* o = reinterpret_cast<uint4*>(dst + n * D + 16 * c);
+  o[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  o[1] = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                       cudaStream_t s) {
@@ -676,8 +713,17 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtens
   const int qpt = kTR / p.G;
   const long long items = (long long)((p.M + qpt - 1) / qpt) * p.Hkv;
   const dim3 grid((unsigned)std::min<long long>(items, std::max(p.nsm, 1)), 1, 1);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace
@@ -687,6 +733,23 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtens
 bool attention_tc_applies(const AttnParams& p, bool q8) {
   return !q8 && p.M * p.G > 16 && p.nsplit == 1 && (p.D == 64 || p.D == 128) && (p.kv_row_bytes % 16) == 0 &&
          p.G <= 16 && kTR % p.G == 0;
+}
+
+cudaError_t launch_kv_q8_stage(const void* k, const void* v, long long rows, int D, void* kf, void* vf,
+                               cudaStream_t s) {
+  const long long threads = rows * (D / 16);
+  if (threads == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)((threads + 255) / 256), 2, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kv_q8_stage_kernel, static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v),
+                            rows, D, static_cast<__half*>(kf), static_cast<__half*>(vf));
 }
 
 cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -124,6 +124,10 @@ cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 // tm_k, tm_v: [Hkv][T][D] of the caches, boxes of [1][128 keys][64 d]; all
 // with the 128-byte swizzle)
 bool attention_tc_applies(const AttnParams& p, bool q8);
+// Q8_0 caches K and V ([rows][D / 32 blocks]) decoded to fp16 kf, vf
+// ([rows][D]), for the tensor-core path
+cudaError_t launch_kv_q8_stage(const void* k, const void* v, long long rows, int D, void* kf, void* vf,
+                               cudaStream_t s);
 cudaError_t launch_attention_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                 const CUtensorMap& tm_v, cudaStream_t s);
 

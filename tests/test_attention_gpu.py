@@ -65,7 +65,7 @@ def test_key_split_matches_single_pass(codec):
     H, Hkv, M, T, D = 8, 2, 1, 4096, 128
     assert m.load().m4q_attention_workspace_bytes(H, Hkv, M, T, D) > 0
     Osplit, ref = run(codec, H, Hkv, M, T, D, T - M, True, seed=3)
-    Oone, _ = run(codec, H, Hkv, M, T, D, T - M, True, seed=3, workspace=None)
+    Oone, _ = run(codec, H, Hkv, M, T, D, T - M, True, seed=3, workspace=False)
     assert_close(Osplit, ref, "split")
     assert_close(Oone, ref, "single pass")
     assert np.abs(Osplit.astype(np.float64) - Oone.astype(np.float64)).max() < 2e-3
@@ -157,3 +157,33 @@ def test_attention_many_row_tiles(G, D):
             O = host(m.attention(dev(Q), dev(K), dev(V), F16, Hkv, T, q_offset=T - M, causal=causal))
             ref = oracle.attention(Q, K, V, F16, H, Hkv, M, T, D, T - M, causal, rows=rows)
             assert_close(O[rows], ref, "many tiles G=%d D=%d %s causal=%d" % (G, D, tag, causal))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_q8_prefill_staged_equals_f16_on_decoded_cache(D):
+    # A prefill-sized call on a Q8_0 cache (enough row tiles that the keys
+    # are not split) decodes both caches to fp16 in the workspace and runs
+    # the fp16 tensor-core path: bit for bit the fp16 call on the decoded
+    # cache.  Without a workspace the Q8_0 cache is decoded tile by tile in
+    # the attention kernel (oracle tolerance).
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, Hkv = 16, 4
+    M = (2 * sms * 64) // (4 * Hkv) + 53
+    T = M + 70
+    rows = list(range(0, M, 29)) + [M - 1]
+    Q = dev(synth.queries(H, M, D, seed=61))
+    K8 = synth.kv_cache(Q8, Hkv, T, D, seed=62, name="K")
+    V8 = synth.kv_cache(Q8, Hkv, T, D, seed=62, name="V")
+    lib = m.load()
+    assert lib.m4q_attention_workspace(Q8, H, Hkv, M, T, D) == 2 * Hkv * T * D * 2
+    assert lib.m4q_attention_workspace(F16, H, Hkv, M, T, D) == 0
+    Kf = m.dequant(dev(K8.reshape(Hkv * T, -1)), Q8, Hkv * T, D).reshape(Hkv, T, D)
+    Vf = m.dequant(dev(V8.reshape(Hkv * T, -1)), Q8, Hkv * T, D).reshape(Hkv, T, D)
+    ref = oracle.attention(host(Q), K8, V8, Q8, H, Hkv, M, T, D, T - M, True, rows=rows)
+    O8 = host(m.attention(Q, dev(K8), dev(V8), Q8, Hkv, T))
+    Of = host(m.attention(Q, Kf, Vf, F16, Hkv, T))
+    On = host(m.attention(Q, dev(K8), dev(V8), Q8, Hkv, T, workspace=False))
+    assert np.array_equal(O8.view(np.uint16), Of.view(np.uint16))
+    assert_close(O8[rows], ref, "q8 staged D=%d" % D)
+    assert_close(On[rows], ref, "q8 in-kernel decode D=%d" % D)
