@@ -737,7 +737,11 @@ def measure_attention(m, dev, reps=20):
         ms = timed(lambda: m.attention(q, k, v, codec, Hkv, T, q_offset=0, out=o))
         flops = 4.0 * H * D * (M * (M + 1) / 2)
         out["prefill_" + name] = {"workload": "8b_attention_causal_m2048_t2048_%s" % name,
-                                  "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_launch": ms}
+                                  "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_launch": ms,
+                                  "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                  "path": ("tcgen05 attn_tc_kernel" if name == "f16" else
+                                           "Q8_0 caches decoded to fp16 in the workspace, then attn_tc_kernel "
+                                           "(both launches timed)")}
         T = 32768
         q1 = torch.from_numpy(synth.queries(H, 1, D, seed=3)).to(dev)
         kc = [torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=4 + r, name="K")).to(dev) for r in range(2)]
