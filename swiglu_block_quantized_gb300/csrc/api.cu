@@ -578,25 +578,21 @@ bool encode_kv(CUtensorMap* map, const void* base, uint64_t Hkv, uint64_t T, uin
   return encode_cached(map, k, estr, 3);
 }
 
-// A Q8_0 cache under a prefill-sized call takes the tcgen05 path after both
-// caches are decoded to fp16 once (each key tile is read by every row tile
-// of its KV head, so one decode replaces many): the staging needs
-// 2 Hkv T D fp16 values.  False when the shape does not take that path.
+// A Q8_0 cache can take the tcgen05 path after both caches are decoded to
+// fp16 once (each key tile is read by every row tile of its KV head, so one
+// decode replaces many): the staging needs 2 Hkv T D fp16 values.  False
+// when the shape cannot take that path.
 bool q8_staging_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, size_t* bytes) {
   if (H < 1 || Hkv < 1 || M < 1 || T < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return false;
   if (Hkv * T > INT32_MAX || M * (H / Hkv) > INT32_MAX) return false;
-  DevInfo dev;
-  if (current_device_info(&dev) != M4Q_OK) return false;
-  const AttnSplit a = attn_split(H, Hkv, M, T, D, dev.sms);
   m4q::AttnParams p{};
   p.H = (int)H;
   p.Hkv = (int)Hkv;
   p.G = (int)(H / Hkv);
   p.M = (int)M;
   p.D = (int)D;
-  p.nsplit = a.nsplit;
   p.kv_row_bytes = 2 * D;
-  if (!m4q::attention_tc_applies(p, false)) return false;
+  if (!m4q::attention_tc_shape(p)) return false;
   *bytes = (size_t)2 * Hkv * T * D * 2;
   return true;
 }
@@ -626,10 +622,12 @@ size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t 
 }
 
 size_t m4q_attention_workspace(int kv_codec, int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D) {
+  // the path is chosen per call (the causal offset enters the estimate), so
+  // the size covers both: the key split's results and a Q8_0 staging
   const size_t split = m4q_attention_workspace_bytes(H, Hkv, M, T, D);
-  if (kv_codec != M4Q_Q8_0 || split != 0 || M * (H / Hkv) <= 16) return split;
   size_t stage = 0;
-  return q8_staging_bytes(H, Hkv, M, T, D, &stage) ? stage : 0;
+  if (kv_codec != M4Q_Q8_0 || !q8_staging_bytes(H, Hkv, M, T, D, &stage)) return split;
+  return stage > split ? stage : split;
 }
 
 int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int64_t H, int64_t Hkv,
@@ -676,8 +674,10 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   size_t stage = 0;
-  if (kv_codec == M4Q_Q8_0 && a.nsplit == 1 && workspace && q8_staging_bytes(H, Hkv, M, T, D, &stage) &&
-      workspace_bytes >= stage) {
+  m4q::AttnParams pf = p;   // the same call on an fp16 cache (the staged form)
+  pf.kv_row_bytes = 2 * D;
+  if (kv_codec == M4Q_Q8_0 && workspace && q8_staging_bytes(H, Hkv, M, T, D, &stage) && workspace_bytes >= stage &&
+      m4q::attention_tc_applies(pf, true)) {
     // decode both caches to fp16 in the workspace, then the fp16 path
     __half* kf = static_cast<__half*>(workspace);
     __half* vf = kf + (size_t)Hkv * T * D;
@@ -690,7 +690,7 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
     p.kv_vec16 = true;
     kv_codec = M4Q_KV_F16;
   }
-  if (m4q::attention_tc_applies(p, kv_codec == M4Q_Q8_0)) {
+  if (kv_codec == M4Q_KV_F16 && m4q::attention_tc_applies(p, false)) {
     // Q [H][M][D] takes the same form as the caches, in boxes of the
     // 128 / G queries a CTA takes of each head
     CUtensorMap tm_q, tm_k, tm_v;

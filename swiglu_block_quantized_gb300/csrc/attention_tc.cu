@@ -728,11 +728,41 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtens
 
 }  // namespace
 
-// fp16 KV cache, more than 16 rows per KV head, one key split, a group size
-// that divides 128 rows into whole swizzle atoms per head (G <= 16).
+// Shapes the kernel takes: more than 16 rows per KV head, a group size that
+// divides 128 rows into whole swizzle atoms per head (G <= 16), rows of
+// 16-byte multiples.
+bool attention_tc_shape(const AttnParams& p) {
+  return p.M * p.G > 16 && (p.D == 64 || p.D == 128) && (p.kv_row_bytes % 16) == 0 && p.G <= 16 &&
+         kTR % p.G == 0;
+}
+
+// Whether the tcgen05 kernel (after a Q8_0 staging when q8) beats the
+// mma.sync kernel with its key split for this call, by estimated time: the
+// tcgen05 kernel takes an item's key tiles in turn on one SM (about 0.9 us
+// a tile at D = 128), so its time is the larger of the longest item and the
+// SMs' share of all tiles; the split kernel spreads the keys over the SMs
+// at about 170 TFLOP/s.  Measured at the 8B shape: for M = 128 to 512 new
+// queries over 4096 keys the tcgen05 kernel took 36-37 us against 52-149 us.
 bool attention_tc_applies(const AttnParams& p, bool q8) {
-  return !q8 && p.M * p.G > 16 && p.nsplit == 1 && (p.D == 64 || p.D == 128) && (p.kv_row_bytes % 16) == 0 &&
-         p.G <= 16 && kTR % p.G == 0;
+  if (!attention_tc_shape(p)) return false;
+  const int QPT = kTR / p.G;
+  const double rtiles = (double)((p.M + QPT - 1) / QPT), items = rtiles * p.Hkv;
+  // visible keys summed over the queries (closed form of sum_i min(T, q_offset + i + 1))
+  double vis = (double)p.M * p.T;
+  long long last = p.T;   // keys the last row tile sees
+  if (p.causal) {
+    const long long a = (long long)p.q_offset + 1;
+    const long long n1 = std::min<long long>(std::max<long long>((long long)p.T - a + 1, 0), p.M);
+    vis = (double)n1 * a + (double)n1 * (n1 - 1) / 2 + (double)(p.M - n1) * p.T;
+    last = std::min<long long>(p.T, (long long)p.q_offset + p.M);
+  }
+  const double longest = (double)((last + kTK - 1) / kTK);
+  const double total = p.Hkv * (vis / QPT) / kTK + items;   // key tiles over all items (rounded up once each)
+  const double tile_us = p.D == 128 ? 0.9 : 0.55;
+  double tc_us = std::max(longest, total / std::max(p.nsm, 1)) * tile_us + 2.0;
+  if (q8) tc_us += 2.0 + (double)p.Hkv * p.T * p.D * 6.0 / 5.0e6;   // staging: 3 bytes a value, 5 TB/s
+  const double split_us = 4.0 * p.H * p.D * vis / 170.0e6 + 2.0;
+  return tc_us <= split_us;
 }
 
 cudaError_t launch_kv_q8_stage(const void* k, const void* v, long long rows, int D, void* kf, void* vf,

@@ -123,7 +123,8 @@ cudaError_t launch_attention(const AttnParams& p, bool q8, cudaStream_t s);
 // (tm_q: 3-D tensor map [H][M][D] of Q, boxes of [1][128 / G queries][64 d];
 // tm_k, tm_v: [Hkv][T][D] of the caches, boxes of [1][128 keys][64 d]; all
 // with the 128-byte swizzle)
-bool attention_tc_applies(const AttnParams& p, bool q8);
+bool attention_tc_shape(const AttnParams& p);                // the kernel takes the shape
+bool attention_tc_applies(const AttnParams& p, bool q8);     // and is estimated faster than the split kernel
 // Q8_0 caches K and V ([rows][D / 32 blocks]) decoded to fp16 kf, vf
 // ([rows][D]), for the tensor-core path
 cudaError_t launch_kv_q8_stage(const void* k, const void* v, long long rows, int D, void* kf, void* vf,
