@@ -742,6 +742,18 @@ def measure_attention(m, dev, reps=20):
                                   "path": ("tcgen05 attn_tc_kernel" if name == "f16" else
                                            "Q8_0 caches decoded to fp16 in the workspace, then attn_tc_kernel "
                                            "(both launches timed)")}
+        # a prefill chunk: 512 new queries over a 4096-token context
+        Mc, Tc = 512, 4096
+        qc = torch.from_numpy(synth.queries(H, Mc, D, seed=5)).to(dev)
+        kcc = torch.from_numpy(synth.kv_cache(codec, Hkv, Tc, D, seed=6, name="K")).to(dev)
+        vcc = torch.from_numpy(synth.kv_cache(codec, Hkv, Tc, D, seed=6, name="V")).to(dev)
+        oc = torch.empty((Mc, H * D), dtype=torch.float16, device=dev)
+        ms = timed(lambda: m.attention(qc, kcc, vcc, codec, Hkv, Tc, q_offset=Tc - Mc, out=oc))
+        flops = 4.0 * H * D * sum(Tc - Mc + i + 1 for i in range(Mc))
+        out["chunk_" + name] = {"workload": "8b_attention_causal_m512_t4096_%s" % name,
+                                "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_launch": ms,
+                                "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+        del qc, kcc, vcc, oc
         T = 32768
         q1 = torch.from_numpy(synth.queries(H, 1, D, seed=3)).to(dev)
         kc = [torch.from_numpy(synth.kv_cache(codec, Hkv, T, D, seed=4 + r, name="K")).to(dev) for r in range(2)]
