@@ -71,7 +71,7 @@ namespace m4q {
 
 namespace {
 
-constexpr int kTR = 128;   // rows per CTA
+constexpr int kTR = 128;   // rows per work item
 constexpr int kTK = 128;   // keys per tile
 constexpr float kLazy = 8.f;   // reference kept while the row max stays within 2^8 of it
 
