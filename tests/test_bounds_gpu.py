@@ -106,7 +106,7 @@ def test_geglu_and_mlp_in_bounds(libs, M):
 
 @pytest.mark.parametrize("kv", [m.KV_F16, m.Q8_0])
 @pytest.mark.parametrize("H,Hkv,M,T,D", [(8, 2, 200, 200, 64), (4, 4, 33, 161, 128), (8, 2, 1, 4096, 128),
-                                         (32, 8, 4, 3000, 64)])
+                                         (32, 8, 4, 3000, 64), (32, 8, 1100, 1200, 128)])
 def test_attention_in_bounds(libs, kv, H, Hkv, M, T, D):
     Q = dev(synth.queries(H, M, D, seed=T))
     K = dev(synth.kv_cache(kv, Hkv, T, D, seed=T + 1, name="K"))
