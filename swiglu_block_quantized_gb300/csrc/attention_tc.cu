@@ -1,7 +1,9 @@
 // attention_tc.cu -- softmax attention over an fp16 KV cache on the tcgen05
-// tensor cores, for prefill-sized calls (more than 16 rows per KV head, no
-// key split).  Same contract as attention.cu, which keeps decode-sized calls
-// and the Q8_0 cache.
+// tensor cores, for prefill-sized calls (more than 16 rows per KV head) that
+// an estimate of the time gives to it; a Q8_0 cache comes here after
+// kv_q8_stage_kernel (below) has decoded it to fp16 in the caller's
+// workspace.  Same contract as attention.cu, which keeps decode-sized calls
+// and the calls the estimate gives to its key split.
 //
 // Pages: "v0.1 vs v0.2 comparison" 2.3 (Brick 4, FlashAttention with an
 // online softmax) and "Releases" v0.3.0 (GQA, causal mask with a sequence
