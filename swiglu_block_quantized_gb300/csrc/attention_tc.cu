@@ -741,7 +741,7 @@ bool attention_tc_shape(const AttnParams& p) {
 // Whether the tcgen05 kernel (after a Q8_0 staging when q8) beats the
 // mma.sync kernel with its key split for this call, by estimated time: the
 // tcgen05 kernel takes an item's key tiles in turn on one SM (about 0.9 us
-// a tile at D = 128), so its time is the larger of the longest item and the
+// a tile, at D = 64 as at 128), so its time is the larger of the longest item and the
 // SMs' share of all tiles; the split kernel spreads the keys over the SMs
 // at about 170 TFLOP/s.  Measured at the 8B shape: for M = 128 to 512 new
 // queries over 4096 keys the tcgen05 kernel took 36-37 us against 52-149 us.
@@ -760,7 +760,7 @@ bool attention_tc_applies(const AttnParams& p, bool q8) {
   }
   const double longest = (double)((last + kTK - 1) / kTK);
   const double total = p.Hkv * (vis / QPT) / kTK + items;   // key tiles over all items (rounded up once each)
-  const double tile_us = p.D == 128 ? 0.9 : 0.55;
+  const double tile_us = 0.9;   // D = 64 tiles cost about as much: the softmax, not the MMA, sets it
   double tc_us = std::max(longest, total / std::max(p.nsm, 1)) * tile_us + 2.0;
   if (q8) tc_us += 2.0 + (double)p.Hkv * p.T * p.D * 6.0 / 5.0e6;   // staging: 3 bytes a value, 5 TB/s
   const double split_us = 4.0 * p.H * p.D * vis / 170.0e6 + 2.0;
