@@ -529,21 +529,23 @@ int m4q_repack(const void* W, int codec, int64_t N, int64_t K, void* Wplanar, m4
 namespace {
 
 // Key split of an attention call: CTAs = row tiles x KV heads; when that
-// leaves the GPU under two CTAs per SM (three for the at-most-16-row decode
-// kernel, which fits three per SM), split the keys (tiles of 64) so the grid
-// reaches about that, each split keeping at least two tiles.
+// leaves the GPU under `per_sm` CTAs per SM (what the tiled kernel fits:
+// two, for its registers or, decoding over an fp16 cache, its three-stage
+// tile pipeline; three for the decode kernel over a Q8_0 cache), split the
+// keys (tiles of 64) so the grid reaches about that, each split keeping at
+// least two tiles.
 struct AttnSplit {
   int rtiles, nsplit, tsplit;
   size_t ws_bytes;
 };
 
-AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, int sms) {
+AttnSplit attn_split(int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D, int sms, int per_sm) {
   AttnSplit a;
   const int64_t R = M * (H / Hkv);
   a.rtiles = (int)((R + 63) / 64);
   const int64_t ctas = (int64_t)a.rtiles * Hkv;
   const int64_t ktiles = (T + 63) / 64;
-  const int64_t target = (R <= 16 ? 3 : 2) * (int64_t)sms;
+  const int64_t target = (int64_t)per_sm * sms;
   int64_t ns = 1;
   if (ctas < target) {
     ns = (target + ctas - 1) / ctas;
@@ -618,7 +620,8 @@ size_t m4q_attention_workspace_bytes(int64_t H, int64_t Hkv, int64_t M, int64_t 
   if (H < 1 || Hkv < 1 || M < 1 || T < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
   DevInfo dev;
   if (current_device_info(&dev) != M4Q_OK) return 0;
-  return attn_split(H, Hkv, M, T, D, dev.sms).ws_bytes;
+  // the larger of the two codecs' splits (a Q8_0 decode splits into more)
+  return attn_split(H, Hkv, M, T, D, dev.sms, M * (H / Hkv) <= 16 ? 3 : 2).ws_bytes;
 }
 
 size_t m4q_attention_workspace(int kv_codec, int64_t H, int64_t Hkv, int64_t M, int64_t T, int64_t D) {
@@ -640,7 +643,7 @@ int m4q_attention(const void* Q, const void* K, const void* V, int kv_codec, int
   rc = current_device_info(&dev);
   if (rc != M4Q_OK) return rc;
   if (!dev.sm103) return M4Q_ERR_UNSUPPORTED_DEVICE;
-  AttnSplit a = attn_split(H, Hkv, M, T, D, dev.sms);
+  AttnSplit a = attn_split(H, Hkv, M, T, D, dev.sms, (M * (H / Hkv) <= 16 && kv_codec == M4Q_Q8_0) ? 3 : 2);
   if (a.nsplit > 1 && (!workspace || workspace_bytes < a.ws_bytes)) {
     a.nsplit = 1;   // no room for partial results: one CTA walks all keys
     a.tsplit = (int)(((T + 63) / 64) * 64);

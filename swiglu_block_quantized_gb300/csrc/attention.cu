@@ -74,6 +74,7 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 template <int D, bool Q8>
 struct AttnCfg {
@@ -81,10 +82,18 @@ struct AttnCfg {
   static constexpr int kPitch = (D + 8) * 2;                   // padded fp16 row in shared memory
   static constexpr int kTile = kKeys * kPitch;                 // one padded fp16 tile
   static constexpr int kRaw = kKeys * kRowBytes;               // one packed Q8_0 tile
-  // Q8_0: packed K and V tiles, double-buffered, then the decoded K and V
-  // tiles.  fp16: the padded K and V tiles, double-buffered.
-  static constexpr int kSmem = Q8 ? 4 * kRaw + 2 * kTile : 4 * kTile;
+  // Q8_0: packed K and V tiles in NS stages, then the decoded K and V
+  // tiles.  fp16: the padded K and V tiles in NS stages.
+  template <int NS>
+  static constexpr int smem() { return Q8 ? 2 * NS * kRaw + 2 * kTile : 2 * NS * kTile; }
 };
+
+// Stages of the K/V tile pipeline: three when the warps split the keys of a
+// few rows over an fp16 cache (decode: little compute per tile to hide a
+// tile's load behind; two CTAs per SM then), else two (the Q8_0 decode is
+// bound by its arithmetic, and gains more from a third CTA per SM).
+template <bool KS, bool Q8>
+constexpr int kAttnStages = (KS && !Q8) ? 3 : 2;
 
 // Start the asynchronous copy of keys [k0, min(k0 + 64, T)) of one KV head:
 // packed rows as they are (Q8_0), or fp16 rows into the padded tile, whose
@@ -252,16 +261,28 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   // stage s: Q8_0 packed K at 2 s * kRaw, V at (2 s + 1) * kRaw; fp16 padded
   // K at 2 s * kTile, V at (2 s + 1) * kTile
   constexpr int kStage = Q8 ? Cfg::kRaw : Cfg::kTile;
-  uint8_t* dec = smem + 4 * Cfg::kRaw;   // Q8_0: decoded K, then V
-  if (kbeg < kend) issue_tile<D, Q8>(smem, smem + kStage, khead, vhead, kbeg, p.T, p.kv_vec16, p.status);
+  constexpr int NS = kAttnStages<KS, Q8>;
+  uint8_t* dec = smem + 2 * NS * Cfg::kRaw;   // Q8_0: decoded K, then V
+  // tiles 0 .. NS - 2 in flight before the loop; tile it + NS - 1 issued once
+  // tile it has landed and every warp is done with tile it - 1
+#pragma unroll
+  for (int s0 = 0; s0 < NS - 1; ++s0)
+    if (kbeg + s0 * kKeys < kend)
+      issue_tile<D, Q8>(smem + 2 * s0 * kStage, smem + (2 * s0 + 1) * kStage, khead, vhead, kbeg + s0 * kKeys, p.T,
+                        p.kv_vec16, p.status);
   int it = 0;
   for (int k0 = kbeg; k0 < kend; k0 += kKeys, ++it) {
-    const int st = it & 1;
-    cp_async_wait_all();
+    const int st = it % NS;
+    // this tile's copy group is the oldest outstanding one: wait for all but
+    // the ones issued after it
+    if (NS == 3 && k0 + kKeys < kend) cp_async_wait_one();
+    else cp_async_wait_all();
     __syncthreads();   // this tile has landed; every warp is done with the previous one
-    if (k0 + kKeys < kend)
-      issue_tile<D, Q8>(smem + 2 * (st ^ 1) * kStage, smem + (2 * (st ^ 1) + 1) * kStage, khead, vhead,
-                        k0 + kKeys, p.T, p.kv_vec16, p.status);
+    if (k0 + (NS - 1) * kKeys < kend) {
+      const int sn = (it + NS - 1) % NS;
+      issue_tile<D, Q8>(smem + 2 * sn * kStage, smem + (2 * sn + 1) * kStage, khead, vhead, k0 + (NS - 1) * kKeys,
+                        p.T, p.kv_vec16, p.status);
+    }
     const uint8_t* Kt;
     const uint8_t* Vt;
     if constexpr (Q8) {
@@ -500,7 +521,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
 template <int D, bool Q8, bool KS>
 cudaError_t launch_attn_dqk(const AttnParams& p, cudaStream_t s) {
   auto kern = attn_kernel<D, Q8, KS>;
-  constexpr int kSmem = AttnCfg<D, Q8>::kSmem;
+  constexpr int kSmem = AttnCfg<D, Q8>::template smem<kAttnStages<KS, Q8>>();
   static_assert(4 * 16 * D * 4 + 4 * 16 * 8 <= kSmem, "warp merge buffer");
   std::atomic<unsigned long long>& configured = attr_flag<std::integer_sequence<int, 3, D, Q8, KS>>();
   int dev = 0;
