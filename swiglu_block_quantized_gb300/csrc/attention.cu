@@ -147,36 +147,63 @@ __device__ __forceinline__ void issue_tile(uint8_t* kdst, uint8_t* vdst, const u
 // Decode a packed Q8_0 tile (rows of D / 32 blocks) into the padded fp16
 // tile: RNE(q * d) per value, the weights' exact decode.  Rows at or past
 // `valid` are written as zeros.  A warp takes 32 consecutive rows of one
-// block column, so the branch on the block's alignment is uniform: a block
-// at an even index starts 4-byte aligned (rows are 4-byte multiples) and is
-// read as 9 words; one at an odd index starts 2 bytes past a word and is
-// read as 10 words and shifted.  Those reads may run up to 4 bytes past the
-// block (into the next row, or the next buffer for the tile's last row);
-// the extra bytes are never used.
+// block column, so its reads share one alignment:
+//   - rows of a multiple of 8 bytes (D = 128): five 8-byte reads from the
+//     8-byte boundary at or before the block, which it starts sh = 34 blk
+//     mod 8 bytes into (0, 2, 4 or 6); conflict-free, as the 16 lanes of a
+//     half-warp read consecutive rows 34 words apart;
+//   - otherwise a block at an even index starts 4-byte aligned (rows are
+//     4-byte multiples) and is read as 9 words; one at an odd index starts 2
+//     bytes past a word and is read as 10 words and shifted.
+// Those reads may run up to 4 bytes past the block (into the next row, or
+// the next buffer for the tile's last row); the extra bytes are never used.
 template <int D>
 __device__ __forceinline__ void decode_q8_tile(uint8_t* dst, const uint8_t* raw, int valid) {
   using Cfg = AttnCfg<D, true>;
   const DecK K = make_deck();
   constexpr int kBlk = D / 32;
   constexpr int kUnits = kKeys * kBlk / 128;
+  static_assert(kKeys == 64, "two block columns per 128 threads");
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
-    const int unit = threadIdx.x + 128 * u;
-    const int blk = unit / kKeys, rr = unit % kKeys;
+    // unit = threadIdx.x + 128 u: row unit % 64, block column 2 u + (threadIdx.x >> 6)
+    const int h = threadIdx.x >> 6, rr = threadIdx.x & 63, blk = 2 * u + h;
     uint4* out = reinterpret_cast<uint4*>(dst + rr * Cfg::kPitch + 64 * blk);
     if (rr < valid) {
       const int off = rr * Cfg::kRowBytes + 34 * blk;
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(raw + (off & ~3));
       uint32_t w[9];
-      if ((off & 3) == 0) {
-#pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = src[i];
-      } else {
+      if constexpr (Cfg::kRowBytes % 8 == 0) {
+        // sh = (68 u + 34 h) mod 8 = 4 (u & 1) + 2 h
+        const uint2* src = reinterpret_cast<const uint2*>(raw + (off & ~7));
         uint32_t a[10];
 #pragma unroll
-        for (int i = 0; i < 10; ++i) a[i] = src[i];
+        for (int i = 0; i < 5; ++i) {
+          const uint2 x = src[i];
+          a[2 * i] = x.x;
+          a[2 * i + 1] = x.y;
+        }
+        uint32_t b[10];
 #pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = __funnelshift_r(a[i], a[i + 1], 16);
+        for (int i = 0; i < 10; ++i) b[i] = (u & 1) ? (i < 9 ? a[i + 1] : 0u) : a[i];
+        if (h) {
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = __funnelshift_r(b[i], b[i + 1], 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = b[i];
+        }
+      } else {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(raw + (off & ~3));
+        if ((off & 3) == 0) {
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = src[i];
+        } else {
+          uint32_t a[10];
+#pragma unroll
+          for (int i = 0; i < 10; ++i) a[i] = src[i];
+#pragma unroll
+          for (int i = 0; i < 9; ++i) w[i] = __funnelshift_r(a[i], a[i + 1], 16);
+        }
       }
       const uint32_t d2 = dup_scale(u16_at(w, 0));
       uint32_t v[16];
@@ -211,6 +238,8 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   const int wrow = KS ? 0 : 16 * warp;           // first row of this warp in the tile
   const int kw = KS ? 16 * warp : 0;             // first key of this warp in a key tile
   const bool active = rt * kRows + wrow < R;     // this warp has a row to compute
+  pdl_launch_dependents();
+  pdl_wait();   // every global access below comes after the previous kernel
 
   // This thread's two rows (g and g + 8 of the warp's 16).
   int qi[2], qh[2], lim[2];
@@ -473,6 +502,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long base = (long long)hk * rows_pad + r;          // slot of split s: base + s * stride
   const long long stride = (long long)p.Hkv * rows_pad;
+  // No early launch_dependents here: a kernel after this one (the next
+  // attention launch) then starts only when these CTAs have left the SMs,
+  // so the attention grid, one full wave at three CTAs per SM over a Q8_0
+  // cache, is never split by a CTA of this kernel.
+  pdl_wait();   // the splits come from the attention kernel before it
   float m = -INFINITY;
   for (int s = threadIdx.x; s < p.nsplit; s += 256) m = fmaxf(m, p.ws_ml[base + s * stride].x);
 #pragma unroll
@@ -518,6 +552,24 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   }
 }
 
+// Launch with programmatic dependent launch (unless M4Q_PDL=0): the kernel
+// may be scheduled while the previous kernel of the stream finishes, and
+// waits for it (griddepcontrol.wait) before its first global access.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, dim3 grid, unsigned block, int smem, cudaStream_t s, const AttnParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int D, bool Q8, bool KS>
 cudaError_t launch_attn_dqk(const AttnParams& p, cudaStream_t s) {
   auto kern = attn_kernel<D, Q8, KS>;
@@ -533,12 +585,9 @@ cudaError_t launch_attn_dqk(const AttnParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const dim3 grid((unsigned)p.rtiles, (unsigned)p.Hkv, (unsigned)p.nsplit);
-  kern<<<grid, 128, kSmem, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)p.rtiles, (unsigned)p.Hkv, (unsigned)p.nsplit), 128, kSmem, s, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  attn_combine_kernel<D><<<(unsigned)((long long)p.Hkv * p.M * p.G), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel<D>, dim3((unsigned)((long long)p.Hkv * p.M * p.G)), 256, 0, s, p);
 }
 
 }  // namespace
