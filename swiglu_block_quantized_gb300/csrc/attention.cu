@@ -292,10 +292,15 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   constexpr int kStage = Q8 ? Cfg::kRaw : Cfg::kTile;
   constexpr int NS = kAttnStages<KS, Q8>;
   uint8_t* dec = smem + 2 * NS * Cfg::kRaw;   // Q8_0: decoded K, then V
-  // tiles 0 .. NS - 2 in flight before the loop; tile it + NS - 1 issued once
-  // tile it has landed and every warp is done with tile it - 1
+  // fp16: tiles 0 .. NS - 2 in flight before the loop; tile it + NS - 1
+  // issued once tile it has landed and every warp is done with tile it - 1.
+  // Q8_0: a packed stage is free again once its tile is decoded, so tiles
+  // 0 .. NS - 1 go before the loop and tile it + NS right after tile it's
+  // decode: NS tiles in flight while the warps run the MMAs.
+  constexpr int kAhead = Q8 ? NS : NS - 1;
+  static_assert(kAhead >= 1 && kAhead <= 2, "copy groups waited for below");
 #pragma unroll
-  for (int s0 = 0; s0 < NS - 1; ++s0)
+  for (int s0 = 0; s0 < kAhead; ++s0)
     if (kbeg + s0 * kKeys < kend)
       issue_tile<D, Q8>(smem + 2 * s0 * kStage, smem + (2 * s0 + 1) * kStage, khead, vhead, kbeg + s0 * kKeys, p.T,
                         p.kv_vec16, p.status);
@@ -303,24 +308,27 @@ __global__ void __launch_bounds__(128, KS ? 3 : 2) attn_kernel(const AttnParams 
   for (int k0 = kbeg; k0 < kend; k0 += kKeys, ++it) {
     const int st = it % NS;
     // this tile's copy group is the oldest outstanding one: wait for all but
-    // the ones issued after it
-    if (NS == 3 && k0 + kKeys < kend) cp_async_wait_one();
+    // the one issued after it
+    if (kAhead == 2 && k0 + kKeys < kend) cp_async_wait_one();
     else cp_async_wait_all();
     __syncthreads();   // this tile has landed; every warp is done with the previous one
-    if (k0 + (NS - 1) * kKeys < kend) {
-      const int sn = (it + NS - 1) % NS;
-      issue_tile<D, Q8>(smem + 2 * sn * kStage, smem + (2 * sn + 1) * kStage, khead, vhead, k0 + (NS - 1) * kKeys,
-                        p.T, p.kv_vec16, p.status);
-    }
     const uint8_t* Kt;
     const uint8_t* Vt;
     if constexpr (Q8) {
       decode_q8_tile<D>(dec, smem + 2 * st * kStage, kend - k0);
       decode_q8_tile<D>(dec + Cfg::kTile, smem + (2 * st + 1) * kStage, kend - k0);
-      __syncthreads();
+      __syncthreads();   // decoded: packed stage st is free
+      if (k0 + NS * kKeys < kend)
+        issue_tile<D, Q8>(smem + 2 * st * kStage, smem + (2 * st + 1) * kStage, khead, vhead, k0 + NS * kKeys, p.T,
+                          p.kv_vec16, p.status);
       Kt = dec;
       Vt = dec + Cfg::kTile;
     } else {
+      if (k0 + (NS - 1) * kKeys < kend) {
+        const int sn = (it + NS - 1) % NS;
+        issue_tile<D, Q8>(smem + 2 * sn * kStage, smem + (2 * sn + 1) * kStage, khead, vhead,
+                          k0 + (NS - 1) * kKeys, p.T, p.kv_vec16, p.status);
+      }
       Kt = smem + 2 * st * kStage;
       Vt = smem + (2 * st + 1) * kStage;
     }
